@@ -1,0 +1,211 @@
+"""Thin ctypes binding of the C ABI in include/lbkv.h.
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity and passed as raw pointers with the current CUDA stream. Every step
+of the computation runs in the CUDA library; if the library is missing this
+module raises instead of falling back to anything else.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+TOKENWISE = 0
+CHANNELWISE = 1
+
+STATUS = {0: "LBKV_OK", -1: "LBKV_EINVAL", -2: "LBKV_EALIGN", -3: "LBKV_EUNSUPPORTED",
+          -4: "LBKV_EWORKSPACE", -5: "LBKV_ECUDA", -6: "LBKV_EDEVICE"}
+
+EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_device_status", "lbkv_strerror")
+
+
+class LbkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({strerror(status)})")
+
+
+class Desc(ctypes.Structure):
+    """Mirror of lbkv_desc."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("sm_scale", ctypes.c_float),
+        ("k_win", ctypes.c_void_p), ("v_win", ctypes.c_void_p), ("win_lens", ctypes.c_void_p),
+        ("win_cap", ctypes.c_int32), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Load liblbkv.so (built by bit_kv_cache_split_gb300.build.build()); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library {p} is missing; run bit_kv_cache_split_gb300.build.build() first")
+        L = ctypes.CDLL(p)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        L.lbkv_workspace_bytes.restype = ctypes.c_size_t
+        L.lbkv_workspace_bytes.argtypes = [ctypes.POINTER(Desc), i32, i32, i32, i32]
+        L.lbkv_decode_attn.restype = i32
+        L.lbkv_decode_attn.argtypes = [ctypes.POINTER(Desc)] + [vp] * 8 + [i32] * 4 + [vp, vp]
+        L.lbkv_pack.restype = i32
+        L.lbkv_pack.argtypes = [ctypes.POINTER(Desc), vp, vp, i32, i32, i32, vp, vp, vp, vp]
+        L.lbkv_device_status.restype = i32
+        L.lbkv_device_status.argtypes = [ctypes.POINTER(Desc), vp, ctypes.POINTER(ctypes.c_int32)]
+        L.lbkv_strerror.restype = ctypes.c_char_p
+        L.lbkv_strerror.argtypes = [i32]
+        if path is None:
+            _lib = L
+        return L
+
+
+def strerror(status: int) -> str:
+    try:
+        return load().lbkv_strerror(int(status)).decode()
+    except RuntimeError:
+        return STATUS.get(status, "unknown")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def make_desc(batch, num_q_heads, num_kv_heads, max_seq_len, head_dim=128, sm_scale=0.0, k_win=None,
+              v_win=None, win_lens=None, workspace=None) -> Desc:
+    d = Desc()
+    d.batch, d.num_q_heads, d.num_kv_heads = int(batch), int(num_q_heads), int(num_kv_heads)
+    d.head_dim, d.max_seq_len, d.sm_scale = int(head_dim), int(max_seq_len), float(sm_scale)
+    d.k_win = None if k_win is None else k_win.data_ptr()
+    d.v_win = None if v_win is None else v_win.data_ptr()
+    d.win_lens = None if win_lens is None else win_lens.data_ptr()
+    d.win_cap = 0 if k_win is None else int(k_win.shape[2])
+    d.workspace = None if workspace is None else workspace.data_ptr()
+    d.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return d
+
+
+def workspace_bytes(batch, num_q_heads, num_kv_heads, max_seq_len, bits, k_layout, v_layout, group,
+                    window: bool = False, head_dim=128) -> int:
+    """Workspace size for a call with these shapes (0 when the arguments are invalid)."""
+    d = make_desc(batch, num_q_heads, num_kv_heads, max_seq_len, head_dim)
+    if window:
+        d.k_win = d.v_win = d.win_lens = 16  # any non-null value: only presence matters here
+        d.win_cap = 1
+    return int(load().lbkv_workspace_bytes(ctypes.byref(d), bits, k_layout, v_layout, group))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """Zero-filled byte tensor, 256-byte aligned (torch's allocator aligns to 512)."""
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def decode_attn(q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, *, bits, k_layout=TOKENWISE,
+                v_layout=TOKENWISE, group=128, sm_scale=0.0, k_win=None, v_win=None, win_lens=None,
+                out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Decode attention through lbkv_decode_attn. Shapes as in include/lbkv.h.
+
+    q bf16 [B][Hq][D]; k_codes/v_codes uint8 [B][Hkv][T_cap][D*bits/8]; scales/offsets fp16;
+    seq_lens int32 [B] on the device. Returns out bf16 [B][Hq][D] (allocated when not given).
+    """
+    B, Hq, D = q.shape
+    Hkv, T = k_codes.shape[1], k_codes.shape[2]
+    _check(q, "q", torch.bfloat16)
+    for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
+        _check(t, name, torch.uint8, (B, Hkv, T, D * bits // 8))
+    for name, t in (("k_scale", k_scale), ("k_off", k_off), ("v_scale", v_scale), ("v_off", v_off)):
+        _check(t, name, torch.float16)
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    if k_win is not None:
+        _check(k_win, "k_win", torch.bfloat16)
+        _check(v_win, "v_win", torch.bfloat16, tuple(k_win.shape))
+        _check(win_lens, "win_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _check(out, "out", torch.bfloat16, (B, Hq, D))
+    L = load()
+    if workspace is None:
+        n = workspace_bytes(B, Hq, Hkv, T, bits, k_layout, v_layout, group, window=k_win is not None)
+        if n == 0:
+            raise LbkvError(-3 if bits in (2, 4) else -1, "lbkv_workspace_bytes")
+        workspace = alloc_workspace(n, q.device)
+    d = make_desc(B, Hq, Hkv, T, D, sm_scale, k_win, v_win, win_lens, workspace)
+    st = L.lbkv_decode_attn(ctypes.byref(d), _ptr(q), _ptr(k_codes), _ptr(k_scale), _ptr(k_off), _ptr(v_codes),
+                            _ptr(v_scale), _ptr(v_off), _ptr(seq_lens), int(bits), int(k_layout), int(v_layout),
+                            int(group), _ptr(out), _stream_ptr(stream))
+    if st != 0:
+        raise LbkvError(st, "lbkv_decode_attn")
+    return out
+
+
+def pack(x, seq_lens, *, bits, layout=TOKENWISE, group=128, codes=None, scale=None, off=None, stream=None):
+    """Quantize bf16 x [B][Hkv][T_cap][D] through lbkv_pack. Returns (codes, scale, off)."""
+    _check(x, "x", torch.bfloat16)
+    B, Hkv, T, D = x.shape
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    sshape = (B, Hkv, T, D // group) if layout == TOKENWISE else (B, Hkv, T // group, D)
+    if codes is None:
+        codes = torch.empty((B, Hkv, T, D * bits // 8), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.zeros(sshape, dtype=torch.float16, device=x.device)
+    if off is None:
+        off = torch.zeros(sshape, dtype=torch.float16, device=x.device)
+    _check(codes, "codes", torch.uint8, (B, Hkv, T, D * bits // 8))
+    _check(scale, "scale", torch.float16, sshape)
+    _check(off, "off", torch.float16, sshape)
+    d = make_desc(B, 1, Hkv, T, D)
+    d.num_q_heads = Hkv
+    st = load().lbkv_pack(ctypes.byref(d), _ptr(x), _ptr(seq_lens), int(bits), int(layout), int(group),
+                          _ptr(codes), _ptr(scale), _ptr(off), _stream_ptr(stream))
+    if st != 0:
+        raise LbkvError(st, "lbkv_pack")
+    return codes, scale, off
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Read and clear the device status word (synchronizes the stream). Returns the code (0 = fine)."""
+    d = Desc()
+    d.workspace = workspace.data_ptr()
+    d.workspace_bytes = workspace.numel() * workspace.element_size()
+    code = ctypes.c_int32(0)
+    st = load().lbkv_device_status(ctypes.byref(d), _stream_ptr(stream), ctypes.byref(code))
+    if st not in (0, -6):
+        raise LbkvError(st, "lbkv_device_status")
+    return int(code.value)

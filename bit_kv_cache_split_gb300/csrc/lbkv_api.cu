@@ -1,0 +1,284 @@
+// lbkv_api.cu -- the C ABI (include/lbkv.h): argument validation, split-KV
+// planning, workspace layout and kernel launches. Nothing here allocates,
+// frees or synchronizes (except lbkv_device_status, documented as such).
+#include <atomic>
+#include <cmath>
+
+#include "lbkv.h"
+#include "lbkv_internal.h"
+
+namespace lbkv {
+
+// Merges the splits of one (sequence, query head): out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+__global__ void __launch_bounds__(128) split_combine_kernel(const float2* __restrict__ part_ml,
+                                                             const float* __restrict__ part_o, int s_tot,
+                                                             __nv_bfloat16* __restrict__ out) {
+  const int bh = blockIdx.x, ch = threadIdx.x;
+  const float2* ml = part_ml + (size_t)bh * s_tot;
+  const float* po = part_o + (size_t)bh * s_tot * kHeadDim;
+  float M = -INFINITY;
+  for (int s = 0; s < s_tot; ++s) M = fmaxf(M, ml[s].x);
+  float acc = 0.f, l = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < s_tot; ++s) {
+      const float2 x = ml[s];
+      const float sc = (x.x == -INFINITY) ? 0.f : fast_exp2(x.x - M);
+      l = fmaf(sc, x.y, l);
+      acc = fmaf(sc, po[(size_t)s * kHeadDim + ch], acc);
+    }
+  }
+  out[(size_t)bh * kHeadDim + ch] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
+}
+
+}  // namespace lbkv
+
+using namespace lbkv;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_optin[kMaxDevices];
+
+int current_device_props(int* sms, int* smem_optin) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LBKV_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return LBKV_ECUDA;
+  int s = g_sm_count[dev].load(std::memory_order_relaxed);
+  int m = g_smem_optin[dev].load(std::memory_order_relaxed);
+  if (s <= 0 || m <= 0) {
+    if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LBKV_ECUDA;
+    if (cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return LBKV_ECUDA;
+    g_sm_count[dev].store(s, std::memory_order_relaxed);
+    g_smem_optin[dev].store(m, std::memory_order_relaxed);
+  }
+  *sms = s;
+  *smem_optin = m;
+  return LBKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+struct Plan {
+  int hq, nt, gv;
+  int splits, s_tot, slots_per_split;
+  int n_ring, slot_bytes, slot_tx, smem_bytes;
+  int off_vc, off_ks, off_kz, off_vs, off_vz, sz_k, sz_v;
+  size_t off_ml, off_o, ws_bytes;
+};
+
+// Validates shapes and format, then fixes the split count and the ring.
+int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl) {
+  if (!d) return LBKV_EINVAL;
+  if (d->batch < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0) return LBKV_EINVAL;
+  if (d->num_q_heads % d->num_kv_heads) return LBKV_EINVAL;
+  if (d->head_dim != kHeadDim) return LBKV_EUNSUPPORTED;
+  if (d->max_seq_len <= 0 || d->max_seq_len % kSlotTokens) return LBKV_EINVAL;
+  if (bits != 2 && bits != 4) return LBKV_EINVAL;
+  if ((kl != LBKV_TOKENWISE && kl != LBKV_CHANNELWISE) || (vl != LBKV_TOKENWISE && vl != LBKV_CHANNELWISE))
+    return LBKV_EINVAL;
+  if (group != 32 && group != 64 && group != 128) return LBKV_EUNSUPPORTED;
+  const int hq = d->num_q_heads / d->num_kv_heads;
+  if (hq != 1 && hq != 2 && hq != 4 && hq != 8) return LBKV_EUNSUPPORTED;
+  const bool win = d->k_win != nullptr;
+  if (win != (d->v_win != nullptr) || win != (d->win_lens != nullptr)) return LBKV_EINVAL;
+  if (win && (d->win_cap <= 0 || d->win_cap > 128)) return LBKV_EINVAL;
+  pl->hq = hq;
+  pl->nt = hq > 4 ? 2 : 1;
+  // A token-wise V side with G channel groups feeds G separately scaled copies of P
+  // (operand-fold); the kernel holds at most two PV n-tiles of 8 columns.
+  const int groups_v = (vl == LBKV_TOKENWISE) ? kHeadDim / group : 1;
+  if (groups_v > 2 || pl->nt * groups_v > 2) return LBKV_EUNSUPPORTED;
+  pl->gv = groups_v;
+
+  int sms = 0, smem_optin = 0;
+  int st = current_device_props(&sms, &smem_optin);
+  if (st) return st;
+
+  // ring slot: K codes | V codes | K scale | K offset | V scale | V offset
+  const int rb = kHeadDim * bits / 8;
+  pl->sz_k = (kl == LBKV_TOKENWISE) ? kSlotTokens * (kHeadDim / group) * 2 : (kSlotTokens / group) * kHeadDim * 2;
+  pl->sz_v = (vl == LBKV_TOKENWISE) ? kSlotTokens * (kHeadDim / group) * 2 : (kSlotTokens / group) * kHeadDim * 2;
+  pl->off_vc = kSlotTokens * rb;
+  pl->off_ks = 2 * kSlotTokens * rb;
+  pl->off_kz = pl->off_ks + pl->sz_k;
+  pl->off_vs = pl->off_kz + pl->sz_k;
+  pl->off_vz = pl->off_vs + pl->sz_v;
+  pl->slot_tx = pl->off_vz + pl->sz_v;
+  pl->slot_bytes = (int)round_up((size_t)pl->slot_tx, 128);
+  const int budget = smem_optin - kRingOffset;
+  int n_ring = budget / pl->slot_bytes;
+  if (n_ring > kMaxRing) n_ring = kMaxRing;
+  n_ring -= n_ring % kQuads;
+  if (n_ring < 2 * kQuads || (size_t)n_ring * pl->slot_bytes < (size_t)kMergeBytes) return LBKV_EUNSUPPORTED;
+  pl->n_ring = n_ring;
+  pl->smem_bytes = kRingOffset + n_ring * pl->slot_bytes;
+
+  // Split count: minimise waves * (slots per CTA + fill), one CTA per SM.
+  const long long units = (long long)d->batch * d->num_kv_heads;
+  const int spu = d->max_seq_len / kSlotTokens;
+  int best_s = 1;
+  double best_cost = 1e300;
+  if (units > 0) {
+    const int s_max = spu < 64 ? spu : 64;
+    for (int s = 1; s <= s_max; ++s) {
+      const long long ctas = units * s;
+      const double waves = std::ceil((double)ctas / sms);
+      const double per = std::ceil((double)spu / s) + 3.0;
+      const double cost = waves * per;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best_s = s;
+      }
+    }
+  }
+  pl->splits = best_s;
+  pl->slots_per_split = (spu + best_s - 1) / best_s;
+  pl->s_tot = best_s + (win ? 1 : 0);
+
+  const size_t rows = (size_t)d->batch * d->num_q_heads * pl->s_tot;
+  pl->off_ml = 256;
+  pl->off_o = round_up(pl->off_ml + rows * sizeof(float2), 256);
+  pl->ws_bytes = round_up(pl->off_o + rows * kHeadDim * sizeof(float), 256);
+  return LBKV_OK;
+}
+
+DecodeKernel pick_kernel(int bits, int kl, int vl, int nt, int gv) {
+  return bits == 2 ? decode_kernel_int2(kl, vl, nt, gv) : decode_kernel_int4(kl, vl, nt, gv);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lbkv_workspace_bytes(const lbkv_desc* desc, int bits, int k_layout, int v_layout, int group) {
+  Plan pl;
+  if (make_plan(desc, bits, k_layout, v_layout, group, &pl) != LBKV_OK) return 0;
+  return pl.ws_bytes;
+}
+
+int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_codes, const void* k_scale,
+                     const void* k_off, const uint8_t* v_codes, const void* v_scale, const void* v_off,
+                     const int32_t* seq_lens, int bits, int k_layout, int v_layout, int group, void* out,
+                     lbkv_stream_t stream) {
+  Plan pl;
+  int st = make_plan(desc, bits, k_layout, v_layout, group, &pl);
+  if (st) return st;
+  if (desc->batch == 0) return LBKV_OK;
+  const void* ptrs[] = {q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, out};
+  for (const void* p : ptrs)
+    if (!p) return LBKV_EINVAL;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LBKV_EALIGN;
+  if (desc->k_win && (!aligned16(desc->k_win) || !aligned16(desc->v_win))) return LBKV_EALIGN;
+  if (!desc->workspace || desc->workspace_bytes < pl.ws_bytes) return LBKV_EWORKSPACE;
+  if (reinterpret_cast<uintptr_t>(desc->workspace) & 255u) return LBKV_EALIGN;
+  DecodeKernel kern = pick_kernel(bits, k_layout, v_layout, pl.nt, pl.gv);
+  if (!kern) return LBKV_EUNSUPPORTED;
+
+  uint8_t* ws = static_cast<uint8_t*>(desc->workspace);
+  DecodeParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_codes = k_codes;
+  p.k_scale = static_cast<const __half*>(k_scale);
+  p.k_off = static_cast<const __half*>(k_off);
+  p.v_codes = v_codes;
+  p.v_scale = static_cast<const __half*>(v_scale);
+  p.v_off = static_cast<const __half*>(v_off);
+  p.seq_lens = seq_lens;
+  p.k_win = static_cast<const __nv_bfloat16*>(desc->k_win);
+  p.v_win = static_cast<const __nv_bfloat16*>(desc->v_win);
+  p.win_lens = desc->win_lens;
+  p.part_ml = reinterpret_cast<float2*>(ws + pl.off_ml);
+  p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
+  p.status = reinterpret_cast<int32_t*>(ws);
+  p.B = desc->batch;
+  p.Hq = desc->num_q_heads;
+  p.Hkv = desc->num_kv_heads;
+  p.hq = pl.hq;
+  p.T_cap = desc->max_seq_len;
+  p.group = group;
+  p.win_cap = desc->k_win ? desc->win_cap : 0;
+  const float sigma = desc->sm_scale > 0.f ? desc->sm_scale : 1.f / std::sqrt((float)desc->head_dim);
+  p.sl2 = sigma * 1.4426950408889634f;
+  p.splits = pl.splits;
+  p.s_tot = pl.s_tot;
+  p.slots_per_split = pl.slots_per_split;
+  p.n_ring = pl.n_ring;
+  p.slot_bytes = pl.slot_bytes;
+  p.slot_tx = pl.slot_tx;
+  p.off_vc = pl.off_vc;
+  p.off_ks = pl.off_ks;
+  p.off_kz = pl.off_kz;
+  p.off_vs = pl.off_vs;
+  p.off_vz = pl.off_vz;
+  p.sz_k_bytes = pl.sz_k;
+  p.sz_v_bytes = pl.sz_v;
+
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           pl.smem_bytes) != cudaSuccess)
+    return LBKV_ECUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dim3 grid((unsigned)pl.s_tot, (unsigned)desc->num_kv_heads, (unsigned)desc->batch);
+  kern<<<grid, kThreads, pl.smem_bytes, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;
+  split_combine_kernel<<<(unsigned)(desc->batch * desc->num_q_heads), kHeadDim, 0, s>>>(
+      p.part_ml, p.part_o, pl.s_tot, static_cast<__nv_bfloat16*>(out));
+  if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;
+  return LBKV_OK;
+}
+
+int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_lens, int bits, int layout, int group,
+              uint8_t* codes, void* scale, void* off, lbkv_stream_t stream) {
+  if (!desc) return LBKV_EINVAL;
+  if (desc->batch < 0 || desc->num_kv_heads <= 0) return LBKV_EINVAL;
+  if (desc->head_dim != kHeadDim) return LBKV_EUNSUPPORTED;
+  if (desc->max_seq_len <= 0 || desc->max_seq_len % kSlotTokens) return LBKV_EINVAL;
+  if (bits != 2 && bits != 4) return LBKV_EINVAL;
+  if (layout != LBKV_TOKENWISE && layout != LBKV_CHANNELWISE) return LBKV_EINVAL;
+  if (group != 32 && group != 64 && group != 128) return LBKV_EUNSUPPORTED;
+  if (desc->batch == 0) return LBKV_OK;
+  const void* ptrs[] = {x, seq_lens, codes, scale, off};
+  for (const void* p : ptrs)
+    if (!p) return LBKV_EINVAL;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LBKV_EALIGN;
+  PackArgs a{static_cast<const __nv_bfloat16*>(x), seq_lens, desc->batch, desc->num_kv_heads, desc->max_seq_len,
+             bits, layout, group, codes, static_cast<__half*>(scale), static_cast<__half*>(off)};
+  if (launch_pack(a, reinterpret_cast<cudaStream_t>(stream)) != 0) return LBKV_ECUDA;
+  return LBKV_OK;
+}
+
+int lbkv_device_status(const lbkv_desc* desc, lbkv_stream_t stream, int32_t* code) {
+  if (!desc) return LBKV_EINVAL;
+  if (!desc->workspace || desc->workspace_bytes < 256) return LBKV_EWORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, desc->workspace, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return LBKV_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LBKV_ECUDA;
+  if (code) *code = host;
+  if (host != 0) {
+    if (cudaMemsetAsync(desc->workspace, 0, sizeof(int32_t), s) != cudaSuccess) return LBKV_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LBKV_ECUDA;
+    return LBKV_EDEVICE;
+  }
+  return LBKV_OK;
+}
+
+const char* lbkv_strerror(int status) {
+  switch (status) {
+    case LBKV_OK: return "success";
+    case LBKV_EINVAL: return "invalid argument (null pointer, size or range)";
+    case LBKV_EALIGN: return "pointer not aligned (16 bytes; workspace 256 bytes)";
+    case LBKV_EUNSUPPORTED: return "valid but unsupported combination of shape and format";
+    case LBKV_EWORKSPACE: return "workspace missing or smaller than lbkv_workspace_bytes";
+    case LBKV_ECUDA: return "CUDA launch or runtime error";
+    case LBKV_EDEVICE: return "a kernel reported a device-side error (bounded wait ran out)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,159 @@
+// lbkv_device.cuh -- sm_103a building blocks: mbarrier ring, bulk copies into
+// shared memory, the e4m3 tensor-core product and the bit tricks that turn
+// packed 2-/4-bit codes into e4m3 operands.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lbkv {
+
+// Device status codes written to the workspace status word instead of hanging.
+enum : int32_t {
+  kStatusConsumerTimeout = 1,
+  kStatusProducerTimeout = 2,
+  kStatusDrainTimeout = 3,
+};
+
+// A bounded wait gives up after this many nanoseconds of wall time.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Slow path of a bounded wait: polls until the phase completes or about one
+// second of wall time has passed; then records `code` and returns false.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int32_t* status, int32_t code) {
+  const uint64_t t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicExch(status, code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status, int32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, status, code);
+}
+
+// Bulk (non-tensor) copy global -> shared, completing on an mbarrier.
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read exactly once (the streamed cache).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Named barrier among `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ------------------------------------------------------- tensor-core product
+// D[16x8] += A[16x32] * B[32x8], e4m3 inputs, fp32 accumulators.
+// Fragments (lane = 4*g + c): A reg0 row g k 4c..4c+3, reg1 row g+8 k 4c..4c+3,
+// reg2 row g k 16+4c.., reg3 row g+8 k 16+4c..; B reg0 k 4c..4c+3 col g,
+// reg1 k 16+4c.. col g; D d0,d1 row g cols 2c,2c+1; d2,d3 row g+8.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------ conversions
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Exact split of two non-negative-or-signed finite values x0, x1 (already
+// scaled into e4m3 range) into e4m3 pairs hi + lo: hi = e4m3(fp16(x)),
+// lo = e4m3(fp16(x) - hi); the subtraction is exact in fp16 because hi lies
+// within a factor of two of x (or is zero). Byte 0 holds x0, byte 1 x1.
+__device__ __forceinline__ void split_e4m3_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  uint32_t h2, back, res;
+  uint16_t h, l;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(h2));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(h));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(res) : "r"(h2), "r"(back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(res));
+  hi = h;
+  lo = l;
+}
+
+// 4x4 byte transpose: out[b] byte j = in[j] byte b.
+__device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t (&t)[4]) {
+  const uint32_t x0 = prmt(w0, w1, 0x5140), x1 = prmt(w0, w1, 0x7362);
+  const uint32_t y0 = prmt(w2, w3, 0x5140), y1 = prmt(w2, w3, 0x7362);
+  t[0] = prmt(x0, y0, 0x5410);
+  t[1] = prmt(x0, y0, 0x7632);
+  t[2] = prmt(x1, y1, 0x5410);
+  t[3] = prmt(x1, y1, 0x7632);
+}
+
+// 2^e for integer e in [-126, 127], exactly.
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// floor(log2(x)) for a positive normal float.
+__device__ __forceinline__ int ilog2f(float x) { return ((__float_as_int(x) >> 23) & 0xff) - 127; }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace lbkv

@@ -1,0 +1,147 @@
+/*
+ * lbkv.h -- C ABI of a GB300 (sm_103a) library for single-token decode
+ * attention read directly from a 2- or 4-bit affine-quantized KV cache.
+ *
+ * What it computes. For every sequence b and query head h (KV head
+ * kv = h / (Hq / Hkv)) over the L_b cached tokens, optionally followed by a
+ * window of full-precision bf16 tokens:
+ *     out[b][h] = sum_t softmax_t(sigma * Q[b][h] . K_t) * V_t
+ * where every cached value is s * q + z: an unsigned b-bit code q sharing one
+ * fp16 scale s and one fp16 offset z with its group ("FOSCAR speeds up 2-bit
+ * KV decode -- Affine folding of KV dequantization", quantization-format
+ * paragraph). The library never materialises s * q + z: following the fold
+ * rule and fold table of that explainer (and the abstract of "FOSCAR:
+ * Accelerating Decode Attention over 2- and 4-Bit KV Caches through Affine
+ * Folding", arXiv:2611.09722), it applies s and z once per group, either to a
+ * partial result (acc-fold: token-wise K, channel-wise V) or to the other
+ * operand (operand-fold: channel-wise K, token-wise V); key corrections land
+ * before the softmax and value corrections before the final division.
+ *
+ * Layout (all device memory, dense, row-major, owned by the caller):
+ *   q          bf16  [B][Hq][D]
+ *   k_codes    uint8 [B][Hkv][T_cap][D*bits/8]   (same for v_codes)
+ *              code i of a byte sits in bits [bits*i, bits*i + bits);
+ *              codes run along head_dim (channel d is code d of its row)
+ *   token-wise scale/offset   fp16 [B][Hkv][T_cap][D/group]
+ *              (one pair per token per group of `group` channels)
+ *   channel-wise scale/offset fp16 [B][Hkv][T_cap/group][D]
+ *              (one pair per channel per block of `group` tokens; a block
+ *              that ends past L_b covers only the valid tokens)
+ *   seq_lens   int32 [B], 0 <= L_b <= T_cap (tokens >= L_b are ignored)
+ *   out        bf16  [B][Hq][D]
+ *
+ * Conventions shared by every entry point:
+ *   - all pointers are device pointers, 16-byte aligned, owned by the caller;
+ *     the library never allocates, frees or synchronizes (except
+ *     lbkv_device_status, which is documented as synchronizing);
+ *   - calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *   - arguments are validated before anything is launched; on a validation
+ *     error nothing is written and a negative lbkv_status is returned;
+ *   - a launch failure returns LBKV_ECUDA (cudaGetLastError after launch);
+ *   - the calls are thread-safe (no global mutable state besides a per-device
+ *     cache of the multiprocessor count).
+ */
+#ifndef LBKV_H
+#define LBKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LBKV_API __attribute__((visibility("default")))
+#else
+#define LBKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; declared here so that callers need no CUDA header. */
+typedef struct CUstream_st* lbkv_stream_t;
+
+/* Group orientation of a cache side ("FOSCAR speeds up 2-bit KV decode", fold table). */
+typedef enum {
+  LBKV_TOKENWISE = 0,   /* a group is `group` consecutive channels of one token */
+  LBKV_CHANNELWISE = 1  /* a group is `group` consecutive tokens of one channel */
+} lbkv_layout;
+
+typedef enum {
+  LBKV_OK = 0,
+  LBKV_EINVAL = -1,        /* a null pointer, a bad size or an out-of-range argument */
+  LBKV_EALIGN = -2,        /* a pointer that is not 16-byte aligned */
+  LBKV_EUNSUPPORTED = -3,  /* valid but not implemented (see lbkv_decode_attn) */
+  LBKV_EWORKSPACE = -4,    /* workspace missing or smaller than lbkv_workspace_bytes */
+  LBKV_ECUDA = -5,         /* a CUDA launch or runtime call failed */
+  LBKV_EDEVICE = -6        /* a kernel reported a device-side error (lbkv_device_status) */
+} lbkv_status;
+
+/* Shapes, scale, optional bf16 window and workspace of one decode call. */
+typedef struct lbkv_desc {
+  int32_t batch;         /* B >= 0 */
+  int32_t num_q_heads;   /* Hq, a multiple of num_kv_heads */
+  int32_t num_kv_heads;  /* Hkv >= 1; Hq / Hkv must be 1, 2, 4 or 8 */
+  int32_t head_dim;      /* D; must be 128 */
+  int32_t max_seq_len;   /* T_cap: token stride of codes and scales, a positive multiple of 128 */
+  float sm_scale;        /* softmax scale sigma; <= 0 selects 1/sqrt(head_dim) */
+  const void* k_win;     /* bf16 [B][Hkv][win_cap][D] tokens attended after the cached ones, or NULL */
+  const void* v_win;     /* bf16 [B][Hkv][win_cap][D], NULL exactly when k_win is NULL */
+  const int32_t* win_lens; /* int32 [B], 0 <= win_lens[b] <= win_cap; NULL when k_win is NULL */
+  int32_t win_cap;       /* 1..128 when k_win is set */
+  void* workspace;       /* device scratch of >= lbkv_workspace_bytes(...) bytes, 256-byte aligned;
+                            zero-filled once after allocation (its first 256 bytes hold the
+                            device status word); reusable by calls in stream order */
+  size_t workspace_bytes;
+} lbkv_desc;
+
+/* Bytes of workspace lbkv_decode_attn needs for this descriptor and format on
+ * the current device (the split-KV partials: a running maximum, a softmax
+ * denominator and a head_dim vector per query head and split). Returns 0 when
+ * the arguments are invalid. Reads only desc's shape fields. */
+LBKV_API size_t lbkv_workspace_bytes(const lbkv_desc* desc, int bits, int k_layout, int v_layout, int group);
+
+/* Decode attention for one new token per sequence, split-KV over the cache.
+ *   q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, out: see the layout above;
+ *   bits: 2 or 4; k_layout / v_layout: lbkv_layout; group: 32, 64 or 128
+ *   (a divisor of head_dim for a token-wise side, a token count for a
+ *   channel-wise side).
+ * Supported: every combination of bits, layouts and group above with
+ *   Hq/Hkv in {1, 2, 4, 8}, except on a token-wise V side group 32, and
+ *   group 64 with Hq/Hkv = 8 (LBKV_EUNSUPPORTED).
+ * Precision: tensor-core products on exact e4m3 images of the codes; the query
+ * and the softmax weights enter as an exact-or-nearly-exact sum of two e4m3
+ * parts; accumulation and every fold step in fp32; output rounded to bf16.
+ * Errors: LBKV_EINVAL / LBKV_EALIGN / LBKV_EUNSUPPORTED / LBKV_EWORKSPACE before
+ * any launch; LBKV_ECUDA on a launch failure. A sequence with no cached and no
+ * window tokens yields a zero output row. */
+LBKV_API int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_codes, const void* k_scale,
+                     const void* k_off, const uint8_t* v_codes, const void* v_scale, const void* v_off,
+                     const int32_t* seq_lens, int bits, int k_layout, int v_layout, int group, void* out,
+                     lbkv_stream_t stream);
+
+/* Quantize a bf16 cache side x [B][Hkv][T_cap][D] into the layout above
+ * (the value model s * q + z is the explainer's quantization-format
+ * paragraph; the quantizer is this library's reading): per group
+ *   s = fp16((max - min) / (2^bits - 1)), z = fp16(min),
+ *   q = clamp(round_half_even((x - z) / s), 0, 2^bits - 1), q = 0 when s == 0,
+ * each operation in IEEE single precision rounded on its own. A channel-wise
+ * group that ends past L_b uses only its valid tokens. Codes of tokens
+ * t >= L_b are written as 0; their scales and offsets are left untouched.
+ * Uses desc's batch, num_kv_heads, head_dim (128) and max_seq_len only.
+ * Errors as for lbkv_decode_attn. */
+LBKV_API int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_lens, int bits, int layout, int group,
+              uint8_t* codes, void* scale, void* off, lbkv_stream_t stream);
+
+/* Reads and clears the device status word that kernels set instead of
+ * hanging (a bounded wait that ran out). Synchronizes `stream`. Returns
+ * LBKV_OK, LBKV_EDEVICE (the word was set; *code receives it when code is
+ * not NULL) or LBKV_ECUDA / LBKV_EINVAL / LBKV_EWORKSPACE. */
+LBKV_API int lbkv_device_status(const lbkv_desc* desc, lbkv_stream_t stream, int32_t* code);
+
+/* Static English text for a status value. */
+LBKV_API const char* lbkv_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LBKV_H */

@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads,
+exports every function include/lbkv.h declares, and rejects invalid arguments
+before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_kv_cache_split_gb300 import _binding, build
+
+    build.build()
+    return _binding.load()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*LBKV_API\s+[\w\s\*]+?\b(lbkv_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("lbkv_decode_attn", "lbkv_pack", "lbkv_workspace_bytes", "lbkv_strerror", "lbkv_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_texts(lib):
+    from bit_kv_cache_split_gb300 import _binding
+
+    for st in _binding.STATUS:
+        assert lib.lbkv_strerror(st)
+    assert lib.lbkv_strerror(0) == b"success"
+    assert b"unknown" in lib.lbkv_strerror(12345)
+
+
+def _desc(**kw):
+    from bit_kv_cache_split_gb300 import _binding
+
+    d = _binding.make_desc(kw.pop("B", 1), kw.pop("Hq", 32), kw.pop("Hkv", 8), kw.pop("T", 4096),
+                           kw.pop("D", 128))
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("kwargs,fmt,want", [
+    (dict(), (3, 0, 0, 128), -1),              # bits
+    (dict(), (2, 2, 0, 128), -1),              # layout
+    (dict(), (2, 0, 0, 16), -3),               # group
+    (dict(D=64), (2, 0, 0, 128), -3),          # head_dim
+    (dict(Hq=30, Hkv=8), (2, 0, 0, 128), -1),  # Hq % Hkv
+    (dict(Hq=24, Hkv=8), (2, 0, 0, 128), -3),  # Hq/Hkv = 3
+    (dict(T=1000), (2, 0, 0, 128), -1),        # T_cap not a multiple of 128
+    (dict(T=0), (2, 0, 0, 128), -1),
+    (dict(B=-1), (2, 0, 0, 128), -1),
+    (dict(), (2, 0, 0, 32), -3),               # token-wise V with 4 channel groups
+    (dict(Hq=64, Hkv=8), (2, 0, 0, 64), -3),   # token-wise V, 2 groups x 8 query heads
+])
+def test_invalid_decode_arguments_rejected_before_launch(lib, kwargs, fmt, want):
+    d = _desc(**kwargs)
+    null = ctypes.c_void_p(0)
+    st = lib.lbkv_decode_attn(ctypes.byref(d), *([null] * 8), *fmt, null, null)
+    assert st == want
+    assert lib.lbkv_workspace_bytes(ctypes.byref(d), *fmt) == 0
+
+
+def test_window_arguments_validated(lib):
+    d = _desc()
+    d.k_win = 4096  # v_win and win_lens left NULL
+    null = ctypes.c_void_p(0)
+    assert lib.lbkv_decode_attn(ctypes.byref(d), *([null] * 8), 2, 0, 0, 128, null, null) == -1
+    d.v_win = d.win_lens = 4096
+    d.win_cap = 129
+    assert lib.lbkv_decode_attn(ctypes.byref(d), *([null] * 8), 2, 0, 0, 128, null, null) == -1
+
+
+@pytest.mark.parametrize("fmt,want", [((3, 0, 128), -1), ((2, 5, 128), -1), ((2, 0, 100), -3)])
+def test_invalid_pack_arguments_rejected(lib, fmt, want):
+    d = _desc()
+    null = ctypes.c_void_p(0)
+    assert lib.lbkv_pack(ctypes.byref(d), null, null, *fmt, null, null, null, null) == want
+
+
+def test_null_descriptor(lib):
+    null = ctypes.c_void_p(0)
+    assert lib.lbkv_decode_attn(None, *([null] * 8), 2, 0, 0, 128, null, null) == -1
+    assert lib.lbkv_pack(None, null, null, 2, 0, 128, null, null, null, null) == -1
+    assert lib.lbkv_workspace_bytes(None, 2, 0, 0, 128) == 0
+    assert lib.lbkv_device_status(None, null, None) == -1
+
+
+def test_empty_batch_is_a_no_op_without_pointers(lib):
+    # B = 0 validates the shapes and returns before any launch; a GPU-less host
+    # can still reject it with LBKV_ECUDA when the device cannot be queried.
+    d = _desc(B=0)
+    null = ctypes.c_void_p(0)
+    assert lib.lbkv_decode_attn(ctypes.byref(d), *([null] * 8), 2, 0, 0, 128, null, null) in (0, -5)
+    assert lib.lbkv_pack(ctypes.byref(d), null, null, 2, 0, 128, null, null, null, null) == 0

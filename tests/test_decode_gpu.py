@@ -1,0 +1,235 @@
+"""Parity of the CUDA decode path (through the C ABI) with the fp64 oracle.
+
+Bar: bf16 output within max-abs 5e-3 and relative L2 3e-3 of the oracle run
+on the same quantized cache, for every K/V layout pair at INT2 and INT4, over
+ragged lengths that span several 128-token slots and end mid-slot, GQA 1..8,
+groups 32/64/128, a bf16 window, empty sequences and peaked softmaxes; at
+the full benchmark sizes on sampled (sequence, KV head) units."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_kv_cache_split_gb300 import inputs
+from tests.helpers import to_oracle
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 5e-3
+REL_L2 = 3e-3
+
+
+@pytest.fixture(scope="module")
+def lbkv():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import bit_kv_cache_split_gb300 as m
+
+    m.build.build()
+    m.load()
+    oracle.build()
+    return m
+
+
+def run_gpu(m, t, wl, **kw):
+    dev = {k: v.cuda() for k, v in t.items()}
+    win = {}
+    if "k_win" in dev:
+        win = dict(k_win=dev["k_win"], v_win=dev["v_win"], win_lens=dev["win_lens"])
+    out = m.decode_attn(dev["q"], dev["k_codes"], dev["k_scale"], dev["k_off"], dev["v_codes"], dev["v_scale"],
+                        dev["v_off"], dev["seq_lens"], bits=wl.bits, k_layout=wl.k_layout, v_layout=wl.v_layout,
+                        group=wl.group, sm_scale=wl.sm_scale, **win, **kw)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def errors(got, ref):
+    d = got - ref
+    return float(np.max(np.abs(d))), float(np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-30))
+
+
+def assert_parity(got, ref, what=""):
+    mx, rl2 = errors(got, ref)
+    assert np.all(np.isfinite(got)), what
+    assert mx <= MAX_ABS and rl2 <= REL_L2, f"{what}: max-abs {mx:.3e}, rel-L2 {rl2:.3e}"
+    return mx, rl2
+
+
+def check(m, wl, **kw):
+    t = inputs.generate(wl, "cpu")
+    got = run_gpu(m, t, wl, **kw)
+    ref = oracle.decode_ref(to_oracle(t, wl))
+    return assert_parity(got, ref, wl.name)
+
+
+def _wl(bits, kl, vl, g=128, hq=4, lens=(300, 1000, 129), seed=0, **kw):
+    s = (0.01, 0.1) if bits == 2 else (0.002, 0.02)
+    return inputs.Workload(f"b{bits}-k{kl}-v{vl}-g{g}-hq{hq}", len(lens), 2 * hq, 2, list(lens), bits=bits,
+                           k_layout=kl, v_layout=vl, group=g, s_range=s, seed=seed, **kw)
+
+
+def test_tiny_int2_full_output(lbkv):
+    """Batch 1, 1 KV head, 4 query heads, 512 tokens, INT2 token-wise g=128 (seed 0)."""
+    check(lbkv, inputs.tiny_int2())
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("kl,vl", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_layout_pairs(lbkv, bits, kl, vl):
+    check(lbkv, _wl(bits, kl, vl, seed=10 * bits + 2 * kl + vl))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("hq", [1, 2, 4, 8])
+def test_gqa_ratios(lbkv, bits, hq):
+    check(lbkv, _wl(bits, 0, 0, hq=hq, lens=(777, 64), seed=hq))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("g", [32, 64])
+@pytest.mark.parametrize("kl,vl", [(0, 1), (1, 1), (1, 0), (0, 0)])
+def test_group_sizes(lbkv, bits, g, kl, vl):
+    if vl == 0 and g == 32:
+        pytest.skip("token-wise V with four channel groups is not supported")
+    check(lbkv, _wl(bits, kl, vl, g=g, lens=(513, 95), seed=g + bits))
+
+
+@pytest.mark.parametrize("hq", [1, 2, 4])
+def test_tokenwise_v_two_groups_all_gqa(lbkv, hq):
+    check(lbkv, _wl(2, 0, 0, g=64, hq=hq, lens=(400,), seed=7))
+
+
+def test_window(lbkv):
+    wl = _wl(2, 0, 0, lens=(600, 0, 37), seed=5, window=128)
+    t = inputs.generate(wl, "cpu")
+    t["win_lens"] = torch.tensor([128, 17, 0], dtype=torch.int32)
+    got = run_gpu(lbkv, t, wl)
+    ref = oracle.decode_ref(to_oracle(t, wl))
+    assert_parity(got, ref, "window")
+
+
+def test_empty_and_single_token_sequences(lbkv):
+    wl = _wl(2, 0, 0, lens=(0, 1, 128, 129), seed=3)
+    t = inputs.generate(wl, "cpu")
+    got = run_gpu(lbkv, t, wl)
+    assert np.all(got[0] == 0)
+    assert_parity(got, oracle.decode_ref(to_oracle(t, wl)), "empty/single")
+
+
+@pytest.mark.parametrize("kl,vl", [(0, 0), (1, 1)])
+def test_peaked_softmax(lbkv, kl, vl):
+    """Large scores: most weight on a few tokens, exercising the running maximum."""
+    check(lbkv, _wl(2, kl, vl, lens=(2000, 333), seed=21, q_std=6.0, sm_scale=0.5))
+
+
+def test_full_capacity_and_padding_garbage(lbkv):
+    """seq_len == T_cap, and NaN patterns in padding scales must not leak."""
+    wl = _wl(4, 0, 0, lens=(256, 130), seed=8)
+    t = inputs.generate(wl, "cpu")
+    t["k_scale"][1, :, 130:] = float("nan")
+    t["v_scale"][1, :, 130:] = float("nan")
+    t["v_off"][1, :, 130:] = float("inf")
+    got = run_gpu(lbkv, t, wl)
+    assert_parity(got, oracle.decode_ref(to_oracle(t, wl)), "padding")
+
+
+def test_repeat_calls_are_bitwise_identical(lbkv):
+    wl = _wl(2, 0, 0, lens=(3000, 17), seed=30)
+    t = inputs.generate(wl, "cpu")
+    a = run_gpu(lbkv, t, wl)
+    b = run_gpu(lbkv, t, wl)
+    assert np.array_equal(a, b)
+
+
+def test_unsupported_combination_raises(lbkv):
+    wl = _wl(2, 0, 0, g=32, lens=(10,))
+    t = {k: v.cuda() for k, v in inputs.generate(wl, "cpu").items()}
+    with pytest.raises(lbkv.LbkvError) as e:
+        lbkv.decode_attn(t["q"], t["k_codes"], t["k_scale"], t["k_off"], t["v_codes"], t["v_scale"], t["v_off"],
+                         t["seq_lens"], bits=2, group=32)
+    assert e.value.status == -3
+
+
+def test_no_device_status_after_calls(lbkv):
+    wl = _wl(2, 1, 0, lens=(900,), seed=31)
+    t = {k: v.cuda() for k, v in inputs.generate(wl, "cpu").items()}
+    n = lbkv.workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.t_cap, 2, 1, 0, 128)
+    ws = lbkv._binding.alloc_workspace(n, "cuda")
+    lbkv.decode_attn(t["q"], t["k_codes"], t["k_scale"], t["k_off"], t["v_codes"], t["v_scale"], t["v_off"],
+                     t["seq_lens"], bits=2, k_layout=1, workspace=ws)
+    assert lbkv.device_status(ws) == 0
+
+
+# ------------------------------------------------------------ full sizes
+
+def unit_slice(t, wl, b, kvh):
+    """The tensors of one (sequence, KV head) unit as a batch-1, 1-KV-head problem."""
+    hq = wl.hq_per_kv
+    sub = {}
+    for k, v in t.items():
+        if k == "q":
+            sub[k] = v[b:b + 1, kvh * hq:(kvh + 1) * hq]
+        elif k in ("seq_lens", "win_lens"):
+            sub[k] = v[b:b + 1]
+        else:
+            sub[k] = v[b:b + 1, kvh:kvh + 1]
+        sub[k] = sub[k].contiguous().cpu()
+    w = inputs.Workload(wl.name, 1, hq, 1, [wl.lens[b]], bits=wl.bits, k_layout=wl.k_layout, v_layout=wl.v_layout,
+                        group=wl.group, sm_scale=wl.sm_scale, window=wl.window)
+    assert w.t_cap == wl.t_cap or w.t_cap <= wl.t_cap
+    return sub, w
+
+
+def sampled_parity(m, wl, units):
+    t = inputs.generate(wl, "cuda")
+    win = {}
+    if "k_win" in t:
+        win = dict(k_win=t["k_win"], v_win=t["v_win"], win_lens=t["win_lens"])
+    out = m.decode_attn(t["q"], t["k_codes"], t["k_scale"], t["k_off"], t["v_codes"], t["v_scale"], t["v_off"],
+                        t["seq_lens"], bits=wl.bits, k_layout=wl.k_layout, v_layout=wl.v_layout, group=wl.group,
+                        **win)
+    torch.cuda.synchronize()
+    got_all = out.float().cpu().numpy().astype(np.float64)
+    hq = wl.hq_per_kv
+    worst = (0.0, 0.0)
+    for b, kvh in units:
+        sub, w = unit_slice(t, wl, b, kvh)
+        x = to_oracle(sub, w)
+        x.T_cap = wl.t_cap
+        ref = oracle.decode_ref(x)[0]
+        got = got_all[b, kvh * hq:(kvh + 1) * hq]
+        mx, rl2 = assert_parity(got, ref, f"{wl.name} unit ({b},{kvh})")
+        worst = (max(worst[0], mx), max(worst[1], rl2))
+    del t
+    torch.cuda.empty_cache()
+    return worst
+
+
+@pytest.mark.parametrize("batch,ctx", [(1, 131072), (8, 32768), (64, 131072)])
+def test_int2_full_size_sampled(lbkv, batch, ctx):
+    wl = inputs.decode_int2(batch, ctx)
+    sampled_parity(lbkv, wl, [(0, 0), (batch - 1, 7), (batch // 2, 3)])
+
+
+@pytest.mark.parametrize("batch,ctx", [(1, 32768), (64, 131072)])
+def test_int4_full_size_sampled(lbkv, batch, ctx):
+    wl = inputs.decode_int4(batch, ctx)
+    sampled_parity(lbkv, wl, [(0, 0), (batch - 1, 5)])
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("kl,vl", [(1, 0), (0, 1)])
+def test_mixed_layouts_ragged_sampled(lbkv, bits, kl, vl):
+    """Batch 16, lengths uniform in [1K, 64K] and never a multiple of 128."""
+    wl = inputs.mixed_layout(bits, kl, vl)
+    sampled_parity(lbkv, wl, [(0, 0), (5, 4), (15, 7), (int(np.argmin(wl.lens)), 1)])
+
+
+@pytest.mark.parametrize("g,hq", [(128, 4), (64, 2), (128, 8), (32, 1)])
+def test_long_context_window_sampled(lbkv, g, hq):
+    """100,000-token context: 99,872 INT2 tokens + a 128-token bf16 window."""
+    if g == 32:
+        pytest.skip("token-wise V with four channel groups is not supported")
+    wl = inputs.long_context(1, group=g, hq_per_kv=hq)
+    sampled_parity(lbkv, wl, [(0, 0), (0, wl.num_kv_heads - 1)])

@@ -1,0 +1,74 @@
+"""The CUDA quantizer (lbkv_pack) is bit-exact with the oracle's, and a packed
+cache decodes to the oracle's output on that same packed cache."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_kv_cache_split_gb300 import inputs
+from tests.helpers import bits16, to_oracle
+from tests.test_decode_gpu import assert_parity, lbkv  # noqa: F401  (fixture)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_pack_bit_exact(lbkv, bits, layout, g):
+    x, lens = inputs.generate_pack_source(3, 2, [515, 128, 1], seed=2)
+    x = x * 3.0
+    x = x.to(torch.bfloat16)
+    sentinel = 0x1234
+    B, H, T, D = x.shape
+    sshape = (B, H, T, D // g) if layout == 0 else (B, H, T // g, D)
+    s0 = torch.full(sshape, sentinel, dtype=torch.int16).view(torch.float16)
+    codes, s, z = lbkv.pack(x.cuda(), lens.cuda(), bits=bits, layout=layout, group=g, scale=s0.clone().cuda(),
+                            off=s0.clone().cuda())
+    torch.cuda.synchronize()
+    rc, rs, rz = oracle.pack(bits16(x), lens.numpy(), bits, layout, g,
+                             scale_init=np.full(sshape, sentinel, np.uint16), off_init=np.full(sshape, sentinel, np.uint16))
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(bits16(s), rs)
+    assert np.array_equal(bits16(z), rz)
+
+
+def test_pack_special_values(lbkv):
+    """Constant groups, exact ties, signed zeros and large magnitudes."""
+    rng = np.random.default_rng(5)
+    T, D = 128, 128
+    x = rng.standard_normal((1, 1, T, D)).astype(np.float32)
+    x[0, 0, 0] = 0.75                       # constant token
+    x[0, 0, 1, :4] = [0, 0.5, 1.5, 3]       # ties inside a group
+    x[0, 0, 2] = 0.0
+    x[0, 0, 2, ::2] = -0.0                  # signed zeros
+    x[0, 0, 3] *= 1000.0
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    lens = torch.tensor([T], dtype=torch.int32)
+    for bits in (2, 4):
+        for layout, g in ((0, 32), (0, 128), (1, 128)):
+            codes, s, z = lbkv.pack(xt.cuda(), lens.cuda(), bits=bits, layout=layout, group=g)
+            rc, rs, rz = oracle.pack(bits16(xt), lens.numpy(), bits, layout, g)
+            assert np.array_equal(codes.cpu().numpy(), rc), (bits, layout, g)
+            assert np.array_equal(bits16(s), rs) and np.array_equal(bits16(z), rz), (bits, layout, g)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("kl,vl", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_quantize_then_decode(lbkv, bits, kl, vl):
+    """bf16 K/V ~ N(0, 1) -> lbkv_pack -> lbkv_decode_attn, against the oracle on the packed cache."""
+    B, Hkv, hq, g = 2, 2, 4, 128
+    lens = [700, 259]
+    k, lt = inputs.generate_pack_source(B, Hkv, lens, seed=2)
+    v, _ = inputs.generate_pack_source(B, Hkv, lens, seed=12)
+    q = torch.randn((B, Hkv * hq, 128), generator=torch.Generator().manual_seed(22)).to(torch.bfloat16)
+    kc, ks, kz = lbkv.pack(k.cuda(), lt.cuda(), bits=bits, layout=kl, group=g)
+    vc, vs, vz = lbkv.pack(v.cuda(), lt.cuda(), bits=bits, layout=vl, group=g)
+    out = lbkv.decode_attn(q.cuda(), kc, ks, kz, vc, vs, vz, lt.cuda(), bits=bits, k_layout=kl, v_layout=vl, group=g)
+    torch.cuda.synchronize()
+    wl = inputs.Workload("packed", B, Hkv * hq, Hkv, lens, bits=bits, k_layout=kl, v_layout=vl, group=g)
+    t = dict(q=q, k_codes=kc.cpu(), k_scale=ks.cpu(), k_off=kz.cpu(), v_codes=vc.cpu(), v_scale=vs.cpu(),
+             v_off=vz.cpu(), seq_lens=lt)
+    ref = oracle.decode_ref(to_oracle(t, wl))
+    assert_parity(out.float().cpu().numpy().astype(np.float64), ref, f"packed b{bits} k{kl} v{vl}")
