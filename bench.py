@@ -1,0 +1,492 @@
+#!/usr/bin/env python
+"""Decode-attention benchmark over a 2-/4-bit affine-quantized KV cache on GB300.
+
+Metric: decode-attention µs per call and achieved HBM GB/s (fraction of the
+measured peak), INT2 and INT4. One step = one call of lbkv_decode_attn (the
+whole hot path: split-KV decode with affine folding and the split merge, one
+kernel launch) over one batch of seeded synthetic inputs already resident in
+HBM. Headline workload: INT2 token-wise K/V, group 128, 32 query / 8 KV heads,
+head_dim 128, batch 32, 32K context. The other workloads run as a sweep.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {lbkv,reference}] [--no-sweep]
+Under torchrun (N > 1) every rank runs its own replica on its GPU (the path
+shards by sequence and KV head with no exchange); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from bit_kv_cache_split_gb300 import inputs  # noqa: E402
+
+METRIC = "decode-attn µs/call and achieved HBM GB/s (% of GB300 peak), INT2/INT4"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+HEADLINE = dict(batch=32, ctx=32768)
+
+
+# ------------------------------------------------------------------ bytes
+
+def algorithmic_bytes(wl: inputs.Workload) -> int:
+    """Bytes one call must move at minimum: codes, scales, offsets, Q, output, lengths
+    (and the bf16 window). Split-workspace traffic is not counted."""
+    D, Hkv, g = wl.head_dim, wl.num_kv_heads, wl.group
+    total = 0
+    for L in wl.lens:
+        codes = 2 * L * D * wl.bits // 8
+        sz = 0
+        for layout in (wl.k_layout, wl.v_layout):
+            if layout == inputs.TOKENWISE:
+                sz += L * (D // g) * 4
+            else:
+                sz += math.ceil(L / g) * D * 4
+        total += Hkv * (codes + sz)
+    total += 2 * wl.batch * wl.num_q_heads * D * 2 + 4 * wl.batch
+    if wl.window:
+        total += wl.batch * Hkv * wl.window * D * 2 * 2 + 4 * wl.batch
+    return total
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_kv_cache_split_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.idx = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [p for (t, p) in self.samples if t0 <= t <= t1] or [p for (_, p) in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[4 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------------ device timing
+
+class Case:
+    """Device-resident replicas of one workload plus output and workspace."""
+
+    def __init__(self, wl: inputs.Workload, device, min_footprint=4 * L2_BYTES, max_replicas=256):
+        import bit_kv_cache_split_gb300 as pkg
+
+        self.pkg, self.wl = pkg, wl
+        self.bytes = algorithmic_bytes(wl)
+        r = max(2, math.ceil(min_footprint / max(self.bytes, 1)))
+        self.replicas = []
+        for i in range(min(r, max_replicas)):
+            w = inputs.Workload(**{**wl.__dict__, "seed": wl.seed + 1000 * i})
+            self.replicas.append(inputs.generate(w, device))
+        self.out = torch.empty((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device=device)
+        n = pkg.workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.t_cap, wl.bits, wl.k_layout,
+                                wl.v_layout, wl.group, window=bool(wl.window))
+        self.ws = pkg._binding.alloc_workspace(n, device)
+        self.footprint = sum(sum(x.numel() * x.element_size() for x in rep.values()) for rep in self.replicas)
+
+    def call(self, i, stream=None):
+        t = self.replicas[i % len(self.replicas)]
+        win = {}
+        if "k_win" in t:
+            win = dict(k_win=t["k_win"], v_win=t["v_win"], win_lens=t["win_lens"])
+        self.pkg.decode_attn(t["q"], t["k_codes"], t["k_scale"], t["k_off"], t["v_codes"], t["v_scale"], t["v_off"],
+                             t["seq_lens"], bits=self.wl.bits, k_layout=self.wl.k_layout, v_layout=self.wl.v_layout,
+                             group=self.wl.group, sm_scale=self.wl.sm_scale, out=self.out, workspace=self.ws,
+                             stream=stream, **win)
+
+    def time(self, steps, warmup, barrier=None):
+        """Average ms per call over exactly `steps` calls: the calls are captured once in a
+        CUDA graph (no host launch overhead between them) and the replay is timed with CUDA
+        events on the launching stream. L2 is flushed before the timed replay, and
+        consecutive calls read different replicas."""
+        for i in range(warmup):
+            self.call(i)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for i in range(steps):
+                    self.call(warmup + i)
+        torch.cuda.current_stream().wait_stream(side)
+        graph.replay()  # untimed: the graph's first launch uploads it
+        torch.cuda.synchronize()
+        flush = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=self.out.device)
+        flush.zero_()
+        del flush
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        graph.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        del graph
+        return e0.elapsed_time(e1) / steps
+
+    def free(self):
+        self.replicas.clear()
+        self.out = self.ws = None
+
+
+def time_e2e(wl, steps, warmup, device):
+    """Same metric through the public API from pinned host buffers: every step copies the
+    step's inputs host->device, decodes, and reads the output back."""
+    import bit_kv_cache_split_gb300 as pkg
+
+    host = {k: v.pin_memory() for k, v in inputs.generate(wl, "cpu").items()}
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    out_h = torch.empty((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16).pin_memory()
+    out_d = torch.empty_like(out_h, device=device)
+    n = pkg.workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.t_cap, wl.bits, wl.k_layout, wl.v_layout,
+                            wl.group, window=bool(wl.window))
+    ws = pkg._binding.alloc_workspace(n, device)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        win = {}
+        if "k_win" in dev:
+            win = dict(k_win=dev["k_win"], v_win=dev["v_win"], win_lens=dev["win_lens"])
+        pkg.decode_attn(dev["q"], dev["k_codes"], dev["k_scale"], dev["k_off"], dev["v_codes"], dev["v_scale"],
+                        dev["v_off"], dev["seq_lens"], bits=wl.bits, k_layout=wl.k_layout, v_layout=wl.v_layout,
+                        group=wl.group, out=out_d, workspace=ws, **win)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_throughput(wl, target_s=12.0, max_units=None, threads=0):
+    """The fp64 oracle on a bounded sample of `wl`: whole (sequence, KV head) units, all
+    their query heads. Returns (GB/s of algorithmic bytes, seconds, units, threads, rows)."""
+    import oracle
+
+    oracle.build()
+    hq = wl.hq_per_kv
+    per_unit = max(1, algorithmic_bytes(wl) // max(1, wl.batch * wl.num_kv_heads))
+
+    def sample(n_units):
+        b_needed = math.ceil(n_units / wl.num_kv_heads)
+        w = inputs.Workload(**{**wl.__dict__, "batch": b_needed,
+                               "seq_lens": wl.lens[:b_needed] if not isinstance(wl.seq_lens, int) else wl.seq_lens})
+        t = inputs.generate(w, "cpu")
+        x = oracle.inputs_from_tensors(t, bits=w.bits, k_layout=w.k_layout, v_layout=w.v_layout, group=w.group,
+                                       Hkv=w.num_kv_heads, T_cap=w.t_cap, sm_scale=w.sm_scale)
+        rows = [(u // w.num_kv_heads, (u % w.num_kv_heads) * hq + i) for u in range(n_units) for i in range(hq)]
+        nthreads = threads or os.cpu_count() or 1
+        t0 = time.perf_counter()
+        oracle.decode_ref(x, rows=rows, n_threads=nthreads)
+        return time.perf_counter() - t0, min(nthreads, len(rows)), len(rows)
+
+    cores = os.cpu_count() or 1
+    n = max(1, cores // hq)
+    if max_units is not None:
+        n = min(n, max_units)
+    dt, used, rows = sample(n)
+    total_units = wl.batch * wl.num_kv_heads
+    if dt < target_s / 4:
+        cap = total_units if max_units is None else max_units
+        n2 = min(cap, max(n, int(n * target_s / max(dt, 1e-3))))
+        if n2 > n:
+            n = n2
+            dt, used, rows = sample(n)
+    return n * per_unit / dt / 1e9, dt, n, used, rows
+
+
+# ------------------------------------------------------------------ main
+
+def sweep_workloads():
+    ws = []
+    for b in inputs.BATCHES:
+        for ctx in inputs.CONTEXTS:
+            ws.append(inputs.decode_int2(b, ctx))
+    for b in inputs.BATCHES:
+        for ctx in inputs.CONTEXTS:
+            ws.append(inputs.decode_int4(b, ctx))
+    for bits in (2, 4):
+        for kl, vl in ((1, 0), (0, 1)):
+            ws.append(inputs.mixed_layout(bits, kl, vl))
+    for b in (1, 16, 64):
+        ws.append(inputs.long_context(b))
+    for g in (32, 64, 128):
+        for hq in (1, 2, 4, 8):
+            ws.append(inputs.long_context(16, group=g, hq_per_kv=hq))
+    return ws
+
+
+def run_sweep(device, peak):
+    import bit_kv_cache_split_gb300 as pkg
+
+    rows = []
+    for wl in sweep_workloads():
+        try:
+            case = Case(wl, device)
+            ms = case.time(steps=20, warmup=3)
+        except pkg.LbkvError as e:
+            rows.append({"workload": wl.name, "unsupported": str(e)})
+            torch.cuda.empty_cache()
+            continue
+        gbs = case.bytes / (ms * 1e-3) / 1e9
+        rows.append({"workload": wl.name, "us_per_call": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peak, 3), "bytes": case.bytes})
+        case.free()
+        torch.cuda.empty_cache()
+    return rows
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reference_arm(args, world, rank):
+    """The CPU oracle as the reference arm, timed on the host cores."""
+    if rank != 0:
+        return
+    wl = inputs.decode_int2(**HEADLINE)
+    hq = wl.hq_per_kv
+    cores = os.cpu_count() or 1
+    units = max(1, cores // hq)
+    vals, secs, used = [], [], 1
+    for i in range(args.warmup + args.steps):
+        gbs, dt, n, used, rows = oracle_throughput(wl, target_s=0.0, max_units=units)
+        if i >= args.warmup:
+            vals.append(gbs)
+            secs.append(dt)
+    value = statistics.mean(vals) if vals else 0.0
+    ms = statistics.mean(secs) * 1e3 if secs else 0.0
+    sample = f"{units} of {wl.batch * wl.num_kv_heads} (sequence, KV head) units of {wl.name}, all {hq} query heads"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.batch, "ctx": HEADLINE["ctx"], "q_heads": wl.num_q_heads,
+                       "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "bits": wl.bits, "group": wl.group,
+                       "layout": "token-wise K / token-wise V", "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="lbkv", choices=["lbkv", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_info()
+
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+
+    import bit_kv_cache_split_gb300 as pkg
+
+    pkg.build.build()
+    pkg.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+        barrier = dist.barrier
+
+    peak, peak_kind = measured_hbm_peak()
+    wl = inputs.decode_int2(**HEADLINE)
+    case = Case(wl, device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_pre = time.time()
+    end = time.time() + 1.0  # untimed load so that clock samples fall under load
+    i = 0
+    while time.time() < end:
+        case.call(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    ms = case.time(args.steps, args.warmup, barrier)
+    t_end = time.time()
+    time.sleep(0.3)
+    sampler.stop()
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = pkg.device_status(case.ws)
+    footprint = case.footprint
+    n_rep = len(case.replicas)
+    case.free()
+    torch.cuda.empty_cache()
+
+    step_bytes = algorithmic_bytes(wl)
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    clocks = sampler.summary(t_pre, t_end)
+
+    e2e_ms, h2d, d2h = time_e2e(wl, max(3, min(args.steps, 20)), 2, device)
+    e2e_val = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    sweep = None
+    if not args.no_sweep and rank == 0:
+        sweep = run_sweep(device, peak)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        gbs, dt, n, used, rows = oracle_throughput(wl, target_s=12.0)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+               "sample": f"{n} of {wl.batch * wl.num_kv_heads} (sequence, KV head) units of {wl.name} "
+                         f"({rows} query rows, {dt:.1f} s), generated on the host with the same recipe"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32",
+            "data": "synthetic (seeded; codes uniform, s~U[0.01,0.1], z~U[-0.2,0.2], Q~N(0,1) bf16)",
+            "config": {"workload": wl.name, "batch": wl.batch, "ctx": HEADLINE["ctx"], "q_heads": wl.num_q_heads,
+                       "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "bits": wl.bits, "group": wl.group,
+                       "layout": "token-wise K / token-wise V", "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {n_rep} rotating replicas, {footprint / 1e9:.2f} GB, "
+                             f"L2 flushed before the timed graph replay"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl.name),
+                         "peak_kind": f"{peak_kind} copy bandwidth", "kernel": "split_decode_kernel INT2 token-wise",
+                         "bytes_per_launch": step_bytes},
+            "clocks": clocks,
+            "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": args.steps,
+            "device_status": status,
+            "cpu_baseline": cpu,
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -3,34 +3,11 @@
 // frees or synchronizes (except lbkv_device_status, documented as such).
 #include <atomic>
 #include <cmath>
+#include <mutex>
+#include <unordered_map>
 
 #include "lbkv.h"
 #include "lbkv_internal.h"
-
-namespace lbkv {
-
-// Merges the splits of one (sequence, query head): out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(128) split_combine_kernel(const float2* __restrict__ part_ml,
-                                                             const float* __restrict__ part_o, int s_tot,
-                                                             __nv_bfloat16* __restrict__ out) {
-  const int bh = blockIdx.x, ch = threadIdx.x;
-  const float2* ml = part_ml + (size_t)bh * s_tot;
-  const float* po = part_o + (size_t)bh * s_tot * kHeadDim;
-  float M = -INFINITY;
-  for (int s = 0; s < s_tot; ++s) M = fmaxf(M, ml[s].x);
-  float acc = 0.f, l = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < s_tot; ++s) {
-      const float2 x = ml[s];
-      const float sc = (x.x == -INFINITY) ? 0.f : fast_exp2(x.x - M);
-      l = fmaf(sc, x.y, l);
-      acc = fmaf(sc, po[(size_t)s * kHeadDim + ch], acc);
-    }
-  }
-  out[(size_t)bh * kHeadDim + ch] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
-}
-
-}  // namespace lbkv
 
 using namespace lbkv;
 
@@ -57,6 +34,22 @@ int current_device_props(int* sms, int* smem_optin) {
   return LBKV_OK;
 }
 
+// Opt-in shared memory is set once per (device, kernel): later calls skip the driver call.
+std::mutex g_attr_mu;
+std::unordered_map<uint64_t, int> g_attr_smem;
+
+int ensure_smem_attr(const void* fn, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LBKV_ECUDA;
+  const uint64_t key = (reinterpret_cast<uint64_t>(fn) << 6) ^ (uint64_t)dev;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  auto it = g_attr_smem.find(key);
+  if (it != g_attr_smem.end() && it->second >= bytes) return LBKV_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return LBKV_ECUDA;
+  g_attr_smem[key] = bytes;
+  return LBKV_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
@@ -66,7 +59,7 @@ struct Plan {
   int splits, s_tot, slots_per_split;
   int n_ring, slot_bytes, slot_tx, smem_bytes;
   int off_vc, off_ks, off_kz, off_vs, off_vz, sz_k, sz_v;
-  size_t off_ml, off_o, ws_bytes;
+  size_t off_done, off_ml, off_o, ws_bytes;
 };
 
 // Validates shapes and format, then fixes the split count and the ring.
@@ -138,15 +131,19 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   pl->slots_per_split = (spu + best_s - 1) / best_s;
   pl->s_tot = best_s + (win ? 1 : 0);
 
+  // workspace: status word | per-unit split counters | (m, l) partials | O partials
   const size_t rows = (size_t)d->batch * d->num_q_heads * pl->s_tot;
-  pl->off_ml = 256;
+  pl->off_done = 256;
+  pl->off_ml = round_up(pl->off_done + (size_t)units * sizeof(int32_t), 256);
   pl->off_o = round_up(pl->off_ml + rows * sizeof(float2), 256);
   pl->ws_bytes = round_up(pl->off_o + rows * kHeadDim * sizeof(float), 256);
   return LBKV_OK;
 }
 
-DecodeKernel pick_kernel(int bits, int kl, int vl, int nt, int gv) {
-  return bits == 2 ? decode_kernel_int2(kl, vl, nt, gv) : decode_kernel_int4(kl, vl, nt, gv);
+DecodeKernel pick_kernel(int bits, int kl, int vl, int nt, int group) {
+  const int log2g = group == 128 ? 7 : group == 64 ? 6 : 5;
+  if (bits == 2) return kl ? decode_kernel_int2_k1(vl, nt, log2g) : decode_kernel_int2_k0(vl, nt, log2g);
+  return kl ? decode_kernel_int4_k1(vl, nt, log2g) : decode_kernel_int4_k0(vl, nt, log2g);
 }
 
 }  // namespace
@@ -175,7 +172,7 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   if (desc->k_win && (!aligned16(desc->k_win) || !aligned16(desc->v_win))) return LBKV_EALIGN;
   if (!desc->workspace || desc->workspace_bytes < pl.ws_bytes) return LBKV_EWORKSPACE;
   if (reinterpret_cast<uintptr_t>(desc->workspace) & 255u) return LBKV_EALIGN;
-  DecodeKernel kern = pick_kernel(bits, k_layout, v_layout, pl.nt, pl.gv);
+  DecodeKernel kern = pick_kernel(bits, k_layout, v_layout, pl.nt, group);
   if (!kern) return LBKV_EUNSUPPORTED;
 
   uint8_t* ws = static_cast<uint8_t*>(desc->workspace);
@@ -194,12 +191,13 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.part_ml = reinterpret_cast<float2*>(ws + pl.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.status = reinterpret_cast<int32_t*>(ws);
+  p.done = reinterpret_cast<int32_t*>(ws + pl.off_done);
+  p.out = static_cast<__nv_bfloat16*>(out);
   p.B = desc->batch;
   p.Hq = desc->num_q_heads;
   p.Hkv = desc->num_kv_heads;
   p.hq = pl.hq;
   p.T_cap = desc->max_seq_len;
-  p.group = group;
   p.win_cap = desc->k_win ? desc->win_cap : 0;
   const float sigma = desc->sm_scale > 0.f ? desc->sm_scale : 1.f / std::sqrt((float)desc->head_dim);
   p.sl2 = sigma * 1.4426950408889634f;
@@ -217,15 +215,10 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.sz_k_bytes = pl.sz_k;
   p.sz_v_bytes = pl.sz_v;
 
-  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           pl.smem_bytes) != cudaSuccess)
-    return LBKV_ECUDA;
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem_bytes) != LBKV_OK) return LBKV_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   dim3 grid((unsigned)pl.s_tot, (unsigned)desc->num_kv_heads, (unsigned)desc->batch);
   kern<<<grid, kThreads, pl.smem_bytes, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;
-  split_combine_kernel<<<(unsigned)(desc->batch * desc->num_q_heads), kHeadDim, 0, s>>>(
-      p.part_ml, p.part_o, pl.s_tot, static_cast<__nv_bfloat16*>(out));
   if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;
   return LBKV_OK;
 }

@@ -1,0 +1,23 @@
+// lbkv_decode_int2_k1.cu -- instantiations of the split-decode kernel for 2-bit
+// codes with a channel-wise K side.
+#include "lbkv_internal.h"
+
+namespace lbkv {
+
+DecodeKernel decode_kernel_int2_k1(int vl, int nt, int log2g) {
+#define LBKV_PICK(VL, NT, LG) \
+  if (vl == VL && nt == NT && log2g == LG) return &split_decode_kernel<Cfg<2, 1, VL, NT, LG>>;
+  LBKV_PICK(0, 1, 7)
+  LBKV_PICK(0, 2, 7)
+  LBKV_PICK(0, 1, 6)
+  LBKV_PICK(1, 1, 7)
+  LBKV_PICK(1, 2, 7)
+  LBKV_PICK(1, 1, 6)
+  LBKV_PICK(1, 2, 6)
+  LBKV_PICK(1, 1, 5)
+  LBKV_PICK(1, 2, 5)
+#undef LBKV_PICK
+  return nullptr;
+}
+
+}  // namespace lbkv

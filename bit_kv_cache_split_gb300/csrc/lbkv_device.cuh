@@ -134,6 +134,50 @@ __device__ __forceinline__ void split_e4m3_pair(float x0, float x1, uint32_t& hi
   lo = l;
 }
 
+// As split_e4m3_pair, and also returns the values actually fed, hi + lo, as
+// floats (exact: hi + lo has at most ten significant bits).
+__device__ __forceinline__ void split_e4m3_pair_fed(float x0, float x1, uint32_t& hi, uint32_t& lo, float& f0,
+                                                    float& f1) {
+  uint32_t h2, back, res, lback, fed;
+  uint16_t h, l;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(h2));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(h));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(res) : "r"(h2), "r"(back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(res));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lback) : "h"(l));
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(fed) : "r"(back), "r"(lback));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&fed));
+  hi = h;
+  lo = l;
+  f0 = f.x;
+  f1 = f.y;
+}
+
+// Three-part split x = hi + lo + lo2 (about twelve significant bits, the
+// precision of the fp16 value it starts from). Both subtractions are exact.
+__device__ __forceinline__ void split3_e4m3_pair(float x0, float x1, uint32_t& hi, uint32_t& lo, uint32_t& lo2) {
+  uint32_t h2, back, r1, back1, r2;
+  uint16_t h, l, l2;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(h2));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(h));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r1) : "r"(h2), "r"(back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(r1));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back1) : "h"(l));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r2) : "r"(r1), "r"(back1));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l2) : "r"(r2));
+  hi = h;
+  lo = l;
+  lo2 = l2;
+}
+
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // 4x4 byte transpose: out[b] byte j = in[j] byte b.
 __device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t (&t)[4]) {
   const uint32_t x0 = prmt(w0, w1, 0x5140), x1 = prmt(w0, w1, 0x7362);

@@ -88,9 +88,12 @@ typedef struct lbkv_desc {
   const void* v_win;     /* bf16 [B][Hkv][win_cap][D], NULL exactly when k_win is NULL */
   const int32_t* win_lens; /* int32 [B], 0 <= win_lens[b] <= win_cap; NULL when k_win is NULL */
   int32_t win_cap;       /* 1..128 when k_win is set */
-  void* workspace;       /* device scratch of >= lbkv_workspace_bytes(...) bytes, 256-byte aligned;
-                            zero-filled once after allocation (its first 256 bytes hold the
-                            device status word); reusable by calls in stream order */
+  void* workspace;       /* device scratch of >= lbkv_workspace_bytes(...) bytes, 256-byte aligned,
+                            zero-filled once after allocation: it holds the device status word,
+                            one split counter per (sequence, KV head) that every call leaves at
+                            zero, and the split partials. Calls that share a workspace must be
+                            ordered (one stream); concurrent calls need their own. After
+                            lbkv_device_status reports an error, zero it again. */
   size_t workspace_bytes;
 } lbkv_desc;
 

@@ -191,6 +191,26 @@ class DecodeInputs:
                      p(self.seq_lens), p(self.k_win), p(self.v_win), p(self.win_lens), self.win_cap)
 
 
+def _bits16(t) -> np.ndarray:
+    import torch
+
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def inputs_from_tensors(t: dict, *, bits, k_layout, v_layout, group, Hkv, T_cap, sm_scale=0.0) -> DecodeInputs:
+    """Host copies of torch tensors (q, codes, fp16 scales/offsets, seq_lens, optional window)
+    as oracle inputs. Only marshalling: raw bit patterns are passed through unchanged."""
+    kw = {}
+    if "k_win" in t:
+        kw = dict(k_win=_bits16(t["k_win"]), v_win=_bits16(t["v_win"]), win_lens=t["win_lens"].cpu().numpy(),
+                  win_cap=t["k_win"].shape[2])
+    return DecodeInputs(
+        q=_bits16(t["q"]), k_codes=t["k_codes"].cpu().numpy(), k_scale=_bits16(t["k_scale"]),
+        k_off=_bits16(t["k_off"]), v_codes=t["v_codes"].cpu().numpy(), v_scale=_bits16(t["v_scale"]),
+        v_off=_bits16(t["v_off"]), seq_lens=t["seq_lens"].cpu().numpy(), bits=bits, k_layout=k_layout,
+        v_layout=v_layout, group=group, Hkv=Hkv, T_cap=T_cap, sm_scale=sm_scale, **kw)
+
+
 def decode_ref(x: DecodeInputs, rows=None, n_threads: int = 0) -> np.ndarray:
     """Plain definition: dequantize, textbook softmax attention. Returns fp64.
 

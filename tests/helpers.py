@@ -27,18 +27,10 @@ def bits16(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def to_oracle(t: dict, wl, rows_unit=None) -> oracle.DecodeInputs:
+def to_oracle(t: dict, wl) -> oracle.DecodeInputs:
     """Marshal generated tensors into oracle inputs (host copies of every array)."""
-    kw = {}
-    if "k_win" in t:
-        kw = dict(k_win=bits16(t["k_win"]), v_win=bits16(t["v_win"]),
-                  win_lens=t["win_lens"].cpu().numpy(), win_cap=t["k_win"].shape[2])
-    return oracle.DecodeInputs(
-        q=bits16(t["q"]), k_codes=t["k_codes"].cpu().numpy(), k_scale=bits16(t["k_scale"]),
-        k_off=bits16(t["k_off"]), v_codes=t["v_codes"].cpu().numpy(), v_scale=bits16(t["v_scale"]),
-        v_off=bits16(t["v_off"]), seq_lens=t["seq_lens"].cpu().numpy(), bits=wl.bits,
-        k_layout=wl.k_layout, v_layout=wl.v_layout, group=wl.group, Hkv=wl.num_kv_heads,
-        T_cap=wl.t_cap, sm_scale=wl.sm_scale, **kw)
+    return oracle.inputs_from_tensors(t, bits=wl.bits, k_layout=wl.k_layout, v_layout=wl.v_layout, group=wl.group,
+                                      Hkv=wl.num_kv_heads, T_cap=wl.t_cap, sm_scale=wl.sm_scale)
 
 
 def np_unpack(codes: np.ndarray, bits: int) -> np.ndarray:
