@@ -528,6 +528,10 @@ static void quantize_group(const float* x, int n, int bits, uint16_t* s_out, uin
     if (x[i] < mn) mn = x[i];
     if (x[i] > mx) mx = x[i];
   }
+  /* a signed zero extreme is read as +0 (x + 0 maps -0 to +0 and keeps every
+   * other value), so that s and z never carry a negative zero */
+  mn = mn + 0.0f;
+  mx = mx + 0.0f;
   volatile float range = mx - mn;
   volatile float step = range / (float)((1 << bits) - 1);
   uint16_t sh = oracle_f64_to_fp16((double)step);

@@ -355,3 +355,12 @@ def test_pack_scale_offset_are_fp16_of_group_extremes(oracle_lib, bits):
     assert step.dtype == np.float32
     assert np.array_equal(z, mn.astype(np.float16).view(np.uint16))
     assert np.array_equal(s, step.astype(np.float16).view(np.uint16))
+
+
+def test_pack_signed_zero_extremes_read_as_positive_zero(oracle_lib):
+    """A group whose minimum (or maximum) is -0 stores z = +0 and s = +0 (this library's
+    reading of the quantizer: scale and offset never carry a negative zero)."""
+    x = np.zeros((1, 1, 128, 128), np.float32)
+    x[0, 0, :, ::2] = -0.0
+    codes, s, z = oracle.pack(_bf16_from(x), [128], 2, 0, 32)
+    assert np.all(s == 0) and np.all(z == 0) and np.all(codes == 0)
