@@ -21,9 +21,10 @@ TOKENWISE = 0
 CHANNELWISE = 1
 
 STATUS = {0: "LBKV_OK", -1: "LBKV_EINVAL", -2: "LBKV_EALIGN", -3: "LBKV_EUNSUPPORTED",
-          -4: "LBKV_EWORKSPACE", -5: "LBKV_ECUDA", -6: "LBKV_EDEVICE"}
+          -4: "LBKV_EWORKSPACE", -5: "LBKV_ECUDA", -6: "LBKV_EDEVICE", -7: "LBKV_ESCRATCH"}
 
-EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_device_status", "lbkv_strerror")
+EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_device_status", "lbkv_strerror",
+           "lbkv_decode_attn_noalloc", "lbkv_noalloc_scratch_bytes")
 
 
 class LbkvError(RuntimeError):
@@ -70,6 +71,10 @@ def load(path: Optional[str] = None):
         L.lbkv_pack.argtypes = [ctypes.POINTER(Desc), vp, vp, i32, i32, i32, vp, vp, vp, vp]
         L.lbkv_device_status.restype = i32
         L.lbkv_device_status.argtypes = [ctypes.POINTER(Desc), vp, ctypes.POINTER(ctypes.c_int32)]
+        L.lbkv_decode_attn_noalloc.restype = i32
+        L.lbkv_decode_attn_noalloc.argtypes = [ctypes.POINTER(Desc)] + [vp] * 8 + [i32] * 4 + [vp, vp]
+        L.lbkv_noalloc_scratch_bytes.restype = ctypes.c_size_t
+        L.lbkv_noalloc_scratch_bytes.argtypes = []
         L.lbkv_strerror.restype = ctypes.c_char_p
         L.lbkv_strerror.argtypes = [i32]
         if path is None:

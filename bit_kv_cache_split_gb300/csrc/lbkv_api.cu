@@ -270,6 +270,7 @@ const char* lbkv_strerror(int status) {
     case LBKV_EWORKSPACE: return "workspace missing or smaller than lbkv_workspace_bytes";
     case LBKV_ECUDA: return "CUDA launch or runtime error";
     case LBKV_EDEVICE: return "a kernel reported a device-side error (bounded wait ran out)";
+    case LBKV_ESCRATCH: return "the call needs more scratch than the fixed no-allocation array holds";
     default: return "unknown status";
   }
 }

@@ -73,7 +73,9 @@ typedef enum {
   LBKV_EUNSUPPORTED = -3,  /* valid but not implemented (see lbkv_decode_attn) */
   LBKV_EWORKSPACE = -4,    /* workspace missing or smaller than lbkv_workspace_bytes */
   LBKV_ECUDA = -5,         /* a CUDA launch or runtime call failed */
-  LBKV_EDEVICE = -6        /* a kernel reported a device-side error (lbkv_device_status) */
+  LBKV_EDEVICE = -6,       /* a kernel reported a device-side error (lbkv_device_status) */
+  LBKV_ESCRATCH = -7       /* lbkv_decode_attn_noalloc: the call needs more scratch than the
+                              library's fixed array holds (lbkv_noalloc_scratch_bytes) */
 } lbkv_status;
 
 /* Shapes, scale, optional bf16 window and workspace of one decode call. */
@@ -134,6 +136,30 @@ LBKV_API int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_
  * Errors as for lbkv_decode_attn. */
 LBKV_API int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_lens, int bits, int layout, int group,
               uint8_t* codes, void* scale, void* off, lbkv_stream_t stream);
+
+/* Same computation and arguments as lbkv_decode_attn, for callers that cannot
+ * allocate device memory (an engine whose allocator owns all device memory, a
+ * plugin that only receives its input and output buffers, a loop where an
+ * allocation is not allowed). desc->workspace and desc->workspace_bytes are
+ * ignored: the split-KV scratch is a fixed array of lbkv_noalloc_scratch_bytes()
+ * bytes (16 MiB) inside this library, which every GPU that loads the library
+ * keeps until the process exits. There is no counterpart on the pages; it only
+ * changes where the scratch lives.
+ *   - A call whose scratch (lbkv_workspace_bytes for the same arguments) would
+ *     exceed that size returns LBKV_ESCRATCH before anything is launched.
+ *   - The first call on each device looks the array's address up with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call on a device shares the array and it keeps the last call's
+ *     contents; the call clears the part that must start at zero. Calls that
+ *     overlap on the GPU (other streams, other threads) race: order them.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. */
+LBKV_API int lbkv_decode_attn_noalloc(const lbkv_desc* desc, const void* q, const uint8_t* k_codes,
+                                      const void* k_scale, const void* k_off, const uint8_t* v_codes,
+                                      const void* v_scale, const void* v_off, const int32_t* seq_lens, int bits,
+                                      int k_layout, int v_layout, int group, void* out, lbkv_stream_t stream);
+
+/* Size in bytes of the fixed scratch array behind lbkv_decode_attn_noalloc. */
+LBKV_API size_t lbkv_noalloc_scratch_bytes(void);
 
 /* Reads and clears the device status word that kernels set instead of
  * hanging (a bounded wait that ran out). Synchronizes `stream`. Returns
