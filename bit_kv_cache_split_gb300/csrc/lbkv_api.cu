@@ -79,12 +79,13 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   if (win != (d->v_win != nullptr) || win != (d->win_lens != nullptr)) return LBKV_EINVAL;
   if (win && (d->win_cap <= 0 || d->win_cap > 128)) return LBKV_EINVAL;
   pl->hq = hq;
-  pl->nt = hq > 4 ? 2 : 1;
-  // A token-wise V side with G channel groups feeds G separately scaled copies of P
-  // (operand-fold); the kernel holds at most two PV n-tiles of 8 columns.
+  // PV columns are (query, V channel group) pairs: a token-wise V side with G channel
+  // groups feeds G separately scaled copies of the weights (operand-fold); the kernel
+  // holds at most two PV n-tiles of 8 columns.
   const int groups_v = (vl == LBKV_TOKENWISE) ? kHeadDim / group : 1;
-  if (groups_v > 2 || pl->nt * groups_v > 2) return LBKV_EUNSUPPORTED;
   pl->gv = groups_v;
+  pl->nt = (hq * groups_v + 7) / 8;
+  if (pl->nt > 2) return LBKV_EUNSUPPORTED;
 
   int sms = 0, smem_optin = 0;
   int st = current_device_props(&sms, &smem_optin);
@@ -140,10 +141,10 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   return LBKV_OK;
 }
 
-DecodeKernel pick_kernel(int bits, int kl, int vl, int nt, int group) {
+DecodeKernel pick_kernel(int bits, int kl, int vl, int ntv, int group) {
   const int log2g = group == 128 ? 7 : group == 64 ? 6 : 5;
-  if (bits == 2) return kl ? decode_kernel_int2_k1(vl, nt, log2g) : decode_kernel_int2_k0(vl, nt, log2g);
-  return kl ? decode_kernel_int4_k1(vl, nt, log2g) : decode_kernel_int4_k0(vl, nt, log2g);
+  if (bits == 2) return kl ? decode_kernel_int2_k1(vl, ntv, log2g) : decode_kernel_int2_k0(vl, ntv, log2g);
+  return kl ? decode_kernel_int4_k1(vl, ntv, log2g) : decode_kernel_int4_k0(vl, ntv, log2g);
 }
 
 }  // namespace

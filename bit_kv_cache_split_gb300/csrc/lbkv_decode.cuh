@@ -19,19 +19,18 @@
 // merges its warps into one split partial, and the last split of a
 // (sequence, KV head) to finish merges all splits into the bf16 output.
 //
-// Operands. A 2-bit code q masked into the low bits of a byte is the e4m3
-// value q * 2^-9 (subnormal), and 4*q at bits 2..3 is 4q * 2^-9; a 4-bit code
-// in the low nibble is q * 2^-9 (the subnormal and first normal binade of
-// e4m3 are evenly spaced). So one LOP3 turns four packed codes into four e4m3
-// tensor-core inputs, with a power-of-two position factor folded into the
-// other operand. The query enters as the exact two-part e4m3 split hi + lo of
-// its bf16 value (three parts when a channel-wise K scale multiplies it first);
-// the softmax weights enter as a two-part split, and the running denominator
-// and the value offsets are summed from the weights actually fed, so the
-// result is an exact attention under the fed weights. Both products run on
-// mma.sync m16n8k32 e4m3 (full-rate fp8 tensor cores), accumulating in fp32:
-//   QK^T: rows = 16 tokens, k = 32 channels, cols = (query, part);
-//   PV:   rows = 16 channels, k = 32 tokens, cols = (query[, group], part).
+// Operands. OR-ing a code q (times a power-of-two position factor m) into the
+// mantissa of the fp16 magic number 1024 gives the exact fp16 value 1024 + m q,
+// two codes per LOP3; the factor 1/m is folded into the other operand and the
+// bias 1024 is cancelled inside the tensor core by starting each accumulator at
+// -1024 * (sum of the other operand as fed). The bf16 query is exact in fp16;
+// the softmax weights are fed as fp16 (11 bits), and the running denominator
+// and the value offsets are summed from the weights actually fed, so the result
+// is an exact attention under the fed weights. Both products run on mma.sync
+// m16n8k16 fp16 with fp32 accumulators (on sm_103 this is a native tensor-core
+// instruction; the e4m3 form is not, it converts its operands to fp16 first):
+//   QK^T: rows = 16 tokens, k = 16 channels, cols = queries;
+//   PV:   rows = 16 channels, k = 16 tokens, cols = (query[, channel group]).
 #pragma once
 
 #include <type_traits>
@@ -85,50 +84,57 @@ struct DecodeParams {
 };
 
 // Compile-time shape of one kernel variant.
-template <int BITS_, int KL_, int VL_, int NT_, int LOG2G_>
+template <int BITS_, int KL_, int VL_, int NTV_, int LOG2G_>
 struct Cfg {
-  static constexpr int BITS = BITS_, KL = KL_, VL = VL_, NT = NT_;
+  static constexpr int BITS = BITS_, KL = KL_, VL = VL_, NTV = NTV_;
   static constexpr int G = 1 << LOG2G_;                    // group size
   static constexpr int GK = (KL == 0) ? kHeadDim / G : 1;  // K channel groups per token
   static constexpr int GV = (VL == 0) ? kHeadDim / G : 1;  // V channel groups per token
-  static constexpr int KSG = 4 / GK;                       // QK k-steps per K channel group
-  static constexpr int NTK = (KL == 1) ? 2 * NT : NT;      // QK n-tiles (3-part query: 2 per slot)
-  static constexpr int NTV = NT * GV;                      // PV n-tiles
+  static constexpr int KSG = G / 16;                       // QK k-steps per K channel group
   static constexpr int RB = kHeadDim * BITS / 8;           // bytes per token row of codes
-  static_assert(NTV <= 2, "at most two PV n-tiles");
+  static_assert(NTV >= 1 && NTV <= 2, "one or two PV n-tiles");
   static_assert(G >= kChunk, "a chunk never straddles a token group");
 };
 
-// Channel fed at k-slot kappa of QK^T k-step ks (see the A-fragment build).
+// Channel fed at k-slot kappa (0..15) of QK^T k-step ks (0..7); see the K operand build.
 template <int BITS>
 __device__ __forceinline__ int qk_channel(int ks, int kappa) {
-  const int c = (kappa & 15) >> 2, j = kappa & 3, r = kappa >> 4;
-  if (BITS == 2) return 32 * ks + 16 * (c >> 1) + 4 * j + (c & 1) + 2 * r;
-  return 32 * ks + 8 * c + 2 * j + r;
+  const int blk = ks >> 1, h = ks & 1, c = (kappa & 7) >> 1, e = kappa & 1, up = kappa >> 3;
+  const int p = 2 * h + up;
+  if (BITS == 2) return 32 * blk + 16 * (c >> 1) + 4 * (c & 1) + 8 * e + p;
+  return 32 * blk + 8 * c + 4 * e + p;
 }
-// Position factor of the e4m3 image of channel ch on the K side.
+// Power-of-two position factor of the fp16 image of K channel ch (1024 + factor * q).
 template <int BITS>
 __device__ __forceinline__ float k_mult(int ch) {
-  return (BITS == 2 && (ch & 1)) ? 4.f : 1.f;
+  if (BITS == 2) return (float)(1 << (2 * (ch & 3)));
+  return (ch & 1) ? 16.f : 1.f;
+}
+// Position factor of V m-tile mt (both of its rows).
+template <int BITS>
+__host__ __device__ constexpr float v_mult(int mt) {
+  return BITS == 2 ? (float)(1 << (2 * (mt <= 4 ? mt : mt - 5))) : ((mt & 1) ? 16.f : 1.f);
 }
 
-// Builds one B-fragment register for QK^T: four e4m3 bytes of part `part`
-// (0 = hi, 1 = lo) of x[0..3].
-__device__ __forceinline__ uint32_t pack_split4(const float (&x)[4], int part) {
-  uint32_t h01, l01, h23, l23;
-  split_e4m3_pair(x[0], x[1], h01, l01);
-  split_e4m3_pair(x[2], x[3], h23, l23);
-  return part ? (l01 | (l23 << 16)) : (h01 | (h23 << 16));
+// fp16 images (1024 + factor * code) of position p of an 8-code (INT2) or 4-code
+// (INT4) group of two 16-bit halves: one LOP3 (plus a shared shift).
+__device__ __forceinline__ uint32_t int2_half2(uint32_t x, uint32_t xs10, int p) {
+  return p <= 4 ? and_or(x, 0x00030003u << (2 * p), kMagic2) : and_or(xs10, 0x00030003u << (2 * (p - 5)), kMagic2);
+}
+__device__ __forceinline__ uint32_t int4_half2(uint32_t x, uint32_t xs8, int p) {
+  const uint32_t src = p < 2 ? x : xs8;
+  return and_or(src, (p & 1) ? 0x00F000F0u : 0x000F000Fu, kMagic2);
 }
 
-// Per-warp state, held in registers.
+// Per-warp state, held in registers. Each lane scores queries 2c and 2c+1.
 template <class C>
 struct WarpState {
-  uint32_t qB[4][C::NTK][2];  // QK^T B fragments
-  float sA[C::NT];            // token-wise K: score factor of this lane's query
-  int qrow[C::NT];            // this lane's query (clamped), per n-tile
-  float m_run[C::NT], l_part[C::NT], zacc[C::NT][C::GV];
-  float o_run[8][2][C::NTV];
+  uint32_t qB[8][2];      // QK^T B fragments (fp16 pairs of Q' = Q 2^e / factor)
+  float c1[2][C::GK];     // token-wise K: 1024 * sum of Q' over a channel group (magic bias)
+  float aq[2];            // token-wise K: sigma log2(e) 2^-e
+  float bz[2][C::GK];     // token-wise K: sigma log2(e) sum of Q over a channel group
+  float m_run[2], l_part[2], zacc[2][C::GV];
+  float o_run[8][2][C::NTV][2];  // [m-tile][row half][n-tile][column]
 };
 
 // Everything one chunk of 32 tokens needs from shared memory.
@@ -140,203 +146,218 @@ struct ChunkSmem {
   const __half* vs;
   const __half* vz;
   const float* sQ;
-  const float* sBz;
+  const int* sEq;
 };
 
-// One 32-token chunk: QK^T with the K fold, online softmax, P (or P') split,
-// PV with the V fold. FULL: all 32 tokens valid (no masking).
+// One 32-token chunk: QK^T with the K fold, online softmax, weights, PV with the
+// V fold. FULL: all 32 tokens valid (no masking).
 template <class C, bool FULL>
 __device__ __forceinline__ void process_chunk(WarpState<C>& st, const ChunkSmem& sm, int rel0, int nv, int hq,
                                               float sl2, int lane) {
-  constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, NT = C::NT, GV = C::GV, NTK = C::NTK, NTV = C::NTV;
+  constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NTV = C::NTV;
   constexpr int RB = C::RB, D = kHeadDim;
-  const int g = lane >> 2, c = lane & 3;
-  const int qi_b = g >> 1, qpart = g & 1;
   constexpr unsigned FULLMASK = 0xffffffffu;
+  const int g = lane >> 2, c = lane & 3;
 
   // ---------------------------------------------------- channel-wise K: Q' per token group
-  float cwA[NT], cwB[NT];
+  // Operand-fold: Q' = Q * s_tau / factor, scaled by 2^e into fp16; the offset becomes
+  // sum_d Q_d z_tau,d, one constant per (query, token group), added before the softmax.
+  float cwA[2] = {0.f, 0.f}, cwB[2] = {0.f, 0.f}, cwC[2] = {0.f, 0.f};
   if (KL == 1) {
-    const int tau_rel = rel0 / C::G;  // compile-time power of two
+    const int tau_rel = rel0 / C::G;
     const __half* s_tau = sm.ks + tau_rel * D;
     const __half* z_tau = sm.kz + tau_rel * D;
+    const int q = g;  // this lane's B column
+    const bool live = q < hq;
+    float x[8][2][2];
+    float amax = 0.f, zsum = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int i = 4 * nt + qi_b;
-      const bool live = i < hq;
-      float xs[4][2][4];
-      float amax = 0.f, zsum = 0.f;
+    for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
+      for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int ch = qk_channel<BITS>(ks, 16 * rr + 4 * c + jj);
-            const float qv = live ? sm.sQ[i * D + ch] : 0.f;
-            const float v = qv * __half2float(s_tau[ch]) * (1.f / k_mult<BITS>(ch));
-            xs[ks][rr][jj] = v;
-            amax = fmaxf(amax, fabsf(v));
-            zsum = fmaf(qv, __half2float(z_tau[ch]), zsum);
-          }
-      amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
-      zsum += __shfl_xor_sync(FULLMASK, zsum, 1);
-      zsum += __shfl_xor_sync(FULLMASK, zsum, 2);
-      int e = 0;
-      if (amax > 0.f) e = min(100, max(-100, 7 - ilog2f(amax)));
-      const float sc = exp2i(e);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          uint32_t h01, l01, m01, h23, l23, m23;
-          split3_e4m3_pair(xs[ks][rr][0] * sc, xs[ks][rr][1] * sc, h01, l01, m01);
-          split3_e4m3_pair(xs[ks][rr][2] * sc, xs[ks][rr][3] * sc, h23, l23, m23);
-          st.qB[ks][2 * nt][rr] = qpart ? (l01 | (l23 << 16)) : (h01 | (h23 << 16));
-          st.qB[ks][2 * nt + 1][rr] = qpart ? 0u : (m01 | (m23 << 16));
+        for (int e = 0; e < 2; ++e) {
+          const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
+          const float qv = live ? sm.sQ[q * D + ch] : 0.f;
+          const float v = qv * __half2float(s_tau[ch]) * (1.f / k_mult<BITS>(ch));
+          x[ks][r][e] = v;
+          amax = fmaxf(amax, fabsf(v));
+          zsum = fmaf(qv, __half2float(z_tau[ch]), zsum);
         }
-      // the S-fragment lanes of query c + 4nt read B column 2c, held by lane 8c
-      const float fa = sl2 * exp2i(9 - e), fb = sl2 * zsum;
-      cwA[nt] = __shfl_sync(FULLMASK, fa, 8 * c);
-      cwB[nt] = __shfl_sync(FULLMASK, fb, 8 * c);
+    amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
+    zsum += __shfl_xor_sync(FULLMASK, zsum, 1);
+    zsum += __shfl_xor_sync(FULLMASK, zsum, 2);
+    int e2 = 0;
+    if (amax > 0.f) e2 = min(100, max(-100, 13 - ilog2f(amax)));
+    const float sc = exp2i(e2);
+    float fed = 0.f;  // sum of the fp16 values actually fed (for the magic bias)
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t h2 = f16x2_from(x[ks][r][0] * sc, x[ks][r][1] * sc);
+        st.qB[ks][r] = h2;
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        fed += f.x + f.y;
+      }
+    fed += __shfl_xor_sync(FULLMASK, fed, 1);
+    fed += __shfl_xor_sync(FULLMASK, fed, 2);
+    const float fa = sl2 * exp2i(-e2), fb = sl2 * zsum, fc = kMagicF * fed;
+#pragma unroll
+    for (int ql = 0; ql < 2; ++ql) {  // query 2c + ql is B column 2c + ql, held by lane 8c + 4ql
+      cwA[ql] = __shfl_sync(FULLMASK, fa, 8 * c + 4 * ql);
+      cwB[ql] = __shfl_sync(FULLMASK, fb, 8 * c + 4 * ql);
+      cwC[ql] = __shfl_sync(FULLMASK, fc, 8 * c + 4 * ql);
     }
   }
 
   // ---------------------------------------------------- QK^T with the K fold
-  float S[2][2][NT];  // [m-tile][row half][n-tile], log2 domain
+  // S[mt][row][ql]: token 16 mt + 8 row + g of the chunk, query 2c + ql (log2 domain).
+  float S[2][2][2];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
-    const int row0 = rel0 + 16 * mt + g;  // slot-relative tokens of this lane's rows
+    const int row0 = rel0 + 16 * mt + g;
     const int row1 = row0 + 8;
-    float acc[NTK][4];
-    float sfold[2][NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sfold[0][nt] = sfold[1][nt] = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < NTK; ++nt)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) acc[nt][u] = 0.f;
-    uint32_t w0[4], w1[4];
     const uint32_t* r0p = reinterpret_cast<const uint32_t*>(sm.kc + row0 * RB);
     const uint32_t* r1p = reinterpret_cast<const uint32_t*>(sm.kc + row1 * RB);
+    uint32_t w0[4], w1[4], s0w[4], s1w[4];
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const int wi = (BITS == 2) ? 2 * ks + (c >> 1) : 4 * ks + c;
-      w0[ks] = r0p[wi];
-      w1[ks] = r1p[wi];
+    for (int blk = 0; blk < 4; ++blk) {
+      if (BITS == 2) {
+        // lanes with odd c take codes 4..7 and 12..15 of the word: shift them into 0..3
+        const int sh = 8 * (c & 1);
+        w0[blk] = r0p[2 * blk + (c >> 1)] >> sh;
+        w1[blk] = r1p[2 * blk + (c >> 1)] >> sh;
+      } else {
+        w0[blk] = r0p[4 * blk + c];
+        w1[blk] = r1p[4 * blk + c];
+        s0w[blk] = w0[blk] >> 8;
+        s1w[blk] = w1[blk] >> 8;
+      }
     }
-    const uint32_t m2 = (c & 1) ? 0x0C0C0C0Cu : 0x03030303u;
+    float sfold[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    float acc[4];
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
+    for (int ks = 0; ks < 8; ++ks) {
+      const int blk = ks >> 1, h = ks & 1;
+      if (KL == 0 ? (ks % C::KSG == 0) : (ks == 0)) {
+        // token-wise K: a fresh accumulator per channel group; channel-wise K: one for all
+        // 128 channels (the scale is already in Q'). Each starts at minus the magic bias.
+        const float b0 = (KL == 0) ? st.c1[0][ks / C::KSG] : cwC[0];
+        const float b1 = (KL == 0) ? st.c1[1][ks / C::KSG] : cwC[1];
+        acc[0] = -b0;
+        acc[1] = -b1;
+        acc[2] = -b0;
+        acc[3] = -b1;
+      }
       uint32_t a0, a1, a2, a3;
       if (BITS == 2) {
-        a0 = w0[ks] & m2;
-        a1 = w1[ks] & m2;
-        a2 = (w0[ks] >> 4) & m2;
-        a3 = (w1[ks] >> 4) & m2;
+        const uint32_t mA = 0x00030003u << (4 * h), mB = 0x00030003u << (4 * h + 2);
+        a0 = and_or(w0[blk], mA, kMagic2);
+        a1 = and_or(w1[blk], mA, kMagic2);
+        a2 = and_or(w0[blk], mB, kMagic2);
+        a3 = and_or(w1[blk], mB, kMagic2);
       } else {
-        a0 = w0[ks] & 0x0F0F0F0Fu;
-        a1 = w1[ks] & 0x0F0F0F0Fu;
-        a2 = (w0[ks] >> 4) & 0x0F0F0F0Fu;
-        a3 = (w1[ks] >> 4) & 0x0F0F0F0Fu;
+        a0 = int4_half2(w0[blk], s0w[blk], 2 * h);
+        a1 = int4_half2(w1[blk], s1w[blk], 2 * h);
+        a2 = int4_half2(w0[blk], s0w[blk], 2 * h + 1);
+        a3 = int4_half2(w1[blk], s1w[blk], 2 * h + 1);
       }
-#pragma unroll
-      for (int nt = 0; nt < NTK; ++nt) mma_e4m3(acc[nt], a0, a1, a2, a3, st.qB[ks][nt][0], st.qB[ks][nt][1]);
-      if (KL == 0 && ((ks + 1) % C::KSG) == 0) {
+      mma_f16(acc, a0, a1, a2, a3, st.qB[ks][0], st.qB[ks][1]);
+      if (KL == 0 && (ks + 1) % C::KSG == 0) {
         // acc-fold of one channel group: s * (raw partial) + z * sum(Q over the group)
-        constexpr int GK = C::GK;
         const int grp = ks / C::KSG;
         const float s0 = __half2float(sm.ks[row0 * GK + grp]);
         const float z0 = __half2float(sm.kz[row0 * GK + grp]);
         const float s1 = __half2float(sm.ks[row1 * GK + grp]);
         const float z1 = __half2float(sm.kz[row1 * GK + grp]);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float raw0 = acc[nt][0] + acc[nt][1], raw1 = acc[nt][2] + acc[nt][3];
-          const float bz = sm.sBz[st.qrow[nt] * 4 + grp];
-          sfold[0][nt] = fmaf(s0 * st.sA[nt], raw0, fmaf(z0, bz, sfold[0][nt]));
-          sfold[1][nt] = fmaf(s1 * st.sA[nt], raw1, fmaf(z1, bz, sfold[1][nt]));
-#pragma unroll
-          for (int u = 0; u < 4; ++u) acc[nt][u] = 0.f;
+        for (int ql = 0; ql < 2; ++ql) {
+          sfold[0][ql] = fmaf(s0 * st.aq[ql], acc[ql], fmaf(z0, st.bz[ql][grp], sfold[0][ql]));
+          sfold[1][ql] = fmaf(s1 * st.aq[ql], acc[2 + ql], fmaf(z1, st.bz[ql][grp], sfold[1][ql]));
         }
       }
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float s0v, s1v;
+    for (int ql = 0; ql < 2; ++ql) {
+      float v0, v1;
       if (KL == 0) {
-        s0v = sfold[0][nt];
-        s1v = sfold[1][nt];
+        v0 = sfold[0][ql];
+        v1 = sfold[1][ql];
       } else {
-        s0v = fmaf(cwA[nt], (acc[2 * nt][0] + acc[2 * nt][1]) + acc[2 * nt + 1][0], cwB[nt]);
-        s1v = fmaf(cwA[nt], (acc[2 * nt][2] + acc[2 * nt][3]) + acc[2 * nt + 1][2], cwB[nt]);
+        v0 = fmaf(cwA[ql], acc[ql], cwB[ql]);
+        v1 = fmaf(cwA[ql], acc[2 + ql], cwB[ql]);
       }
       if (FULL) {
-        S[mt][0][nt] = s0v;
-        S[mt][1][nt] = s1v;
+        S[mt][0][ql] = v0;
+        S[mt][1][ql] = v1;
       } else {
-        const int t0rel = 16 * mt + g;
-        S[mt][0][nt] = (t0rel < nv) ? s0v : -INFINITY;
-        S[mt][1][nt] = (t0rel + 8 < nv) ? s1v : -INFINITY;
+        const int t0 = 16 * mt + g;
+        S[mt][0][ql] = (t0 < nv) ? v0 : -INFINITY;
+        S[mt][1][ql] = (t0 + 8 < nv) ? v1 : -INFINITY;
       }
     }
   }
 
   // ---------------------------------------------------- online softmax
-  // This lane's tokens, chunk-relative: T0 = g, T1 = g+8, T2 = g+16, T3 = g+24.
-  float P[NT][4];
-  float alpha[NT];
+  // This lane's tokens, chunk-relative: T_k = g + 8k, k = 2 mt + row.
+  float P[2][4];
+  float alpha[2];
   bool rescale = false;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    float mx = fmaxf(fmaxf(S[0][0][nt], S[0][1][nt]), fmaxf(S[1][0][nt], S[1][1][nt]));
+  for (int ql = 0; ql < 2; ++ql) {
+    float mx = fmaxf(fmaxf(S[0][0][ql], S[0][1][ql]), fmaxf(S[1][0][ql], S[1][1][ql]));
     mx = fmaxf(mx, __shfl_xor_sync(FULLMASK, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(FULLMASK, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(FULLMASK, mx, 16));
-    const float m_new = fmaxf(st.m_run[nt], mx);
-    rescale |= (m_new > st.m_run[nt]);
-    alpha[nt] = (m_new == -INFINITY) ? 1.f : fast_exp2(st.m_run[nt] - m_new);
+    const float m_new = fmaxf(st.m_run[ql], mx);
+    rescale |= (m_new > st.m_run[ql]);
+    alpha[ql] = (m_new == -INFINITY) ? 1.f : fast_exp2(st.m_run[ql] - m_new);
     const float mref = (m_new == -INFINITY) ? 0.f : m_new;
-    st.m_run[nt] = m_new;
-    P[nt][0] = fast_exp2(S[0][0][nt] - mref);
-    P[nt][1] = fast_exp2(S[0][1][nt] - mref);
-    P[nt][2] = fast_exp2(S[1][0][nt] - mref);
-    P[nt][3] = fast_exp2(S[1][1][nt] - mref);
+    st.m_run[ql] = m_new;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) P[ql][k] = fast_exp2(S[k >> 1][k & 1][ql] - mref);
   }
   if (__any_sync(FULLMASK, rescale)) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      st.l_part[nt] *= alpha[nt];
+    for (int ql = 0; ql < 2; ++ql) {
+      st.l_part[ql] *= alpha[ql];
 #pragma unroll
-      for (int u = 0; u < GV; ++u) st.zacc[nt][u] *= alpha[nt];
+      for (int u = 0; u < GV; ++u) st.zacc[ql][u] *= alpha[ql];
     }
-    // running output column combo c + 4v belongs to query (c + 4v) / GV
+    // output column 8v + 2c + e is combo (query, group) = ((8v + 2c + e) / GV, % GV)
 #pragma unroll
-    for (int v = 0; v < NTV; ++v) {
-      float av;
-      if (GV == 1) {
-        av = alpha[v];
-      } else {
-        const int i = (c + 4 * v) / GV;
-        av = __shfl_sync(FULLMASK, alpha[0], i & 3);
-      }
+    for (int v = 0; v < NTV; ++v)
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        st.o_run[mt][0][v] *= av;
-        st.o_run[mt][1][v] *= av;
+      for (int e = 0; e < 2; ++e) {
+        float av;
+        if (GV == 1 && NTV == 1) {
+          av = alpha[e];
+        } else {
+          const int q = (8 * v + 2 * c + e) / GV;
+          const float a0 = __shfl_sync(FULLMASK, alpha[0], 4 * g + (q >> 1));
+          const float a1 = __shfl_sync(FULLMASK, alpha[1], 4 * g + (q >> 1));
+          av = (q & 1) ? a1 : a0;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          st.o_run[mt][0][v][e] *= av;
+          st.o_run[mt][1][v][e] *= av;
+        }
       }
-    }
   }
 
-  // ---------------------------------------------------- weights -> e4m3 hi/lo words
-  // Token-wise V (operand-fold): the fed weight of token t for channel group u is
-  // P_t * s_t,u scaled by 2^eP; channel-wise V: P_t * 2^7. The denominator and the
-  // value offsets are summed from the fed weights w_t (fed / scale).
+  // ---------------------------------------------------- weights -> fp16 words
+  // Token-wise V (operand-fold): fed weight P_t * s_t,u * 2^eP per channel group u;
+  // channel-wise V: P_t * 2^13. The denominator and value offsets are summed from
+  // the fed weights w_t = fed / scale; the PV accumulators start at -1024 * sum(fed)
+  // per column, which removes the magic bias of the V operand exactly.
   const int tok0 = rel0 + g;
-  uint32_t pw[NT][GV][2];
-  float inv_ps = 1.f;    // 2^-eP
-  float psum_chunk[NT];  // channel-wise V: sum of fed weights over the chunk
+  uint32_t pw[2][GV][2];  // [query][group][pair (T0,T1) / (T2,T3)]
+  float colb[2][GV];      // -1024 * sum of fed weights over the chunk (reduced)
+  float inv_ps = 1.f;
+  float psum[2];          // channel-wise V: sum of fed weights over the chunk (reduced)
   if (VL == 0) {
     float sv[GV][4];
     uint32_t smax = 0;
@@ -345,165 +366,189 @@ __device__ __forceinline__ void process_chunk(WarpState<C>& st, const ChunkSmem&
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const bool ok = FULL || (g + 8 * k < nv);
-        const __half h = sm.vs[(tok0 + 8 * k) * GV + u];
-        sv[u][k] = ok ? __half2float(h) : 0.f;
-        smax = max(smax, ok ? (uint32_t)(__half_as_ushort(h) & 0x7fffu) : 0u);
+        const __half hv = sm.vs[(tok0 + 8 * k) * GV + u];
+        sv[u][k] = ok ? __half2float(hv) : 0.f;
+        smax = max(smax, ok ? (uint32_t)(__half_as_ushort(hv) & 0x7fffu) : 0u);
       }
     smax = max(smax, __shfl_xor_sync(FULLMASK, smax, 4));
     smax = max(smax, __shfl_xor_sync(FULLMASK, smax, 8));
     smax = max(smax, __shfl_xor_sync(FULLMASK, smax, 16));
     const float smaxf = __half2float(__ushort_as_half((unsigned short)smax));
-    int e = 0;
-    if (smaxf > 0.f) e = min(100, max(-100, 7 - ilog2f(smaxf)));
-    const float ps = exp2i(e);
-    inv_ps = exp2i(-e);
-    float rs[GV][4];  // 2^-eP / s (unused when s == 0: the weight is then P itself)
+    int e2 = 0;
+    if (smaxf > 0.f) e2 = min(100, max(-100, 13 - ilog2f(smaxf)));
+    const float ps = exp2i(e2);
+    inv_ps = exp2i(-e2);
 #pragma unroll
-    for (int u = 0; u < GV; ++u)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) rs[u][k] = (sv[u][k] != 0.f) ? fast_rcp(sv[u][k]) * inv_ps : 0.f;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int ql = 0; ql < 2; ++ql) {
       float lsum = 0.f;
 #pragma unroll
       for (int u = 0; u < GV; ++u) {
-        float x[4], f[4];
+        float f[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) x[k] = P[nt][k] * sv[u][k] * ps;
-        uint32_t h01, l01, h23, l23;
-        split_e4m3_pair_fed(x[0], x[1], h01, l01, f[0], f[1]);
-        split_e4m3_pair_fed(x[2], x[3], h23, l23, f[2], f[3]);
-        pw[nt][u][0] = h01 | (h23 << 16);
-        pw[nt][u][1] = l01 | (l23 << 16);
-        float zt = 0.f;
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint32_t h2 = f16x2_from(P[ql][2 * kk] * sv[u][2 * kk] * ps, P[ql][2 * kk + 1] * sv[u][2 * kk + 1] * ps);
+          pw[ql][u][kk] = h2;
+          const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          f[2 * kk] = ff.x;
+          f[2 * kk + 1] = ff.y;
+        }
+        float zt = 0.f, fs = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float w = (sv[u][k] != 0.f) ? f[k] * rs[u][k] : P[nt][k];
+          const float w = (sv[u][k] != 0.f) ? f[k] * (fast_rcp(sv[u][k]) * inv_ps) : P[ql][k];
           const bool ok = FULL || (g + 8 * k < nv);
           const float zz = ok ? __half2float(sm.vz[(tok0 + 8 * k) * GV + u]) : 0.f;
           zt = fmaf(w, zz, zt);
+          fs += f[k];
           if (u == 0) lsum += w;
         }
-        st.zacc[nt][u] += zt;
+        st.zacc[ql][u] += zt;
+        fs += __shfl_xor_sync(FULLMASK, fs, 4);
+        fs += __shfl_xor_sync(FULLMASK, fs, 8);
+        fs += __shfl_xor_sync(FULLMASK, fs, 16);
+        colb[ql][u] = -kMagicF * fs;
       }
-      st.l_part[nt] += lsum;
+      st.l_part[ql] += lsum;
+      psum[ql] = 0.f;
     }
   } else {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float f[4];
-      uint32_t h01, l01, h23, l23;
-      split_e4m3_pair_fed(P[nt][0] * 128.f, P[nt][1] * 128.f, h01, l01, f[0], f[1]);
-      split_e4m3_pair_fed(P[nt][2] * 128.f, P[nt][3] * 128.f, h23, l23, f[2], f[3]);
-      pw[nt][0][0] = h01 | (h23 << 16);
-      pw[nt][0][1] = l01 | (l23 << 16);
-      float ps = ((f[0] + f[1]) + (f[2] + f[3])) * (1.f / 128.f);
-      st.l_part[nt] += ps;
-      ps += __shfl_xor_sync(FULLMASK, ps, 4);
-      ps += __shfl_xor_sync(FULLMASK, ps, 8);
-      ps += __shfl_xor_sync(FULLMASK, ps, 16);
-      psum_chunk[nt] = ps;
+    for (int ql = 0; ql < 2; ++ql) {
+      float fs = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t h2 = f16x2_from(P[ql][2 * kk] * 8192.f, P[ql][2 * kk + 1] * 8192.f);
+        pw[ql][0][kk] = h2;
+        const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        fs += ff.x + ff.y;
+      }
+      st.l_part[ql] += fs * (1.f / 8192.f);
+      fs += __shfl_xor_sync(FULLMASK, fs, 4);
+      fs += __shfl_xor_sync(FULLMASK, fs, 8);
+      fs += __shfl_xor_sync(FULLMASK, fs, 16);
+      psum[ql] = fs * (1.f / 8192.f);
+      colb[ql][0] = -kMagicF * fs;
     }
   }
 
-  // ---------------------------------------------------- PV B fragments
-  // Column n = 8v + g of n-tile v is combo (4v + g/2), part g&1; combo = query * GV +
-  // group. k-slot 4c + jj holds chunk token c + 8jj (reg0), k-slot 16 + 4c + jj holds
-  // token c + 4 + 8jj (reg1): the T0..T3 of lane 4*c' + (query & 3), c' = c or c + 4.
-  uint32_t pB[NTV][2];
+  // ---------------------------------------------------- PV B fragments and accumulator start
+  // B column n = g of n-tile v is combo 8v + g; k-slots 2c, 2c+1 of PV k-step kk hold
+  // chunk tokens c + 16kk and c + 8 + 16kk (the pair kk of lane 4c + q/2), and k-slots
+  // 2c+8, 2c+9 the same tokens of lane 4(c+4) + q/2.
+  uint32_t pB[NTV][2][2];  // [n-tile][kk][reg]
 #pragma unroll
   for (int v = 0; v < NTV; ++v) {
-    const int combo = 4 * v + (g >> 1);
-    const int i = combo / GV, u_need = combo % GV, part = g & 1;
-    const int src0 = 4 * c + (i & 3), src1 = 4 * (c + 4) + (i & 3);
-    const int ntq = (GV == 1) ? v : 0;  // query slot of the source lane
-    uint32_t b0 = 0, b1 = 0;
+    const int col = 8 * v + g;
+    const int q = col / GV, u_need = col % GV;
+    const int src0 = 4 * c + (q >> 1), src1 = 4 * (c + 4) + (q >> 1);
+    const bool live = q < hq;
 #pragma unroll
-    for (int u = 0; u < GV; ++u)
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t b0 = 0, b1 = 0;
 #pragma unroll
-      for (int pp = 0; pp < 2; ++pp) {
-        const uint32_t x0 = __shfl_sync(FULLMASK, pw[ntq][u][pp], src0);
-        const uint32_t x1 = __shfl_sync(FULLMASK, pw[ntq][u][pp], src1);
-        if (u == u_need && pp == part) {
-          b0 = x0;
-          b1 = x1;
+      for (int ql = 0; ql < 2; ++ql)
+#pragma unroll
+        for (int u = 0; u < GV; ++u) {
+          const uint32_t x0 = __shfl_sync(FULLMASK, pw[ql][u][kk], src0);
+          const uint32_t x1 = __shfl_sync(FULLMASK, pw[ql][u][kk], src1);
+          if (ql == (q & 1) && u == u_need) {
+            b0 = x0;
+            b1 = x1;
+          }
         }
-      }
-    const bool live = i < hq;
-    pB[v][0] = live ? b0 : 0u;
-    pB[v][1] = live ? b1 : 0u;
+      pB[v][kk][0] = live ? b0 : 0u;
+      pB[v][kk][1] = live ? b1 : 0u;
+    }
   }
+  float cb[NTV][2];  // starting value of output column 8v + 2c + e
+#pragma unroll
+  for (int v = 0; v < NTV; ++v)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      if (GV == 1 && NTV == 1) {
+        cb[v][e] = colb[e][0];
+      } else {
+        const int col = 8 * v + 2 * c + e;
+        const int q = col / GV, u_need = col % GV;
+        float x = 0.f;
+#pragma unroll
+        for (int ql = 0; ql < 2; ++ql)
+#pragma unroll
+          for (int u = 0; u < GV; ++u) {
+            const float y = __shfl_sync(FULLMASK, colb[ql][u], 4 * g + (q >> 1));
+            if (ql == (q & 1) && u == u_need) x = y;
+          }
+        cb[v][e] = x;
+      }
+    }
 
   // ---------------------------------------------------- PV
+  // Row half `row` of m-tile mt is channel 16g + 8row + mt (INT2) or
+  // 16g + 8(mt/4) + 4row + mt%4 (INT4), with factor v_mult(mt).
   float accv[8][NTV][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-    for (int v = 0; v < NTV; ++v)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) accv[mt][v][u] = 0.f;
-  if (BITS == 2) {
-    uint32_t wa[4], wb[4];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      wa[jj] = reinterpret_cast<const uint32_t*>(sm.vc + (rel0 + c + 8 * jj) * RB)[g];
-      wb[jj] = reinterpret_cast<const uint32_t*>(sm.vc + (rel0 + c + 4 + 8 * jj) * RB)[g];
+    for (int v = 0; v < NTV; ++v) {
+      accv[mt][v][0] = cb[v][0];
+      accv[mt][v][1] = cb[v][1];
+      accv[mt][v][2] = cb[v][0];
+      accv[mt][v][3] = cb[v][1];
     }
-    uint32_t ta[4], tb[4];
-    transpose4x4(wa[0], wa[1], wa[2], wa[3], ta);
-    transpose4x4(wb[0], wb[1], wb[2], wb[3], tb);
 #pragma unroll
-    for (int bb = 0; bb < 4; ++bb) {
-      const uint32_t a_p0 = ta[bb] & 0x03030303u, a_p1 = ta[bb] & 0x0C0C0C0Cu;
-      const uint32_t a_p2 = (ta[bb] >> 4) & 0x03030303u, a_p3 = (ta[bb] >> 4) & 0x0C0C0C0Cu;
-      const uint32_t b_p0 = tb[bb] & 0x03030303u, b_p1 = tb[bb] & 0x0C0C0C0Cu;
-      const uint32_t b_p2 = (tb[bb] >> 4) & 0x03030303u, b_p3 = (tb[bb] >> 4) & 0x0C0C0C0Cu;
+  for (int kk = 0; kk < 2; ++kk) {
+    const int tA = rel0 + c + 16 * kk, tB = tA + 4;
+    if (BITS == 2) {
+      const uint32_t wa0 = reinterpret_cast<const uint32_t*>(sm.vc + tA * RB)[g];
+      const uint32_t wa1 = reinterpret_cast<const uint32_t*>(sm.vc + (tA + 8) * RB)[g];
+      const uint32_t wb0 = reinterpret_cast<const uint32_t*>(sm.vc + tB * RB)[g];
+      const uint32_t wb1 = reinterpret_cast<const uint32_t*>(sm.vc + (tB + 8) * RB)[g];
+      const uint32_t xal = prmt(wa0, wa1, 0x5410), xah = prmt(wa0, wa1, 0x7632);
+      const uint32_t xbl = prmt(wb0, wb1, 0x5410), xbh = prmt(wb0, wb1, 0x7632);
+      const uint32_t sal = xal >> 10, sah = xah >> 10, sbl = xbl >> 10, sbh = xbh >> 10;
 #pragma unroll
-      for (int v = 0; v < NTV; ++v) {
-        mma_e4m3(accv[2 * bb][v], a_p0, a_p1, b_p0, b_p1, pB[v][0], pB[v][1]);
-        mma_e4m3(accv[2 * bb + 1][v], a_p2, a_p3, b_p2, b_p3, pB[v][0], pB[v][1]);
+      for (int mt = 0; mt < 8; ++mt) {
+        const uint32_t a0 = int2_half2(xal, sal, mt), a1 = int2_half2(xah, sah, mt);
+        const uint32_t a2 = int2_half2(xbl, sbl, mt), a3 = int2_half2(xbh, sbh, mt);
+#pragma unroll
+        for (int v = 0; v < NTV; ++v) mma_f16(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1]);
       }
-    }
-  } else {
-    uint2 wa[4], wb[4];
+    } else {
+      const uint2 wa0 = reinterpret_cast<const uint2*>(sm.vc + tA * RB)[g];
+      const uint2 wa1 = reinterpret_cast<const uint2*>(sm.vc + (tA + 8) * RB)[g];
+      const uint2 wb0 = reinterpret_cast<const uint2*>(sm.vc + tB * RB)[g];
+      const uint2 wb1 = reinterpret_cast<const uint2*>(sm.vc + (tB + 8) * RB)[g];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      wa[jj] = reinterpret_cast<const uint2*>(sm.vc + (rel0 + c + 8 * jj) * RB)[g];
-      wb[jj] = reinterpret_cast<const uint2*>(sm.vc + (rel0 + c + 4 + 8 * jj) * RB)[g];
-    }
+      for (int uu = 0; uu < 2; ++uu) {
+        const uint32_t ea0 = uu ? wa0.y : wa0.x, ea1 = uu ? wa1.y : wa1.x;
+        const uint32_t eb0 = uu ? wb0.y : wb0.x, eb1 = uu ? wb1.y : wb1.x;
+        const uint32_t xal = prmt(ea0, ea1, 0x5410), xah = prmt(ea0, ea1, 0x7632);
+        const uint32_t xbl = prmt(eb0, eb1, 0x5410), xbh = prmt(eb0, eb1, 0x7632);
+        const uint32_t sal = xal >> 8, sah = xah >> 8, sbl = xbl >> 8, sbh = xbh >> 8;
 #pragma unroll
-    for (int uu = 0; uu < 2; ++uu) {
-      uint32_t ta[4], tb[4];
-      if (uu == 0) {
-        transpose4x4(wa[0].x, wa[1].x, wa[2].x, wa[3].x, ta);
-        transpose4x4(wb[0].x, wb[1].x, wb[2].x, wb[3].x, tb);
-      } else {
-        transpose4x4(wa[0].y, wa[1].y, wa[2].y, wa[3].y, ta);
-        transpose4x4(wb[0].y, wb[1].y, wb[2].y, wb[3].y, tb);
-      }
+        for (int pp = 0; pp < 4; ++pp) {
+          const int mt = 4 * uu + pp;
+          const uint32_t a0 = int4_half2(xal, sal, pp), a1 = int4_half2(xah, sah, pp);
+          const uint32_t a2 = int4_half2(xbl, sbl, pp), a3 = int4_half2(xbh, sbh, pp);
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        const uint32_t a_lo = ta[bb] & 0x0F0F0F0Fu, a_hi = (ta[bb] >> 4) & 0x0F0F0F0Fu;
-        const uint32_t b_lo = tb[bb] & 0x0F0F0F0Fu, b_hi = (tb[bb] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-        for (int v = 0; v < NTV; ++v) mma_e4m3(accv[4 * uu + bb][v], a_lo, a_hi, b_lo, b_hi, pB[v][0], pB[v][1]);
+          for (int v = 0; v < NTV; ++v) mma_f16(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1]);
+        }
       }
     }
   }
 
   // ---------------------------------------------------- V fold into the running output
-  // Row half rh of m-tile mt is channel 16g + 2mt + rh; its e4m3 image carries a
-  // position factor 4 when BITS == 2 and rh == 1.
   if (VL == 0) {
-    const float f0 = 512.f * inv_ps;
-    const float f1 = (BITS == 2 ? 128.f : 512.f) * inv_ps;
 #pragma unroll
-    for (int v = 0; v < NTV; ++v)
+    for (int mt = 0; mt < 8; ++mt) {
+      const float f = inv_ps * (1.f / v_mult<BITS>(mt));
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        st.o_run[mt][0][v] = fmaf(accv[mt][v][0] + accv[mt][v][1], f0, st.o_run[mt][0][v]);
-        st.o_run[mt][1][v] = fmaf(accv[mt][v][2] + accv[mt][v][3], f1, st.o_run[mt][1][v]);
-      }
+      for (int v = 0; v < NTV; ++v)
+#pragma unroll
+        for (int row = 0; row < 2; ++row)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) st.o_run[mt][row][v][e] = fmaf(accv[mt][v][2 * row + e], f, st.o_run[mt][row][v][e]);
+    }
   } else {
     // acc-fold per token group: s_tau,d * (raw partial) + z_tau,d * sum_t w_t
     const int tau_rel = rel0 / C::G;
@@ -512,15 +557,13 @@ __device__ __forceinline__ void process_chunk(WarpState<C>& st, const ChunkSmem&
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-      for (int rh = 0; rh < 2; ++rh) {
-        const int ch = 16 * g + 2 * mt + rh;
-        const float s = __half2float(s_tau[ch]) * ((BITS == 2 && rh) ? 1.f : 4.f);
+      for (int row = 0; row < 2; ++row) {
+        const int ch = (BITS == 2) ? 16 * g + 8 * row + mt : 16 * g + 8 * (mt >> 2) + 4 * row + (mt & 3);
+        const float s = __half2float(s_tau[ch]) * (1.f / (8192.f * v_mult<BITS>(mt)));
         const float z = __half2float(z_tau[ch]);
 #pragma unroll
-        for (int v = 0; v < NTV; ++v) {
-          const float raw = accv[mt][v][2 * rh] + accv[mt][v][2 * rh + 1];
-          st.o_run[mt][rh][v] = fmaf(s, raw, fmaf(z, psum_chunk[v], st.o_run[mt][rh][v]));
-        }
+        for (int e = 0; e < 2; ++e)
+          st.o_run[mt][row][0][e] = fmaf(s, accv[mt][0][2 * row + e], fmaf(z, psum[e], st.o_run[mt][row][0][e]));
       }
   }
 }
@@ -530,7 +573,7 @@ __device__ __forceinline__ void process_chunk(WarpState<C>& st, const ChunkSmem&
 // ------------------------------------------------------------------------
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, NT = C::NT, GV = C::GV, NTV = C::NTV;
+  constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NTV = C::NTV;
   constexpr int RB = C::RB, D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -607,6 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
       sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
     named_sync(1, 32 * kConsumerWarps);
     if (warp < hq) {
+      // query exponent e: max |Q / factor| * 2^e in [2^13, 2^14), so Q * 2^e / factor is an
+      // exact fp16 (a bf16 has 8 significant bits); channel-group sums of Q for the K offset
       const int i = warp;
       float amax = 0.f;
       float gs = 0.f;
@@ -619,7 +664,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, o));
-      // channel-group sums of Q (token-wise K offset term): lanes of one group are contiguous
       constexpr int lanes_per_group = C::G / 4;  // 8, 16 or 32
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -627,53 +671,67 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
         if (o < lanes_per_group) gs += other;
       }
       int e = 0;
-      if (amax > 0.f) e = min(100, max(-100, 7 - ilog2f(amax)));
+      if (amax > 0.f) e = min(100, max(-100, 13 - ilog2f(amax)));
       if (lane == 0) {
         sEq[i] = e;
-        sAq[i] = p.sl2 * exp2i(9 - e);
+        sAq[i] = p.sl2 * exp2i(-e);
       }
       if (KL == 0 && (lane % lanes_per_group) == 0) sBz[i * 4 + lane / lanes_per_group] = p.sl2 * gs;
     }
     named_sync(1, 32 * kConsumerWarps);
 
     WarpState<C> st;
-    const int qi_b = g >> 1, qpart = g & 1;
     if (KL == 0) {
-      // token-wise K: the exact hi/lo split of Q * 2^e / position factor, fixed for the CTA
+      // token-wise K: B fragments Q' = Q 2^e / factor (exact fp16), fixed for the CTA, and
+      // the magic bias 1024 * sum of Q' per channel group
+      const int q = g;
+      const bool live = q < hq;
+      const float sc = live ? exp2i(sEq[q]) : 0.f;
+      float gsum[GK];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int i = 4 * nt + qi_b;
-        const bool live = i < hq;
-        const float sc = live ? exp2i(sEq[i]) : 0.f;
+      for (int u = 0; u < GK; ++u) gsum[u] = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
+      for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            float x[4];
+        for (int r = 0; r < 2; ++r) {
+          float x[2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int ch = qk_channel<BITS>(ks, 16 * r + 4 * c + j);
-              x[j] = live ? sQ[i * D + ch] * sc * (1.f / k_mult<BITS>(ch)) : 0.f;
-            }
-            st.qB[ks][nt][r] = pack_split4(x, qpart);
+          for (int e = 0; e < 2; ++e) {
+            const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
+            x[e] = live ? sQ[q * D + ch] * sc * (1.f / k_mult<BITS>(ch)) : 0.f;
           }
+          st.qB[ks][r] = f16x2_from(x[0], x[1]);
+          gsum[ks / C::KSG] += x[0] + x[1];
+        }
+#pragma unroll
+      for (int u = 0; u < GK; ++u) {
+        gsum[u] += __shfl_xor_sync(FULLMASK, gsum[u], 1);
+        gsum[u] += __shfl_xor_sync(FULLMASK, gsum[u], 2);
+      }
+#pragma unroll
+      for (int ql = 0; ql < 2; ++ql) {  // query 2c + ql is B column 2c + ql, held by lane 8c + 4ql
+        const int qq = min(2 * c + ql, hq - 1);
+        st.aq[ql] = sAq[qq];
+#pragma unroll
+        for (int u = 0; u < GK; ++u) {
+          st.c1[ql][u] = kMagicF * __shfl_sync(FULLMASK, gsum[u], 8 * c + 4 * ql);
+          st.bz[ql][u] = sBz[qq * 4 + u];
+        }
       }
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      st.qrow[nt] = min(c + 4 * nt, hq - 1);
-      st.sA[nt] = sAq[st.qrow[nt]];
-      st.m_run[nt] = -INFINITY;
-      st.l_part[nt] = 0.f;
+    for (int ql = 0; ql < 2; ++ql) {
+      st.m_run[ql] = -INFINITY;
+      st.l_part[ql] = 0.f;
 #pragma unroll
-      for (int u = 0; u < GV; ++u) st.zacc[nt][u] = 0.f;
+      for (int u = 0; u < GV; ++u) st.zacc[ql][u] = 0.f;
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-      for (int rh = 0; rh < 2; ++rh)
+      for (int row = 0; row < 2; ++row)
 #pragma unroll
-        for (int v = 0; v < NTV; ++v) st.o_run[mt][rh][v] = 0.f;
+        for (int v = 0; v < NTV; ++v) st.o_run[mt][row][v][0] = st.o_run[mt][row][v][1] = 0.f;
 
     const int quad = warp >> 2, sub = warp & 3;
     const int rel0 = kChunk * sub;  // chunk start inside a slot
@@ -692,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
       sm.vs = reinterpret_cast<const __half*>(slot + p.off_vs);
       sm.vz = reinterpret_cast<const __half*>(slot + p.off_vz);
       sm.sQ = sQ;
-      sm.sBz = sBz;
+      sm.sEq = sEq;
       const int tc = (j0 + j) * kSlotTokens + rel0;  // chunk start token
       const int nv = min(kChunk, L - tc);            // valid tokens in the chunk
       if (nv == kChunk)
@@ -714,50 +772,56 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
       float* sM = reinterpret_cast<float*>(ring);  // [warps][kMaxHq]
       float* sL = sM + kConsumerWarps * kMaxHq;    // [warps][kMaxHq]
       float* sO = sL + kConsumerWarps * kMaxHq;    // [warps][kMaxHq][D]
-      float zsum[NT][GV];
+      float zsum[2][GV];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float l = st.l_part[nt];
+      for (int ql = 0; ql < 2; ++ql) {
+        float l = st.l_part[ql];
         l += __shfl_xor_sync(FULLMASK, l, 4);
         l += __shfl_xor_sync(FULLMASK, l, 8);
         l += __shfl_xor_sync(FULLMASK, l, 16);
 #pragma unroll
         for (int u = 0; u < GV; ++u) {
-          float z = st.zacc[nt][u];
+          float z = st.zacc[ql][u];
           z += __shfl_xor_sync(FULLMASK, z, 4);
           z += __shfl_xor_sync(FULLMASK, z, 8);
           z += __shfl_xor_sync(FULLMASK, z, 16);
-          zsum[nt][u] = z;
+          zsum[ql][u] = z;
         }
-        const int i = c + 4 * nt;
+        const int i = 2 * c + ql;
         if (g == 0 && i < hq) {
-          sM[warp * kMaxHq + i] = st.m_run[nt];
+          sM[warp * kMaxHq + i] = st.m_run[ql];
           sL[warp * kMaxHq + i] = l;
         }
       }
+      // output column 8v + 2c + e is (query, group) = (col / GV, col % GV); its channels are
+      // this lane's 16, all in channel group 16g / G
+      const int u_lane = (16 * g) / C::G;
 #pragma unroll
-      for (int v = 0; v < NTV; ++v) {
-        const int combo = c + 4 * v;
-        const int i = combo / GV, u = combo % GV;
-        // the value-offset term of (query i, group u) lives on the S lanes of query i
-        float zt = 0.f;
-        if (VL == 0) {
-          const int ntq = (GV == 1) ? v : 0;
+      for (int v = 0; v < NTV; ++v)
 #pragma unroll
-          for (int uu = 0; uu < GV; ++uu) {
-            const float x = __shfl_sync(FULLMASK, zsum[ntq][uu], i & 3);
-            if (uu == u) zt = x;
+        for (int e = 0; e < 2; ++e) {
+          const int col = 8 * v + 2 * c + e;
+          const int i = col / GV, u = col % GV;
+          float zt = 0.f;
+          if (VL == 0) {  // the value-offset term of (query i, group u) lives on lane i/2
+#pragma unroll
+            for (int ql = 0; ql < 2; ++ql)
+#pragma unroll
+              for (int uu = 0; uu < GV; ++uu) {
+                const float x = __shfl_sync(FULLMASK, zsum[ql][uu], i >> 1);
+                if (ql == (i & 1) && uu == u) zt = x;
+              }
+          }
+          if (i < hq && (GV == 1 || u == u_lane)) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+              for (int row = 0; row < 2; ++row) {
+                const int ch = (BITS == 2) ? 16 * g + 8 * row + mt : 16 * g + 8 * (mt >> 2) + 4 * row + (mt & 3);
+                sO[(warp * kMaxHq + i) * D + ch] = st.o_run[mt][row][v][e] + zt;
+              }
           }
         }
-        const bool mine = (i < hq) && (GV == 1 || (16 * g) / (kHeadDim / GV) == u);
-        if (mine) {
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-            for (int rh = 0; rh < 2; ++rh)
-              sO[(warp * kMaxHq + i) * D + 16 * g + 2 * mt + rh] = st.o_run[mt][rh][v] + zt;
-        }
-      }
     }
   }
 

@@ -4,18 +4,17 @@
 
 namespace lbkv {
 
-DecodeKernel decode_kernel_int2_k1(int vl, int nt, int log2g) {
-#define LBKV_PICK(VL, NT, LG) \
-  if (vl == VL && nt == NT && log2g == LG) return &split_decode_kernel<Cfg<2, 1, VL, NT, LG>>;
+DecodeKernel decode_kernel_int2_k1(int vl, int ntv, int log2g) {
+#define LBKV_PICK(VL, NTV, LG) \
+  if (vl == VL && ntv == NTV && log2g == LG) return &split_decode_kernel<Cfg<2, 1, VL, NTV, LG>>;
   LBKV_PICK(0, 1, 7)
-  LBKV_PICK(0, 2, 7)
   LBKV_PICK(0, 1, 6)
+  LBKV_PICK(0, 2, 6)
+  LBKV_PICK(0, 1, 5)
+  LBKV_PICK(0, 2, 5)
   LBKV_PICK(1, 1, 7)
-  LBKV_PICK(1, 2, 7)
   LBKV_PICK(1, 1, 6)
-  LBKV_PICK(1, 2, 6)
   LBKV_PICK(1, 1, 5)
-  LBKV_PICK(1, 2, 5)
 #undef LBKV_PICK
   return nullptr;
 }

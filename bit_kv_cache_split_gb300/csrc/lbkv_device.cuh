@@ -111,6 +111,36 @@ __device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D[16x8] += A[16x16] * B[16x8], fp16 inputs, fp32 accumulators.
+// Fragments (lane = 4*g + c): A reg0 row g k 2c,2c+1; reg1 row g+8 k 2c,2c+1;
+// reg2 row g k 2c+8,2c+9; reg3 row g+8 k 2c+8,2c+9 (low half = lower k);
+// B reg0 k 2c,2c+1 col g; reg1 k 2c+8,2c+9 col g; D as for the e4m3 form.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// fp16 magic number 1024: OR-ing a small integer m into its mantissa gives the
+// fp16 value 1024 + m exactly (m < 1024), two lanes at a time.
+constexpr uint32_t kMagic2 = 0x64006400u;
+constexpr float kMagicF = 1024.f;
+
+// (a & b) | c in one LOP3.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t f16x2_from(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ------------------------------------------------------------ conversions
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;

@@ -19,11 +19,11 @@ int launch_pack(const PackArgs& a, cudaStream_t stream);
 
 using DecodeKernel = void (*)(const DecodeParams);
 
-// Instantiated kernel for (v_layout, query n-tiles, log2 group) of one bit width and
+// Instantiated kernel for (v_layout, PV n-tiles, log2 group) of one bit width and
 // K layout, or nullptr when that combination is not built.
-DecodeKernel decode_kernel_int2_k0(int vl, int nt, int log2g);
-DecodeKernel decode_kernel_int2_k1(int vl, int nt, int log2g);
-DecodeKernel decode_kernel_int4_k0(int vl, int nt, int log2g);
-DecodeKernel decode_kernel_int4_k1(int vl, int nt, int log2g);
+DecodeKernel decode_kernel_int2_k0(int vl, int ntv, int log2g);
+DecodeKernel decode_kernel_int2_k1(int vl, int ntv, int log2g);
+DecodeKernel decode_kernel_int4_k0(int vl, int ntv, int log2g);
+DecodeKernel decode_kernel_int4_k1(int vl, int ntv, int log2g);
 
 }  // namespace lbkv

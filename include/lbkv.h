@@ -111,11 +111,12 @@ LBKV_API size_t lbkv_workspace_bytes(const lbkv_desc* desc, int bits, int k_layo
  *   (a divisor of head_dim for a token-wise side, a token count for a
  *   channel-wise side).
  * Supported: every combination of bits, layouts and group above with
- *   Hq/Hkv in {1, 2, 4, 8}, except on a token-wise V side group 32, and
- *   group 64 with Hq/Hkv = 8 (LBKV_EUNSUPPORTED).
- * Precision: tensor-core products on exact e4m3 images of the codes; the query
- * and the softmax weights enter as an exact-or-nearly-exact sum of two e4m3
- * parts; accumulation and every fold step in fp32; output rounded to bf16.
+ *   Hq/Hkv in {1, 2, 4, 8}, except a token-wise V side with group 32 and
+ *   Hq/Hkv = 8 (LBKV_EUNSUPPORTED).
+ * Precision: tensor-core products on exact fp16 images of the codes; the bf16
+ * query enters exactly (fp16; rounded to fp16 after a channel-wise K scale
+ * multiplies it) and the softmax weights as fp16; accumulation and every fold
+ * step in fp32; output rounded to bf16.
  * Errors: LBKV_EINVAL / LBKV_EALIGN / LBKV_EUNSUPPORTED / LBKV_EWORKSPACE before
  * any launch; LBKV_ECUDA on a launch failure. A sequence with no cached and no
  * window tokens yields a zero output row. */

@@ -90,14 +90,14 @@ def test_gqa_ratios(lbkv, bits, hq):
 @pytest.mark.parametrize("g", [32, 64])
 @pytest.mark.parametrize("kl,vl", [(0, 1), (1, 1), (1, 0), (0, 0)])
 def test_group_sizes(lbkv, bits, g, kl, vl):
-    if vl == 0 and g == 32:
-        pytest.skip("token-wise V with four channel groups is not supported")
     check(lbkv, _wl(bits, kl, vl, g=g, lens=(513, 95), seed=g + bits))
 
 
-@pytest.mark.parametrize("hq", [1, 2, 4])
-def test_tokenwise_v_two_groups_all_gqa(lbkv, hq):
-    check(lbkv, _wl(2, 0, 0, g=64, hq=hq, lens=(400,), seed=7))
+@pytest.mark.parametrize("g,hq", [(64, 1), (64, 2), (64, 4), (64, 8), (32, 1), (32, 2), (32, 4)])
+@pytest.mark.parametrize("kl", [0, 1])
+def test_tokenwise_v_channel_groups_all_gqa(lbkv, g, hq, kl):
+    """Token-wise V with 2 or 4 value channel groups: (query, group) output columns."""
+    check(lbkv, _wl(2, kl, 0, g=g, hq=hq, lens=(400, 37), seed=7 + hq))
 
 
 def test_window(lbkv):
@@ -143,7 +143,9 @@ def test_repeat_calls_are_bitwise_identical(lbkv):
 
 
 def test_unsupported_combination_raises(lbkv):
-    wl = _wl(2, 0, 0, g=32, lens=(10,))
+    """Token-wise V with 4 channel groups and 8 query heads per KV head: 32 output
+    column pairs, more than the kernel's two n-tiles hold."""
+    wl = _wl(2, 0, 0, g=32, hq=8, lens=(10,))
     t = {k: v.cuda() for k, v in inputs.generate(wl, "cpu").items()}
     with pytest.raises(lbkv.LbkvError) as e:
         lbkv.decode_attn(t["q"], t["k_codes"], t["k_scale"], t["k_off"], t["v_codes"], t["v_scale"], t["v_off"],
@@ -229,7 +231,5 @@ def test_mixed_layouts_ragged_sampled(lbkv, bits, kl, vl):
 @pytest.mark.parametrize("g,hq", [(128, 4), (64, 2), (128, 8), (32, 1)])
 def test_long_context_window_sampled(lbkv, g, hq):
     """100,000-token context: 99,872 INT2 tokens + a 128-token bf16 window."""
-    if g == 32:
-        pytest.skip("token-wise V with four channel groups is not supported")
     wl = inputs.long_context(1, group=g, hq_per_kv=hq)
     sampled_parity(lbkv, wl, [(0, 0), (0, wl.num_kv_heads - 1)])
