@@ -55,9 +55,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 struct Plan {
-  int hq, nt, gv;
-  int splits, s_tot, slots_per_split;
-  int n_ring, slot_bytes, slot_tx, smem_bytes;
+  int hq, mode, gv;
+  int splits, s_tot, items_per_split, unit_tokens;
+  int ring_per_warp, entry_bytes, entry_tx, smem_bytes;
   int off_vc, off_ks, off_kz, off_vs, off_vz, sz_k, sz_v;
   size_t off_done, off_ml, off_o, ws_bytes;
 };
@@ -84,43 +84,47 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   // holds at most two PV n-tiles of 8 columns.
   const int groups_v = (vl == LBKV_TOKENWISE) ? kHeadDim / group : 1;
   pl->gv = groups_v;
-  pl->nt = (hq * groups_v + 7) / 8;
-  if (pl->nt > 2) return LBKV_EUNSUPPORTED;
+  pl->mode = decode_mode(hq * groups_v);
+  if (pl->mode < 0) return LBKV_EUNSUPPORTED;
 
   int sms = 0, smem_optin = 0;
   int st = current_device_props(&sms, &smem_optin);
   if (st) return st;
 
-  // ring slot: K codes | V codes | K scale | K offset | V scale | V offset
+  // ring entry (one item of `ut` tokens): K codes | V codes | K scale | K offset | V scale | V offset
+  const int ut = kChunk * unit_chunks(bits, pl->mode);
   const int rb = kHeadDim * bits / 8;
-  pl->sz_k = (kl == LBKV_TOKENWISE) ? kSlotTokens * (kHeadDim / group) * 2 : (kSlotTokens / group) * kHeadDim * 2;
-  pl->sz_v = (vl == LBKV_TOKENWISE) ? kSlotTokens * (kHeadDim / group) * 2 : (kSlotTokens / group) * kHeadDim * 2;
-  pl->off_vc = kSlotTokens * rb;
-  pl->off_ks = 2 * kSlotTokens * rb;
+  const int cw_rows = ut >= group ? ut / group : 1;  // channel-wise s/z rows an item touches
+  pl->unit_tokens = ut;
+  pl->sz_k = (kl == LBKV_TOKENWISE) ? ut * (kHeadDim / group) * 2 : cw_rows * kHeadDim * 2;
+  pl->sz_v = (vl == LBKV_TOKENWISE) ? ut * (kHeadDim / group) * 2 : cw_rows * kHeadDim * 2;
+  pl->off_vc = ut * rb;
+  pl->off_ks = 2 * ut * rb;
   pl->off_kz = pl->off_ks + pl->sz_k;
   pl->off_vs = pl->off_kz + pl->sz_k;
   pl->off_vz = pl->off_vs + pl->sz_v;
-  pl->slot_tx = pl->off_vz + pl->sz_v;
-  pl->slot_bytes = (int)round_up((size_t)pl->slot_tx, 128);
+  pl->entry_tx = pl->off_vz + pl->sz_v;
+  pl->entry_bytes = (int)round_up((size_t)pl->entry_tx, 128);
   const int budget = smem_optin - kRingOffset;
-  int n_ring = budget / pl->slot_bytes;
-  if (n_ring > kMaxRing) n_ring = kMaxRing;
-  n_ring -= n_ring % kQuads;
-  if (n_ring < 2 * kQuads || (size_t)n_ring * pl->slot_bytes < (size_t)kMergeBytes) return LBKV_EUNSUPPORTED;
-  pl->n_ring = n_ring;
-  pl->smem_bytes = kRingOffset + n_ring * pl->slot_bytes;
+  int r_w = budget / (kConsumerWarps * pl->entry_bytes);
+  if (r_w > kMaxRing / kConsumerWarps) r_w = kMaxRing / kConsumerWarps;
+  if (r_w < 1 || (size_t)kConsumerWarps * r_w * pl->entry_bytes < (size_t)kMergeBytes) return LBKV_EUNSUPPORTED;
+  pl->ring_per_warp = r_w;
+  pl->smem_bytes = kRingOffset + kConsumerWarps * r_w * pl->entry_bytes;
 
-  // Split count: minimise waves * (slots per CTA + fill), one CTA per SM.
+  // Split count: minimise waves * (items per warp + fill), one CTA per SM; time in
+  // units of one warp's 128-token item.
   const long long units = (long long)d->batch * d->num_kv_heads;
-  const int spu = d->max_seq_len / kSlotTokens;
+  const int ipu = d->max_seq_len / ut;  // items per (sequence, KV head)
   int best_s = 1;
   double best_cost = 1e300;
   if (units > 0) {
-    const int s_max = spu < 64 ? spu : 64;
+    const int s_max = ipu < 64 ? ipu : 64;
     for (int s = 1; s <= s_max; ++s) {
       const long long ctas = units * s;
       const double waves = std::ceil((double)ctas / sms);
-      const double per = std::ceil((double)spu / s) + 3.0;
+      const int ips = (ipu + s - 1) / s;
+      const double per = std::ceil((double)ips / kConsumerWarps) * ut / 128.0 + 2.0;
       const double cost = waves * per;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
@@ -129,7 +133,7 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
     }
   }
   pl->splits = best_s;
-  pl->slots_per_split = (spu + best_s - 1) / best_s;
+  pl->items_per_split = (ipu + best_s - 1) / best_s;
   pl->s_tot = best_s + (win ? 1 : 0);
 
   // workspace: status word | per-unit split counters | (m, l) partials | O partials
@@ -141,10 +145,14 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   return LBKV_OK;
 }
 
-DecodeKernel pick_kernel(int bits, int kl, int vl, int ntv, int group) {
-  const int log2g = group == 128 ? 7 : group == 64 ? 6 : 5;
-  if (bits == 2) return kl ? decode_kernel_int2_k1(vl, ntv, log2g) : decode_kernel_int2_k0(vl, ntv, log2g);
-  return kl ? decode_kernel_int4_k1(vl, ntv, log2g) : decode_kernel_int4_k0(vl, ntv, log2g);
+DecodeKernel pick_kernel(int bits, int kl, int vl, int mode, int group) {
+  const int lg = group == 128 ? 7 : group == 64 ? 6 : 5;
+  if (bits == 2) {
+    if (kl == 0) return vl ? decode_kernel<2, 0, 1>(mode, lg) : decode_kernel<2, 0, 0>(mode, lg);
+    return vl ? decode_kernel<2, 1, 1>(mode, lg) : decode_kernel<2, 1, 0>(mode, lg);
+  }
+  if (kl == 0) return vl ? decode_kernel<4, 0, 1>(mode, lg) : decode_kernel<4, 0, 0>(mode, lg);
+  return vl ? decode_kernel<4, 1, 1>(mode, lg) : decode_kernel<4, 1, 0>(mode, lg);
 }
 
 }  // namespace
@@ -173,7 +181,7 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   if (desc->k_win && (!aligned16(desc->k_win) || !aligned16(desc->v_win))) return LBKV_EALIGN;
   if (!desc->workspace || desc->workspace_bytes < pl.ws_bytes) return LBKV_EWORKSPACE;
   if (reinterpret_cast<uintptr_t>(desc->workspace) & 255u) return LBKV_EALIGN;
-  DecodeKernel kern = pick_kernel(bits, k_layout, v_layout, pl.nt, group);
+  DecodeKernel kern = pick_kernel(bits, k_layout, v_layout, pl.mode, group);
   if (!kern) return LBKV_EUNSUPPORTED;
 
   uint8_t* ws = static_cast<uint8_t*>(desc->workspace);
@@ -204,10 +212,10 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.sl2 = sigma * 1.4426950408889634f;
   p.splits = pl.splits;
   p.s_tot = pl.s_tot;
-  p.slots_per_split = pl.slots_per_split;
-  p.n_ring = pl.n_ring;
-  p.slot_bytes = pl.slot_bytes;
-  p.slot_tx = pl.slot_tx;
+  p.items_per_split = pl.items_per_split;
+  p.ring_per_warp = pl.ring_per_warp;
+  p.entry_bytes = pl.entry_bytes;
+  p.entry_tx = pl.entry_tx;
   p.off_vc = pl.off_vc;
   p.off_ks = pl.off_ks;
   p.off_kz = pl.off_kz;

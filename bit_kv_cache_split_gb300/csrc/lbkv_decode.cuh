@@ -10,30 +10,36 @@
 // group boundary) and fold table (token-wise K: acc-fold, channel-wise K:
 // operand-fold on Q, token-wise V: operand-fold on P, channel-wise V: acc-fold).
 //
-// Kernel design (sm_103a). One CTA per (sequence, KV head, split) streams
-// its 128-token slots of packed codes and fp16 scales/offsets through a ring
-// in shared memory with 1-D bulk copies issued by a producer warp (mbarrier
-// full/empty pairs, bounded waits, no multicast). The consumer warps form
-// quads; the quads own the ring slots in turn and each warp of a quad takes a
-// 32-token chunk of the slot with its own online-softmax state. The CTA then
-// merges its warps into one split partial, and the last split of a
-// (sequence, KV head) to finish merges all splits into the bf16 output.
+// Kernel design (sm_103a). One CTA per (sequence, KV head, split); the split's
+// tokens form items of 32, 64 or 128 tokens dealt to the 8 warps in turn. Each
+// warp streams its items' packed codes and fp16 scales/offsets through its own
+// ring in shared memory with 1-D bulk copies that it issues itself (an mbarrier
+// per entry, bounded waits, no multicast), so no warp waits on another's
+// progress. Per item a warp scores all its tokens (QK^T with the K fold),
+// updates its running maximum once, then forms the weights and accumulates PV
+// chunk by chunk with the V fold. The CTA then merges its warps into one split
+// partial, and the last split of a (sequence, KV head) to finish merges all
+// splits into the bf16 output.
 //
 // Operands. OR-ing a code q (times a power-of-two position factor m) into the
 // mantissa of the fp16 magic number 1024 gives the exact fp16 value 1024 + m q,
 // two codes per LOP3; the factor 1/m is folded into the other operand and the
-// bias 1024 is cancelled inside the tensor core by starting each accumulator at
-// -1024 * (sum of the other operand as fed). The bf16 query is exact in fp16;
-// the softmax weights are fed as fp16 (11 bits), and the running denominator
-// and the value offsets are summed from the weights actually fed, so the result
-// is an exact attention under the fed weights. Both products run on mma.sync
-// m16n8k16 fp16 with fp32 accumulators (on sm_103 this is a native tensor-core
-// instruction; the e4m3 form is not, it converts its operands to fp16 first):
+// bias 1024 * (sum of the other operand as fed) is removed inside the fp32
+// accumulator: each accumulator starts at (or, continuing, is lowered by) minus
+// the bias of the operands it is about to take, so it never holds more than one
+// 32-token chunk's (PV) or one channel group's (QK^T) bias.
+// The bf16 query is exact in fp16; the softmax weights are fed as fp16.
+// Both products run on mma.sync m16n8k16 fp16 with fp32 accumulators (native
+// on sm_103; the e4m3 form of mma.sync converts its operands to fp16 first):
 //   QK^T: rows = 16 tokens, k = 16 channels, cols = queries;
-//   PV:   rows = 16 channels, k = 16 tokens, cols = (query[, channel group]).
+//   PV:   rows = 16 channels, k = 16 tokens, cols = (query, V channel group).
+//
+// Columns. The (query, V channel group) pairs of one KV head ("combos";
+// hq * GV of them, GV = channel groups of a token-wise V side, else 1) sit on
+// the 8 columns of the tiles in one of three modes: up to 4 combos, each on
+// two adjacent columns (a lane then handles one combo); 8 combos, one per
+// column; 16 combos on two PV n-tiles.
 #pragma once
-
-#include <type_traits>
 
 #include "lbkv_device.cuh"
 
@@ -45,18 +51,29 @@ namespace lbkv {
 
 constexpr int kHeadDim = 128;
 constexpr int kSlotTokens = 128;
-constexpr int kChunk = 32;  // tokens per consumer warp step
+constexpr int kChunk = 32;  // tokens of one QK^T / PV tile pass
 constexpr int kConsumerWarps = LBKV_CONSUMER_WARPS;
-static_assert(kConsumerWarps % 4 == 0, "consumer warps come in quads");
-constexpr int kQuads = kConsumerWarps / 4;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kMaxRing = 48;
+constexpr int kThreads = 32 * kConsumerWarps;
+constexpr int kMaxRing = 48;  // ring entries of all warps (one mbarrier each)
 constexpr int kMaxHq = 8;
-// shared-memory map: barriers | Q (fp32) and per-query constants | ring
-constexpr int kBarBytes = 2 * kMaxRing * 8;
+// shared-memory map: barriers | Q (fp32) and per-query constants | rings
+constexpr int kBarBytes = kMaxRing * 8;
 constexpr int kRingOffset = 8192;
 static_assert(kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq) <= kRingOffset, "prologue fits");
 constexpr int kMergeBytes = kConsumerWarps * kMaxHq * (kHeadDim + 2) * 4;
+
+constexpr int kModeDup = 0;   // <= 4 combos: combo k on columns 2k, 2k+1
+constexpr int kModePair = 1;  // 8 combos: combo k on column k
+constexpr int kModeWide = 2;  // 16 combos: combo k on column k % 8 of PV n-tile k / 8
+
+__host__ __device__ constexpr int decode_mode(int combos) {
+  return combos <= 4 ? kModeDup : combos == 8 ? kModePair : combos == 16 ? kModeWide : -1;
+}
+// 32-token chunks per item: 4 (128 tokens) where two ring entries per warp fit and
+// the registers allow it, else fewer.
+__host__ __device__ constexpr int unit_chunks(int bits, int mode) {
+  return mode == kModeWide ? 1 : bits == 2 ? 4 : 2;
+}
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -77,24 +94,55 @@ struct DecodeParams {
   __nv_bfloat16* out;
   int B, Hq, Hkv, hq, T_cap, win_cap;
   float sl2;  // softmax scale times log2(e)
-  int splits, s_tot, slots_per_split;
-  int n_ring, slot_bytes, slot_tx;
-  int off_vc, off_ks, off_kz, off_vs, off_vz;  // byte offsets inside a slot
-  int sz_k_bytes, sz_v_bytes;                  // bytes of one scale (or offset) array per slot
+  int splits, s_tot, items_per_split;
+  int ring_per_warp, entry_bytes, entry_tx;
+  int off_vc, off_ks, off_kz, off_vs, off_vz;  // byte offsets inside a ring entry
+  int sz_k_bytes, sz_v_bytes;                  // bytes of one scale (or offset) array per entry
 };
 
 // Compile-time shape of one kernel variant.
-template <int BITS_, int KL_, int VL_, int NTV_, int LOG2G_>
+template <int BITS_, int KL_, int VL_, int MODE_, int LOG2G_>
 struct Cfg {
-  static constexpr int BITS = BITS_, KL = KL_, VL = VL_, NTV = NTV_;
+  static constexpr int BITS = BITS_, KL = KL_, VL = VL_, MODE = MODE_;
   static constexpr int G = 1 << LOG2G_;                    // group size
   static constexpr int GK = (KL == 0) ? kHeadDim / G : 1;  // K channel groups per token
   static constexpr int GV = (VL == 0) ? kHeadDim / G : 1;  // V channel groups per token
   static constexpr int KSG = G / 16;                       // QK k-steps per K channel group
   static constexpr int RB = kHeadDim * BITS / 8;           // bytes per token row of codes
-  static_assert(NTV >= 1 && NTV <= 2, "one or two PV n-tiles");
+  static constexpr bool DUP = (MODE == kModeDup);
+  static constexpr int NTV = (MODE == kModeWide) ? 2 : 1;  // PV n-tiles
+  // query slots per lane (QK^T accumulator columns 2c + j); owned combos per lane
+  static constexpr int NQ = (MODE == kModeWide || (MODE == kModePair && GV == 1)) ? 2 : 1;
+  static constexpr int NO = DUP ? 1 : 2 * NTV;
+  static constexpr int NCH = unit_chunks(BITS, MODE);  // chunks per item
+  static constexpr int UNIT = kChunk * NCH;             // tokens per item
   static_assert(G >= kChunk, "a chunk never straddles a token group");
+  static_assert(MODE != kModeWide || GV >= 2, "16 combos need several V channel groups");
 };
+
+// Query carried by QK^T column n, or -1 when the column carries no combo.
+template <class C>
+__device__ __forceinline__ int qk_query(int n, int hq) {
+  if (C::DUP) {
+    const int k = n >> 1;
+    return k < hq * C::GV ? k / C::GV : -1;
+  }
+  if (C::MODE == kModePair) return n / C::GV;
+  return (8 * (n & 1) + 2 * (n >> 1)) / C::GV;
+}
+// Owned combo o of lane c: its combo index, query slot and V channel group.
+template <class C>
+__device__ __forceinline__ int own_combo(int c, int o) {
+  return C::DUP ? c : 8 * (o >> 1) + 2 * c + (o & 1);
+}
+template <class C>
+__host__ __device__ constexpr int own_slot(int o) {
+  return C::MODE == kModeWide ? (o >> 1) : (C::NQ == 2 ? o : 0);
+}
+template <class C>
+__device__ __forceinline__ int own_group(int c, int o) {
+  return C::DUP ? c % C::GV : (2 * c + (o & 1)) % C::GV;
+}
 
 // Channel fed at k-slot kappa (0..15) of QK^T k-step ks (0..7); see the K operand build.
 template <int BITS>
@@ -115,6 +163,11 @@ template <int BITS>
 __host__ __device__ constexpr float v_mult(int mt) {
   return BITS == 2 ? (float)(1 << (2 * (mt <= 4 ? mt : mt - 5))) : ((mt & 1) ? 16.f : 1.f);
 }
+// Offset, among the 16 channels 16g..16g+15 of a lane, of PV row half `row` of m-tile mt.
+template <int BITS>
+__host__ __device__ constexpr int pv_channel(int mt, int row) {
+  return BITS == 2 ? 8 * row + mt : 8 * (mt >> 2) + 4 * row + (mt & 3);
+}
 
 // fp16 images (1024 + factor * code) of position p of an 8-code (INT2) or 4-code
 // (INT4) group of two 16-bit halves: one LOP3 (plus a shared shift).
@@ -126,383 +179,209 @@ __device__ __forceinline__ uint32_t int4_half2(uint32_t x, uint32_t xs8, int p) 
   return and_or(src, (p & 1) ? 0x00F000F0u : 0x000F000Fu, kMagic2);
 }
 
-// Per-warp state, held in registers. Each lane scores queries 2c and 2c+1.
+__device__ __forceinline__ float2 half2_to_float2(uint32_t h2) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// Per-warp state, held in registers.
 template <class C>
 struct WarpState {
-  uint32_t qB[8][2];      // QK^T B fragments (fp16 pairs of Q' = Q 2^e / factor)
-  float c1[2][C::GK];     // token-wise K: 1024 * sum of Q' over a channel group (magic bias)
-  float aq[2];            // token-wise K: sigma log2(e) 2^-e
-  float bz[2][C::GK];     // token-wise K: sigma log2(e) sum of Q over a channel group
-  float m_run[2], l_part[2], zacc[2][C::GV];
-  float o_run[8][2][C::NTV][2];  // [m-tile][row half][n-tile][column]
+  uint32_t qB[8][2];         // QK^T B fragments of this lane's column (token-wise K)
+  float kbias[2][C::GK];     // token-wise K: -1024 * sum of Q' per group, accumulator columns 2c, 2c+1
+  float pa[C::NQ];           // token-wise K: sigma log2(e) 2^-e (scores are kept in units of it); else 1
+  float bzq[C::NQ][C::GK];   // token-wise K: 2^e * sum of Q over a channel group
+  float m_run[C::NQ], l[C::NQ];
+  float zacc[C::NO];         // token-wise V: sum_t P_t z_t per owned combo
+  float o_run[8][2][C::NQ];  // [m-tile][row half][live column]
 };
 
-// Everything one chunk of 32 tokens needs from shared memory.
-struct ChunkSmem {
+// Shared-memory view of one ring entry.
+struct SlotSmem {
   const uint8_t* kc;
   const uint8_t* vc;
   const __half* ks;
   const __half* kz;
   const __half* vs;
   const __half* vz;
-  const float* sQ;
-  const int* sEq;
 };
 
-// One 32-token chunk: QK^T with the K fold, online softmax, weights, PV with the
-// V fold. FULL: all 32 tokens valid (no masking).
-template <class C, bool FULL>
-__device__ __forceinline__ void process_chunk(WarpState<C>& st, const ChunkSmem& sm, int rel0, int nv, int hq,
-                                              float sl2, int lane) {
-  constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NTV = C::NTV;
-  constexpr int RB = C::RB, D = kHeadDim;
+// Per-lane constants of the column layout.
+struct LaneCols {
+  int g, c, lane, hq, u_lane;
+  int e_live;  // GV >= 2: accumulator column (0/1) of an owned pair whose V group is u_lane, or -1
+};
+
+// Channel-wise K: Q' = Q * s_tau / factor scaled by 2^e2 into exact fp16 for the
+// token group tau whose s/z rows are s_tau/z_tau; the offset becomes sum_d Q_d z_tau,d
+// (one constant per query and group, added before the softmax).
+template <class C>
+__device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)[C::NQ], float (&cwB)[C::NQ],
+                                              float (&cwneg)[2], const __half* s_tau, const __half* z_tau,
+                                              const float* sQ, float sl2, const LaneCols& lc) {
+  constexpr int BITS = C::BITS, D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
-  const int g = lane >> 2, c = lane & 3;
-
-  // ---------------------------------------------------- channel-wise K: Q' per token group
-  // Operand-fold: Q' = Q * s_tau / factor, scaled by 2^e into fp16; the offset becomes
-  // sum_d Q_d z_tau,d, one constant per (query, token group), added before the softmax.
-  float cwA[2] = {0.f, 0.f}, cwB[2] = {0.f, 0.f}, cwC[2] = {0.f, 0.f};
-  if (KL == 1) {
-    const int tau_rel = rel0 / C::G;
-    const __half* s_tau = sm.ks + tau_rel * D;
-    const __half* z_tau = sm.kz + tau_rel * D;
-    const int q = g;  // this lane's B column
-    const bool live = q < hq;
-    float x[8][2][2];
-    float amax = 0.f, zsum = 0.f;
+  const int c = lc.c;
+  const int qb = qk_query<C>(lc.g, lc.hq);  // this lane's B column is column g
+  const bool live = qb >= 0;
+  float x[8][2][2];
+  float amax = 0.f, zsum = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
+  for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-      for (int r = 0; r < 2; ++r)
+    for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
-          const float qv = live ? sm.sQ[q * D + ch] : 0.f;
-          const float v = qv * __half2float(s_tau[ch]) * (1.f / k_mult<BITS>(ch));
-          x[ks][r][e] = v;
-          amax = fmaxf(amax, fabsf(v));
-          zsum = fmaf(qv, __half2float(z_tau[ch]), zsum);
-        }
-    amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
-    zsum += __shfl_xor_sync(FULLMASK, zsum, 1);
-    zsum += __shfl_xor_sync(FULLMASK, zsum, 2);
-    int e2 = 0;
-    if (amax > 0.f) e2 = min(100, max(-100, 13 - ilog2f(amax)));
-    const float sc = exp2i(e2);
-    float fed = 0.f;  // sum of the fp16 values actually fed (for the magic bias)
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint32_t h2 = f16x2_from(x[ks][r][0] * sc, x[ks][r][1] * sc);
-        st.qB[ks][r] = h2;
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-        fed += f.x + f.y;
+      for (int e = 0; e < 2; ++e) {
+        const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
+        const float qv = live ? sQ[qb * D + ch] : 0.f;
+        const float v = qv * __half2float(s_tau[ch]) * (1.f / k_mult<BITS>(ch));
+        x[ks][r][e] = v;
+        amax = fmaxf(amax, fabsf(v));
+        zsum = fmaf(qv, __half2float(z_tau[ch]), zsum);
       }
-    fed += __shfl_xor_sync(FULLMASK, fed, 1);
-    fed += __shfl_xor_sync(FULLMASK, fed, 2);
-    const float fa = sl2 * exp2i(-e2), fb = sl2 * zsum, fc = kMagicF * fed;
+  amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
+  zsum += __shfl_xor_sync(FULLMASK, zsum, 1);
+  zsum += __shfl_xor_sync(FULLMASK, zsum, 2);
+  int e2 = 0;
+  if (amax > 0.f) e2 = min(100, max(-100, 13 - ilog2f(amax)));
+  const float sc = exp2i(e2);
+  float fed = 0.f;  // sum of the fp16 values actually fed (for the magic bias)
 #pragma unroll
-    for (int ql = 0; ql < 2; ++ql) {  // query 2c + ql is B column 2c + ql, held by lane 8c + 4ql
-      cwA[ql] = __shfl_sync(FULLMASK, fa, 8 * c + 4 * ql);
-      cwB[ql] = __shfl_sync(FULLMASK, fb, 8 * c + 4 * ql);
-      cwC[ql] = __shfl_sync(FULLMASK, fc, 8 * c + 4 * ql);
+  for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t h2 = f16x2_from(x[ks][r][0] * sc, x[ks][r][1] * sc);
+      qB[ks][r] = h2;
+      const float2 f = half2_to_float2(h2);
+      fed += f.x + f.y;
     }
+  fed += __shfl_xor_sync(FULLMASK, fed, 1);
+  fed += __shfl_xor_sync(FULLMASK, fed, 2);
+  const float fa = sl2 * exp2i(-e2), fb = sl2 * zsum, fc = -kMagicF * fed;
+  // accumulator column 2c + j is B column 2c + j, held by lane 4 (2c + j)
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) cwneg[jj] = __shfl_sync(FULLMASK, fc, 8 * c + 4 * jj);
+#pragma unroll
+  for (int j = 0; j < C::NQ; ++j) {
+    cwA[j] = __shfl_sync(FULLMASK, fa, 8 * c + 4 * j);
+    cwB[j] = __shfl_sync(FULLMASK, fb, 8 * c + 4 * j);
   }
+}
 
-  // ---------------------------------------------------- QK^T with the K fold
-  // S[mt][row][ql]: token 16 mt + 8 row + g of the chunk, query 2c + ql (log2 domain).
-  float S[2][2][2];
+// QK^T of one 32-token chunk starting at entry token rel0, with the K fold.
+// x[mt][row][j]: token rel0 + 16 mt + 2 g + row, query slot j; token-wise K in
+// units of pa[j], channel-wise K in log2 units.
+template <class C>
+__device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpState<C>& st, const uint32_t (&qB)[8][2],
+                                         const float (&cwA)[C::NQ], const float (&cwB)[C::NQ],
+                                         const float (&cwneg)[2], const SlotSmem& sm, int rel0, const LaneCols& lc) {
+  constexpr int BITS = C::BITS, KL = C::KL, GK = C::GK, RB = C::RB, NQ = C::NQ;
+  const int g = lc.g, c = lc.c;
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
-    const int row0 = rel0 + 16 * mt + g;
-    const int row1 = row0 + 8;
-    const uint32_t* r0p = reinterpret_cast<const uint32_t*>(sm.kc + row0 * RB);
-    const uint32_t* r1p = reinterpret_cast<const uint32_t*>(sm.kc + row1 * RB);
-    uint32_t w0[4], w1[4], s0w[4], s1w[4];
+    const int tA = rel0 + 16 * mt + 2 * g;  // row g is token tA, row g+8 token tA+1
+    const uint32_t* rA = reinterpret_cast<const uint32_t*>(sm.kc + tA * RB);
+    const uint32_t* rB = reinterpret_cast<const uint32_t*>(sm.kc + (tA + 1) * RB);
+    uint32_t wA[4], wB[4], sA[4], sB[4];
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk) {
       if (BITS == 2) {
         // lanes with odd c take codes 4..7 and 12..15 of the word: shift them into 0..3
         const int sh = 8 * (c & 1);
-        w0[blk] = r0p[2 * blk + (c >> 1)] >> sh;
-        w1[blk] = r1p[2 * blk + (c >> 1)] >> sh;
+        wA[blk] = rA[2 * blk + (c >> 1)] >> sh;
+        wB[blk] = rB[2 * blk + (c >> 1)] >> sh;
       } else {
-        w0[blk] = r0p[4 * blk + c];
-        w1[blk] = r1p[4 * blk + c];
-        s0w[blk] = w0[blk] >> 8;
-        s1w[blk] = w1[blk] >> 8;
+        wA[blk] = rA[4 * blk + c];
+        wB[blk] = rB[4 * blk + c];
+        sA[blk] = wA[blk] >> 8;
+        sB[blk] = wB[blk] >> 8;
       }
     }
-    float sfold[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    float xs[2][NQ];
+#pragma unroll
+    for (int row = 0; row < 2; ++row)
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) xs[row][j] = 0.f;
     float acc[4];
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int blk = ks >> 1, h = ks & 1;
-      if (KL == 0 ? (ks % C::KSG == 0) : (ks == 0)) {
-        // token-wise K: a fresh accumulator per channel group; channel-wise K: one for all
-        // 128 channels (the scale is already in Q'). Each starts at minus the magic bias.
-        const float b0 = (KL == 0) ? st.c1[0][ks / C::KSG] : cwC[0];
-        const float b1 = (KL == 0) ? st.c1[1][ks / C::KSG] : cwC[1];
-        acc[0] = -b0;
-        acc[1] = -b1;
-        acc[2] = -b0;
-        acc[3] = -b1;
-      }
       uint32_t a0, a1, a2, a3;
       if (BITS == 2) {
         const uint32_t mA = 0x00030003u << (4 * h), mB = 0x00030003u << (4 * h + 2);
-        a0 = and_or(w0[blk], mA, kMagic2);
-        a1 = and_or(w1[blk], mA, kMagic2);
-        a2 = and_or(w0[blk], mB, kMagic2);
-        a3 = and_or(w1[blk], mB, kMagic2);
+        a0 = and_or(wA[blk], mA, kMagic2);
+        a1 = and_or(wB[blk], mA, kMagic2);
+        a2 = and_or(wA[blk], mB, kMagic2);
+        a3 = and_or(wB[blk], mB, kMagic2);
       } else {
-        a0 = int4_half2(w0[blk], s0w[blk], 2 * h);
-        a1 = int4_half2(w1[blk], s1w[blk], 2 * h);
-        a2 = int4_half2(w0[blk], s0w[blk], 2 * h + 1);
-        a3 = int4_half2(w1[blk], s1w[blk], 2 * h + 1);
+        a0 = int4_half2(wA[blk], sA[blk], 2 * h);
+        a1 = int4_half2(wB[blk], sB[blk], 2 * h);
+        a2 = int4_half2(wA[blk], sA[blk], 2 * h + 1);
+        a3 = int4_half2(wB[blk], sB[blk], 2 * h + 1);
       }
-      mma_f16(acc, a0, a1, a2, a3, st.qB[ks][0], st.qB[ks][1]);
+      if (KL == 0 ? (ks % C::KSG == 0) : (ks == 0)) {
+        // a fresh accumulator per K channel group (token-wise K) or per token group
+        // (channel-wise K), starting at minus the magic bias
+        const float b0 = (KL == 0) ? st.kbias[0][ks / C::KSG] : cwneg[0];
+        const float b1 = (KL == 0) ? st.kbias[1][ks / C::KSG] : cwneg[1];
+        mma_f16_c(acc, a0, a1, a2, a3, qB[ks][0], qB[ks][1], b0, b1, b0, b1);
+      } else {
+        mma_f16(acc, a0, a1, a2, a3, qB[ks][0], qB[ks][1]);
+      }
       if (KL == 0 && (ks + 1) % C::KSG == 0) {
-        // acc-fold of one channel group: s * (raw partial) + z * sum(Q over the group)
+        // acc-fold of one channel group: s * (raw partial) + z * 2^e sum(Q over the group)
         const int grp = ks / C::KSG;
-        const float s0 = __half2float(sm.ks[row0 * GK + grp]);
-        const float z0 = __half2float(sm.kz[row0 * GK + grp]);
-        const float s1 = __half2float(sm.ks[row1 * GK + grp]);
-        const float z1 = __half2float(sm.kz[row1 * GK + grp]);
-#pragma unroll
-        for (int ql = 0; ql < 2; ++ql) {
-          sfold[0][ql] = fmaf(s0 * st.aq[ql], acc[ql], fmaf(z0, st.bz[ql][grp], sfold[0][ql]));
-          sfold[1][ql] = fmaf(s1 * st.aq[ql], acc[2 + ql], fmaf(z1, st.bz[ql][grp], sfold[1][ql]));
-        }
-      }
-    }
-#pragma unroll
-    for (int ql = 0; ql < 2; ++ql) {
-      float v0, v1;
-      if (KL == 0) {
-        v0 = sfold[0][ql];
-        v1 = sfold[1][ql];
-      } else {
-        v0 = fmaf(cwA[ql], acc[ql], cwB[ql]);
-        v1 = fmaf(cwA[ql], acc[2 + ql], cwB[ql]);
-      }
-      if (FULL) {
-        S[mt][0][ql] = v0;
-        S[mt][1][ql] = v1;
-      } else {
-        const int t0 = 16 * mt + g;
-        S[mt][0][ql] = (t0 < nv) ? v0 : -INFINITY;
-        S[mt][1][ql] = (t0 + 8 < nv) ? v1 : -INFINITY;
-      }
-    }
-  }
-
-  // ---------------------------------------------------- online softmax
-  // This lane's tokens, chunk-relative: T_k = g + 8k, k = 2 mt + row.
-  float P[2][4];
-  float alpha[2];
-  bool rescale = false;
-#pragma unroll
-  for (int ql = 0; ql < 2; ++ql) {
-    float mx = fmaxf(fmaxf(S[0][0][ql], S[0][1][ql]), fmaxf(S[1][0][ql], S[1][1][ql]));
-    mx = fmaxf(mx, __shfl_xor_sync(FULLMASK, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(FULLMASK, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(FULLMASK, mx, 16));
-    const float m_new = fmaxf(st.m_run[ql], mx);
-    rescale |= (m_new > st.m_run[ql]);
-    alpha[ql] = (m_new == -INFINITY) ? 1.f : fast_exp2(st.m_run[ql] - m_new);
-    const float mref = (m_new == -INFINITY) ? 0.f : m_new;
-    st.m_run[ql] = m_new;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) P[ql][k] = fast_exp2(S[k >> 1][k & 1][ql] - mref);
-  }
-  if (__any_sync(FULLMASK, rescale)) {
-#pragma unroll
-    for (int ql = 0; ql < 2; ++ql) {
-      st.l_part[ql] *= alpha[ql];
-#pragma unroll
-      for (int u = 0; u < GV; ++u) st.zacc[ql][u] *= alpha[ql];
-    }
-    // output column 8v + 2c + e is combo (query, group) = ((8v + 2c + e) / GV, % GV)
-#pragma unroll
-    for (int v = 0; v < NTV; ++v)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float av;
-        if (GV == 1 && NTV == 1) {
-          av = alpha[e];
+        float s0, s1, z0, z1;
+        if (GK == 1) {
+          const float2 s2 = half2_to_float2(*reinterpret_cast<const uint32_t*>(sm.ks + tA));
+          const float2 z2 = half2_to_float2(*reinterpret_cast<const uint32_t*>(sm.kz + tA));
+          s0 = s2.x, s1 = s2.y, z0 = z2.x, z1 = z2.y;
         } else {
-          const int q = (8 * v + 2 * c + e) / GV;
-          const float a0 = __shfl_sync(FULLMASK, alpha[0], 4 * g + (q >> 1));
-          const float a1 = __shfl_sync(FULLMASK, alpha[1], 4 * g + (q >> 1));
-          av = (q & 1) ? a1 : a0;
+          s0 = __half2float(sm.ks[tA * GK + grp]);
+          s1 = __half2float(sm.ks[(tA + 1) * GK + grp]);
+          z0 = __half2float(sm.kz[tA * GK + grp]);
+          z1 = __half2float(sm.kz[(tA + 1) * GK + grp]);
         }
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          st.o_run[mt][0][v][e] *= av;
-          st.o_run[mt][1][v][e] *= av;
+        for (int j = 0; j < NQ; ++j) {
+          xs[0][j] = fmaf(s0, acc[j], fmaf(z0, st.bzq[j][grp], xs[0][j]));
+          xs[1][j] = fmaf(s1, acc[2 + j], fmaf(z1, st.bzq[j][grp], xs[1][j]));
         }
       }
-  }
-
-  // ---------------------------------------------------- weights -> fp16 words
-  // Token-wise V (operand-fold): fed weight P_t * s_t,u * 2^eP per channel group u;
-  // channel-wise V: P_t * 2^13. The denominator and value offsets are summed from
-  // the fed weights w_t = fed / scale; the PV accumulators start at -1024 * sum(fed)
-  // per column, which removes the magic bias of the V operand exactly.
-  const int tok0 = rel0 + g;
-  uint32_t pw[2][GV][2];  // [query][group][pair (T0,T1) / (T2,T3)]
-  float colb[2][GV];      // -1024 * sum of fed weights over the chunk (reduced)
-  float inv_ps = 1.f;
-  float psum[2];          // channel-wise V: sum of fed weights over the chunk (reduced)
-  if (VL == 0) {
-    float sv[GV][4];
-    uint32_t smax = 0;
-#pragma unroll
-    for (int u = 0; u < GV; ++u)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const bool ok = FULL || (g + 8 * k < nv);
-        const __half hv = sm.vs[(tok0 + 8 * k) * GV + u];
-        sv[u][k] = ok ? __half2float(hv) : 0.f;
-        smax = max(smax, ok ? (uint32_t)(__half_as_ushort(hv) & 0x7fffu) : 0u);
-      }
-    smax = max(smax, __shfl_xor_sync(FULLMASK, smax, 4));
-    smax = max(smax, __shfl_xor_sync(FULLMASK, smax, 8));
-    smax = max(smax, __shfl_xor_sync(FULLMASK, smax, 16));
-    const float smaxf = __half2float(__ushort_as_half((unsigned short)smax));
-    int e2 = 0;
-    if (smaxf > 0.f) e2 = min(100, max(-100, 13 - ilog2f(smaxf)));
-    const float ps = exp2i(e2);
-    inv_ps = exp2i(-e2);
-#pragma unroll
-    for (int ql = 0; ql < 2; ++ql) {
-      float lsum = 0.f;
-#pragma unroll
-      for (int u = 0; u < GV; ++u) {
-        float f[4];
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const uint32_t h2 = f16x2_from(P[ql][2 * kk] * sv[u][2 * kk] * ps, P[ql][2 * kk + 1] * sv[u][2 * kk + 1] * ps);
-          pw[ql][u][kk] = h2;
-          const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-          f[2 * kk] = ff.x;
-          f[2 * kk + 1] = ff.y;
-        }
-        float zt = 0.f, fs = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float w = (sv[u][k] != 0.f) ? f[k] * (fast_rcp(sv[u][k]) * inv_ps) : P[ql][k];
-          const bool ok = FULL || (g + 8 * k < nv);
-          const float zz = ok ? __half2float(sm.vz[(tok0 + 8 * k) * GV + u]) : 0.f;
-          zt = fmaf(w, zz, zt);
-          fs += f[k];
-          if (u == 0) lsum += w;
-        }
-        st.zacc[ql][u] += zt;
-        fs += __shfl_xor_sync(FULLMASK, fs, 4);
-        fs += __shfl_xor_sync(FULLMASK, fs, 8);
-        fs += __shfl_xor_sync(FULLMASK, fs, 16);
-        colb[ql][u] = -kMagicF * fs;
-      }
-      st.l_part[ql] += lsum;
-      psum[ql] = 0.f;
     }
-  } else {
 #pragma unroll
-    for (int ql = 0; ql < 2; ++ql) {
-      float fs = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const uint32_t h2 = f16x2_from(P[ql][2 * kk] * 8192.f, P[ql][2 * kk + 1] * 8192.f);
-        pw[ql][0][kk] = h2;
-        const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-        fs += ff.x + ff.y;
-      }
-      st.l_part[ql] += fs * (1.f / 8192.f);
-      fs += __shfl_xor_sync(FULLMASK, fs, 4);
-      fs += __shfl_xor_sync(FULLMASK, fs, 8);
-      fs += __shfl_xor_sync(FULLMASK, fs, 16);
-      psum[ql] = fs * (1.f / 8192.f);
-      colb[ql][0] = -kMagicF * fs;
-    }
-  }
-
-  // ---------------------------------------------------- PV B fragments and accumulator start
-  // B column n = g of n-tile v is combo 8v + g; k-slots 2c, 2c+1 of PV k-step kk hold
-  // chunk tokens c + 16kk and c + 8 + 16kk (the pair kk of lane 4c + q/2), and k-slots
-  // 2c+8, 2c+9 the same tokens of lane 4(c+4) + q/2.
-  uint32_t pB[NTV][2][2];  // [n-tile][kk][reg]
-#pragma unroll
-  for (int v = 0; v < NTV; ++v) {
-    const int col = 8 * v + g;
-    const int q = col / GV, u_need = col % GV;
-    const int src0 = 4 * c + (q >> 1), src1 = 4 * (c + 4) + (q >> 1);
-    const bool live = q < hq;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      uint32_t b0 = 0, b1 = 0;
-#pragma unroll
-      for (int ql = 0; ql < 2; ++ql)
-#pragma unroll
-        for (int u = 0; u < GV; ++u) {
-          const uint32_t x0 = __shfl_sync(FULLMASK, pw[ql][u][kk], src0);
-          const uint32_t x1 = __shfl_sync(FULLMASK, pw[ql][u][kk], src1);
-          if (ql == (q & 1) && u == u_need) {
-            b0 = x0;
-            b1 = x1;
-          }
-        }
-      pB[v][kk][0] = live ? b0 : 0u;
-      pB[v][kk][1] = live ? b1 : 0u;
-    }
-  }
-  float cb[NTV][2];  // starting value of output column 8v + 2c + e
-#pragma unroll
-  for (int v = 0; v < NTV; ++v)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      if (GV == 1 && NTV == 1) {
-        cb[v][e] = colb[e][0];
+    for (int j = 0; j < NQ; ++j) {
+      if (KL == 0) {
+        x[mt][0][j] = xs[0][j];
+        x[mt][1][j] = xs[1][j];
       } else {
-        const int col = 8 * v + 2 * c + e;
-        const int q = col / GV, u_need = col % GV;
-        float x = 0.f;
-#pragma unroll
-        for (int ql = 0; ql < 2; ++ql)
-#pragma unroll
-          for (int u = 0; u < GV; ++u) {
-            const float y = __shfl_sync(FULLMASK, colb[ql][u], 4 * g + (q >> 1));
-            if (ql == (q & 1) && u == u_need) x = y;
-          }
-        cb[v][e] = x;
+        x[mt][0][j] = fmaf(cwA[j], acc[j], cwB[j]);
+        x[mt][1][j] = fmaf(cwA[j], acc[2 + j], cwB[j]);
       }
     }
+  }
+}
 
-  // ---------------------------------------------------- PV
-  // Row half `row` of m-tile mt is channel 16g + 8row + mt (INT2) or
-  // 16g + 8(mt/4) + 4row + mt%4 (INT4), with factor v_mult(mt).
-  float accv[8][NTV][4];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-    for (int v = 0; v < NTV; ++v) {
-      accv[mt][v][0] = cb[v][0];
-      accv[mt][v][1] = cb[v][1];
-      accv[mt][v][2] = cb[v][0];
-      accv[mt][v][3] = cb[v][1];
-    }
+// PV of one 32-token chunk: accv[mt][v] (+)= V^T[16 channels x 16 tokens] * B.
+// Row half `row` of m-tile mt is channel 16 g + pv_channel(mt, row). fresh: the
+// accumulators start at cb (minus the magic bias of each column) instead of
+// continuing.
+template <class C>
+__device__ __forceinline__ void pv_chunk(float (&accv)[8][C::NTV][4], const uint32_t (&pB)[C::NTV][2][2],
+                                         const SlotSmem& sm, int rel0, const LaneCols& lc, bool fresh,
+                                         const float (&cb)[C::NTV][2]) {
+  constexpr int BITS = C::BITS, RB = C::RB, NTV = C::NTV;
+  const int g = lc.g, c = lc.c;
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
-    const int tA = rel0 + c + 16 * kk, tB = tA + 4;
+    // k-slots 2c, 2c+1 are tokens tA, tA+1; k-slots 2c+8, 2c+9 are tokens tA+8, tA+9
+    const int tA = rel0 + 16 * kk + 2 * c;
+    const bool first = fresh && kk == 0;
     if (BITS == 2) {
       const uint32_t wa0 = reinterpret_cast<const uint32_t*>(sm.vc + tA * RB)[g];
-      const uint32_t wa1 = reinterpret_cast<const uint32_t*>(sm.vc + (tA + 8) * RB)[g];
-      const uint32_t wb0 = reinterpret_cast<const uint32_t*>(sm.vc + tB * RB)[g];
-      const uint32_t wb1 = reinterpret_cast<const uint32_t*>(sm.vc + (tB + 8) * RB)[g];
+      const uint32_t wa1 = reinterpret_cast<const uint32_t*>(sm.vc + (tA + 1) * RB)[g];
+      const uint32_t wb0 = reinterpret_cast<const uint32_t*>(sm.vc + (tA + 8) * RB)[g];
+      const uint32_t wb1 = reinterpret_cast<const uint32_t*>(sm.vc + (tA + 9) * RB)[g];
       const uint32_t xal = prmt(wa0, wa1, 0x5410), xah = prmt(wa0, wa1, 0x7632);
       const uint32_t xbl = prmt(wb0, wb1, 0x5410), xbh = prmt(wb0, wb1, 0x7632);
       const uint32_t sal = xal >> 10, sah = xah >> 10, sbl = xbl >> 10, sbh = xbh >> 10;
@@ -511,13 +390,19 @@ __device__ __forceinline__ void process_chunk(WarpState<C>& st, const ChunkSmem&
         const uint32_t a0 = int2_half2(xal, sal, mt), a1 = int2_half2(xah, sah, mt);
         const uint32_t a2 = int2_half2(xbl, sbl, mt), a3 = int2_half2(xbh, sbh, mt);
 #pragma unroll
-        for (int v = 0; v < NTV; ++v) mma_f16(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1]);
+        for (int v = 0; v < NTV; ++v) {
+          if (first)
+            mma_f16_c(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1], cb[v][0], cb[v][1], cb[v][0],
+                        cb[v][1]);
+          else
+            mma_f16(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1]);
+        }
       }
     } else {
       const uint2 wa0 = reinterpret_cast<const uint2*>(sm.vc + tA * RB)[g];
-      const uint2 wa1 = reinterpret_cast<const uint2*>(sm.vc + (tA + 8) * RB)[g];
-      const uint2 wb0 = reinterpret_cast<const uint2*>(sm.vc + tB * RB)[g];
-      const uint2 wb1 = reinterpret_cast<const uint2*>(sm.vc + (tB + 8) * RB)[g];
+      const uint2 wa1 = reinterpret_cast<const uint2*>(sm.vc + (tA + 1) * RB)[g];
+      const uint2 wb0 = reinterpret_cast<const uint2*>(sm.vc + (tA + 8) * RB)[g];
+      const uint2 wb1 = reinterpret_cast<const uint2*>(sm.vc + (tA + 9) * RB)[g];
 #pragma unroll
       for (int uu = 0; uu < 2; ++uu) {
         const uint32_t ea0 = uu ? wa0.y : wa0.x, ea1 = uu ? wa1.y : wa1.x;
@@ -531,50 +416,341 @@ __device__ __forceinline__ void process_chunk(WarpState<C>& st, const ChunkSmem&
           const uint32_t a0 = int4_half2(xal, sal, pp), a1 = int4_half2(xah, sah, pp);
           const uint32_t a2 = int4_half2(xbl, sbl, pp), a3 = int4_half2(xbh, sbh, pp);
 #pragma unroll
-          for (int v = 0; v < NTV; ++v) mma_f16(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1]);
+          for (int v = 0; v < NTV; ++v) {
+            if (first)
+              mma_f16_c(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1], cb[v][0], cb[v][1], cb[v][0],
+                        cb[v][1]);
+            else
+              mma_f16(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1]);
+          }
         }
       }
     }
   }
+}
 
-  // ---------------------------------------------------- V fold into the running output
-  if (VL == 0) {
+// Live output column i of a lane: owned combo index, or -1 when the lane's V group
+// matches neither combo of the pair.
+template <class C>
+__device__ __forceinline__ int live_own(int i, const LaneCols& lc) {
+  if (C::DUP) return 0;
+  if (C::GV == 1) return i;
+  return lc.e_live < 0 ? -1 : 2 * i + lc.e_live;
+}
+// PV n-tile and accumulator column (0/1 within the lane's pair) of live column i.
+template <class C>
+__device__ __forceinline__ int live_tile(int i) {
+  return (C::MODE == kModeWide) ? i : 0;
+}
+template <class C>
+__device__ __forceinline__ int live_col(int i, const LaneCols& lc) {
+  return C::DUP ? 0 : (C::GV == 1 ? i : max(lc.e_live, 0));
+}
+
+// Token-wise V: operand-fold of one chunk (the scale is already in the weights):
+// running output += (bias-free accumulator) * 2^-eP / factor.
+template <class C>
+__device__ __forceinline__ void fold_tokenwise_v(WarpState<C>& st, const float (&accv)[8][C::NTV][4], float inv_ps,
+                                                 const LaneCols& lc) {
+#pragma unroll
+  for (int i = 0; i < C::NQ; ++i) {
+    const int v = live_tile<C>(i), e = live_col<C>(i, lc);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      const float f = inv_ps * (1.f / v_mult<BITS>(mt));
+      const float f = inv_ps * (1.f / v_mult<C::BITS>(mt));
 #pragma unroll
-      for (int v = 0; v < NTV; ++v)
-#pragma unroll
-        for (int row = 0; row < 2; ++row)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) st.o_run[mt][row][v][e] = fmaf(accv[mt][v][2 * row + e], f, st.o_run[mt][row][v][e]);
+      for (int row = 0; row < 2; ++row) {
+        const float a = (e == 0) ? accv[mt][v][2 * row] : accv[mt][v][2 * row + 1];
+        st.o_run[mt][row][i] = fmaf(a, f, st.o_run[mt][row][i]);
+      }
     }
-  } else {
-    // acc-fold per token group: s_tau,d * (raw partial) + z_tau,d * sum_t w_t
-    const int tau_rel = rel0 / C::G;
-    const __half* s_tau = sm.vs + tau_rel * D;
-    const __half* z_tau = sm.vz + tau_rel * D;
+  }
+}
+
+// Channel-wise V: acc-fold of one token group tau whose s/z rows are s_tau/z_tau:
+// running output += s_tau,d * (bias-free accumulator) / (2^13 factor) + z_tau,d * W,
+// W = sum of the group's weights (fed sum / 2^13) per owned combo.
+template <class C>
+__device__ __forceinline__ void fold_channelwise_v(WarpState<C>& st, const float (&accv)[8][C::NTV][4],
+                                                   const float (&Wg)[C::NO], const __half* s_tau,
+                                                   const __half* z_tau, const LaneCols& lc) {
+  constexpr int BITS = C::BITS;
+  const uint4* sp = reinterpret_cast<const uint4*>(s_tau + 16 * lc.g);
+  const uint4* zp = reinterpret_cast<const uint4*>(z_tau + 16 * lc.g);
+  const uint4 s_lo = sp[0], s_hi = sp[1], z_lo = zp[0], z_hi = zp[1];
+  const uint32_t sw[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+  const uint32_t zw[8] = {z_lo.x, z_lo.y, z_lo.z, z_lo.w, z_hi.x, z_hi.y, z_hi.z, z_hi.w};
+#pragma unroll
+  for (int i = 0; i < C::NQ; ++i) {
+    const int v = live_tile<C>(i), e = live_col<C>(i, lc);
+    const float W = Wg[C::DUP ? 0 : i] * (1.f / 8192.f);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
       for (int row = 0; row < 2; ++row) {
-        const int ch = (BITS == 2) ? 16 * g + 8 * row + mt : 16 * g + 8 * (mt >> 2) + 4 * row + (mt & 3);
-        const float s = __half2float(s_tau[ch]) * (1.f / (8192.f * v_mult<BITS>(mt)));
-        const float z = __half2float(z_tau[ch]);
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          st.o_run[mt][row][0][e] = fmaf(s, accv[mt][0][2 * row + e], fmaf(z, psum[e], st.o_run[mt][row][0][e]));
+        const int k = pv_channel<BITS>(mt, row);
+        const float2 s2 = half2_to_float2(sw[k >> 1]);
+        const float2 z2 = half2_to_float2(zw[k >> 1]);
+        const float s = (k & 1) ? s2.y : s2.x;
+        const float z = (k & 1) ? z2.y : z2.x;
+        const float a = (e == 0) ? accv[mt][v][2 * row] : accv[mt][v][2 * row + 1];
+        st.o_run[mt][row][i] = fmaf(s * (1.f / (8192.f * v_mult<BITS>(mt))), a, fmaf(z, W, st.o_run[mt][row][i]));
       }
   }
 }
 
+// One warp unit: the NCH chunks of 32 tokens of one ring entry. nv: valid tokens
+// of the entry (all UNIT valid when FULL).
+template <class C, bool FULL>
+__device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& sm, int nv, const float* sQ, float sl2,
+                                             const LaneCols& lc) {
+  constexpr int KL = C::KL, VL = C::VL, GV = C::GV, NQ = C::NQ, NO = C::NO, NTV = C::NTV;
+  constexpr int NCH = C::NCH, D = kHeadDim;
+  constexpr unsigned FULLMASK = 0xffffffffu;
+  const int g = lc.g, c = lc.c;
+
+  // ------------------------------------------------ phase 1: scores of the whole unit
+  float x[NCH][2][2][NQ];
+  uint32_t qB[8][2];
+  float cwA[NQ], cwB[NQ], cwneg[2] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < NQ; ++j) cwA[j] = cwB[j] = 0.f;
+  if (KL == 0) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) qB[ks][0] = st.qB[ks][0], qB[ks][1] = st.qB[ks][1];
+  }
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int rel0 = kChunk * ch;
+    if (!FULL && rel0 >= nv) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int row = 0; row < 2; ++row)
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) x[ch][mt][row][j] = -INFINITY;
+      continue;
+    }
+    if (KL == 1 && (ch == 0 || (C::G <= C::UNIT && (kChunk * ch) % C::G == 0))) {
+      const int tau = rel0 / C::G;
+      channelwise_q<C>(qB, cwA, cwB, cwneg, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
+    }
+    qk_chunk<C>(x[ch], st, qB, cwA, cwB, cwneg, sm, rel0, lc);
+    if (!FULL) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int row = 0; row < 2; ++row)
+#pragma unroll
+          for (int j = 0; j < NQ; ++j)
+            if (rel0 + 16 * mt + 2 * g + row >= nv) x[ch][mt][row][j] = -INFINITY;
+    }
+  }
+
+  // ------------------------------------------------ running maximum, once per unit
+  float nm[NQ];
+  {
+    float mx[NQ];
+    bool grow = false;
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+        m = fmaxf(m, fmaxf(fmaxf(x[ch][0][0][j], x[ch][0][1][j]), fmaxf(x[ch][1][0][j], x[ch][1][1][j])));
+      m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, 4));
+      m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, 8));
+      m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, 16));
+      mx[j] = fmaxf(st.m_run[j], m);
+      grow |= (mx[j] > st.m_run[j]);
+    }
+    if (__any_sync(FULLMASK, grow)) {
+      float alpha[NQ];
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) {
+        alpha[j] = (mx[j] == st.m_run[j]) ? 1.f : fast_exp2(st.pa[j] * (st.m_run[j] - mx[j]));
+        st.l[j] *= alpha[j];
+      }
+#pragma unroll
+      for (int o = 0; o < NO; ++o) st.zacc[o] *= alpha[own_slot<C>(o)];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int row = 0; row < 2; ++row)
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] *= alpha[i];
+    }
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      st.m_run[j] = mx[j];
+      nm[j] = -st.pa[j] * mx[j];
+    }
+  }
+
+  // ------------------------------------------------ token-wise V: weight exponent of the unit
+  // Fed weight P_t s_t,u 2^eP with max(s) 2^eP in [2^13, 2^14) over the unit's valid
+  // tokens: the fed values stay in the fp16 normal range.
+  float ps = 8192.f, inv_ps = 1.f / 8192.f;
+  if (VL == 0) {
+    constexpr int WORDS = C::UNIT * GV / 2;  // scale words (two halves) of the unit
+    static_assert(WORDS % 32 == 0, "scale words spread evenly over the lanes");
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(sm.vs);
+    uint32_t smax = 0;
+#pragma unroll
+    for (int k = 0; k < WORDS / 32; ++k) {
+      const int w = lc.lane + 32 * k;
+      const uint32_t s01 = sw[w];
+      const bool ok0 = FULL || ((2 * w) / GV < nv), ok1 = FULL || ((2 * w + 1) / GV < nv);
+      const uint32_t m0 = ok0 ? (s01 & 0x7fffu) : 0u, m1 = ok1 ? ((s01 >> 16) & 0x7fffu) : 0u;
+      smax = max(smax, max(m0, m1));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) smax = max(smax, __shfl_xor_sync(FULLMASK, smax, o));
+    const float smaxf = __half2float(__ushort_as_half((unsigned short)smax));
+    int e2 = 0;
+    if (smaxf > 0.f) e2 = min(100, max(-100, 13 - ilog2f(smaxf)));
+    ps = exp2i(e2);
+    inv_ps = exp2i(-e2);
+  }
+
+  // ------------------------------------------------ phase 2: weights, PV, V fold
+  // Each chunk's PV accumulators start at (token-wise V) or are lowered by (channel-wise
+  // V, later chunks of a token group) minus 1024 * the chunk's fed-weight sum, so that
+  // the fp32 accumulator never carries more than one chunk's magic bias.
+  float accv[8][NTV][4];
+  float Wg[NO];  // channel-wise V: fed-weight sum of the current token group
+#pragma unroll
+  for (int o = 0; o < NO; ++o) Wg[o] = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int rel0 = kChunk * ch;
+    if (!FULL && rel0 >= nv) break;
+    const bool fresh = (VL == 0) || (ch == 0) || (C::G <= C::UNIT && (kChunk * ch) % C::G == 0);
+    float P[2][2][NQ];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int row = 0; row < 2; ++row)
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) P[mt][row][j] = fast_exp2(fmaf(st.pa[j], x[ch][mt][row][j], nm[j]));
+    // fed weights: pw[o][mt] = (token 16mt+2g, token 16mt+2g+1) for owned combo o
+    uint32_t pw[NO][2];
+    float Fc[NO];
+#pragma unroll
+    for (int o = 0; o < NO; ++o) Fc[o] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int tA = rel0 + 16 * mt + 2 * g;
+      const bool ok0 = FULL || (tA < nv), ok1 = FULL || (tA + 1 < nv);
+      if (VL == 0) {
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) st.l[j] += P[mt][0][j] + P[mt][1][j];
+      }
+#pragma unroll
+      for (int o = 0; o < NO; ++o) {
+        const int j = own_slot<C>(o);
+        float f0, f1;
+        if (VL == 0) {
+          // token-wise V scale and offset of tokens tA, tA+1 in this combo's V group
+          uint32_t s01, z01;
+          if (GV == 1) {
+            s01 = *reinterpret_cast<const uint32_t*>(sm.vs + tA);
+            z01 = *reinterpret_cast<const uint32_t*>(sm.vz + tA);
+          } else {
+            const int u = own_group<C>(c, o);
+            s01 = (uint32_t)__half_as_ushort(sm.vs[tA * GV + u]) |
+                  ((uint32_t)__half_as_ushort(sm.vs[(tA + 1) * GV + u]) << 16);
+            z01 = (uint32_t)__half_as_ushort(sm.vz[tA * GV + u]) |
+                  ((uint32_t)__half_as_ushort(sm.vz[(tA + 1) * GV + u]) << 16);
+          }
+          const float2 s2 = half2_to_float2(s01), z2 = half2_to_float2(z01);
+          // padding tokens carry weight 0 and may hold any scale bits (even NaN)
+          const float sv0 = ok0 ? s2.x : 0.f, sv1 = ok1 ? s2.y : 0.f;
+          const float zv0 = ok0 ? z2.x : 0.f, zv1 = ok1 ? z2.y : 0.f;
+          f0 = P[mt][0][j] * (sv0 * ps);
+          f1 = P[mt][1][j] * (sv1 * ps);
+          st.zacc[o] = fmaf(P[mt][0][j], zv0, fmaf(P[mt][1][j], zv1, st.zacc[o]));
+        } else {
+          f0 = P[mt][0][j] * 8192.f;
+          f1 = P[mt][1][j] * 8192.f;
+        }
+        pw[o][mt] = f16x2_from(f0, f1);
+        const float2 fb = half2_to_float2(pw[o][mt]);
+        Fc[o] += fb.x + fb.y;
+      }
+    }
+#pragma unroll
+    for (int o = 0; o < NO; ++o) {
+      if (VL == 1) st.l[own_slot<C>(o)] += Fc[o] * (1.f / 8192.f);  // this lane's tokens
+      Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 4);
+      Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 8);
+      Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 16);
+      if (VL == 1) Wg[o] += Fc[o];
+    }
+    // accumulator column (v, 2c + e) holds owned combo (DUP ? 0 : 2v + e)
+    float cb[NTV][2];
+#pragma unroll
+    for (int v = 0; v < NTV; ++v)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) cb[v][e] = -kMagicF * Fc[C::DUP ? 0 : 2 * v + e];
+    if (!fresh) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int v = 0; v < NTV; ++v)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (!C::DUP || e == 0) {  // the duplicate column of a pair is never read
+              accv[mt][v][e] += cb[v][e];
+              accv[mt][v][2 + e] += cb[v][e];
+            }
+    }
+    // PV B fragments: column n = g of n-tile v belongs to lane c_o = g/2 of each token
+    // row group; k-slots 2c, 2c+1 (tokens 16kk + 2c + {0,1}) come from lane 4c + c_o and
+    // k-slots 2c+8, 2c+9 from lane 4(c+4) + c_o, word kk of the owned combo.
+    uint32_t pB[NTV][2][2];
+    const int src0 = 4 * c + (g >> 1), src1 = 4 * (c + 4) + (g >> 1);
+#pragma unroll
+    for (int v = 0; v < NTV; ++v)
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        if (C::DUP) {
+          pB[v][kk][0] = __shfl_sync(FULLMASK, pw[0][kk], src0);
+          pB[v][kk][1] = __shfl_sync(FULLMASK, pw[0][kk], src1);
+        } else {
+          const uint32_t x00 = __shfl_sync(FULLMASK, pw[2 * v][kk], src0);
+          const uint32_t x01 = __shfl_sync(FULLMASK, pw[2 * v + 1][kk], src0);
+          const uint32_t x10 = __shfl_sync(FULLMASK, pw[2 * v][kk], src1);
+          const uint32_t x11 = __shfl_sync(FULLMASK, pw[2 * v + 1][kk], src1);
+          pB[v][kk][0] = (g & 1) ? x01 : x00;
+          pB[v][kk][1] = (g & 1) ? x11 : x10;
+        }
+      }
+    pv_chunk<C>(accv, pB, sm, rel0, lc, fresh, cb);
+
+    if (VL == 0) {
+      fold_tokenwise_v<C>(st, accv, inv_ps, lc);
+    } else {
+      const bool last = (ch == NCH - 1) || (!FULL && rel0 + kChunk >= nv);
+      const bool group_end = C::G <= C::UNIT && ((kChunk * (ch + 1)) % C::G == 0);
+      if (last || group_end) {
+        const int tau = rel0 / C::G;  // token-group row of the entry
+        fold_channelwise_v<C>(st, accv, Wg, sm.vs + tau * D, sm.vz + tau * D, lc);
+#pragma unroll
+        for (int o = 0; o < NO; ++o) Wg[o] = 0.f;
+      }
+    }
+    if (!FULL && rel0 + kChunk >= nv) break;
+  }
+}
+
 // ------------------------------------------------------------------------
-// The kernel: see the file comment. C = Cfg<BITS, KL, VL, NT, LOG2G>.
+// The kernel: see the file comment. C = Cfg<BITS, KL, VL, MODE, LOG2G>.
 // ------------------------------------------------------------------------
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NTV = C::NTV;
-  constexpr int RB = C::RB, D = kHeadDim;
+  constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NQ = C::NQ, NO = C::NO;
+  constexpr int RB = C::RB, D = kHeadDim, UNIT = C::UNIT;
   constexpr unsigned FULLMASK = 0xffffffffu;
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -585,248 +761,250 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
   const int unit = b * p.Hkv + kvh;
   const int L = min(max(p.seq_lens[b], 0), p.T_cap);  // device value: clamped, never trusted
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);      // full[kMaxRing], empty[kMaxRing]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);      // full[warp][ring_per_warp]
   float* sQ = reinterpret_cast<float*>(smem + kBarBytes);  // [kMaxHq][D]
   float* sAq = sQ + kMaxHq * D;                            // [kMaxHq] token-wise K score factor
   int* sEq = reinterpret_cast<int*>(sAq + kMaxHq);         // [kMaxHq] query exponent
-  float* sBz = sAq + 2 * kMaxHq;                           // [kMaxHq][4] offset factor per channel group
+  float* sBz = sAq + 2 * kMaxHq;                           // [kMaxHq][4] 2^e * sum of Q per channel group
   uint8_t* ring = smem + kRingOffset;
-  const uint32_t bar0 = smem_addr(bars);
-  auto full_bar = [&](int r) { return bar0 + 8u * r; };
-  auto empty_bar = [&](int r) { return bar0 + 8u * (kMaxRing + r); };
+  const int R = p.ring_per_warp;
+  const uint32_t bar_w = smem_addr(bars) + 8u * (uint32_t)(warp * R);
+  uint8_t* ring_w = ring + (size_t)warp * R * p.entry_bytes;
 
+  // Items of UNIT tokens: this split's items i0 .. i0+n-1; item i0 + warp + 8k is this
+  // warp's k-th and lives in entry k % R of the warp's own ring.
   const bool window_cta = (split == p.splits);
-  const int n_slots_total = (L + kSlotTokens - 1) / kSlotTokens;
-  const int j0 = split * p.slots_per_split;
-  const int n = window_cta ? 0 : max(0, min(j0 + p.slots_per_split, n_slots_total) - j0);
+  const int n_items_total = (L + UNIT - 1) / UNIT;
+  const int i0 = split * p.items_per_split;
+  const int n = window_cta ? 0 : max(0, min(i0 + p.items_per_split, n_items_total) - i0);
+  const int nk = (n > warp) ? (n - warp + kConsumerWarps - 1) / kConsumerWarps : 0;
 
-  if (threadIdx.x == 0) {
-    for (int r = 0; r < p.n_ring; ++r) {
-      mbar_init(full_bar(r), 1);
-      mbar_init(empty_bar(r), 4);
-    }
+  // Issue the bulk copies of this warp's k-th item into entry k % R (lane 0 only).
+  auto issue = [&](int k) {
+    const int r = k % R;
+    const size_t t0 = (size_t)(i0 + warp + kConsumerWarps * k) * UNIT;
+    const size_t row0 = (size_t)unit * p.T_cap + t0;
+    const size_t blocks = (size_t)p.T_cap / C::G;
+    const uint32_t dst = smem_addr(ring_w + (size_t)r * p.entry_bytes);
+    const uint32_t fb = bar_w + 8u * r;
+    const uint64_t pol = l2_evict_first_policy();
+    mbar_arrive_expect_tx(fb, p.entry_tx);
+    bulk_g2s(dst, p.k_codes + row0 * RB, UNIT * RB, fb, pol);
+    bulk_g2s(dst + p.off_vc, p.v_codes + row0 * RB, UNIT * RB, fb, pol);
+    const size_t ks0 = (KL == 0) ? row0 * C::GK : ((size_t)unit * blocks + t0 / C::G) * kHeadDim;
+    const size_t vs0 = (VL == 0) ? row0 * C::GV : ((size_t)unit * blocks + t0 / C::G) * kHeadDim;
+    bulk_g2s(dst + p.off_ks, p.k_scale + ks0, p.sz_k_bytes, fb, pol);
+    bulk_g2s(dst + p.off_kz, p.k_off + ks0, p.sz_k_bytes, fb, pol);
+    bulk_g2s(dst + p.off_vs, p.v_scale + vs0, p.sz_v_bytes, fb, pol);
+    bulk_g2s(dst + p.off_vz, p.v_off + vs0, p.sz_v_bytes, fb, pol);
+  };
+
+  int issued = 0;
+  if (lane == 0) {
+    for (int r = 0; r < R; ++r) mbar_init(bar_w + 8u * r, 1);
     mbar_init_fence();
+    for (; issued < min(R, nk); ++issued) issue(issued);
   }
-  __syncthreads();
+  issued = __shfl_sync(FULLMASK, issued, 0);
 
   bool failed = false;
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      const uint32_t ring0 = smem_addr(ring);
-      const size_t blocks = (size_t)p.T_cap / C::G;
-      int issued = 0, r = 0, phase = 0;
-      for (int j = 0; j < n; ++j) {
-        if (j >= p.n_ring && !mbar_wait(empty_bar(r), phase ^ 1, p.status, kStatusProducerTimeout)) break;
-        const size_t t0 = (size_t)(j0 + j) * kSlotTokens;
-        const size_t row0 = (size_t)unit * p.T_cap + t0;
-        const uint32_t dst = ring0 + (uint32_t)r * p.slot_bytes;
-        const uint32_t fb = full_bar(r);
-        mbar_arrive_expect_tx(fb, p.slot_tx);
-        bulk_g2s(dst, p.k_codes + row0 * RB, kSlotTokens * RB, fb, pol);
-        bulk_g2s(dst + p.off_vc, p.v_codes + row0 * RB, kSlotTokens * RB, fb, pol);
-        const size_t ks0 = (KL == 0) ? row0 * C::GK : ((size_t)unit * blocks + t0 / C::G) * kHeadDim;
-        const size_t vs0 = (VL == 0) ? row0 * C::GV : ((size_t)unit * blocks + t0 / C::G) * kHeadDim;
-        bulk_g2s(dst + p.off_ks, p.k_scale + ks0, p.sz_k_bytes, fb, pol);
-        bulk_g2s(dst + p.off_kz, p.k_off + ks0, p.sz_k_bytes, fb, pol);
-        bulk_g2s(dst + p.off_vs, p.v_scale + vs0, p.sz_v_bytes, fb, pol);
-        bulk_g2s(dst + p.off_vz, p.v_off + vs0, p.sz_v_bytes, fb, pol);
-        issued = j + 1;
-        if (++r == p.n_ring) {
-          r = 0;
-          phase ^= 1;
-        }
-      }
-      // every copy issued must have landed before shared memory is reused or freed
-      for (int j = max(0, issued - p.n_ring); j < issued; ++j)
-        if (!mbar_wait(full_bar(j % p.n_ring), (j / p.n_ring) & 1, p.status, kStatusDrainTimeout)) break;
+  // Stage Q (fp32) and the per-query constants.
+  for (int idx = threadIdx.x; idx < hq * D; idx += kThreads)
+    sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
+  __syncthreads();
+  if (warp < hq) {
+    // query exponent e: max |Q / factor| * 2^e in [2^13, 2^14), so Q * 2^e / factor is an
+    // exact fp16 (a bf16 has 8 significant bits); channel-group sums of Q for the K offset
+    const int i = warp;
+    float amax = 0.f;
+    float gs = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int ch = 4 * lane + u;
+      const float v = sQ[i * D + ch];
+      amax = fmaxf(amax, fabsf(v) * (1.f / k_mult<BITS>(ch)));
+      gs += v;
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, o));
+    constexpr int lanes_per_group = C::G / 4;  // 8, 16 or 32
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float other = __shfl_xor_sync(FULLMASK, gs, o);
+      if (o < lanes_per_group) gs += other;
+    }
+    int e = 0;
+    if (amax > 0.f) e = min(100, max(-100, 13 - ilog2f(amax)));
+    if (lane == 0) {
+      sEq[i] = e;
+      sAq[i] = p.sl2 * exp2i(-e);
+    }
+    if (KL == 0 && (lane % lanes_per_group) == 0) sBz[i * 4 + lane / lanes_per_group] = exp2i(e) * gs;
+  }
+  __syncthreads();
+
+  LaneCols lc;
+  lc.g = g;
+  lc.c = c;
+  lc.lane = lane;
+  lc.hq = hq;
+  lc.u_lane = (GV == 1) ? 0 : (16 * g) / C::G;  // V channel group of this lane's 16 channels
+  if (GV >= 2) {
+    const int el = ((lc.u_lane - 2 * c) % GV + GV) % GV;
+    lc.e_live = el <= 1 ? el : -1;
   } else {
-    // ----------------------------------------------------------- consumers
-    // Stage Q (fp32) and the per-query constants.
-    for (int idx = threadIdx.x; idx < hq * D; idx += 32 * kConsumerWarps)
-      sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
-    named_sync(1, 32 * kConsumerWarps);
-    if (warp < hq) {
-      // query exponent e: max |Q / factor| * 2^e in [2^13, 2^14), so Q * 2^e / factor is an
-      // exact fp16 (a bf16 has 8 significant bits); channel-group sums of Q for the K offset
-      const int i = warp;
-      float amax = 0.f;
-      float gs = 0.f;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int ch = 4 * lane + u;
-        const float v = sQ[i * D + ch];
-        amax = fmaxf(amax, fabsf(v) * (1.f / k_mult<BITS>(ch)));
-        gs += v;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, o));
-      constexpr int lanes_per_group = C::G / 4;  // 8, 16 or 32
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float other = __shfl_xor_sync(FULLMASK, gs, o);
-        if (o < lanes_per_group) gs += other;
-      }
-      int e = 0;
-      if (amax > 0.f) e = min(100, max(-100, 13 - ilog2f(amax)));
-      if (lane == 0) {
-        sEq[i] = e;
-        sAq[i] = p.sl2 * exp2i(-e);
-      }
-      if (KL == 0 && (lane % lanes_per_group) == 0) sBz[i * 4 + lane / lanes_per_group] = p.sl2 * gs;
-    }
-    named_sync(1, 32 * kConsumerWarps);
+    lc.e_live = 0;
+  }
 
-    WarpState<C> st;
-    if (KL == 0) {
-      // token-wise K: B fragments Q' = Q 2^e / factor (exact fp16), fixed for the CTA, and
-      // the magic bias 1024 * sum of Q' per channel group
-      const int q = g;
-      const bool live = q < hq;
-      const float sc = live ? exp2i(sEq[q]) : 0.f;
-      float gsum[GK];
+  WarpState<C> st;
+  if (KL == 0) {
+    // token-wise K: B fragments Q' = Q 2^e / factor (exact fp16) of this lane's column
+    // (column g), fixed for the CTA, and minus the magic bias 1024 * sum of Q' per channel
+    // group of accumulator columns 2c and 2c+1
+    const int qb = qk_query<C>(g, hq);
+    const bool live = qb >= 0;
+    const float sc = live ? exp2i(sEq[qb]) : 0.f;
+    float gsum[GK];
 #pragma unroll
-      for (int u = 0; u < GK; ++u) gsum[u] = 0.f;
+    for (int u = 0; u < GK; ++u) gsum[u] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+    for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float x[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
-            x[e] = live ? sQ[q * D + ch] * sc * (1.f / k_mult<BITS>(ch)) : 0.f;
-          }
-          st.qB[ks][r] = f16x2_from(x[0], x[1]);
-          gsum[ks / C::KSG] += x[0] + x[1];
-        }
-#pragma unroll
-      for (int u = 0; u < GK; ++u) {
-        gsum[u] += __shfl_xor_sync(FULLMASK, gsum[u], 1);
-        gsum[u] += __shfl_xor_sync(FULLMASK, gsum[u], 2);
-      }
-#pragma unroll
-      for (int ql = 0; ql < 2; ++ql) {  // query 2c + ql is B column 2c + ql, held by lane 8c + 4ql
-        const int qq = min(2 * c + ql, hq - 1);
-        st.aq[ql] = sAq[qq];
-#pragma unroll
-        for (int u = 0; u < GK; ++u) {
-          st.c1[ql][u] = kMagicF * __shfl_sync(FULLMASK, gsum[u], 8 * c + 4 * ql);
-          st.bz[ql][u] = sBz[qq * 4 + u];
-        }
-      }
-    }
-#pragma unroll
-    for (int ql = 0; ql < 2; ++ql) {
-      st.m_run[ql] = -INFINITY;
-      st.l_part[ql] = 0.f;
-#pragma unroll
-      for (int u = 0; u < GV; ++u) st.zacc[ql][u] = 0.f;
-    }
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int row = 0; row < 2; ++row)
-#pragma unroll
-        for (int v = 0; v < NTV; ++v) st.o_run[mt][row][v][0] = st.o_run[mt][row][v][1] = 0.f;
-
-    const int quad = warp >> 2, sub = warp & 3;
-    const int rel0 = kChunk * sub;  // chunk start inside a slot
-    int r = quad, phase = 0;        // ring slot and its phase for slot j
-    for (int j = quad; j < n; j += kQuads) {
-      if (!mbar_wait(full_bar(r), phase, p.status, kStatusConsumerTimeout)) {
-        failed = true;
-        break;
-      }
-      const uint8_t* slot = ring + (size_t)r * p.slot_bytes;
-      ChunkSmem sm;
-      sm.kc = slot;
-      sm.vc = slot + p.off_vc;
-      sm.ks = reinterpret_cast<const __half*>(slot + p.off_ks);
-      sm.kz = reinterpret_cast<const __half*>(slot + p.off_kz);
-      sm.vs = reinterpret_cast<const __half*>(slot + p.off_vs);
-      sm.vz = reinterpret_cast<const __half*>(slot + p.off_vz);
-      sm.sQ = sQ;
-      sm.sEq = sEq;
-      const int tc = (j0 + j) * kSlotTokens + rel0;  // chunk start token
-      const int nv = min(kChunk, L - tc);            // valid tokens in the chunk
-      if (nv == kChunk)
-        process_chunk<C, true>(st, sm, rel0, nv, hq, p.sl2, lane);
-      else if (nv > 0)
-        process_chunk<C, false>(st, sm, rel0, nv, hq, p.sl2, lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(r));
-      r += kQuads;
-      if (r >= p.n_ring) {
-        r -= p.n_ring;
-        phase ^= 1;
-      }
-    }
-
-    // ---------------------------------------------------- warp results
-    if (!window_cta) {
-      named_sync(1, 32 * kConsumerWarps);  // every slot consumed: the ring is free
-      float* sM = reinterpret_cast<float*>(ring);  // [warps][kMaxHq]
-      float* sL = sM + kConsumerWarps * kMaxHq;    // [warps][kMaxHq]
-      float* sO = sL + kConsumerWarps * kMaxHq;    // [warps][kMaxHq][D]
-      float zsum[2][GV];
-#pragma unroll
-      for (int ql = 0; ql < 2; ++ql) {
-        float l = st.l_part[ql];
-        l += __shfl_xor_sync(FULLMASK, l, 4);
-        l += __shfl_xor_sync(FULLMASK, l, 8);
-        l += __shfl_xor_sync(FULLMASK, l, 16);
-#pragma unroll
-        for (int u = 0; u < GV; ++u) {
-          float z = st.zacc[ql][u];
-          z += __shfl_xor_sync(FULLMASK, z, 4);
-          z += __shfl_xor_sync(FULLMASK, z, 8);
-          z += __shfl_xor_sync(FULLMASK, z, 16);
-          zsum[ql][u] = z;
-        }
-        const int i = 2 * c + ql;
-        if (g == 0 && i < hq) {
-          sM[warp * kMaxHq + i] = st.m_run[ql];
-          sL[warp * kMaxHq + i] = l;
-        }
-      }
-      // output column 8v + 2c + e is (query, group) = (col / GV, col % GV); its channels are
-      // this lane's 16, all in channel group 16g / G
-      const int u_lane = (16 * g) / C::G;
-#pragma unroll
-      for (int v = 0; v < NTV; ++v)
+      for (int r = 0; r < 2; ++r) {
+        float xx[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int col = 8 * v + 2 * c + e;
-          const int i = col / GV, u = col % GV;
-          float zt = 0.f;
-          if (VL == 0) {  // the value-offset term of (query i, group u) lives on lane i/2
-#pragma unroll
-            for (int ql = 0; ql < 2; ++ql)
-#pragma unroll
-              for (int uu = 0; uu < GV; ++uu) {
-                const float x = __shfl_sync(FULLMASK, zsum[ql][uu], i >> 1);
-                if (ql == (i & 1) && uu == u) zt = x;
-              }
-          }
-          if (i < hq && (GV == 1 || u == u_lane)) {
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-              for (int row = 0; row < 2; ++row) {
-                const int ch = (BITS == 2) ? 16 * g + 8 * row + mt : 16 * g + 8 * (mt >> 2) + 4 * row + (mt & 3);
-                sO[(warp * kMaxHq + i) * D + ch] = st.o_run[mt][row][v][e] + zt;
-              }
-          }
+          const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
+          xx[e] = live ? sQ[qb * D + ch] * sc * (1.f / k_mult<BITS>(ch)) : 0.f;
         }
+        st.qB[ks][r] = f16x2_from(xx[0], xx[1]);
+        gsum[ks / C::KSG] += xx[0] + xx[1];
+      }
+#pragma unroll
+    for (int u = 0; u < GK; ++u) {
+      gsum[u] += __shfl_xor_sync(FULLMASK, gsum[u], 1);
+      gsum[u] += __shfl_xor_sync(FULLMASK, gsum[u], 2);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+      for (int u = 0; u < GK; ++u) st.kbias[jj][u] = -kMagicF * __shfl_sync(FULLMASK, gsum[u], 8 * c + 4 * jj);
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      const int qs = qk_query<C>(2 * c + j, hq);
+      st.pa[j] = qs >= 0 ? sAq[qs] : 1.f;
+#pragma unroll
+      for (int u = 0; u < GK; ++u) st.bzq[j][u] = qs >= 0 ? sBz[qs * 4 + u] : 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) st.pa[j] = 1.f;
+  }
+#pragma unroll
+  for (int j = 0; j < NQ; ++j) {
+    st.m_run[j] = -INFINITY;
+    st.l[j] = 0.f;
+  }
+#pragma unroll
+  for (int o = 0; o < NO; ++o) st.zacc[o] = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int row = 0; row < 2; ++row)
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] = 0.f;
+
+  // ------------------------------------------------------------ this warp's items
+  int k = 0;
+  for (; k < nk; ++k) {
+    const int r = k % R;
+    if (!mbar_wait(bar_w + 8u * r, (k / R) & 1, p.status, kStatusConsumerTimeout)) {
+      failed = true;
+      break;
+    }
+    const uint8_t* e = ring_w + (size_t)r * p.entry_bytes;
+    SlotSmem sm;
+    sm.kc = e;
+    sm.vc = e + p.off_vc;
+    sm.ks = reinterpret_cast<const __half*>(e + p.off_ks);
+    sm.kz = reinterpret_cast<const __half*>(e + p.off_kz);
+    sm.vs = reinterpret_cast<const __half*>(e + p.off_vs);
+    sm.vz = reinterpret_cast<const __half*>(e + p.off_vz);
+    const int nv = min(UNIT, L - (i0 + warp + kConsumerWarps * k) * UNIT);  // valid tokens, >= 1
+    if (nv == UNIT)
+      process_unit<C, true>(st, sm, nv, sQ, p.sl2, lc);
+    else
+      process_unit<C, false>(st, sm, nv, sQ, p.sl2, lc);
+    __syncwarp();
+    if (k + R < nk) {
+      // the entry's reads are done: refill it with item k + R
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(k + R);
+      }
+      ++issued;
+    }
+  }
+  if (failed && lane == 0) {
+    // every copy issued must have landed before shared memory is reused or freed
+    for (int kk = k; kk < issued; ++kk)
+      if (!mbar_wait(bar_w + 8u * (kk % R), (kk / R) & 1, p.status, kStatusDrainTimeout)) break;
+  }
+  __syncwarp();
+
+  // ---------------------------------------------------- warp results
+  if (!window_cta) {
+    __syncthreads();  // every entry consumed: the ring is free
+    float* sM = reinterpret_cast<float*>(ring);  // [warps][kMaxHq]
+    float* sL = sM + kConsumerWarps * kMaxHq;    // [warps][kMaxHq]
+    float* sO = sL + kConsumerWarps * kMaxHq;    // [warps][kMaxHq][D]
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      float l = st.l[j];
+      l += __shfl_xor_sync(FULLMASK, l, 4);
+      l += __shfl_xor_sync(FULLMASK, l, 8);
+      l += __shfl_xor_sync(FULLMASK, l, 16);
+      const int q = qk_query<C>(2 * c + j, hq);
+      if (g == 0 && q >= 0) {
+        sM[warp * kMaxHq + q] = (st.m_run[j] == -INFINITY) ? -INFINITY : st.pa[j] * st.m_run[j];
+        sL[warp * kMaxHq + q] = l;
+      }
+    }
+    float zs[NO];
+#pragma unroll
+    for (int o = 0; o < NO; ++o) {
+      float z = st.zacc[o];
+      z += __shfl_xor_sync(FULLMASK, z, 4);
+      z += __shfl_xor_sync(FULLMASK, z, 8);
+      z += __shfl_xor_sync(FULLMASK, z, 16);
+      zs[o] = z;
+    }
+    // live column i holds owned combo o = (query, V group); this lane's 16 channels
+    // 16g..16g+15 all lie in V group u_lane
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      const int o = live_own<C>(i, lc);
+      if (o < 0) continue;
+      const int combo = own_combo<C>(c, o);
+      if (combo >= hq * GV || combo % GV != lc.u_lane) continue;
+      const int q = combo / GV;
+      float zt = 0.f;
+      if (VL == 0) {
+#pragma unroll
+        for (int oo = 0; oo < NO; ++oo)
+          if (oo == o) zt = zs[oo];
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int row = 0; row < 2; ++row)
+          sO[(warp * kMaxHq + q) * D + 16 * g + pv_channel<BITS>(mt, row)] = st.o_run[mt][row][i] + zt;
     }
   }
 
   // ---------------------------------------------------- window split
-  if (window_cta && warp < kConsumerWarps) {
+  if (window_cta) {
     float* sM = reinterpret_cast<float*>(ring);
     float* sL = sM + kConsumerWarps * kMaxHq;
     float* sO = sL + kConsumerWarps * kMaxHq;
@@ -879,11 +1057,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
 
   // ---------------------------------------------------- merge the warps, write the partial
   __syncthreads();
-  if (warp < kConsumerWarps && !failed) {
+  if (!failed) {
     const float* sM = reinterpret_cast<const float*>(ring);
     const float* sL = sM + kConsumerWarps * kMaxHq;
     const float* sO = sL + kConsumerWarps * kMaxHq;
-    for (int idx = threadIdx.x; idx < hq * D; idx += 32 * kConsumerWarps) {
+    for (int idx = threadIdx.x; idx < hq * D; idx += kThreads) {
       const int i = idx / D, ch = idx % D;
       float M = -INFINITY;
 #pragma unroll

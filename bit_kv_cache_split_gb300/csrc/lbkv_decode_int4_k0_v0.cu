@@ -1,0 +1,23 @@
+// lbkv_decode_int4_k0_v0.cu -- instantiations of the split-decode kernel for
+// 4-bit codes with a token-wise K side and a token-wise V side.
+#include "lbkv_internal.h"
+
+namespace lbkv {
+
+template <>
+DecodeKernel decode_kernel<4, 0, 0>(int mode, int log2g) {
+#define LBKV_PICK(M, LG) \
+  if (mode == M && log2g == LG) return &split_decode_kernel<Cfg<4, 0, 0, M, LG>>;
+  LBKV_PICK(kModeDup, 7)
+  LBKV_PICK(kModePair, 7)
+  LBKV_PICK(kModeDup, 6)
+  LBKV_PICK(kModePair, 6)
+  LBKV_PICK(kModeWide, 6)
+  LBKV_PICK(kModeDup, 5)
+  LBKV_PICK(kModePair, 5)
+  LBKV_PICK(kModeWide, 5)
+#undef LBKV_PICK
+  return nullptr;
+}
+
+}  // namespace lbkv

@@ -12,9 +12,8 @@ namespace lbkv {
 
 // Device status codes written to the workspace status word instead of hanging.
 enum : int32_t {
-  kStatusConsumerTimeout = 1,
-  kStatusProducerTimeout = 2,
-  kStatusDrainTimeout = 3,
+  kStatusConsumerTimeout = 1,  // a warp waited ~1 s for its own bulk copies
+  kStatusDrainTimeout = 3,     // after that, the copies still in flight did not land
 };
 
 // A bounded wait gives up after this many nanoseconds of wall time.
@@ -93,6 +92,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// Orders this thread's earlier generic-proxy shared-memory accesses before its later
+// async-proxy ones (a bulk copy refilling a buffer that was just read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Named barrier among `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -121,6 +126,15 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A * B + C with a separate starting value C (the first product of a chain).
+__device__ __forceinline__ void mma_f16_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
 
 // fp16 magic number 1024: OR-ing a small integer m into its mantissa gives the

@@ -19,11 +19,18 @@ int launch_pack(const PackArgs& a, cudaStream_t stream);
 
 using DecodeKernel = void (*)(const DecodeParams);
 
-// Instantiated kernel for (v_layout, PV n-tiles, log2 group) of one bit width and
-// K layout, or nullptr when that combination is not built.
-DecodeKernel decode_kernel_int2_k0(int vl, int ntv, int log2g);
-DecodeKernel decode_kernel_int2_k1(int vl, int ntv, int log2g);
-DecodeKernel decode_kernel_int4_k0(int vl, int ntv, int log2g);
-DecodeKernel decode_kernel_int4_k1(int vl, int ntv, int log2g);
+// Instantiated kernel for (column mode, log2 group) of one bit width and K/V
+// layout pair, or nullptr when that combination is not built. One translation
+// unit per specialisation.
+template <int BITS, int KL, int VL>
+DecodeKernel decode_kernel(int mode, int log2g);
+template <> DecodeKernel decode_kernel<2, 0, 0>(int, int);
+template <> DecodeKernel decode_kernel<2, 0, 1>(int, int);
+template <> DecodeKernel decode_kernel<2, 1, 0>(int, int);
+template <> DecodeKernel decode_kernel<2, 1, 1>(int, int);
+template <> DecodeKernel decode_kernel<4, 0, 0>(int, int);
+template <> DecodeKernel decode_kernel<4, 0, 1>(int, int);
+template <> DecodeKernel decode_kernel<4, 1, 0>(int, int);
+template <> DecodeKernel decode_kernel<4, 1, 1>(int, int);
 
 }  // namespace lbkv
