@@ -55,14 +55,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 struct Plan {
-  int hq, mode, gv;
-  int splits, s_tot, items_per_split, unit_tokens;
-  int ring_per_warp, entry_bytes, entry_tx, smem_bytes;
+  int hq, mode, gv, win;
+  int unit_tokens, ipu, n_cta, n_slots;
+  long long tot_items;
+  int ring_off, ring_per_warp, entry_bytes, entry_tx, smem_bytes;
   int off_vc, off_ks, off_kz, off_vs, off_vz, sz_k, sz_v;
   size_t off_done, off_ml, off_o, ws_bytes;
 };
 
-// Validates shapes and format, then fixes the split count and the ring.
+// Validates shapes and format, then fixes the persistent grid and the rings.
 int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl) {
   if (!d) return LBKV_EINVAL;
   if (d->batch < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0) return LBKV_EINVAL;
@@ -105,39 +106,27 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   pl->off_vz = pl->off_vs + pl->sz_v;
   pl->entry_tx = pl->off_vz + pl->sz_v;
   pl->entry_bytes = (int)round_up((size_t)pl->entry_tx, 128);
-  const int budget = smem_optin - kRingOffset;
+  pl->ring_off = kPrologueBytes + merge_bytes(hq);
+  const int budget = smem_optin - pl->ring_off;
   int r_w = budget / (kConsumerWarps * pl->entry_bytes);
   if (r_w > kMaxRing / kConsumerWarps) r_w = kMaxRing / kConsumerWarps;
-  if (r_w < 1 || (size_t)kConsumerWarps * r_w * pl->entry_bytes < (size_t)kMergeBytes) return LBKV_EUNSUPPORTED;
+  if (r_w < 1) return LBKV_EUNSUPPORTED;
   pl->ring_per_warp = r_w;
-  pl->smem_bytes = kRingOffset + kConsumerWarps * r_w * pl->entry_bytes;
+  pl->smem_bytes = pl->ring_off + kConsumerWarps * r_w * pl->entry_bytes;
 
-  // Split count: minimise waves * (items per warp + fill), one CTA per SM; time in
-  // units of one warp's 128-token item.
+  // Persistent grid: the items of all pairs (ipu per pair) split evenly over at most
+  // one CTA per SM. A pair spans at most ceil(n_cta / pairs) + 1 CTAs, each writing
+  // one partial slot; one more slot holds the window's partial.
   const long long units = (long long)d->batch * d->num_kv_heads;
-  const int ipu = d->max_seq_len / ut;  // items per (sequence, KV head)
-  int best_s = 1;
-  double best_cost = 1e300;
-  if (units > 0) {
-    const int s_max = ipu < 64 ? ipu : 64;
-    for (int s = 1; s <= s_max; ++s) {
-      const long long ctas = units * s;
-      const double waves = std::ceil((double)ctas / sms);
-      const int ips = (ipu + s - 1) / s;
-      const double per = std::ceil((double)ips / kConsumerWarps) * ut / 128.0 + 2.0;
-      const double cost = waves * per;
-      if (cost < best_cost - 1e-9) {
-        best_cost = cost;
-        best_s = s;
-      }
-    }
-  }
-  pl->splits = best_s;
-  pl->items_per_split = (ipu + best_s - 1) / best_s;
-  pl->s_tot = best_s + (win ? 1 : 0);
+  pl->win = win ? 1 : 0;
+  pl->ipu = d->max_seq_len / ut;
+  pl->tot_items = units * pl->ipu;
+  pl->n_cta = (int)(pl->tot_items < sms ? pl->tot_items : sms);
+  pl->n_slots = 0;
+  if (units > 0) pl->n_slots = (int)((pl->n_cta + units - 1) / units) + 1 + pl->win;
 
-  // workspace: status word | per-unit split counters | (m, l) partials | O partials
-  const size_t rows = (size_t)d->batch * d->num_q_heads * pl->s_tot;
+  // workspace: status word | per-pair counters | (m, l) partials | O partials
+  const size_t rows = (size_t)units * pl->n_slots * hq;
   pl->off_done = 256;
   pl->off_ml = round_up(pl->off_done + (size_t)units * sizeof(int32_t), 256);
   pl->off_o = round_up(pl->off_ml + rows * sizeof(float2), 256);
@@ -210,9 +199,12 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.win_cap = desc->k_win ? desc->win_cap : 0;
   const float sigma = desc->sm_scale > 0.f ? desc->sm_scale : 1.f / std::sqrt((float)desc->head_dim);
   p.sl2 = sigma * 1.4426950408889634f;
-  p.splits = pl.splits;
-  p.s_tot = pl.s_tot;
-  p.items_per_split = pl.items_per_split;
+  p.tot_items = pl.tot_items;
+  p.ipu = pl.ipu;
+  p.n_cta = pl.n_cta;
+  p.n_slots = pl.n_slots;
+  p.has_win = pl.win;
+  p.ring_off = pl.ring_off;
   p.ring_per_warp = pl.ring_per_warp;
   p.entry_bytes = pl.entry_bytes;
   p.entry_tx = pl.entry_tx;
@@ -226,8 +218,8 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
 
   if (ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem_bytes) != LBKV_OK) return LBKV_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  dim3 grid((unsigned)pl.s_tot, (unsigned)desc->num_kv_heads, (unsigned)desc->batch);
-  kern<<<grid, kThreads, pl.smem_bytes, s>>>(p);
+  if (pl.win && launch_window_partial(p, s) != 0) return LBKV_ECUDA;
+  kern<<<(unsigned)pl.n_cta, kThreads, pl.smem_bytes, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;
   return LBKV_OK;
 }

@@ -10,16 +10,18 @@
 // group boundary) and fold table (token-wise K: acc-fold, channel-wise K:
 // operand-fold on Q, token-wise V: operand-fold on P, channel-wise V: acc-fold).
 //
-// Kernel design (sm_103a). One CTA per (sequence, KV head, split); the split's
-// tokens form items of 32, 64 or 128 tokens dealt to the 8 warps in turn. Each
-// warp streams its items' packed codes and fp16 scales/offsets through its own
-// ring in shared memory with 1-D bulk copies that it issues itself (an mbarrier
-// per entry, bounded waits, no multicast), so no warp waits on another's
-// progress. Per item a warp scores all its tokens (QK^T with the K fold),
-// updates its running maximum once, then forms the weights and accumulates PV
-// chunk by chunk with the V fold. The CTA then merges its warps into one split
-// partial, and the last split of a (sequence, KV head) to finish merges all
-// splits into the bf16 output.
+// Kernel design (sm_103a). A persistent grid, one CTA per SM. The tokens of all
+// (sequence, KV head) pairs form items of 32, 64 or 128 tokens in one sequence;
+// each CTA takes an equal contiguous share and deals it to its 8 warps in turn.
+// Each warp streams its items' packed codes and fp16 scales/offsets through its
+// own ring in shared memory with 1-D bulk copies that it issues itself (an
+// mbarrier per entry, bounded waits, no multicast), so no warp waits on
+// another's progress. Per item a warp scores all its tokens (QK^T with the K
+// fold), updates its running maximum once, then forms the weights and
+// accumulates PV chunk by chunk with the V fold. Where the CTA's share moves to
+// the next pair, its warps merge into one partial for the pair; the last CTA of
+// a pair to finish merges the pair's partials into the bf16 output. A bf16
+// window after the cached tokens is scored by a separate small kernel first.
 //
 // Operands. OR-ing a code q (times a power-of-two position factor m) into the
 // mantissa of the fp16 magic number 1024 gives the exact fp16 value 1024 + m q,
@@ -56,11 +58,14 @@ constexpr int kConsumerWarps = LBKV_CONSUMER_WARPS;
 constexpr int kThreads = 32 * kConsumerWarps;
 constexpr int kMaxRing = 48;  // ring entries of all warps (one mbarrier each)
 constexpr int kMaxHq = 8;
-// shared-memory map: barriers | Q (fp32) and per-query constants | rings
+// shared-memory map: barriers | Q (fp32) and per-query constants | merge area | rings
 constexpr int kBarBytes = kMaxRing * 8;
-constexpr int kRingOffset = 8192;
-static_assert(kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq) <= kRingOffset, "prologue fits");
-constexpr int kMergeBytes = kConsumerWarps * kMaxHq * (kHeadDim + 2) * 4;
+constexpr int kPrologueBytes = 8192;
+static_assert(kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq) <= kPrologueBytes, "prologue fits");
+// merge area for hq queries per KV head: per warp (m, l) of kMaxHq queries and o of hq
+__host__ __device__ constexpr int merge_bytes(int hq) {
+  return (4 * kConsumerWarps * (2 * kMaxHq + hq * kHeadDim) + 127) / 128 * 128;
+}
 
 constexpr int kModeDup = 0;   // <= 4 combos: combo k on columns 2k, 2k+1
 constexpr int kModePair = 1;  // 8 combos: combo k on column k
@@ -87,15 +92,17 @@ struct DecodeParams {
   const __nv_bfloat16* k_win;
   const __nv_bfloat16* v_win;
   const int32_t* win_lens;
-  float2* part_ml;  // [B][Hq][s_tot] (running max in log2 units, denominator)
-  float* part_o;    // [B][Hq][s_tot][D] unnormalised output
+  float2* part_ml;  // [B*Hkv][n_slots][hq] (running max in log2 units, denominator)
+  float* part_o;    // [B*Hkv][n_slots][hq][D] unnormalised output
   int32_t* status;
-  int32_t* done;    // [B][Hkv] splits finished; the last one merges and resets it to 0
+  int32_t* done;    // [B*Hkv] CTAs finished with a pair; the last one merges and resets it to 0
   __nv_bfloat16* out;
   int B, Hq, Hkv, hq, T_cap, win_cap;
   float sl2;  // softmax scale times log2(e)
-  int splits, s_tot, items_per_split;
-  int ring_per_warp, entry_bytes, entry_tx;
+  long long tot_items;  // B * Hkv * ipu
+  int ipu, n_cta;       // items per pair (T_cap / UNIT), CTAs of the grid
+  int n_slots, has_win; // partial slots per pair (the last one the window's when has_win)
+  int ring_off, ring_per_warp, entry_bytes, entry_tx;
   int off_vc, off_ks, off_kz, off_vs, off_vz;  // byte offsets inside a ring entry
   int sz_k_bytes, sz_v_bytes;                  // bytes of one scale (or offset) array per entry
 };
@@ -268,7 +275,7 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
   }
 }
 
-// QK^T of one 32-token chunk starting at entry token rel0, with the K fold.
+// QK^T of one 32-token chunk starting at slot token rel0, with the K fold.
 // x[mt][row][j]: token rel0 + 16 mt + 2 g + row, query slot j; token-wise K in
 // units of pa[j], channel-wise K in log2 units.
 template <class C>
@@ -745,6 +752,28 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
 }
 
 // ------------------------------------------------------------------------
+// Work split. The items (UNIT tokens) of all (sequence, KV head) pairs form one
+// sequence, pair u owning items u*ipu .. u*ipu+ipu-1 (ipu = T_cap / UNIT; items
+// past the sequence length are empty). CTA c of the persistent grid takes items
+// first_item(c) .. first_item(c+1)-1 and deals them to its warps in turn.
+// ------------------------------------------------------------------------
+__host__ __device__ inline long long first_item(long long c, long long tot, long long n_cta) {
+  return c * tot / n_cta;
+}
+// The CTA whose range holds item x.
+__host__ __device__ inline int cta_of(long long x, long long tot, long long n_cta) {
+  return (int)(((x + 1) * n_cta - 1) / tot);
+}
+
+// Writes one merged partial (or, when it is the only one, the output) of pair u:
+// the CTA's warps deposited (m, l, o) per query in the merge area.
+struct MergeArea {
+  float* m;  // [warps][kMaxHq] running maximum (log2 units)
+  float* l;  // [warps][kMaxHq] denominator
+  float* o;  // [warps][hq][D] unnormalised output
+};
+
+// ------------------------------------------------------------------------
 // The kernel: see the file comment. C = Cfg<BITS, KL, VL, MODE, LOG2G>.
 // ------------------------------------------------------------------------
 template <class C>
@@ -756,34 +785,31 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int cta = blockIdx.x;
   const int hq = p.hq;
-  const int unit = b * p.Hkv + kvh;
-  const int L = min(max(p.seq_lens[b], 0), p.T_cap);  // device value: clamped, never trusted
+  const long long X0 = first_item(cta, p.tot_items, p.n_cta);
+  const long long X1 = first_item(cta + 1, p.tot_items, p.n_cta);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);      // full[warp][ring_per_warp]
   float* sQ = reinterpret_cast<float*>(smem + kBarBytes);  // [kMaxHq][D]
   float* sAq = sQ + kMaxHq * D;                            // [kMaxHq] token-wise K score factor
   int* sEq = reinterpret_cast<int*>(sAq + kMaxHq);         // [kMaxHq] query exponent
   float* sBz = sAq + 2 * kMaxHq;                           // [kMaxHq][4] 2^e * sum of Q per channel group
-  uint8_t* ring = smem + kRingOffset;
+  MergeArea ma;
+  ma.m = reinterpret_cast<float*>(smem + kPrologueBytes);
+  ma.l = ma.m + kConsumerWarps * kMaxHq;
+  ma.o = ma.l + kConsumerWarps * kMaxHq;
+  uint8_t* ring = smem + p.ring_off;
+  __shared__ int s_last;
+
   const int R = p.ring_per_warp;
   const uint32_t bar_w = smem_addr(bars) + 8u * (uint32_t)(warp * R);
   uint8_t* ring_w = ring + (size_t)warp * R * p.entry_bytes;
 
-  // Items of UNIT tokens: this split's items i0 .. i0+n-1; item i0 + warp + 8k is this
-  // warp's k-th and lives in entry k % R of the warp's own ring.
-  const bool window_cta = (split == p.splits);
-  const int n_items_total = (L + UNIT - 1) / UNIT;
-  const int i0 = split * p.items_per_split;
-  const int n = window_cta ? 0 : max(0, min(i0 + p.items_per_split, n_items_total) - i0);
-  const int nk = (n > warp) ? (n - warp + kConsumerWarps - 1) / kConsumerWarps : 0;
-
-  // Issue the bulk copies of this warp's k-th item into entry k % R (lane 0 only).
-  auto issue = [&](int k) {
-    const int r = k % R;
-    const size_t t0 = (size_t)(i0 + warp + kConsumerWarps * k) * UNIT;
-    const size_t row0 = (size_t)unit * p.T_cap + t0;
+  // Bulk copies of item t of pair u into entry r of this warp's ring (lane 0 only).
+  auto copy_item = [&](int u, int t, int r) {
+    const size_t t0 = (size_t)t * UNIT;
+    const size_t row0 = (size_t)u * p.T_cap + t0;
     const size_t blocks = (size_t)p.T_cap / C::G;
     const uint32_t dst = smem_addr(ring_w + (size_t)r * p.entry_bytes);
     const uint32_t fb = bar_w + 8u * r;
@@ -791,174 +817,215 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
     mbar_arrive_expect_tx(fb, p.entry_tx);
     bulk_g2s(dst, p.k_codes + row0 * RB, UNIT * RB, fb, pol);
     bulk_g2s(dst + p.off_vc, p.v_codes + row0 * RB, UNIT * RB, fb, pol);
-    const size_t ks0 = (KL == 0) ? row0 * C::GK : ((size_t)unit * blocks + t0 / C::G) * kHeadDim;
-    const size_t vs0 = (VL == 0) ? row0 * C::GV : ((size_t)unit * blocks + t0 / C::G) * kHeadDim;
+    const size_t ks0 = (KL == 0) ? row0 * C::GK : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
+    const size_t vs0 = (VL == 0) ? row0 * C::GV : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
     bulk_g2s(dst + p.off_ks, p.k_scale + ks0, p.sz_k_bytes, fb, pol);
     bulk_g2s(dst + p.off_kz, p.k_off + ks0, p.sz_k_bytes, fb, pol);
     bulk_g2s(dst + p.off_vs, p.v_scale + vs0, p.sz_v_bytes, fb, pol);
     bulk_g2s(dst + p.off_vz, p.v_off + vs0, p.sz_v_bytes, fb, pol);
   };
 
-  int issued = 0;
+  // This warp's items are local indices warp, warp + W, ... of the CTA range; the
+  // non-empty ones go through entries 0, 1, .., R-1, 0, ... of its ring in order.
+  // Two cursors walk them without divisions: one issuing copies ahead, one consuming.
+  const int NL = (int)(X1 - X0);
+  const int n_pairs = p.B * p.Hkv;
+  struct Cursor {
+    int i, u, t, L;  // local item index, pair, item within the pair, valid tokens of the pair
+  };
+  auto pair_len = [&](int u) { return u < n_pairs ? min(max(__ldg(p.seq_lens + u / p.Hkv), 0), p.T_cap) : 0; };
+  auto cursor_start = [&]() {
+    Cursor k;
+    k.i = warp;
+    const long long x = X0 + warp;
+    k.u = (int)(x / p.ipu);
+    k.t = (int)(x - (long long)k.u * p.ipu);
+    k.L = pair_len(k.u);
+    return k;
+  };
+  auto cursor_next = [&](Cursor& k) {
+    k.i += kConsumerWarps;
+    k.t += kConsumerWarps;
+    if (k.t >= p.ipu) {
+      do {
+        k.t -= p.ipu;
+        ++k.u;
+      } while (k.t >= p.ipu);
+      k.L = (k.i < NL) ? pair_len(k.u) : 0;
+    }
+  };
+  Cursor iss = cursor_start();
+  int r_iss = 0, n_issued = 0;
+  auto issue_next = [&]() {
+    for (; iss.i < NL; cursor_next(iss)) {
+      if (iss.t * UNIT < iss.L) {
+        if (lane == 0) {
+          fence_proxy_async_smem();  // earlier reads of the entry come before its refill
+          copy_item(iss.u, iss.t, r_iss);
+        }
+        ++n_issued;
+        if (++r_iss == R) r_iss = 0;
+        cursor_next(iss);
+        return;
+      }
+    }
+  };
   if (lane == 0) {
     for (int r = 0; r < R; ++r) mbar_init(bar_w + 8u * r, 1);
     mbar_init_fence();
-    for (; issued < min(R, nk); ++issued) issue(issued);
-  }
-  issued = __shfl_sync(FULLMASK, issued, 0);
-
-  bool failed = false;
-
-  // Stage Q (fp32) and the per-query constants.
-  for (int idx = threadIdx.x; idx < hq * D; idx += kThreads)
-    sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
-  __syncthreads();
-  if (warp < hq) {
-    // query exponent e: max |Q / factor| * 2^e in [2^13, 2^14), so Q * 2^e / factor is an
-    // exact fp16 (a bf16 has 8 significant bits); channel-group sums of Q for the K offset
-    const int i = warp;
-    float amax = 0.f;
-    float gs = 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int ch = 4 * lane + u;
-      const float v = sQ[i * D + ch];
-      amax = fmaxf(amax, fabsf(v) * (1.f / k_mult<BITS>(ch)));
-      gs += v;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, o));
-    constexpr int lanes_per_group = C::G / 4;  // 8, 16 or 32
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float other = __shfl_xor_sync(FULLMASK, gs, o);
-      if (o < lanes_per_group) gs += other;
-    }
-    int e = 0;
-    if (amax > 0.f) e = min(100, max(-100, 13 - ilog2f(amax)));
-    if (lane == 0) {
-      sEq[i] = e;
-      sAq[i] = p.sl2 * exp2i(-e);
-    }
-    if (KL == 0 && (lane % lanes_per_group) == 0) sBz[i * 4 + lane / lanes_per_group] = exp2i(e) * gs;
-  }
-  __syncthreads();
-
-  LaneCols lc;
-  lc.g = g;
-  lc.c = c;
-  lc.lane = lane;
-  lc.hq = hq;
-  lc.u_lane = (GV == 1) ? 0 : (16 * g) / C::G;  // V channel group of this lane's 16 channels
-  if (GV >= 2) {
-    const int el = ((lc.u_lane - 2 * c) % GV + GV) % GV;
-    lc.e_live = el <= 1 ? el : -1;
-  } else {
-    lc.e_live = 0;
-  }
-
-  WarpState<C> st;
-  if (KL == 0) {
-    // token-wise K: B fragments Q' = Q 2^e / factor (exact fp16) of this lane's column
-    // (column g), fixed for the CTA, and minus the magic bias 1024 * sum of Q' per channel
-    // group of accumulator columns 2c and 2c+1
-    const int qb = qk_query<C>(g, hq);
-    const bool live = qb >= 0;
-    const float sc = live ? exp2i(sEq[qb]) : 0.f;
-    float gsum[GK];
-#pragma unroll
-    for (int u = 0; u < GK; ++u) gsum[u] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float xx[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
-          xx[e] = live ? sQ[qb * D + ch] * sc * (1.f / k_mult<BITS>(ch)) : 0.f;
-        }
-        st.qB[ks][r] = f16x2_from(xx[0], xx[1]);
-        gsum[ks / C::KSG] += xx[0] + xx[1];
-      }
-#pragma unroll
-    for (int u = 0; u < GK; ++u) {
-      gsum[u] += __shfl_xor_sync(FULLMASK, gsum[u], 1);
-      gsum[u] += __shfl_xor_sync(FULLMASK, gsum[u], 2);
-    }
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-      for (int u = 0; u < GK; ++u) st.kbias[jj][u] = -kMagicF * __shfl_sync(FULLMASK, gsum[u], 8 * c + 4 * jj);
-#pragma unroll
-    for (int j = 0; j < NQ; ++j) {
-      const int qs = qk_query<C>(2 * c + j, hq);
-      st.pa[j] = qs >= 0 ? sAq[qs] : 1.f;
-#pragma unroll
-      for (int u = 0; u < GK; ++u) st.bzq[j][u] = qs >= 0 ? sBz[qs * 4 + u] : 0.f;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < NQ; ++j) st.pa[j] = 1.f;
-  }
-#pragma unroll
-  for (int j = 0; j < NQ; ++j) {
-    st.m_run[j] = -INFINITY;
-    st.l[j] = 0.f;
-  }
-#pragma unroll
-  for (int o = 0; o < NO; ++o) st.zacc[o] = 0.f;
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-    for (int row = 0; row < 2; ++row)
-#pragma unroll
-      for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] = 0.f;
-
-  // ------------------------------------------------------------ this warp's items
-  int k = 0;
-  for (; k < nk; ++k) {
-    const int r = k % R;
-    if (!mbar_wait(bar_w + 8u * r, (k / R) & 1, p.status, kStatusConsumerTimeout)) {
-      failed = true;
-      break;
-    }
-    const uint8_t* e = ring_w + (size_t)r * p.entry_bytes;
-    SlotSmem sm;
-    sm.kc = e;
-    sm.vc = e + p.off_vc;
-    sm.ks = reinterpret_cast<const __half*>(e + p.off_ks);
-    sm.kz = reinterpret_cast<const __half*>(e + p.off_kz);
-    sm.vs = reinterpret_cast<const __half*>(e + p.off_vs);
-    sm.vz = reinterpret_cast<const __half*>(e + p.off_vz);
-    const int nv = min(UNIT, L - (i0 + warp + kConsumerWarps * k) * UNIT);  // valid tokens, >= 1
-    if (nv == UNIT)
-      process_unit<C, true>(st, sm, nv, sQ, p.sl2, lc);
-    else
-      process_unit<C, false>(st, sm, nv, sQ, p.sl2, lc);
-    __syncwarp();
-    if (k + R < nk) {
-      // the entry's reads are done: refill it with item k + R
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue(k + R);
-      }
-      ++issued;
-    }
-  }
-  if (failed && lane == 0) {
-    // every copy issued must have landed before shared memory is reused or freed
-    for (int kk = k; kk < issued; ++kk)
-      if (!mbar_wait(bar_w + 8u * (kk % R), (kk / R) & 1, p.status, kStatusDrainTimeout)) break;
   }
   __syncwarp();
+  for (int r = 0; r < R; ++r) issue_next();
 
-  // ---------------------------------------------------- warp results
-  if (!window_cta) {
-    __syncthreads();  // every entry consumed: the ring is free
-    float* sM = reinterpret_cast<float*>(ring);  // [warps][kMaxHq]
-    float* sL = sM + kConsumerWarps * kMaxHq;    // [warps][kMaxHq]
-    float* sO = sL + kConsumerWarps * kMaxHq;    // [warps][kMaxHq][D]
+  bool failed = false;
+  Cursor con = cursor_start();
+  int r_con = 0, ph_con = 0, n_consumed = 0;
+
+  for (long long x = X0; x < X1;) {
+    // ---------------------------------------------------- segment: the items of pair u
+    const int u = (int)(x / p.ipu);
+    const long long xe = min(X1, (long long)(u + 1) * p.ipu);
+    const int b = u / p.Hkv, kvh = u % p.Hkv;
+    const int L = min(max(__ldg(p.seq_lens + b), 0), p.T_cap);
+
+    // Stage Q (fp32) and the per-query constants of pair u.
+    __syncthreads();  // the previous segment's merge is done with sQ and the merge area
+    for (int idx = threadIdx.x; idx < hq * D; idx += kThreads)
+      sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
+    __syncthreads();
+    if (warp < hq) {
+      // query exponent e: max |Q / factor| * 2^e in [2^13, 2^14), so Q * 2^e / factor is an
+      // exact fp16 (a bf16 has 8 significant bits); channel-group sums of Q for the K offset
+      const int i = warp;
+      float amax = 0.f;
+      float gs = 0.f;
+#pragma unroll
+      for (int uu = 0; uu < 4; ++uu) {
+        const int ch = 4 * lane + uu;
+        const float v = sQ[i * D + ch];
+        amax = fmaxf(amax, fabsf(v) * (1.f / k_mult<BITS>(ch)));
+        gs += v;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, o));
+      constexpr int lanes_per_group = C::G / 4;  // 8, 16 or 32
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float other = __shfl_xor_sync(FULLMASK, gs, o);
+        if (o < lanes_per_group) gs += other;
+      }
+      int e = 0;
+      if (amax > 0.f) e = min(100, max(-100, 13 - ilog2f(amax)));
+      if (lane == 0) {
+        sEq[i] = e;
+        sAq[i] = p.sl2 * exp2i(-e);
+      }
+      if (KL == 0 && (lane % lanes_per_group) == 0) sBz[i * 4 + lane / lanes_per_group] = exp2i(e) * gs;
+    }
+    __syncthreads();
+
+    LaneCols lc;
+    lc.g = g;
+    lc.c = c;
+    lc.lane = lane;
+    lc.hq = hq;
+    lc.u_lane = (GV == 1) ? 0 : (16 * g) / C::G;  // V channel group of this lane's 16 channels
+    if (GV >= 2) {
+      const int el = ((lc.u_lane - 2 * c) % GV + GV) % GV;
+      lc.e_live = el <= 1 ? el : -1;
+    } else {
+      lc.e_live = 0;
+    }
+
+    WarpState<C> st;
+    if (KL == 0) {
+      // token-wise K: B fragments Q' = Q 2^e / factor (exact fp16) of this lane's column
+      // (column g), fixed for the pair, and minus the magic bias 1024 * sum of Q' per
+      // channel group of accumulator columns 2c and 2c+1
+      const int qb = qk_query<C>(g, hq);
+      const bool live = qb >= 0;
+      const float sc = live ? exp2i(sEq[qb]) : 0.f;
+      float gsum[GK];
+#pragma unroll
+      for (int uu = 0; uu < GK; ++uu) gsum[uu] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float xx[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
+            xx[e] = live ? sQ[qb * D + ch] * sc * (1.f / k_mult<BITS>(ch)) : 0.f;
+          }
+          st.qB[ks][r] = f16x2_from(xx[0], xx[1]);
+          gsum[ks / C::KSG] += xx[0] + xx[1];
+        }
+#pragma unroll
+      for (int uu = 0; uu < GK; ++uu) {
+        gsum[uu] += __shfl_xor_sync(FULLMASK, gsum[uu], 1);
+        gsum[uu] += __shfl_xor_sync(FULLMASK, gsum[uu], 2);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int uu = 0; uu < GK; ++uu)
+          st.kbias[jj][uu] = -kMagicF * __shfl_sync(FULLMASK, gsum[uu], 8 * c + 4 * jj);
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) {
+        const int qs = qk_query<C>(2 * c + j, hq);
+        st.pa[j] = qs >= 0 ? sAq[qs] : 1.f;
+#pragma unroll
+        for (int uu = 0; uu < GK; ++uu) st.bzq[j][uu] = qs >= 0 ? sBz[qs * 4 + uu] : 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) st.pa[j] = 1.f;
+    }
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      st.m_run[j] = -INFINITY;
+      st.l[j] = 0.f;
+    }
+#pragma unroll
+    for (int o = 0; o < NO; ++o) st.zacc[o] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int row = 0; row < 2; ++row)
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] = 0.f;
+
+    // ---------------------------------------------------- this warp's items of the segment
+    for (; !failed && con.i < NL && con.u == u; cursor_next(con)) {
+      const int nv = min(UNIT, con.L - con.t * UNIT);  // valid tokens of the item
+      if (nv <= 0) continue;
+      if (!mbar_wait(bar_w + 8u * r_con, ph_con, p.status, kStatusConsumerTimeout)) {
+        failed = true;
+        break;
+      }
+      const uint8_t* en = ring_w + (size_t)r_con * p.entry_bytes;
+      SlotSmem sm;
+      sm.kc = en;
+      sm.vc = en + p.off_vc;
+      sm.ks = reinterpret_cast<const __half*>(en + p.off_ks);
+      sm.kz = reinterpret_cast<const __half*>(en + p.off_kz);
+      sm.vs = reinterpret_cast<const __half*>(en + p.off_vs);
+      sm.vz = reinterpret_cast<const __half*>(en + p.off_vz);
+      if (nv == UNIT)
+        process_unit<C, true>(st, sm, nv, sQ, p.sl2, lc);
+      else
+        process_unit<C, false>(st, sm, nv, sQ, p.sl2, lc);
+      ++n_consumed;
+      if (++r_con == R) {
+        r_con = 0;
+        ph_con ^= 1;
+      }
+      __syncwarp();
+      issue_next();  // refill the entry just read with this warp's next item, if any
+    }
+
+    // ---------------------------------------------------- warp results into the merge area
 #pragma unroll
     for (int j = 0; j < NQ; ++j) {
       float l = st.l[j];
@@ -967,8 +1034,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
       l += __shfl_xor_sync(FULLMASK, l, 16);
       const int q = qk_query<C>(2 * c + j, hq);
       if (g == 0 && q >= 0) {
-        sM[warp * kMaxHq + q] = (st.m_run[j] == -INFINITY) ? -INFINITY : st.pa[j] * st.m_run[j];
-        sL[warp * kMaxHq + q] = l;
+        ma.m[warp * kMaxHq + q] = (st.m_run[j] == -INFINITY) ? -INFINITY : st.pa[j] * st.m_run[j];
+        ma.l[warp * kMaxHq + q] = l;
       }
     }
     float zs[NO];
@@ -999,120 +1066,103 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int row = 0; row < 2; ++row)
-          sO[(warp * kMaxHq + q) * D + 16 * g + pv_channel<BITS>(mt, row)] = st.o_run[mt][row][i] + zt;
+          ma.o[(warp * hq + q) * D + 16 * g + pv_channel<BITS>(mt, row)] = st.o_run[mt][row][i] + zt;
     }
-  }
+    __syncthreads();
 
-  // ---------------------------------------------------- window split
-  if (window_cta) {
-    float* sM = reinterpret_cast<float*>(ring);
-    float* sL = sM + kConsumerWarps * kMaxHq;
-    float* sO = sL + kConsumerWarps * kMaxHq;
-    const int W = min(max(p.win_lens[b], 0), p.win_cap);
-    float m[kMaxHq], l[kMaxHq], o[kMaxHq][4];
-#pragma unroll
-    for (int i = 0; i < kMaxHq; ++i) {
-      m[i] = -INFINITY;
-      l[i] = 0.f;
-      o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    }
-    const size_t wbase = (size_t)unit * p.win_cap;
-    for (int t = warp; t < W; t += kConsumerWarps) {
-      const uint2 kr = reinterpret_cast<const uint2*>(p.k_win + (wbase + t) * D)[lane];
-      const uint2 vr = reinterpret_cast<const uint2*>(p.v_win + (wbase + t) * D)[lane];
-      const __nv_bfloat162* kh = reinterpret_cast<const __nv_bfloat162*>(&kr);
-      const __nv_bfloat162* vh = reinterpret_cast<const __nv_bfloat162*>(&vr);
-      const float2 k01 = __bfloat1622float2(kh[0]), k23 = __bfloat1622float2(kh[1]);
-      const float2 v01 = __bfloat1622float2(vh[0]), v23 = __bfloat1622float2(vh[1]);
-#pragma unroll
-      for (int i = 0; i < kMaxHq; ++i) {
-        if (i >= hq) break;
-        const float* qrow = sQ + i * D + 4 * lane;
-        float d = qrow[0] * k01.x + qrow[1] * k01.y + qrow[2] * k23.x + qrow[3] * k23.y;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(FULLMASK, d, off);
-        const float s = d * p.sl2;
-        const float mn = fmaxf(m[i], s);
-        const float a = fast_exp2(m[i] - mn);
-        const float pr = fast_exp2(s - mn);
-        m[i] = mn;
-        l[i] = l[i] * a + pr;
-        o[i][0] = o[i][0] * a + pr * v01.x;
-        o[i][1] = o[i][1] * a + pr * v01.y;
-        o[i][2] = o[i][2] * a + pr * v23.x;
-        o[i][3] = o[i][3] * a + pr * v23.y;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxHq; ++i) {
-      if (i >= hq) break;
-      if (lane == 0) {
-        sM[warp * kMaxHq + i] = m[i];
-        sL[warp * kMaxHq + i] = l[i];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) sO[(warp * kMaxHq + i) * D + 4 * lane + u] = o[i][u];
-    }
-  }
-
-  // ---------------------------------------------------- merge the warps, write the partial
-  __syncthreads();
-  if (!failed) {
-    const float* sM = reinterpret_cast<const float*>(ring);
-    const float* sL = sM + kConsumerWarps * kMaxHq;
-    const float* sO = sL + kConsumerWarps * kMaxHq;
+    // ---------------------------------------------------- merge the warps
+    // A pair held by this CTA alone (and without a window) is finished here; otherwise
+    // the CTA writes its partial to slot j of the pair and the last contributor to
+    // arrive merges all slots (and the window's) into the output.
+    const int c_first = cta_of((long long)u * p.ipu, p.tot_items, p.n_cta);
+    const int c_last = cta_of((long long)(u + 1) * p.ipu - 1, p.tot_items, p.n_cta);
+    const int n_contrib = c_last - c_first + 1;
+    const bool alone = (n_contrib == 1) && !p.has_win;
     for (int idx = threadIdx.x; idx < hq * D; idx += kThreads) {
       const int i = idx / D, ch = idx % D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sM[w * kMaxHq + i]);
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ma.m[w * kMaxHq + i]);
       float acc = 0.f, lt = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          const float mw = sM[w * kMaxHq + i];
+          const float mw = ma.m[w * kMaxHq + i];
           const float sc = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-          acc = fmaf(sc, sO[(w * kMaxHq + i) * D + ch], acc);
-          lt = fmaf(sc, sL[w * kMaxHq + i], lt);
+          acc = fmaf(sc, ma.o[(w * hq + i) * D + ch], acc);
+          lt = fmaf(sc, ma.l[w * kMaxHq + i], lt);
         }
       }
-      const size_t prow = ((size_t)b * p.Hq + kvh * hq + i) * p.s_tot + split;
-      p.part_o[prow * D + ch] = acc;
-      if (ch == 0) p.part_ml[prow] = make_float2(M, lt);
+      if (alone) {
+        p.out[((size_t)b * p.Hq + kvh * hq + i) * D + ch] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
+      } else {
+        const size_t prow = ((size_t)u * p.n_slots + (cta - c_first)) * hq + i;
+        p.part_o[prow * D + ch] = acc;
+        if (ch == 0) p.part_ml[prow] = make_float2(M, lt);
+      }
     }
+    if (!alone) {
+      // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s (zero when no token at all)
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();  // this CTA's partial is visible before the count says so
+        const int prev = atomicAdd(p.done + u, 1);
+        s_last = (prev == n_contrib - 1);
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        // slots 0 .. n_contrib-1 hold the CTAs' partials, the last slot the window's
+        const int n_used = n_contrib + p.has_win;
+        auto slot_of = [&](int k) { return k < n_contrib ? k : p.n_slots - 1; };
+        // warp i: the maximum over the slots of query i, each slot's scale 2^(m_s - M)
+        // (into the merge area, free again) and the merged denominator
+        float* s_sc = ma.o;                              // [n_used][hq]
+        float* s_l = ma.l;                               // [hq]
+        for (int i = warp; i < hq; i += kConsumerWarps) {
+          float M = -INFINITY;
+          for (int k = lane; k < n_used; k += 32)
+            M = fmaxf(M, __ldcg(&p.part_ml[((size_t)u * p.n_slots + slot_of(k)) * hq + i].x));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULLMASK, M, o));
+          float lt = 0.f;
+          for (int k = lane; k < n_used; k += 32) {
+            const float2 ml = __ldcg(&p.part_ml[((size_t)u * p.n_slots + slot_of(k)) * hq + i]);
+            const float sc = (M == -INFINITY || ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+            s_sc[k * hq + i] = sc;
+            lt = fmaf(sc, ml.y, lt);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(FULLMASK, lt, o);
+          if (lane == 0) s_l[i] = lt;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < hq * D; idx += kThreads) {
+          const int i = idx / D, ch = idx % D;
+          float acc = 0.f;
+#pragma unroll 4
+          for (int k = 0; k < n_used; ++k) {
+            const size_t prow = ((size_t)u * p.n_slots + slot_of(k)) * hq + i;
+            acc = fmaf(s_sc[k * hq + i], __ldcg(&p.part_o[prow * D + ch]), acc);
+          }
+          const float l = s_l[i];
+          p.out[((size_t)b * p.Hq + kvh * hq + i) * D + ch] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
+        }
+        if (threadIdx.x == 0) p.done[u] = 0;  // ready for the next call in stream order
+      }
+    }
+    x = xe;
   }
 
-  // ---------------------------------------------------- the last split merges all splits
-  // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s (zero when no token at all).
-  __shared__ int s_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();  // this CTA's partial is visible before the count says so
-    const int prev = atomicAdd(p.done + unit, 1);
-    s_last = (prev == p.s_tot - 1);
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    for (int idx = threadIdx.x; idx < hq * D; idx += kThreads) {
-      const int i = idx / D, ch = idx % D;
-      const size_t row = (size_t)b * p.Hq + kvh * hq + i;
-      const float2* ml = p.part_ml + row * p.s_tot;
-      const float* po = p.part_o + row * p.s_tot * D;
-      float M = -INFINITY;
-      for (int sp = 0; sp < p.s_tot; ++sp) M = fmaxf(M, __ldcg(&ml[sp].x));
-      float acc = 0.f, l = 0.f;
-      if (M != -INFINITY) {
-        for (int sp = 0; sp < p.s_tot; ++sp) {
-          const float2 x = __ldcg(&ml[sp]);
-          const float sc = (x.x == -INFINITY) ? 0.f : fast_exp2(x.x - M);
-          l = fmaf(sc, x.y, l);
-          acc = fmaf(sc, __ldcg(&po[(size_t)sp * D + ch]), acc);
-        }
+  if (failed && lane == 0) {
+    // every copy issued must have landed before shared memory is freed
+    for (int k = n_consumed; k < n_issued; ++k) {
+      if (!mbar_wait(bar_w + 8u * r_con, ph_con, p.status, kStatusDrainTimeout)) break;
+      if (++r_con == R) {
+        r_con = 0;
+        ph_con ^= 1;
       }
-      p.out[row * D + ch] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
     }
-    if (threadIdx.x == 0) p.done[unit] = 0;  // ready for the next call in stream order
   }
 }
 

@@ -19,6 +19,10 @@ int launch_pack(const PackArgs& a, cudaStream_t stream);
 
 using DecodeKernel = void (*)(const DecodeParams);
 
+// Window partials (one per sequence and KV head) into the last partial slot of each
+// pair; launched before the decode kernel when a bf16 window is present.
+int launch_window_partial(const DecodeParams& p, cudaStream_t stream);
+
 // Instantiated kernel for (column mode, log2 group) of one bit width and K/V
 // layout pair, or nullptr when that combination is not built. One translation
 // unit per specialisation.
