@@ -3,12 +3,15 @@
 
 Metric: decode-attention µs per call and achieved HBM GB/s (fraction of the
 measured peak), INT2 and INT4. One step = one call of lbkv_decode_attn (the
-whole hot path: split-KV decode with affine folding and the split merge, one
-kernel launch) over one batch of seeded synthetic inputs already resident in
-HBM. Headline workload: INT2 token-wise K/V, group 128, 32 query / 8 KV heads,
-head_dim 128, batch 32, 32K context. The other workloads run as a sweep.
+whole hot path: split-KV decode with affine folding and the merge of the
+partials, one kernel launch; two when a bf16 window is present) over one batch
+of seeded synthetic inputs already resident in HBM. Headline workload: INT2
+token-wise K/V, group 128, 32 query / 8 KV heads, head_dim 128, batch 32, 32K
+context. The other workloads run as a sweep.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {lbkv,reference}] [--no-sweep]
+       python bench.py --profile [--bits B] [--batch N] [--ctx T] [--steps K] [--warmup W]
+(--profile: only eager calls of one workload, for ncu captures)
 Under torchrun (N > 1) every rank runs its own replica on its GPU (the path
 shards by sequence and KV head with no exchange); rank 0 prints one JSON line.
 """
@@ -387,6 +390,10 @@ def main():
     ap.add_argument("--impl", default="lbkv", choices=["lbkv", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="eager calls of one workload only (for ncu)")
+    ap.add_argument("--bits", type=int, default=2)
+    ap.add_argument("--batch", type=int, default=HEADLINE["batch"])
+    ap.add_argument("--ctx", type=int, default=HEADLINE["ctx"])
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_info()
@@ -407,6 +414,16 @@ def main():
 
         dist.init_process_group("nccl", device_id=device)
         barrier = dist.barrier
+
+    if args.profile:
+        wl = (inputs.decode_int2 if args.bits == 2 else inputs.decode_int4)(args.batch, args.ctx)
+        case = Case(wl, device, min_footprint=0)
+        for i in range(args.warmup + args.steps):
+            case.call(i)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": wl.name, "calls": args.warmup + args.steps, "bytes_per_call": case.bytes,
+                          "replicas": len(case.replicas)}), flush=True)
+        return
 
     peak, peak_kind = measured_hbm_peak()
     wl = inputs.decode_int2(**HEADLINE)
@@ -461,7 +478,7 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1e3, 2),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32",
             "data": "synthetic (seeded; codes uniform, s~U[0.01,0.1], z~U[-0.2,0.2], Q~N(0,1) bf16)",
             "config": {"workload": wl.name, "batch": wl.batch, "ctx": HEADLINE["ctx"], "q_heads": wl.num_q_heads,
                        "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "bits": wl.bits, "group": wl.group,
