@@ -58,7 +58,7 @@ struct Plan {
   int hq, mode, gv, win;
   int unit_tokens, ipu, n_cta, n_slots;
   long long tot_items;
-  int ring_off, ring_per_warp, entry_bytes, entry_tx, smem_bytes;
+  int ring_off, ring_per_warp, entry_bytes, entry_tx_k, entry_tx_v, smem_bytes, threads;
   int off_vc, off_ks, off_kz, off_vs, off_vz, sz_k, sz_v;
   size_t off_done, off_ml, off_o, ws_bytes;
 };
@@ -92,27 +92,30 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   int st = current_device_props(&sms, &smem_optin);
   if (st) return st;
 
-  // ring entry (one item of `ut` tokens): K codes | V codes | K scale | K offset | V scale | V offset
-  const int ut = kChunk * unit_chunks(bits, pl->mode);
+  // ring entry (one item of `ut` tokens): K codes | K scale | K offset | V codes | V scale | V offset
+  const int ut = kChunk * unit_chunks(bits, pl->mode, group == 128 ? 7 : group == 64 ? 6 : 5);
   const int rb = kHeadDim * bits / 8;
   const int cw_rows = ut >= group ? ut / group : 1;  // channel-wise s/z rows an item touches
   pl->unit_tokens = ut;
   pl->sz_k = (kl == LBKV_TOKENWISE) ? ut * (kHeadDim / group) * 2 : cw_rows * kHeadDim * 2;
   pl->sz_v = (vl == LBKV_TOKENWISE) ? ut * (kHeadDim / group) * 2 : cw_rows * kHeadDim * 2;
-  pl->off_vc = ut * rb;
-  pl->off_ks = 2 * ut * rb;
+  pl->off_ks = ut * rb;
   pl->off_kz = pl->off_ks + pl->sz_k;
-  pl->off_vs = pl->off_kz + pl->sz_k;
+  pl->off_vc = pl->off_kz + pl->sz_k;
+  pl->off_vs = pl->off_vc + ut * rb;
   pl->off_vz = pl->off_vs + pl->sz_v;
-  pl->entry_tx = pl->off_vz + pl->sz_v;
-  pl->entry_bytes = (int)round_up((size_t)pl->entry_tx, 128);
-  pl->ring_off = kPrologueBytes + merge_bytes(hq);
+  pl->entry_tx_k = pl->off_vc;  // the K half: codes, scales, offsets
+  pl->entry_tx_v = ut * rb + 2 * pl->sz_v;
+  pl->entry_bytes = (int)round_up((size_t)(pl->off_vz + pl->sz_v), 128);
+  const int warps = decode_warps(bits, pl->mode);
+  pl->threads = 32 * warps;
+  pl->ring_off = kPrologueBytes + merge_bytes(hq, warps);
   const int budget = smem_optin - pl->ring_off;
-  int r_w = budget / (kConsumerWarps * pl->entry_bytes);
-  if (r_w > kMaxRing / kConsumerWarps) r_w = kMaxRing / kConsumerWarps;
+  int r_w = budget / (warps * pl->entry_bytes);
+  if (r_w > kMaxRing / (2 * warps)) r_w = kMaxRing / (2 * warps);  // two mbarriers per entry
   if (r_w < 1) return LBKV_EUNSUPPORTED;
   pl->ring_per_warp = r_w;
-  pl->smem_bytes = pl->ring_off + kConsumerWarps * r_w * pl->entry_bytes;
+  pl->smem_bytes = pl->ring_off + warps * r_w * pl->entry_bytes;
 
   // Persistent grid: the items of all pairs (ipu per pair) split evenly over at most
   // one CTA per SM. A pair spans at most ceil(n_cta / pairs) + 1 CTAs, each writing
@@ -207,7 +210,8 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.ring_off = pl.ring_off;
   p.ring_per_warp = pl.ring_per_warp;
   p.entry_bytes = pl.entry_bytes;
-  p.entry_tx = pl.entry_tx;
+  p.entry_tx_k = pl.entry_tx_k;
+  p.entry_tx_v = pl.entry_tx_v;
   p.off_vc = pl.off_vc;
   p.off_ks = pl.off_ks;
   p.off_kz = pl.off_kz;
@@ -219,7 +223,7 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   if (ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem_bytes) != LBKV_OK) return LBKV_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pl.win && launch_window_partial(p, s) != 0) return LBKV_ECUDA;
-  kern<<<(unsigned)pl.n_cta, kThreads, pl.smem_bytes, s>>>(p);
+  kern<<<(unsigned)pl.n_cta, (unsigned)pl.threads, pl.smem_bytes, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;
   return LBKV_OK;
 }

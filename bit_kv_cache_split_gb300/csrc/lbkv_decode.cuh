@@ -45,26 +45,28 @@
 
 #include "lbkv_device.cuh"
 
-#ifndef LBKV_CONSUMER_WARPS
-#define LBKV_CONSUMER_WARPS 8
-#endif
-
 namespace lbkv {
 
 constexpr int kHeadDim = 128;
 constexpr int kSlotTokens = 128;
 constexpr int kChunk = 32;  // tokens of one QK^T / PV tile pass
-constexpr int kConsumerWarps = LBKV_CONSUMER_WARPS;
-constexpr int kThreads = 32 * kConsumerWarps;
-constexpr int kMaxRing = 48;  // ring entries of all warps (one mbarrier each)
+constexpr int kMaxRing = 48;    // ring entries of all warps (one mbarrier each)
+constexpr int kMergeWarps = 8;  // warps whose partials the CTA merge reads; any others fold into them first
+constexpr int kWinWarps = 8;    // warps of the window kernel
 constexpr int kMaxHq = 8;
 // shared-memory map: barriers | Q (fp32) and per-query constants | merge area | rings
 constexpr int kBarBytes = kMaxRing * 8;
 constexpr int kPrologueBytes = 8192;
 static_assert(kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq) <= kPrologueBytes, "prologue fits");
-// merge area for hq queries per KV head: per warp (m, l) of kMaxHq queries and o of hq
-__host__ __device__ constexpr int merge_bytes(int hq) {
-  return (4 * kConsumerWarps * (2 * kMaxHq + hq * kHeadDim) + 127) / 128 * 128;
+// Per-lane register state a warp beyond the first kMergeWarps hands over (floats):
+// o_run (16 per live column, up to 2), zacc (up to 4), m and l (up to 2 each).
+constexpr int kStateFloats = 16 * 2 + 4 + 2 * 2;
+// Merge area for hq queries per KV head: per merge warp (m, l) of kMaxHq queries and o of
+// hq queries; with more than kMergeWarps warps it also holds the handed-over states.
+__host__ __device__ constexpr int merge_bytes(int hq, int warps) {
+  const int deposit = 4 * kMergeWarps * (2 * kMaxHq + hq * kHeadDim);
+  const int states = (warps > kMergeWarps) ? 4 * kMergeWarps * 32 * kStateFloats : 0;
+  return ((deposit > states ? deposit : states) + 127) / 128 * 128;
 }
 
 constexpr int kModeDup = 0;   // <= 4 combos: combo k on columns 2k, 2k+1
@@ -74,10 +76,14 @@ constexpr int kModeWide = 2;  // 16 combos: combo k on column k % 8 of PV n-tile
 __host__ __device__ constexpr int decode_mode(int combos) {
   return combos <= 4 ? kModeDup : combos == 8 ? kModePair : combos == 16 ? kModeWide : -1;
 }
-// 32-token chunks per item: 4 (128 tokens) where two ring entries per warp fit and
-// the registers allow it, else fewer.
-__host__ __device__ constexpr int unit_chunks(int bits, int mode) {
-  return mode == kModeWide ? 1 : bits == 2 ? 4 : 2;
+// Warps per CTA: 16 (128 registers each) for up to 8 (query, V group) pairs per KV
+// head, 8 for 16 pairs (whose PV accumulators need more registers).
+__host__ __device__ constexpr int decode_warps(int bits, int mode) { return mode == kModeWide ? 8 : 16; }
+// 32-token chunks per item, such that one ring entry per warp fits in shared memory:
+// 128 tokens at INT2 (64 when group 32 makes the scales and offsets as large as a
+// quarter of the codes), 64 at INT4, 32 for 16 pairs.
+__host__ __device__ constexpr int unit_chunks(int bits, int mode, int log2g) {
+  return mode == kModeWide ? 1 : bits == 2 ? (log2g == 5 ? 2 : 4) : 2;
 }
 
 struct DecodeParams {
@@ -102,8 +108,8 @@ struct DecodeParams {
   long long tot_items;  // B * Hkv * ipu
   int ipu, n_cta;       // items per pair (T_cap / UNIT), CTAs of the grid
   int n_slots, has_win; // partial slots per pair (the last one the window's when has_win)
-  int ring_off, ring_per_warp, entry_bytes, entry_tx;
-  int off_vc, off_ks, off_kz, off_vs, off_vz;  // byte offsets inside a ring entry
+  int ring_off, ring_per_warp, entry_bytes, entry_tx_k, entry_tx_v;
+  int off_ks, off_kz, off_vc, off_vs, off_vz;  // byte offsets inside a ring entry (K codes at 0)
   int sz_k_bytes, sz_v_bytes;                  // bytes of one scale (or offset) array per entry
 };
 
@@ -121,8 +127,10 @@ struct Cfg {
   // query slots per lane (QK^T accumulator columns 2c + j); owned combos per lane
   static constexpr int NQ = (MODE == kModeWide || (MODE == kModePair && GV == 1)) ? 2 : 1;
   static constexpr int NO = DUP ? 1 : 2 * NTV;
-  static constexpr int NCH = unit_chunks(BITS, MODE);  // chunks per item
+  static constexpr int NCH = unit_chunks(BITS, MODE, LOG2G_);  // chunks per item
   static constexpr int UNIT = kChunk * NCH;             // tokens per item
+  static constexpr int WARPS = decode_warps(BITS, MODE);
+  static constexpr int THREADS = 32 * WARPS;
   static_assert(G >= kChunk, "a chunk never straddles a token group");
   static_assert(MODE != kModeWide || GV >= 2, "16 combos need several V channel groups");
 };
@@ -507,10 +515,11 @@ __device__ __forceinline__ void fold_channelwise_v(WarpState<C>& st, const float
 }
 
 // One warp unit: the NCH chunks of 32 tokens of one ring entry. nv: valid tokens
-// of the entry (all UNIT valid when FULL).
-template <class C, bool FULL>
+// of the entry (all UNIT valid when FULL). mid() runs between the QK^T and PV
+// phases and returns false when the V half of the entry did not arrive.
+template <class C, bool FULL, class Mid>
 __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& sm, int nv, const float* sQ, float sl2,
-                                             const LaneCols& lc) {
+                                             const LaneCols& lc, Mid&& mid) {
   constexpr int KL = C::KL, VL = C::VL, GV = C::GV, NQ = C::NQ, NO = C::NO, NTV = C::NTV;
   constexpr int NCH = C::NCH, D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
@@ -594,18 +603,21 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
     }
   }
 
+  // The K half of the entry is no longer read: mid() refills it and waits for the V half.
+  if (!mid()) return;
+
   // ------------------------------------------------ token-wise V: weight exponent of the unit
   // Fed weight P_t s_t,u 2^eP with max(s) 2^eP in [2^13, 2^14) over the unit's valid
   // tokens: the fed values stay in the fp16 normal range.
   float ps = 8192.f, inv_ps = 1.f / 8192.f;
   if (VL == 0) {
     constexpr int WORDS = C::UNIT * GV / 2;  // scale words (two halves) of the unit
-    static_assert(WORDS % 32 == 0, "scale words spread evenly over the lanes");
     const uint32_t* sw = reinterpret_cast<const uint32_t*>(sm.vs);
     uint32_t smax = 0;
 #pragma unroll
-    for (int k = 0; k < WORDS / 32; ++k) {
+    for (int k = 0; k < (WORDS + 31) / 32; ++k) {
       const int w = lc.lane + 32 * k;
+      if (WORDS % 32 != 0 && w >= WORDS) break;
       const uint32_t s01 = sw[w];
       const bool ok0 = FULL || ((2 * w) / GV < nv), ok1 = FULL || ((2 * w + 1) / GV < nv);
       const uint32_t m0 = ok0 ? (s01 & 0x7fffu) : 0u, m1 = ok1 ? ((s01 >> 16) & 0x7fffu) : 0u;
@@ -777,7 +789,7 @@ struct MergeArea {
 // The kernel: see the file comment. C = Cfg<BITS, KL, VL, MODE, LOG2G>.
 // ------------------------------------------------------------------------
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NQ = C::NQ, NO = C::NO;
   constexpr int RB = C::RB, D = kHeadDim, UNIT = C::UNIT;
   constexpr unsigned FULLMASK = 0xffffffffu;
@@ -797,41 +809,53 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
   float* sBz = sAq + 2 * kMaxHq;                           // [kMaxHq][4] 2^e * sum of Q per channel group
   MergeArea ma;
   ma.m = reinterpret_cast<float*>(smem + kPrologueBytes);
-  ma.l = ma.m + kConsumerWarps * kMaxHq;
-  ma.o = ma.l + kConsumerWarps * kMaxHq;
+  ma.l = ma.m + kMergeWarps * kMaxHq;
+  ma.o = ma.l + kMergeWarps * kMaxHq;
   uint8_t* ring = smem + p.ring_off;
   __shared__ int s_last;
 
+  // Each ring entry has a K half (codes, scales, offsets) and a V half, each with its own
+  // mbarrier, so that the next item's K half loads while this item's PV phase runs and
+  // its V half while the next QK^T phase runs.
   const int R = p.ring_per_warp;
-  const uint32_t bar_w = smem_addr(bars) + 8u * (uint32_t)(warp * R);
+  const uint32_t bar_w = smem_addr(bars) + 16u * (uint32_t)(warp * R);
   uint8_t* ring_w = ring + (size_t)warp * R * p.entry_bytes;
+  auto bar_k = [&](int r) { return bar_w + 16u * r; };
+  auto bar_v = [&](int r) { return bar_w + 16u * r + 8u; };
 
-  // Bulk copies of item t of pair u into entry r of this warp's ring (lane 0 only).
-  auto copy_item = [&](int u, int t, int r) {
+  // Bulk copies of the K or V half of item t of pair u into entry r (lane 0 only).
+  auto copy_half = [&](bool v_half, int u, int t, int r) {
     const size_t t0 = (size_t)t * UNIT;
     const size_t row0 = (size_t)u * p.T_cap + t0;
     const size_t blocks = (size_t)p.T_cap / C::G;
     const uint32_t dst = smem_addr(ring_w + (size_t)r * p.entry_bytes);
-    const uint32_t fb = bar_w + 8u * r;
     const uint64_t pol = l2_evict_first_policy();
-    mbar_arrive_expect_tx(fb, p.entry_tx);
-    bulk_g2s(dst, p.k_codes + row0 * RB, UNIT * RB, fb, pol);
-    bulk_g2s(dst + p.off_vc, p.v_codes + row0 * RB, UNIT * RB, fb, pol);
-    const size_t ks0 = (KL == 0) ? row0 * C::GK : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
-    const size_t vs0 = (VL == 0) ? row0 * C::GV : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
-    bulk_g2s(dst + p.off_ks, p.k_scale + ks0, p.sz_k_bytes, fb, pol);
-    bulk_g2s(dst + p.off_kz, p.k_off + ks0, p.sz_k_bytes, fb, pol);
-    bulk_g2s(dst + p.off_vs, p.v_scale + vs0, p.sz_v_bytes, fb, pol);
-    bulk_g2s(dst + p.off_vz, p.v_off + vs0, p.sz_v_bytes, fb, pol);
+    fence_proxy_async_smem();  // earlier reads of the half come before its refill
+    if (!v_half) {
+      const uint32_t fb = bar_k(r);
+      const size_t ks0 = (KL == 0) ? row0 * C::GK : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
+      mbar_arrive_expect_tx(fb, p.entry_tx_k);
+      bulk_g2s(dst, p.k_codes + row0 * RB, UNIT * RB, fb, pol);
+      bulk_g2s(dst + p.off_ks, p.k_scale + ks0, p.sz_k_bytes, fb, pol);
+      bulk_g2s(dst + p.off_kz, p.k_off + ks0, p.sz_k_bytes, fb, pol);
+    } else {
+      const uint32_t fb = bar_v(r);
+      const size_t vs0 = (VL == 0) ? row0 * C::GV : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
+      mbar_arrive_expect_tx(fb, p.entry_tx_v);
+      bulk_g2s(dst + p.off_vc, p.v_codes + row0 * RB, UNIT * RB, fb, pol);
+      bulk_g2s(dst + p.off_vs, p.v_scale + vs0, p.sz_v_bytes, fb, pol);
+      bulk_g2s(dst + p.off_vz, p.v_off + vs0, p.sz_v_bytes, fb, pol);
+    }
   };
 
   // This warp's items are local indices warp, warp + W, ... of the CTA range; the
   // non-empty ones go through entries 0, 1, .., R-1, 0, ... of its ring in order.
-  // Two cursors walk them without divisions: one issuing copies ahead, one consuming.
+  // Cursors walk them without divisions: one per half issuing copies ahead, one consuming.
   const int NL = (int)(X1 - X0);
   const int n_pairs = p.B * p.Hkv;
   struct Cursor {
     int i, u, t, L;  // local item index, pair, item within the pair, valid tokens of the pair
+    int r, n;        // ring entry of the next copy or read, copies issued or items read
   };
   auto pair_len = [&](int u) { return u < n_pairs ? min(max(__ldg(p.seq_lens + u / p.Hkv), 0), p.T_cap) : 0; };
   auto cursor_start = [&]() {
@@ -841,11 +865,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
     k.u = (int)(x / p.ipu);
     k.t = (int)(x - (long long)k.u * p.ipu);
     k.L = pair_len(k.u);
+    k.r = 0;
+    k.n = 0;
     return k;
   };
   auto cursor_next = [&](Cursor& k) {
-    k.i += kConsumerWarps;
-    k.t += kConsumerWarps;
+    k.i += C::WARPS;
+    k.t += C::WARPS;
     if (k.t >= p.ipu) {
       do {
         k.t -= p.ipu;
@@ -854,32 +880,35 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
       k.L = (k.i < NL) ? pair_len(k.u) : 0;
     }
   };
-  Cursor iss = cursor_start();
-  int r_iss = 0, n_issued = 0;
-  auto issue_next = [&]() {
-    for (; iss.i < NL; cursor_next(iss)) {
-      if (iss.t * UNIT < iss.L) {
-        if (lane == 0) {
-          fence_proxy_async_smem();  // earlier reads of the entry come before its refill
-          copy_item(iss.u, iss.t, r_iss);
-        }
-        ++n_issued;
-        if (++r_iss == R) r_iss = 0;
-        cursor_next(iss);
+  // Issue the copies of one half for this warp's next non-empty item, if any.
+  auto issue_next = [&](Cursor& k, bool v_half) {
+    for (; k.i < NL; cursor_next(k)) {
+      if (k.t * UNIT < k.L) {
+        if (lane == 0) copy_half(v_half, k.u, k.t, k.r);
+        ++k.n;
+        if (++k.r == R) k.r = 0;
+        cursor_next(k);
         return;
       }
     }
   };
   if (lane == 0) {
-    for (int r = 0; r < R; ++r) mbar_init(bar_w + 8u * r, 1);
+    for (int r = 0; r < R; ++r) {
+      mbar_init(bar_k(r), 1);
+      mbar_init(bar_v(r), 1);
+    }
     mbar_init_fence();
   }
   __syncwarp();
-  for (int r = 0; r < R; ++r) issue_next();
+  Cursor iss_k = cursor_start(), iss_v = iss_k;
+  for (int r = 0; r < R; ++r) {
+    issue_next(iss_k, false);
+    issue_next(iss_v, true);
+  }
 
   bool failed = false;
   Cursor con = cursor_start();
-  int r_con = 0, ph_con = 0, n_consumed = 0;
+  int ph_con = 0, n_v_read = 0;
 
   for (long long x = X0; x < X1;) {
     // ---------------------------------------------------- segment: the items of pair u
@@ -890,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
 
     // Stage Q (fp32) and the per-query constants of pair u.
     __syncthreads();  // the previous segment's merge is done with sQ and the merge area
-    for (int idx = threadIdx.x; idx < hq * D; idx += kThreads)
+    for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS)
       sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
     __syncthreads();
     if (warp < hq) {
@@ -1000,11 +1029,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
     for (; !failed && con.i < NL && con.u == u; cursor_next(con)) {
       const int nv = min(UNIT, con.L - con.t * UNIT);  // valid tokens of the item
       if (nv <= 0) continue;
-      if (!mbar_wait(bar_w + 8u * r_con, ph_con, p.status, kStatusConsumerTimeout)) {
+      const int r = con.r;
+      if (!mbar_wait(bar_k(r), ph_con, p.status, kStatusConsumerTimeout)) {
         failed = true;
         break;
       }
-      const uint8_t* en = ring_w + (size_t)r_con * p.entry_bytes;
+      const uint8_t* en = ring_w + (size_t)r * p.entry_bytes;
       SlotSmem sm;
       sm.kc = en;
       sm.vc = en + p.off_vc;
@@ -1012,61 +1042,127 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
       sm.kz = reinterpret_cast<const __half*>(en + p.off_kz);
       sm.vs = reinterpret_cast<const __half*>(en + p.off_vs);
       sm.vz = reinterpret_cast<const __half*>(en + p.off_vz);
+      ++con.n;
+      auto mid = [&]() {
+        __syncwarp();
+        issue_next(iss_k, false);  // the K half is read: refill it with the next item's K
+        if (!mbar_wait(bar_v(r), ph_con, p.status, kStatusConsumerTimeout)) {
+          failed = true;
+          return false;
+        }
+        ++n_v_read;
+        return true;
+      };
       if (nv == UNIT)
-        process_unit<C, true>(st, sm, nv, sQ, p.sl2, lc);
+        process_unit<C, true>(st, sm, nv, sQ, p.sl2, lc, mid);
       else
-        process_unit<C, false>(st, sm, nv, sQ, p.sl2, lc);
-      ++n_consumed;
-      if (++r_con == R) {
-        r_con = 0;
+        process_unit<C, false>(st, sm, nv, sQ, p.sl2, lc, mid);
+      if (failed) break;
+      if (++con.r == R) {
+        con.r = 0;
         ph_con ^= 1;
       }
       __syncwarp();
-      issue_next();  // refill the entry just read with this warp's next item, if any
+      issue_next(iss_v, true);  // the V half is read: refill it with the next item's V
+    }
+
+    // ---------------------------------------------------- warps beyond kMergeWarps fold in
+    // Warp w + kMergeWarps hands its register state, lane by lane (same layout), to warp w,
+    // which merges it into its own: running maxima, denominators, offsets and outputs.
+    if (C::WARPS > kMergeWarps) {
+      constexpr int SF = 16 * NQ + NO + 2 * NQ;
+      static_assert(SF <= kStateFloats, "handed-over state fits the merge area");
+      float* xs = ma.m;  // [kMergeWarps][SF][32]
+      if (warp >= kMergeWarps) {
+        float* d = xs + (size_t)(warp - kMergeWarps) * SF * 32 + lane;
+        int k = 0;
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          d[32 * k++] = st.m_run[j];
+          d[32 * k++] = st.l[j];
+        }
+#pragma unroll
+        for (int o = 0; o < NO; ++o) d[32 * k++] = st.zacc[o];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int row = 0; row < 2; ++row)
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) d[32 * k++] = st.o_run[mt][row][i];
+      }
+      __syncthreads();
+      if (warp < kMergeWarps && warp + kMergeWarps < C::WARPS) {
+        const float* d = xs + (size_t)warp * SF * 32 + lane;
+        float aa[NQ], ab[NQ];
+        int k = 0;
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          const float mb = d[32 * k++], lb = d[32 * k++];
+          const float m = fmaxf(st.m_run[j], mb);
+          aa[j] = (st.m_run[j] == m) ? 1.f : fast_exp2(st.pa[j] * (st.m_run[j] - m));
+          ab[j] = (mb == m) ? 1.f : fast_exp2(st.pa[j] * (mb - m));
+          st.m_run[j] = m;
+          st.l[j] = aa[j] * st.l[j] + ab[j] * lb;
+        }
+#pragma unroll
+        for (int o = 0; o < NO; ++o) {
+          const int j = own_slot<C>(o);
+          st.zacc[o] = aa[j] * st.zacc[o] + ab[j] * d[32 * k++];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int row = 0; row < 2; ++row)
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] = aa[i] * st.o_run[mt][row][i] + ab[i] * d[32 * k++];
+      }
+      __syncthreads();
     }
 
     // ---------------------------------------------------- warp results into the merge area
+    if (warp < kMergeWarps) {
 #pragma unroll
-    for (int j = 0; j < NQ; ++j) {
-      float l = st.l[j];
-      l += __shfl_xor_sync(FULLMASK, l, 4);
-      l += __shfl_xor_sync(FULLMASK, l, 8);
-      l += __shfl_xor_sync(FULLMASK, l, 16);
-      const int q = qk_query<C>(2 * c + j, hq);
-      if (g == 0 && q >= 0) {
-        ma.m[warp * kMaxHq + q] = (st.m_run[j] == -INFINITY) ? -INFINITY : st.pa[j] * st.m_run[j];
-        ma.l[warp * kMaxHq + q] = l;
+      for (int j = 0; j < NQ; ++j) {
+        float l = st.l[j];
+        l += __shfl_xor_sync(FULLMASK, l, 4);
+        l += __shfl_xor_sync(FULLMASK, l, 8);
+        l += __shfl_xor_sync(FULLMASK, l, 16);
+        const int q = qk_query<C>(2 * c + j, hq);
+        if (g == 0 && q >= 0) {
+          ma.m[warp * kMaxHq + q] = (st.m_run[j] == -INFINITY) ? -INFINITY : st.pa[j] * st.m_run[j];
+          ma.l[warp * kMaxHq + q] = l;
+        }
       }
-    }
-    float zs[NO];
+      float zs[NO];
 #pragma unroll
-    for (int o = 0; o < NO; ++o) {
-      float z = st.zacc[o];
-      z += __shfl_xor_sync(FULLMASK, z, 4);
-      z += __shfl_xor_sync(FULLMASK, z, 8);
-      z += __shfl_xor_sync(FULLMASK, z, 16);
-      zs[o] = z;
-    }
-    // live column i holds owned combo o = (query, V group); this lane's 16 channels
-    // 16g..16g+15 all lie in V group u_lane
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) {
-      const int o = live_own<C>(i, lc);
-      if (o < 0) continue;
-      const int combo = own_combo<C>(c, o);
-      if (combo >= hq * GV || combo % GV != lc.u_lane) continue;
-      const int q = combo / GV;
-      float zt = 0.f;
-      if (VL == 0) {
-#pragma unroll
-        for (int oo = 0; oo < NO; ++oo)
-          if (oo == o) zt = zs[oo];
+      for (int o = 0; o < NO; ++o) {
+        float z = st.zacc[o];
+        z += __shfl_xor_sync(FULLMASK, z, 4);
+        z += __shfl_xor_sync(FULLMASK, z, 8);
+        z += __shfl_xor_sync(FULLMASK, z, 16);
+        zs[o] = z;
       }
+      // live column i holds owned combo o = (query, V group); this lane's 16 channels
+      // 16g..16g+15 all lie in V group u_lane
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
+      for (int i = 0; i < NQ; ++i) {
+        const int o = live_own<C>(i, lc);
+        if (o < 0) continue;
+        const int combo = own_combo<C>(c, o);
+        if (combo >= hq * GV || combo % GV != lc.u_lane) continue;
+        const int q = combo / GV;
+        float zt = 0.f;
+        if (VL == 0) {
 #pragma unroll
-        for (int row = 0; row < 2; ++row)
-          ma.o[(warp * hq + q) * D + 16 * g + pv_channel<BITS>(mt, row)] = st.o_run[mt][row][i] + zt;
+          for (int oo = 0; oo < NO; ++oo)
+            if (oo == o) zt = zs[oo];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int row = 0; row < 2; ++row)
+            ma.o[(warp * hq + q) * D + 16 * g + pv_channel<BITS>(mt, row)] = st.o_run[mt][row][i] + zt;
+      }
     }
     __syncthreads();
 
@@ -1078,15 +1174,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
     const int c_last = cta_of((long long)(u + 1) * p.ipu - 1, p.tot_items, p.n_cta);
     const int n_contrib = c_last - c_first + 1;
     const bool alone = (n_contrib == 1) && !p.has_win;
-    for (int idx = threadIdx.x; idx < hq * D; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS) {
       const int i = idx / D, ch = idx % D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ma.m[w * kMaxHq + i]);
+      for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, ma.m[w * kMaxHq + i]);
       float acc = 0.f, lt = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < kMergeWarps; ++w) {
           const float mw = ma.m[w * kMaxHq + i];
           const float sc = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
           acc = fmaf(sc, ma.o[(w * hq + i) * D + ch], acc);
@@ -1119,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
         // (into the merge area, free again) and the merged denominator
         float* s_sc = ma.o;                              // [n_used][hq]
         float* s_l = ma.l;                               // [hq]
-        for (int i = warp; i < hq; i += kConsumerWarps) {
+        for (int i = warp; i < hq; i += C::WARPS) {
           float M = -INFINITY;
           for (int k = lane; k < n_used; k += 32)
             M = fmaxf(M, __ldcg(&p.part_ml[((size_t)u * p.n_slots + slot_of(k)) * hq + i].x));
@@ -1137,7 +1233,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
           if (lane == 0) s_l[i] = lt;
         }
         __syncthreads();
-        for (int idx = threadIdx.x; idx < hq * D; idx += kThreads) {
+        for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS) {
           const int i = idx / D, ch = idx % D;
           float acc = 0.f;
 #pragma unroll 4
@@ -1155,13 +1251,17 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(const __grid_
   }
 
   if (failed && lane == 0) {
-    // every copy issued must have landed before shared memory is freed
-    for (int k = n_consumed; k < n_issued; ++k) {
-      if (!mbar_wait(bar_w + 8u * r_con, ph_con, p.status, kStatusDrainTimeout)) break;
-      if (++r_con == R) {
-        r_con = 0;
-        ph_con ^= 1;
-      }
+    // every copy issued must have landed before shared memory is freed: wait (bounded)
+    // for each outstanding half in issue order
+    int rk = 0, pk = 0;
+    for (int k = 0; k < iss_k.n; ++k) {
+      if (k >= con.n && !mbar_wait(bar_k(rk), pk, p.status, kStatusDrainTimeout)) break;
+      if (++rk == R) { rk = 0; pk ^= 1; }
+    }
+    int rv = 0, pv = 0;
+    for (int k = 0; k < iss_v.n; ++k) {
+      if (k >= n_v_read && !mbar_wait(bar_v(rv), pv, p.status, kStatusDrainTimeout)) break;
+      if (++rv == R) { rv = 0; pv ^= 1; }
     }
   }
 }

@@ -6,19 +6,19 @@
 
 namespace lbkv {
 
-__global__ void __launch_bounds__(kThreads, 1) window_partial_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(32 * kWinWarps, 1) window_partial_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
   __shared__ float sQ[kMaxHq * D];
-  __shared__ float sM[kConsumerWarps][kMaxHq];
-  __shared__ float sL[kConsumerWarps][kMaxHq];
-  __shared__ float sO[kConsumerWarps][kMaxHq][D];
+  __shared__ float sM[kWinWarps][kMaxHq];
+  __shared__ float sL[kWinWarps][kMaxHq];
+  __shared__ float sO[kWinWarps][kMaxHq][D];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int hq = p.hq;
   const int u = b * p.Hkv + kvh;
-  for (int idx = threadIdx.x; idx < hq * D; idx += kThreads)
+  for (int idx = threadIdx.x; idx < hq * D; idx += 32 * kWinWarps)
     sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
   __syncthreads();
 
@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kThreads, 1) window_partial_kernel(const __gri
     o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   }
   const size_t wbase = (size_t)u * p.win_cap;
-  for (int t = warp; t < W; t += kConsumerWarps) {
+  for (int t = warp; t < W; t += kWinWarps) {
     const uint2 kr = reinterpret_cast<const uint2*>(p.k_win + (wbase + t) * D)[lane];
     const uint2 vr = reinterpret_cast<const uint2*>(p.v_win + (wbase + t) * D)[lane];
     const __nv_bfloat162* kh = reinterpret_cast<const __nv_bfloat162*>(&kr);
@@ -71,15 +71,15 @@ __global__ void __launch_bounds__(kThreads, 1) window_partial_kernel(const __gri
   __syncthreads();
 
   // merge the warps into the window slot of the pair
-  for (int idx = threadIdx.x; idx < hq * D; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < hq * D; idx += 32 * kWinWarps) {
     const int i = idx / D, ch = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sM[w][i]);
+    for (int w = 0; w < kWinWarps; ++w) M = fmaxf(M, sM[w][i]);
     float acc = 0.f, lt = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < kWinWarps; ++w) {
         const float sc = (sM[w][i] == -INFINITY) ? 0.f : fast_exp2(sM[w][i] - M);
         acc = fmaf(sc, sO[w][i][ch], acc);
         lt = fmaf(sc, sL[w][i], lt);
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) window_partial_kernel(const __gri
 
 int launch_window_partial(const DecodeParams& p, cudaStream_t stream) {
   dim3 grid((unsigned)p.Hkv, (unsigned)p.B);
-  window_partial_kernel<<<grid, kThreads, 0, stream>>>(p);
+  window_partial_kernel<<<grid, 32 * kWinWarps, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
