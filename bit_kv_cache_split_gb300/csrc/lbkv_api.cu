@@ -58,8 +58,7 @@ struct Plan {
   int hq, mode, gv, win;
   int unit_tokens, ipu, n_cta, n_slots;
   long long tot_items;
-  int ring_off, ring_per_warp, entry_bytes, entry_tx_k, entry_tx_v, smem_bytes, threads;
-  int off_vc, off_ks, off_kz, off_vs, off_vz, sz_k, sz_v;
+  int ring_off, ring_per_warp, entry_bytes, smem_bytes, threads;
   size_t off_done, off_ml, off_o, ws_bytes;
 };
 
@@ -92,21 +91,11 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   int st = current_device_props(&sms, &smem_optin);
   if (st) return st;
 
-  // ring entry (one item of `ut` tokens): K codes | K scale | K offset | V codes | V scale | V offset
+  // ring entry: one item of `ut` tokens, K half then V half
   const int ut = kChunk * unit_chunks(bits, pl->mode, group == 128 ? 7 : group == 64 ? 6 : 5);
-  const int rb = kHeadDim * bits / 8;
-  const int cw_rows = ut >= group ? ut / group : 1;  // channel-wise s/z rows an item touches
+  const EntryLayout el = entry_layout(bits, kl, vl, ut, group);
   pl->unit_tokens = ut;
-  pl->sz_k = (kl == LBKV_TOKENWISE) ? ut * (kHeadDim / group) * 2 : cw_rows * kHeadDim * 2;
-  pl->sz_v = (vl == LBKV_TOKENWISE) ? ut * (kHeadDim / group) * 2 : cw_rows * kHeadDim * 2;
-  pl->off_ks = ut * rb;
-  pl->off_kz = pl->off_ks + pl->sz_k;
-  pl->off_vc = pl->off_kz + pl->sz_k;
-  pl->off_vs = pl->off_vc + ut * rb;
-  pl->off_vz = pl->off_vs + pl->sz_v;
-  pl->entry_tx_k = pl->off_vc;  // the K half: codes, scales, offsets
-  pl->entry_tx_v = ut * rb + 2 * pl->sz_v;
-  pl->entry_bytes = (int)round_up((size_t)(pl->off_vz + pl->sz_v), 128);
+  pl->entry_bytes = el.bytes;
   const int warps = decode_warps(bits, pl->mode);
   pl->threads = 32 * warps;
   pl->ring_off = kPrologueBytes + merge_bytes(hq, warps);
@@ -209,16 +198,6 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.has_win = pl.win;
   p.ring_off = pl.ring_off;
   p.ring_per_warp = pl.ring_per_warp;
-  p.entry_bytes = pl.entry_bytes;
-  p.entry_tx_k = pl.entry_tx_k;
-  p.entry_tx_v = pl.entry_tx_v;
-  p.off_vc = pl.off_vc;
-  p.off_ks = pl.off_ks;
-  p.off_kz = pl.off_kz;
-  p.off_vs = pl.off_vs;
-  p.off_vz = pl.off_vz;
-  p.sz_k_bytes = pl.sz_k;
-  p.sz_v_bytes = pl.sz_v;
 
   if (ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem_bytes) != LBKV_OK) return LBKV_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -86,6 +86,26 @@ __host__ __device__ constexpr int unit_chunks(int bits, int mode, int log2g) {
   return mode == kModeWide ? 1 : bits == 2 ? (log2g == 5 ? 2 : 4) : 2;
 }
 
+// Byte layout of one ring entry (one item of `unit` tokens of one pair):
+// K codes | K scales | K offsets | V codes | V scales | V offsets, each part 16-byte
+// aligned; the K half and the V half are filled by separate bulk-copy groups.
+struct EntryLayout {
+  int sz_k, sz_v;                        // bytes of one scale (or offset) array, K and V side
+  int off_ks, off_kz, off_vc, off_vs, off_vz;
+  int tx_k, tx_v, bytes;                 // bytes of the K half, of the V half, entry stride
+};
+__host__ __device__ constexpr int sz_bytes(int layout, int unit, int g) {
+  return layout == 0 ? unit * (kHeadDim / g) * 2 : (unit >= g ? unit / g : 1) * kHeadDim * 2;
+}
+__host__ __device__ constexpr EntryLayout entry_layout(int bits, int kl, int vl, int unit, int g) {
+  const int rb = kHeadDim * bits / 8;
+  const int szk = sz_bytes(kl, unit, g), szv = sz_bytes(vl, unit, g);
+  const int off_ks = unit * rb, off_kz = off_ks + szk, off_vc = off_kz + szk;
+  const int off_vs = off_vc + unit * rb, off_vz = off_vs + szv;
+  return EntryLayout{szk, szv, off_ks, off_kz, off_vc, off_vs, off_vz, off_vc, unit * rb + 2 * szv,
+                     (off_vz + szv + 127) / 128 * 128};
+}
+
 struct DecodeParams {
   const __nv_bfloat16* q;
   const uint8_t* k_codes;
@@ -108,9 +128,7 @@ struct DecodeParams {
   long long tot_items;  // B * Hkv * ipu
   int ipu, n_cta;       // items per pair (T_cap / UNIT), CTAs of the grid
   int n_slots, has_win; // partial slots per pair (the last one the window's when has_win)
-  int ring_off, ring_per_warp, entry_bytes, entry_tx_k, entry_tx_v;
-  int off_ks, off_kz, off_vc, off_vs, off_vz;  // byte offsets inside a ring entry (K codes at 0)
-  int sz_k_bytes, sz_v_bytes;                  // bytes of one scale (or offset) array per entry
+  int ring_off, ring_per_warp;  // shared-memory offset of the rings, entries per warp
 };
 
 // Compile-time shape of one kernel variant.
@@ -131,6 +149,7 @@ struct Cfg {
   static constexpr int UNIT = kChunk * NCH;             // tokens per item
   static constexpr int WARPS = decode_warps(BITS, MODE);
   static constexpr int THREADS = 32 * WARPS;
+  static constexpr EntryLayout E = entry_layout(BITS, KL, VL, UNIT, G);
   static_assert(G >= kChunk, "a chunk never straddles a token group");
   static_assert(MODE != kModeWide || GV >= 2, "16 combos need several V channel groups");
 };
@@ -159,19 +178,36 @@ __device__ __forceinline__ int own_group(int c, int o) {
   return C::DUP ? c % C::GV : (2 * c + (o & 1)) % C::GV;
 }
 
-// Channel fed at k-slot kappa (0..15) of QK^T k-step ks (0..7); see the K operand build.
-template <int BITS>
+// K operand mappings. Block mapping (token-wise K with several channel groups): each
+// k-step stays inside one 32-channel block, lanes with odd c taking the upper byte of
+// each 16-bit half. Wide mapping (one channel group, or channel-wise K): lane c takes
+// whole words of its own 32 channels, all positions of each 16-bit half (positions
+// past the 10-bit mantissa come from the word shifted right by 10 (INT2) or 8 (INT4)).
+template <class C>
+__device__ __forceinline__ constexpr bool qk_wide() {
+  return C::GK == 1;
+}
+// Channel fed at k-slot kappa (0..15) of QK^T k-step ks (0..7).
+template <class C>
 __device__ __forceinline__ int qk_channel(int ks, int kappa) {
-  const int blk = ks >> 1, h = ks & 1, c = (kappa & 7) >> 1, e = kappa & 1, up = kappa >> 3;
-  const int p = 2 * h + up;
-  if (BITS == 2) return 32 * blk + 16 * (c >> 1) + 4 * (c & 1) + 8 * e + p;
+  const int c = (kappa & 7) >> 1, e = kappa & 1, up = kappa >> 3;
+  if (qk_wide<C>()) {
+    if (C::BITS == 2) return 16 * (2 * c + (ks >> 2)) + 8 * e + 2 * (ks & 3) + up;
+    return 8 * (4 * c + (ks >> 1)) + 4 * e + 2 * (ks & 1) + up;
+  }
+  const int blk = ks >> 1, p = 2 * (ks & 1) + up;
+  if (C::BITS == 2) return 32 * blk + 16 * (c >> 1) + 4 * (c & 1) + 8 * e + p;
   return 32 * blk + 8 * c + 4 * e + p;
 }
 // Power-of-two position factor of the fp16 image of K channel ch (1024 + factor * q).
-template <int BITS>
+template <class C>
 __device__ __forceinline__ float k_mult(int ch) {
-  if (BITS == 2) return (float)(1 << (2 * (ch & 3)));
-  return (ch & 1) ? 16.f : 1.f;
+  if (C::BITS == 4) return (ch & 1) ? 16.f : 1.f;
+  if (qk_wide<C>()) {
+    const int p = ch & 7;
+    return (float)(1 << (2 * (p <= 4 ? p : p - 5)));
+  }
+  return (float)(1 << (2 * (ch & 3)));
 }
 // Position factor of V m-tile mt (both of its rows).
 template <int BITS>
@@ -246,9 +282,9 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
     for (int r = 0; r < 2; ++r)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
+        const int ch = qk_channel<C>(ks, 2 * c + 8 * r + e);
         const float qv = live ? sQ[qb * D + ch] : 0.f;
-        const float v = qv * __half2float(s_tau[ch]) * (1.f / k_mult<BITS>(ch));
+        const float v = qv * __half2float(s_tau[ch]) * (1.f / k_mult<C>(ch));
         x[ks][r][e] = v;
         amax = fmaxf(amax, fabsf(v));
         zsum = fmaf(qv, __half2float(z_tau[ch]), zsum);
@@ -298,18 +334,33 @@ __device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpStat
     const uint32_t* rA = reinterpret_cast<const uint32_t*>(sm.kc + tA * RB);
     const uint32_t* rB = reinterpret_cast<const uint32_t*>(sm.kc + (tA + 1) * RB);
     uint32_t wA[4], wB[4], sA[4], sB[4];
+    if (qk_wide<C>()) {
+      if (BITS == 2) {  // words 2c, 2c+1 of each row
+        const uint2 va = reinterpret_cast<const uint2*>(rA)[c], vb = reinterpret_cast<const uint2*>(rB)[c];
+        wA[0] = va.x, wA[1] = va.y, wB[0] = vb.x, wB[1] = vb.y;
 #pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
-      if (BITS == 2) {
-        // lanes with odd c take codes 4..7 and 12..15 of the word: shift them into 0..3
-        const int sh = 8 * (c & 1);
-        wA[blk] = rA[2 * blk + (c >> 1)] >> sh;
-        wB[blk] = rB[2 * blk + (c >> 1)] >> sh;
-      } else {
-        wA[blk] = rA[4 * blk + c];
-        wB[blk] = rB[4 * blk + c];
-        sA[blk] = wA[blk] >> 8;
-        sB[blk] = wB[blk] >> 8;
+        for (int x = 0; x < 2; ++x) sA[x] = wA[x] >> 10, sB[x] = wB[x] >> 10;
+      } else {  // words 4c .. 4c+3 of each row
+        const uint4 va = reinterpret_cast<const uint4*>(rA)[c], vb = reinterpret_cast<const uint4*>(rB)[c];
+        wA[0] = va.x, wA[1] = va.y, wA[2] = va.z, wA[3] = va.w;
+        wB[0] = vb.x, wB[1] = vb.y, wB[2] = vb.z, wB[3] = vb.w;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) sA[x] = wA[x] >> 8, sB[x] = wB[x] >> 8;
+      }
+    } else {
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        if (BITS == 2) {
+          // lanes with odd c take codes 4..7 and 12..15 of the word: shift them into 0..3
+          const int sh = 8 * (c & 1);
+          wA[blk] = rA[2 * blk + (c >> 1)] >> sh;
+          wB[blk] = rB[2 * blk + (c >> 1)] >> sh;
+        } else {
+          wA[blk] = rA[4 * blk + c];
+          wB[blk] = rB[4 * blk + c];
+          sA[blk] = wA[blk] >> 8;
+          sB[blk] = wB[blk] >> 8;
+        }
       }
     }
     float xs[2][NQ];
@@ -322,7 +373,21 @@ __device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpStat
     for (int ks = 0; ks < 8; ++ks) {
       const int blk = ks >> 1, h = ks & 1;
       uint32_t a0, a1, a2, a3;
-      if (BITS == 2) {
+      if (qk_wide<C>()) {
+        if (BITS == 2) {
+          const int x = ks >> 2, p0 = 2 * (ks & 3);
+          a0 = int2_half2(wA[x], sA[x], p0);
+          a1 = int2_half2(wB[x], sB[x], p0);
+          a2 = int2_half2(wA[x], sA[x], p0 + 1);
+          a3 = int2_half2(wB[x], sB[x], p0 + 1);
+        } else {
+          const int x = ks >> 1, p0 = 2 * (ks & 1);
+          a0 = int4_half2(wA[x], sA[x], p0);
+          a1 = int4_half2(wB[x], sB[x], p0);
+          a2 = int4_half2(wA[x], sA[x], p0 + 1);
+          a3 = int4_half2(wB[x], sB[x], p0 + 1);
+        }
+      } else if (BITS == 2) {
         const uint32_t mA = 0x00030003u << (4 * h), mB = 0x00030003u << (4 * h + 2);
         a0 = and_or(wA[blk], mA, kMagic2);
         a1 = and_or(wB[blk], mA, kMagic2);
@@ -527,14 +592,10 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
 
   // ------------------------------------------------ phase 1: scores of the whole unit
   float x[NCH][2][2][NQ];
-  uint32_t qB[8][2];
+  uint32_t qBt[8][2];  // channel-wise K: Q' of the current token group
   float cwA[NQ], cwB[NQ], cwneg[2] = {0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < NQ; ++j) cwA[j] = cwB[j] = 0.f;
-  if (KL == 0) {
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) qB[ks][0] = st.qB[ks][0], qB[ks][1] = st.qB[ks][1];
-  }
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     const int rel0 = kChunk * ch;
@@ -549,9 +610,12 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
     }
     if (KL == 1 && (ch == 0 || (C::G <= C::UNIT && (kChunk * ch) % C::G == 0))) {
       const int tau = rel0 / C::G;
-      channelwise_q<C>(qB, cwA, cwB, cwneg, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
+      channelwise_q<C>(qBt, cwA, cwB, cwneg, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
     }
-    qk_chunk<C>(x[ch], st, qB, cwA, cwB, cwneg, sm, rel0, lc);
+    if constexpr (KL == 0)
+      qk_chunk<C>(x[ch], st, st.qB, cwA, cwB, cwneg, sm, rel0, lc);
+    else
+      qk_chunk<C>(x[ch], st, qBt, cwA, cwB, cwneg, sm, rel0, lc);
     if (!FULL) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
@@ -819,7 +883,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   // its V half while the next QK^T phase runs.
   const int R = p.ring_per_warp;
   const uint32_t bar_w = smem_addr(bars) + 16u * (uint32_t)(warp * R);
-  uint8_t* ring_w = ring + (size_t)warp * R * p.entry_bytes;
+  uint8_t* ring_w = ring + (size_t)warp * R * C::E.bytes;
   auto bar_k = [&](int r) { return bar_w + 16u * r; };
   auto bar_v = [&](int r) { return bar_w + 16u * r + 8u; };
 
@@ -828,23 +892,23 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     const size_t t0 = (size_t)t * UNIT;
     const size_t row0 = (size_t)u * p.T_cap + t0;
     const size_t blocks = (size_t)p.T_cap / C::G;
-    const uint32_t dst = smem_addr(ring_w + (size_t)r * p.entry_bytes);
+    const uint32_t dst = smem_addr(ring_w + (size_t)r * C::E.bytes);
     const uint64_t pol = l2_evict_first_policy();
     fence_proxy_async_smem();  // earlier reads of the half come before its refill
     if (!v_half) {
       const uint32_t fb = bar_k(r);
       const size_t ks0 = (KL == 0) ? row0 * C::GK : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
-      mbar_arrive_expect_tx(fb, p.entry_tx_k);
+      mbar_arrive_expect_tx(fb, C::E.tx_k);
       bulk_g2s(dst, p.k_codes + row0 * RB, UNIT * RB, fb, pol);
-      bulk_g2s(dst + p.off_ks, p.k_scale + ks0, p.sz_k_bytes, fb, pol);
-      bulk_g2s(dst + p.off_kz, p.k_off + ks0, p.sz_k_bytes, fb, pol);
+      bulk_g2s(dst + C::E.off_ks, p.k_scale + ks0, C::E.sz_k, fb, pol);
+      bulk_g2s(dst + C::E.off_kz, p.k_off + ks0, C::E.sz_k, fb, pol);
     } else {
       const uint32_t fb = bar_v(r);
       const size_t vs0 = (VL == 0) ? row0 * C::GV : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
-      mbar_arrive_expect_tx(fb, p.entry_tx_v);
-      bulk_g2s(dst + p.off_vc, p.v_codes + row0 * RB, UNIT * RB, fb, pol);
-      bulk_g2s(dst + p.off_vs, p.v_scale + vs0, p.sz_v_bytes, fb, pol);
-      bulk_g2s(dst + p.off_vz, p.v_off + vs0, p.sz_v_bytes, fb, pol);
+      mbar_arrive_expect_tx(fb, C::E.tx_v);
+      bulk_g2s(dst + C::E.off_vc, p.v_codes + row0 * RB, UNIT * RB, fb, pol);
+      bulk_g2s(dst + C::E.off_vs, p.v_scale + vs0, C::E.sz_v, fb, pol);
+      bulk_g2s(dst + C::E.off_vz, p.v_off + vs0, C::E.sz_v, fb, pol);
     }
   };
 
@@ -880,17 +944,24 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       k.L = (k.i < NL) ? pair_len(k.u) : 0;
     }
   };
-  // Issue the copies of one half for this warp's next non-empty item, if any.
-  auto issue_next = [&](Cursor& k, bool v_half) {
-    for (; k.i < NL; cursor_next(k)) {
-      if (k.t * UNIT < k.L) {
-        if (lane == 0) copy_half(v_half, k.u, k.t, k.r);
-        ++k.n;
-        if (++k.r == R) k.r = 0;
-        cursor_next(k);
-        return;
-      }
+  // The issue cursor stops at this warp's next non-empty item: issue_k() sends its K half,
+  // issue_v() its V half and moves on (the K half always goes first).
+  Cursor iss = cursor_start();
+  bool k_pending = false;
+  auto issue_k = [&]() {
+    while (iss.i < NL && iss.t * UNIT >= iss.L) cursor_next(iss);
+    if (iss.i < NL) {
+      if (lane == 0) copy_half(false, iss.u, iss.t, iss.r);
+      k_pending = true;
     }
+  };
+  auto issue_v = [&]() {
+    if (!k_pending) return;
+    if (lane == 0) copy_half(true, iss.u, iss.t, iss.r);
+    k_pending = false;
+    ++iss.n;
+    if (++iss.r == R) iss.r = 0;
+    cursor_next(iss);
   };
   if (lane == 0) {
     for (int r = 0; r < R; ++r) {
@@ -900,10 +971,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     mbar_init_fence();
   }
   __syncwarp();
-  Cursor iss_k = cursor_start(), iss_v = iss_k;
   for (int r = 0; r < R; ++r) {
-    issue_next(iss_k, false);
-    issue_next(iss_v, true);
+    issue_k();
+    issue_v();
   }
 
   bool failed = false;
@@ -932,7 +1002,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       for (int uu = 0; uu < 4; ++uu) {
         const int ch = 4 * lane + uu;
         const float v = sQ[i * D + ch];
-        amax = fmaxf(amax, fabsf(v) * (1.f / k_mult<BITS>(ch)));
+        amax = fmaxf(amax, fabsf(v) * (1.f / k_mult<C>(ch)));
         gs += v;
       }
 #pragma unroll
@@ -984,8 +1054,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
           float xx[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int ch = qk_channel<BITS>(ks, 2 * c + 8 * r + e);
-            xx[e] = live ? sQ[qb * D + ch] * sc * (1.f / k_mult<BITS>(ch)) : 0.f;
+            const int ch = qk_channel<C>(ks, 2 * c + 8 * r + e);
+            xx[e] = live ? sQ[qb * D + ch] * sc * (1.f / k_mult<C>(ch)) : 0.f;
           }
           st.qB[ks][r] = f16x2_from(xx[0], xx[1]);
           gsum[ks / C::KSG] += xx[0] + xx[1];
@@ -1034,18 +1104,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         failed = true;
         break;
       }
-      const uint8_t* en = ring_w + (size_t)r * p.entry_bytes;
+      const uint8_t* en = ring_w + (size_t)r * C::E.bytes;
       SlotSmem sm;
       sm.kc = en;
-      sm.vc = en + p.off_vc;
-      sm.ks = reinterpret_cast<const __half*>(en + p.off_ks);
-      sm.kz = reinterpret_cast<const __half*>(en + p.off_kz);
-      sm.vs = reinterpret_cast<const __half*>(en + p.off_vs);
-      sm.vz = reinterpret_cast<const __half*>(en + p.off_vz);
+      sm.vc = en + C::E.off_vc;
+      sm.ks = reinterpret_cast<const __half*>(en + C::E.off_ks);
+      sm.kz = reinterpret_cast<const __half*>(en + C::E.off_kz);
+      sm.vs = reinterpret_cast<const __half*>(en + C::E.off_vs);
+      sm.vz = reinterpret_cast<const __half*>(en + C::E.off_vz);
       ++con.n;
       auto mid = [&]() {
         __syncwarp();
-        issue_next(iss_k, false);  // the K half is read: refill it with the next item's K
+        issue_k();  // the K half is read: refill it with the next item's K
         if (!mbar_wait(bar_v(r), ph_con, p.status, kStatusConsumerTimeout)) {
           failed = true;
           return false;
@@ -1063,7 +1133,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         ph_con ^= 1;
       }
       __syncwarp();
-      issue_next(iss_v, true);  // the V half is read: refill it with the next item's V
+      issue_v();  // the V half is read: refill it with the next item's V
     }
 
     // ---------------------------------------------------- warps beyond kMergeWarps fold in
@@ -1254,12 +1324,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     // every copy issued must have landed before shared memory is freed: wait (bounded)
     // for each outstanding half in issue order
     int rk = 0, pk = 0;
-    for (int k = 0; k < iss_k.n; ++k) {
+    for (int k = 0; k < iss.n + (k_pending ? 1 : 0); ++k) {
       if (k >= con.n && !mbar_wait(bar_k(rk), pk, p.status, kStatusDrainTimeout)) break;
       if (++rk == R) { rk = 0; pk ^= 1; }
     }
     int rv = 0, pv = 0;
-    for (int k = 0; k < iss_v.n; ++k) {
+    for (int k = 0; k < iss.n; ++k) {
       if (k >= n_v_read && !mbar_wait(bar_v(rv), pv, p.status, kStatusDrainTimeout)) break;
       if (++rv == R) { rv = 0; pv ^= 1; }
     }
