@@ -56,10 +56,9 @@ size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 struct Plan {
   int hq, mode, gv, win;
-  int unit_tokens, ipu, n_cta, n_slots;
-  long long tot_items;
+  int unit_tokens, n_cta;
   int ring_off, ring_per_warp, entry_bytes, smem_bytes, threads;
-  size_t off_done, off_ml, off_o, ws_bytes;
+  size_t off_done, off_ml, off_o, off_wml, off_wo, ws_bytes;
 };
 
 // Validates shapes and format, then fixes the persistent grid and the rings.
@@ -106,23 +105,21 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   pl->ring_per_warp = r_w;
   pl->smem_bytes = pl->ring_off + warps * r_w * pl->entry_bytes;
 
-  // Persistent grid: the items of all pairs (ipu per pair) split evenly over at most
-  // one CTA per SM. A pair spans at most ceil(n_cta / pairs) + 1 CTAs, each writing
-  // one partial slot; one more slot holds the window's partial.
+  // Persistent grid, one CTA per SM: the kernel splits the items of all pairs (from the
+  // device lengths) evenly over the CTAs. A CTA holds partials of at most two pairs.
   const long long units = (long long)d->batch * d->num_kv_heads;
   pl->win = win ? 1 : 0;
-  pl->ipu = d->max_seq_len / ut;
-  pl->tot_items = units * pl->ipu;
-  pl->n_cta = (int)(pl->tot_items < sms ? pl->tot_items : sms);
-  pl->n_slots = 0;
-  if (units > 0) pl->n_slots = (int)((pl->n_cta + units - 1) / units) + 1 + pl->win;
+  pl->n_cta = sms;
 
-  // workspace: status word | per-pair counters | (m, l) partials | O partials
-  const size_t rows = (size_t)units * pl->n_slots * hq;
+  // workspace: status word | per-pair counters | CTA partials (m, l) | CTA partials O |
+  // window partials (m, l) | window partials O
+  const size_t rows = (size_t)pl->n_cta * 2 * hq, wrows = pl->win ? (size_t)units * hq : 0;
   pl->off_done = 256;
   pl->off_ml = round_up(pl->off_done + (size_t)units * sizeof(int32_t), 256);
   pl->off_o = round_up(pl->off_ml + rows * sizeof(float2), 256);
-  pl->ws_bytes = round_up(pl->off_o + rows * kHeadDim * sizeof(float), 256);
+  pl->off_wml = round_up(pl->off_o + rows * kHeadDim * sizeof(float), 256);
+  pl->off_wo = round_up(pl->off_wml + wrows * sizeof(float2), 256);
+  pl->ws_bytes = round_up(pl->off_wo + wrows * kHeadDim * sizeof(float), 256);
   return LBKV_OK;
 }
 
@@ -180,6 +177,8 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.win_lens = desc->win_lens;
   p.part_ml = reinterpret_cast<float2*>(ws + pl.off_ml);
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
+  p.win_ml = reinterpret_cast<float2*>(ws + pl.off_wml);
+  p.win_o = reinterpret_cast<float*>(ws + pl.off_wo);
   p.status = reinterpret_cast<int32_t*>(ws);
   p.done = reinterpret_cast<int32_t*>(ws + pl.off_done);
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -191,10 +190,7 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.win_cap = desc->k_win ? desc->win_cap : 0;
   const float sigma = desc->sm_scale > 0.f ? desc->sm_scale : 1.f / std::sqrt((float)desc->head_dim);
   p.sl2 = sigma * 1.4426950408889634f;
-  p.tot_items = pl.tot_items;
-  p.ipu = pl.ipu;
   p.n_cta = pl.n_cta;
-  p.n_slots = pl.n_slots;
   p.has_win = pl.win;
   p.ring_off = pl.ring_off;
   p.ring_per_warp = pl.ring_per_warp;

@@ -118,16 +118,16 @@ struct DecodeParams {
   const __nv_bfloat16* k_win;
   const __nv_bfloat16* v_win;
   const int32_t* win_lens;
-  float2* part_ml;  // [B*Hkv][n_slots][hq] (running max in log2 units, denominator)
-  float* part_o;    // [B*Hkv][n_slots][hq][D] unnormalised output
+  float2* part_ml;  // [n_cta][2][hq] partials of the CTAs (running max in log2 units, denominator)
+  float* part_o;    // [n_cta][2][hq][D] unnormalised output
+  float2* win_ml;   // [B*Hkv][hq] the window's partial of each pair
+  float* win_o;     // [B*Hkv][hq][D]
   int32_t* status;
   int32_t* done;    // [B*Hkv] CTAs finished with a pair; the last one merges and resets it to 0
   __nv_bfloat16* out;
   int B, Hq, Hkv, hq, T_cap, win_cap;
   float sl2;  // softmax scale times log2(e)
-  long long tot_items;  // B * Hkv * ipu
-  int ipu, n_cta;       // items per pair (T_cap / UNIT), CTAs of the grid
-  int n_slots, has_win; // partial slots per pair (the last one the window's when has_win)
+  int n_cta, has_win;   // CTAs of the grid; whether a bf16 window is given
   int ring_off, ring_per_warp;  // shared-memory offset of the rings, entries per warp
 };
 
@@ -269,7 +269,7 @@ template <class C>
 __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)[C::NQ], float (&cwB)[C::NQ],
                                               float (&cwneg)[2], const __half* s_tau, const __half* z_tau,
                                               const float* sQ, float sl2, const LaneCols& lc) {
-  constexpr int BITS = C::BITS, D = kHeadDim;
+  constexpr int D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
   const int c = lc.c;
   const int qb = qk_query<C>(lc.g, lc.hq);  // this lane's B column is column g
@@ -828,25 +828,33 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
 }
 
 // ------------------------------------------------------------------------
-// Work split. The items (UNIT tokens) of all (sequence, KV head) pairs form one
-// sequence, pair u owning items u*ipu .. u*ipu+ipu-1 (ipu = T_cap / UNIT; items
-// past the sequence length are empty). CTA c of the persistent grid takes items
-// first_item(c) .. first_item(c+1)-1 and deals them to its warps in turn.
+// Work split. The items (UNIT tokens; the last one of a pair may be partial) of all
+// (sequence, KV head) pairs with tokens form one sequence in pair order. CTA c of the
+// persistent grid takes items first_item(c) .. first_item(c+1)-1 of it and deals them
+// to its warps in turn. Every CTA derives the item counts from the device lengths.
 // ------------------------------------------------------------------------
-__host__ __device__ inline long long first_item(long long c, long long tot, long long n_cta) {
+__device__ __forceinline__ long long first_item(long long c, long long tot, long long n_cta) {
   return c * tot / n_cta;
 }
-// The CTA whose range holds item x.
-__host__ __device__ inline int cta_of(long long x, long long tot, long long n_cta) {
+// The CTA whose range holds item x (the last one among CTAs with equal starts).
+__device__ __forceinline__ int cta_of(long long x, long long tot, long long n_cta) {
   return (int)(((x + 1) * n_cta - 1) / tot);
 }
 
-// Writes one merged partial (or, when it is the only one, the output) of pair u:
-// the CTA's warps deposited (m, l, o) per query in the merge area.
+// The CTA's warps deposit (m, l, o) per query here for the merge of a pair.
 struct MergeArea {
-  float* m;  // [warps][kMaxHq] running maximum (log2 units)
-  float* l;  // [warps][kMaxHq] denominator
-  float* o;  // [warps][hq][D] unnormalised output
+  float* m;  // [kMergeWarps][kMaxHq] running maximum (log2 units)
+  float* l;  // [kMergeWarps][kMaxHq] denominator
+  float* o;  // [kMergeWarps][hq][D] unnormalised output
+};
+
+// Result of the CTA's scan over the sequence lengths.
+struct SplitScan {
+  long long tot;           // items of all pairs
+  long long sum[32];       // per-warp sums of sequence items
+  long long b0_start;      // first item of sequence b0
+  int k0, b0;              // warp chunk and sequence holding the CTA's first item
+  long long k0_base;       // items before warp chunk k0
 };
 
 // ------------------------------------------------------------------------
@@ -855,18 +863,19 @@ struct MergeArea {
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NQ = C::NQ, NO = C::NO;
-  constexpr int RB = C::RB, D = kHeadDim, UNIT = C::UNIT;
+  constexpr int RB = C::RB, D = kHeadDim, UNIT = C::UNIT, W = C::WARPS;
   constexpr unsigned FULLMASK = 0xffffffffu;
   extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ SplitScan ss;
+  __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int cta = blockIdx.x;
   const int hq = p.hq;
-  const long long X0 = first_item(cta, p.tot_items, p.n_cta);
-  const long long X1 = first_item(cta + 1, p.tot_items, p.n_cta);
+  const int n_pairs = p.B * p.Hkv;
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);      // full[warp][ring_per_warp]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);      // per warp and entry: K half, V half
   float* sQ = reinterpret_cast<float*>(smem + kBarBytes);  // [kMaxHq][D]
   float* sAq = sQ + kMaxHq * D;                            // [kMaxHq] token-wise K score factor
   int* sEq = reinterpret_cast<int*>(sAq + kMaxHq);         // [kMaxHq] query exponent
@@ -876,7 +885,69 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   ma.l = ma.m + kMergeWarps * kMaxHq;
   ma.o = ma.l + kMergeWarps * kMaxHq;
   uint8_t* ring = smem + p.ring_off;
-  __shared__ int s_last;
+
+  // Valid tokens of sequence b (device value: clamped, never trusted) and items of one of
+  // its pairs.
+  auto seq_len = [&](int b) { return min(max(__ldg(p.seq_lens + b), 0), p.T_cap); };
+  auto items_of = [&](int L) { return (L + UNIT - 1) / UNIT; };
+
+  // ---------------------------------------------------- the CTA's share of the items
+  {
+    const int chunk = (p.B + W - 1) / W;  // warp w sums sequences [w chunk, (w+1) chunk)
+    const int bb0 = min(p.B, warp * chunk), bb1 = min(p.B, bb0 + chunk);
+    long long s = 0;
+    for (int b = bb0 + lane; b < bb1; b += 32) s += (long long)p.Hkv * items_of(seq_len(b));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULLMASK, s, o);
+    if (lane == 0) ss.sum[warp] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long tot = 0;
+      for (int w = 0; w < W; ++w) tot += ss.sum[w];
+      ss.tot = tot;
+      const long long x0 = first_item(cta, tot, p.n_cta), x1 = first_item(cta + 1, tot, p.n_cta);
+      ss.k0 = W;
+      long long acc = 0;
+      if (x0 < x1)
+        for (int w = 0; w < W; ++w) {
+          if (x0 < acc + ss.sum[w]) {
+            ss.k0 = w;
+            ss.k0_base = acc;
+            break;
+          }
+          acc += ss.sum[w];
+        }
+    }
+    __syncthreads();
+    if (warp == ss.k0) {  // find the sequence holding the first item
+      const long long x0 = first_item(cta, ss.tot, p.n_cta);
+      long long run = ss.k0_base;
+      for (int base = bb0; base < bb1; base += 32) {
+        const int b = base + lane;
+        const long long n = (b < bb1) ? (long long)p.Hkv * items_of(seq_len(b)) : 0;
+        long long incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long y = __shfl_up_sync(FULLMASK, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const long long excl = run + incl - n;
+        const unsigned hit = __ballot_sync(FULLMASK, n > 0 && x0 >= excl && x0 < excl + n);
+        if (hit) {
+          if (lane == __ffs(hit) - 1) {
+            ss.b0 = b;
+            ss.b0_start = excl;
+          }
+          break;
+        }
+        run += __shfl_sync(FULLMASK, incl, 31);
+      }
+    }
+    __syncthreads();
+  }
+  const long long tot = ss.tot;
+  const long long X0 = first_item(cta, tot, p.n_cta), X1 = first_item(cta + 1, tot, p.n_cta);
+  const int NL = (int)(X1 - X0);  // items of this CTA
 
   // Each ring entry has a K half (codes, scales, offsets) and a V half, each with its own
   // mbarrier, so that the next item's K half loads while this item's PV phase runs and
@@ -912,44 +983,51 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     }
   };
 
-  // This warp's items are local indices warp, warp + W, ... of the CTA range; the
-  // non-empty ones go through entries 0, 1, .., R-1, 0, ... of its ring in order.
-  // Cursors walk them without divisions: one per half issuing copies ahead, one consuming.
-  const int NL = (int)(X1 - X0);
-  const int n_pairs = p.B * p.Hkv;
+  // This warp's items are local indices warp, warp + W, ... of the CTA range; they go
+  // through entries 0, 1, .., R-1, 0, ... of its ring in order. Cursors walk them without
+  // divisions (pairs without tokens hold no items and are stepped over).
   struct Cursor {
-    int i, u, t, L;  // local item index, pair, item within the pair, valid tokens of the pair
-    int r, n;        // ring entry of the next copy or read, copies issued or items read
+    int i, u, t, L, n;  // local item index, pair, item within the pair, pair's tokens and items
+    int r;              // ring entry of the next copy or read
   };
-  auto pair_len = [&](int u) { return u < n_pairs ? min(max(__ldg(p.seq_lens + u / p.Hkv), 0), p.T_cap) : 0; };
-  auto cursor_start = [&]() {
-    Cursor k;
-    k.i = warp;
-    const long long x = X0 + warp;
-    k.u = (int)(x / p.ipu);
-    k.t = (int)(x - (long long)k.u * p.ipu);
-    k.L = pair_len(k.u);
-    k.r = 0;
-    k.n = 0;
-    return k;
+  auto set_pair = [&](Cursor& k) {
+    k.L = seq_len(k.u / p.Hkv);
+    k.n = items_of(k.L);
   };
-  auto cursor_next = [&](Cursor& k) {
-    k.i += C::WARPS;
-    k.t += C::WARPS;
-    if (k.t >= p.ipu) {
-      do {
-        k.t -= p.ipu;
+  auto advance = [&](Cursor& k, int step) {  // step items forward (only while inside the range)
+    k.i += step;
+    k.t += step;
+    if (k.i < NL) {
+      while (k.t >= k.n) {
+        k.t -= k.n;
         ++k.u;
-      } while (k.t >= p.ipu);
-      k.L = (k.i < NL) ? pair_len(k.u) : 0;
+        set_pair(k);
+      }
     }
   };
-  // The issue cursor stops at this warp's next non-empty item: issue_k() sends its K half,
+  Cursor start;  // the CTA's first item
+  start.i = 0;
+  start.r = 0;
+  if (NL > 0) {
+    const int L0 = seq_len(ss.b0), n0 = items_of(L0);
+    const long long off = X0 - ss.b0_start;
+    const int kv0 = (int)(off / n0);
+    start.u = ss.b0 * p.Hkv + kv0;
+    start.t = (int)(off - (long long)kv0 * n0);
+    start.L = L0;
+    start.n = n0;
+  } else {
+    start.u = n_pairs;
+    start.t = 0;
+    start.L = start.n = 0;
+  }
+  Cursor iss = start;
+  advance(iss, warp);
+  // The issue cursor points at this warp's next item: issue_k() sends its K half,
   // issue_v() its V half and moves on (the K half always goes first).
-  Cursor iss = cursor_start();
   bool k_pending = false;
+  int n_issued = 0;
   auto issue_k = [&]() {
-    while (iss.i < NL && iss.t * UNIT >= iss.L) cursor_next(iss);
     if (iss.i < NL) {
       if (lane == 0) copy_half(false, iss.u, iss.t, iss.r);
       k_pending = true;
@@ -959,9 +1037,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     if (!k_pending) return;
     if (lane == 0) copy_half(true, iss.u, iss.t, iss.r);
     k_pending = false;
-    ++iss.n;
+    ++n_issued;
     if (++iss.r == R) iss.r = 0;
-    cursor_next(iss);
+    advance(iss, W);
   };
   if (lane == 0) {
     for (int r = 0; r < R; ++r) {
@@ -977,15 +1055,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   }
 
   bool failed = false;
-  Cursor con = cursor_start();
-  int ph_con = 0, n_v_read = 0;
+  Cursor con = start;
+  advance(con, warp);
+  int ph_con = 0, n_k_read = 0, n_v_read = 0;
 
-  for (long long x = X0; x < X1;) {
-    // ---------------------------------------------------- segment: the items of pair u
-    const int u = (int)(x / p.ipu);
-    const long long xe = min(X1, (long long)(u + 1) * p.ipu);
+  // ---------------------------------------------------- segments: the CTA's items of one pair
+  long long x = X0;
+  int u = start.u;
+  long long pair_first = X0 - start.t;  // the pair's first item in the item sequence
+  int pair_n = start.n;
+  while (x < X1) {
+    const long long xe = min(X1, pair_first + pair_n);
     const int b = u / p.Hkv, kvh = u % p.Hkv;
-    const int L = min(max(__ldg(p.seq_lens + b), 0), p.T_cap);
 
     // Stage Q (fp32) and the per-query constants of pair u.
     __syncthreads();  // the previous segment's merge is done with sQ and the merge area
@@ -1096,14 +1177,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] = 0.f;
 
     // ---------------------------------------------------- this warp's items of the segment
-    for (; !failed && con.i < NL && con.u == u; cursor_next(con)) {
-      const int nv = min(UNIT, con.L - con.t * UNIT);  // valid tokens of the item
-      if (nv <= 0) continue;
+    for (; !failed && con.i < NL && con.u == u; advance(con, W)) {
+      const int nv = min(UNIT, con.L - con.t * UNIT);  // valid tokens of the item (>= 1)
       const int r = con.r;
       if (!mbar_wait(bar_k(r), ph_con, p.status, kStatusConsumerTimeout)) {
         failed = true;
         break;
       }
+      ++n_k_read;
       const uint8_t* en = ring_w + (size_t)r * C::E.bytes;
       SlotSmem sm;
       sm.kc = en;
@@ -1112,7 +1193,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       sm.kz = reinterpret_cast<const __half*>(en + C::E.off_kz);
       sm.vs = reinterpret_cast<const __half*>(en + C::E.off_vs);
       sm.vz = reinterpret_cast<const __half*>(en + C::E.off_vz);
-      ++con.n;
       auto mid = [&]() {
         __syncwarp();
         issue_k();  // the K half is read: refill it with the next item's K
@@ -1237,13 +1317,22 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     __syncthreads();
 
     // ---------------------------------------------------- merge the warps
-    // A pair held by this CTA alone (and without a window) is finished here; otherwise
-    // the CTA writes its partial to slot j of the pair and the last contributor to
-    // arrive merges all slots (and the window's) into the output.
-    const int c_first = cta_of((long long)u * p.ipu, p.tot_items, p.n_cta);
-    const int c_last = cta_of((long long)(u + 1) * p.ipu - 1, p.tot_items, p.n_cta);
-    const int n_contrib = c_last - c_first + 1;
-    const bool alone = (n_contrib == 1) && !p.has_win;
+    // A pair held by this CTA alone is finished here (with the window's partial). Otherwise the
+    // CTA writes its partial to its slot (1 when the pair is the second one it holds a
+    // partial of, else 0) and the last contributor to arrive merges all partials (and the
+    // window's) into the output.
+    const long long pair_last = pair_first + pair_n - 1;
+    const int c_first = cta_of(pair_first, tot, p.n_cta), c_last = cta_of(pair_last, tot, p.n_cta);
+    auto slot_of = [&](int cc) {
+      return (cc == c_first && first_item(cc, tot, p.n_cta) < pair_first) ? 1 : 0;
+    };
+    int n_contrib = c_last - c_first + 1;
+    if (tot < p.n_cta) {  // some CTAs hold no item: count only those that do
+      n_contrib = 0;
+      for (int cc = c_first; cc <= c_last; ++cc)
+        n_contrib += first_item(cc + 1, tot, p.n_cta) > first_item(cc, tot, p.n_cta);
+    }
+    const bool alone = (n_contrib == 1);
     for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS) {
       const int i = idx / D, ch = idx % D;
       float M = -INFINITY;
@@ -1260,9 +1349,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         }
       }
       if (alone) {
+        if (p.has_win) {  // merge the window's partial of the pair
+          const size_t wr = (size_t)u * hq + i;
+          const float2 wml = __ldcg(&p.win_ml[wr]);
+          const float Mw = fmaxf(M, wml.x);
+          if (Mw != -INFINITY) {
+            const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - Mw);
+            const float bw = (wml.x == -INFINITY) ? 0.f : fast_exp2(wml.x - Mw);
+            acc = a * acc + bw * __ldcg(&p.win_o[wr * D + ch]);
+            lt = a * lt + bw * wml.y;
+          }
+        }
         p.out[((size_t)b * p.Hq + kvh * hq + i) * D + ch] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
       } else {
-        const size_t prow = ((size_t)u * p.n_slots + (cta - c_first)) * hq + i;
+        const size_t prow = ((size_t)cta * 2 + slot_of(cta)) * hq + i;
         p.part_o[prow * D + ch] = acc;
         if (ch == 0) p.part_ml[prow] = make_float2(M, lt);
       }
@@ -1278,22 +1378,33 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       __syncthreads();
       if (s_last) {
         __threadfence();
-        // slots 0 .. n_contrib-1 hold the CTAs' partials, the last slot the window's
-        const int n_used = n_contrib + p.has_win;
-        auto slot_of = [&](int k) { return k < n_contrib ? k : p.n_slots - 1; };
-        // warp i: the maximum over the slots of query i, each slot's scale 2^(m_s - M)
+        // contributor k < n_span is CTA c_first + k (those without items are skipped); the
+        // window's partial comes last
+        const int n_span = c_last - c_first + 1;
+        const int n_used = n_span + p.has_win;
+        auto row_of = [&](int k, int i) -> long long {  // partial row, or -1 for a CTA without items
+          if (k == n_span) return (long long)u * hq + i;  // window
+          const int cc = c_first + k;
+          if (tot < p.n_cta && first_item(cc + 1, tot, p.n_cta) == first_item(cc, tot, p.n_cta)) return -1;
+          return ((long long)cc * 2 + slot_of(cc)) * hq + i;
+        };
+        auto ml_of = [&](int k, int i) -> float2 {
+          const long long r = row_of(k, i);
+          if (r < 0) return make_float2(-INFINITY, 0.f);
+          return __ldcg(k == n_span ? &p.win_ml[r] : &p.part_ml[r]);
+        };
+        // warp i: the maximum over the partials of query i, each partial's scale 2^(m_s - M)
         // (into the merge area, free again) and the merged denominator
-        float* s_sc = ma.o;                              // [n_used][hq]
-        float* s_l = ma.l;                               // [hq]
-        for (int i = warp; i < hq; i += C::WARPS) {
+        float* s_sc = ma.o;  // [n_used][hq]
+        float* s_l = ma.l;   // [hq]
+        for (int i = warp; i < hq; i += W) {
           float M = -INFINITY;
-          for (int k = lane; k < n_used; k += 32)
-            M = fmaxf(M, __ldcg(&p.part_ml[((size_t)u * p.n_slots + slot_of(k)) * hq + i].x));
+          for (int k = lane; k < n_used; k += 32) M = fmaxf(M, ml_of(k, i).x);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULLMASK, M, o));
           float lt = 0.f;
           for (int k = lane; k < n_used; k += 32) {
-            const float2 ml = __ldcg(&p.part_ml[((size_t)u * p.n_slots + slot_of(k)) * hq + i]);
+            const float2 ml = ml_of(k, i);
             const float sc = (M == -INFINITY || ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
             s_sc[k * hq + i] = sc;
             lt = fmaf(sc, ml.y, lt);
@@ -1308,8 +1419,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
           float acc = 0.f;
 #pragma unroll 4
           for (int k = 0; k < n_used; ++k) {
-            const size_t prow = ((size_t)u * p.n_slots + slot_of(k)) * hq + i;
-            acc = fmaf(s_sc[k * hq + i], __ldcg(&p.part_o[prow * D + ch]), acc);
+            const float sc = s_sc[k * hq + i];
+            if (sc == 0.f) continue;
+            const long long r = row_of(k, i);
+            acc = fmaf(sc, __ldcg(k == n_span ? &p.win_o[r * D + ch] : &p.part_o[r * D + ch]), acc);
           }
           const float l = s_l[i];
           p.out[((size_t)b * p.Hq + kvh * hq + i) * D + ch] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
@@ -1317,19 +1430,44 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         if (threadIdx.x == 0) p.done[u] = 0;  // ready for the next call in stream order
       }
     }
+
+    // next pair with tokens
     x = xe;
+    pair_first += pair_n;
+    if (x < X1) {
+      do {
+        ++u;
+        pair_n = items_of(seq_len(u / p.Hkv));
+      } while (pair_n == 0);
+    }
+  }
+
+  // ---------------------------------------------------- pairs without cached tokens
+  // Their output is the window's attention alone, or zero.
+  for (int bq = cta; bq < p.B; bq += p.n_cta) {
+    if (seq_len(bq) != 0) continue;
+    for (int idx = threadIdx.x; idx < p.Hkv * hq * D; idx += C::THREADS) {
+      const int kv = idx / (hq * D), i = (idx / D) % hq, ch = idx % D;
+      float o = 0.f;
+      if (p.has_win) {
+        const long long r = (long long)(bq * p.Hkv + kv) * hq + i;
+        const float2 ml = __ldcg(&p.win_ml[r]);
+        if (ml.y > 0.f) o = __ldcg(&p.win_o[r * D + ch]) / ml.y;
+      }
+      p.out[((size_t)bq * p.Hq + kv * hq + i) * D + ch] = __float2bfloat16_rn(o);
+    }
   }
 
   if (failed && lane == 0) {
     // every copy issued must have landed before shared memory is freed: wait (bounded)
     // for each outstanding half in issue order
     int rk = 0, pk = 0;
-    for (int k = 0; k < iss.n + (k_pending ? 1 : 0); ++k) {
-      if (k >= con.n && !mbar_wait(bar_k(rk), pk, p.status, kStatusDrainTimeout)) break;
+    for (int k = 0; k < n_issued + (k_pending ? 1 : 0); ++k) {
+      if (k >= n_k_read && !mbar_wait(bar_k(rk), pk, p.status, kStatusDrainTimeout)) break;
       if (++rk == R) { rk = 0; pk ^= 1; }
     }
     int rv = 0, pv = 0;
-    for (int k = 0; k < iss.n; ++k) {
+    for (int k = 0; k < n_issued; ++k) {
       if (k >= n_v_read && !mbar_wait(bar_v(rv), pv, p.status, kStatusDrainTimeout)) break;
       if (++rv == R) { rv = 0; pv ^= 1; }
     }

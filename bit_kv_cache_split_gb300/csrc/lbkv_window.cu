@@ -1,7 +1,7 @@
 // lbkv_window.cu -- attention of each (sequence, KV head) pair's queries over its
 // full-precision bf16 window (the most recent tokens, kept unquantized after the
-// cached ones), written as one partial (m, l, O) into the pair's last partial
-// slot; the decode kernel merges it with the cached tokens' partials.
+// cached ones), written as one partial (m, l, O) per pair; the decode kernel merges
+// it with the cached tokens' partials.
 #include "lbkv_internal.h"
 
 namespace lbkv {
@@ -85,9 +85,9 @@ __global__ void __launch_bounds__(32 * kWinWarps, 1) window_partial_kernel(const
         lt = fmaf(sc, sL[w][i], lt);
       }
     }
-    const size_t prow = ((size_t)u * p.n_slots + (p.n_slots - 1)) * hq + i;
-    p.part_o[prow * D + ch] = acc;
-    if (ch == 0) p.part_ml[prow] = make_float2(M, lt);
+    const size_t prow = (size_t)u * hq + i;
+    p.win_o[prow * D + ch] = acc;
+    if (ch == 0) p.win_ml[prow] = make_float2(M, lt);
   }
 }
 

@@ -72,9 +72,12 @@ def test_noalloc_rejects_scratch_beyond_the_array():
     from bit_kv_cache_split_gb300 import _binding
 
     lib = _binding.load()
-    # 4096 sequences x 64 query heads need far more than 16 MiB of split partials;
-    # the call is rejected before any pointer is touched or anything is launched.
+    # With a bf16 window, 4096 sequences x 64 query heads need one window partial per
+    # (sequence, KV head): far more than 16 MiB. The call is rejected before any pointer
+    # is touched (the window pointers below are never dereferenced) or anything launched.
     d = _binding.make_desc(4096, 64, 8, 1 << 20)
+    d.k_win = d.v_win = d.win_lens = 4096
+    d.win_cap = 128
     null = ctypes.c_void_p(0)
     st = lib.lbkv_decode_attn_noalloc(ctypes.byref(d), *([null] * 8), 2, 0, 0, 128, null, null)
     assert st == -7
