@@ -345,6 +345,23 @@ def run_sweep(device, peak):
     return rows
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time: every rank's timed region is one step of its own replica,
+    and the job is done when the last one is (weak scaling, one process per GPU)."""
+    if world <= 1:
+        return ms
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(step_bytes: int, ms: float, world: int) -> float:
+    """Whole-job GB/s: all ranks' algorithmic bytes over the slowest rank's time."""
+    return world * step_bytes / (ms * 1e-3) / 1e9
+
+
 def dist_info():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -443,12 +460,7 @@ def main():
     t_end = time.time()
     time.sleep(0.3)
     sampler.stop()
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, device)
     status = pkg.device_status(case.ws)
     footprint = case.footprint
     n_rep = len(case.replicas)
@@ -456,12 +468,13 @@ def main():
     torch.cuda.empty_cache()
 
     step_bytes = algorithmic_bytes(wl)
-    value = world * step_bytes / (ms * 1e-3) / 1e9
+    value = job_throughput(step_bytes, ms, world)
     achieved = step_bytes / (ms * 1e-3) / 1e9
     clocks = sampler.summary(t_pre, t_end)
 
     e2e_ms, h2d, d2h = time_e2e(wl, max(3, min(args.steps, 20)), 2, device)
-    e2e_val = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    e2e_val = job_throughput(step_bytes, e2e_ms, world)
 
     sweep = None
     if not args.no_sweep and rank == 0:
