@@ -57,7 +57,9 @@ constexpr int kMaxHq = 8;
 // shared-memory map: barriers | Q (fp32) and per-query constants | merge area | rings
 constexpr int kBarBytes = kMaxRing * 8;
 constexpr int kPrologueBytes = 8192;
-static_assert(kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq) <= kPrologueBytes, "prologue fits");
+// token-wise K: the B fragments of Q' shared by all warps, [k-step][lane] pairs of words
+constexpr int kQbOffset = kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq);
+static_assert(kQbOffset % 16 == 0 && kQbOffset + 8 * 32 * 8 <= kPrologueBytes, "prologue fits");
 // Per-lane register state a warp beyond the first kMergeWarps hands over (floats):
 // o_run (16 per live column, up to 2), zacc (up to 4), m and l (up to 2 each).
 constexpr int kStateFloats = 16 * 2 + 4 + 2 * 2;
@@ -237,7 +239,6 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t h2) {
 // Per-warp state, held in registers.
 template <class C>
 struct WarpState {
-  uint32_t qB[8][2];         // QK^T B fragments of this lane's column (token-wise K)
   float kbias[2][C::GK];     // token-wise K: -1024 * sum of Q' per group, accumulator columns 2c, 2c+1
   float pa[C::NQ];           // token-wise K: sigma log2(e) 2^-e (scores are kept in units of it); else 1
   float bzq[C::NQ][C::GK];   // token-wise K: 2^e * sum of Q over a channel group
@@ -324,6 +325,7 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
 // units of pa[j], channel-wise K in log2 units.
 template <class C>
 __device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpState<C>& st, const uint32_t (&qB)[8][2],
+                                         const uint2* sqb,
                                          const float (&cwA)[C::NQ], const float (&cwB)[C::NQ],
                                          const float (&cwneg)[2], const SlotSmem& sm, int rel0, const LaneCols& lc) {
   constexpr int BITS = C::BITS, KL = C::KL, GK = C::GK, RB = C::RB, NQ = C::NQ;
@@ -399,14 +401,21 @@ __device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpStat
         a2 = int4_half2(wA[blk], sA[blk], 2 * h + 1);
         a3 = int4_half2(wB[blk], sB[blk], 2 * h + 1);
       }
+      uint32_t q0, q1;  // B fragment of this k-step
+      if constexpr (KL == 0) {
+        const uint2 q = sqb[ks * 32 + lc.lane];
+        q0 = q.x, q1 = q.y;
+      } else {
+        q0 = qB[ks][0], q1 = qB[ks][1];
+      }
       if (KL == 0 ? (ks % C::KSG == 0) : (ks == 0)) {
         // a fresh accumulator per K channel group (token-wise K) or per token group
         // (channel-wise K), starting at minus the magic bias
         const float b0 = (KL == 0) ? st.kbias[0][ks / C::KSG] : cwneg[0];
         const float b1 = (KL == 0) ? st.kbias[1][ks / C::KSG] : cwneg[1];
-        mma_f16_c(acc, a0, a1, a2, a3, qB[ks][0], qB[ks][1], b0, b1, b0, b1);
+        mma_f16_c(acc, a0, a1, a2, a3, q0, q1, b0, b1, b0, b1);
       } else {
-        mma_f16(acc, a0, a1, a2, a3, qB[ks][0], qB[ks][1]);
+        mma_f16(acc, a0, a1, a2, a3, q0, q1);
       }
       if (KL == 0 && (ks + 1) % C::KSG == 0) {
         // acc-fold of one channel group: s * (raw partial) + z * 2^e sum(Q over the group)
@@ -584,7 +593,7 @@ __device__ __forceinline__ void fold_channelwise_v(WarpState<C>& st, const float
 // phases and returns false when the V half of the entry did not arrive.
 template <class C, bool FULL, class Mid>
 __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& sm, int nv, const float* sQ, float sl2,
-                                             const LaneCols& lc, Mid&& mid) {
+                                             const uint2* sqb, const LaneCols& lc, Mid&& mid) {
   constexpr int KL = C::KL, VL = C::VL, GV = C::GV, NQ = C::NQ, NO = C::NO, NTV = C::NTV;
   constexpr int NCH = C::NCH, D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
@@ -612,10 +621,7 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
       const int tau = rel0 / C::G;
       channelwise_q<C>(qBt, cwA, cwB, cwneg, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
     }
-    if constexpr (KL == 0)
-      qk_chunk<C>(x[ch], st, st.qB, cwA, cwB, cwneg, sm, rel0, lc);
-    else
-      qk_chunk<C>(x[ch], st, qBt, cwA, cwB, cwneg, sm, rel0, lc);
+    qk_chunk<C>(x[ch], st, qBt, sqb, cwA, cwB, cwneg, sm, rel0, lc);
     if (!FULL) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
@@ -880,6 +886,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   float* sAq = sQ + kMaxHq * D;                            // [kMaxHq] token-wise K score factor
   int* sEq = reinterpret_cast<int*>(sAq + kMaxHq);         // [kMaxHq] query exponent
   float* sBz = sAq + 2 * kMaxHq;                           // [kMaxHq][4] 2^e * sum of Q per channel group
+  uint2* sqb = reinterpret_cast<uint2*>(smem + kQbOffset);  // [8 k-steps][32 lanes] token-wise K
   MergeArea ma;
   ma.m = reinterpret_cast<float*>(smem + kPrologueBytes);
   ma.l = ma.m + kMergeWarps * kMaxHq;
@@ -1129,7 +1136,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
 #pragma unroll
       for (int uu = 0; uu < GK; ++uu) gsum[uu] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t qbw[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           float xx[2];
@@ -1138,9 +1146,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
             const int ch = qk_channel<C>(ks, 2 * c + 8 * r + e);
             xx[e] = live ? sQ[qb * D + ch] * sc * (1.f / k_mult<C>(ch)) : 0.f;
           }
-          st.qB[ks][r] = f16x2_from(xx[0], xx[1]);
+          qbw[r] = f16x2_from(xx[0], xx[1]);
           gsum[ks / C::KSG] += xx[0] + xx[1];
         }
+        // the fragments are the same in every warp: warp 0 publishes them
+        if (warp == 0) sqb[ks * 32 + lane] = make_uint2(qbw[0], qbw[1]);
+      }
 #pragma unroll
       for (int uu = 0; uu < GK; ++uu) {
         gsum[uu] += __shfl_xor_sync(FULLMASK, gsum[uu], 1);
@@ -1176,6 +1187,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
 #pragma unroll
         for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] = 0.f;
 
+    __syncthreads();  // the shared query fragments are in place
+
     // ---------------------------------------------------- this warp's items of the segment
     for (; !failed && con.i < NL && con.u == u; advance(con, W)) {
       const int nv = min(UNIT, con.L - con.t * UNIT);  // valid tokens of the item (>= 1)
@@ -1204,9 +1217,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         return true;
       };
       if (nv == UNIT)
-        process_unit<C, true>(st, sm, nv, sQ, p.sl2, lc, mid);
+        process_unit<C, true>(st, sm, nv, sQ, p.sl2, sqb, lc, mid);
       else
-        process_unit<C, false>(st, sm, nv, sQ, p.sl2, lc, mid);
+        process_unit<C, false>(st, sm, nv, sQ, p.sl2, sqb, lc, mid);
       if (failed) break;
       if (++con.r == R) {
         con.r = 0;
