@@ -95,7 +95,7 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   const EntryLayout el = entry_layout(bits, kl, vl, ut, group);
   pl->unit_tokens = ut;
   pl->entry_bytes = el.bytes;
-  const int warps = decode_warps(bits, pl->mode);
+  const int warps = decode_warps(bits, pl->mode, pl->gv);
   pl->threads = 32 * warps;
   pl->ring_off = kPrologueBytes + merge_bytes(hq, warps);
   const int budget = smem_optin - pl->ring_off;

@@ -78,9 +78,12 @@ constexpr int kModeWide = 2;  // 16 combos: combo k on column k % 8 of PV n-tile
 __host__ __device__ constexpr int decode_mode(int combos) {
   return combos <= 4 ? kModeDup : combos == 8 ? kModePair : combos == 16 ? kModeWide : -1;
 }
-// Warps per CTA: 16 (128 registers each) for up to 8 (query, V group) pairs per KV
-// head, 8 for 16 pairs (whose PV accumulators need more registers).
-__host__ __device__ constexpr int decode_warps(int bits, int mode) { return mode == kModeWide ? 8 : 16; }
+// Warps per CTA: 16 (128 registers each), or 8 where a lane's state needs more
+// registers: 16 pairs per KV head, or 8 pairs that are 8 different queries (two
+// query slots per lane).
+__host__ __device__ constexpr int decode_warps(int bits, int mode, int gv) {
+  return (mode == kModeWide || (mode == kModePair && gv == 1)) ? 8 : 16;
+}
 // 32-token chunks per item, such that one ring entry per warp fits in shared memory:
 // 128 tokens at INT2 (64 when group 32 makes the scales and offsets as large as a
 // quarter of the codes), 64 at INT4, 32 for 16 pairs.
@@ -149,7 +152,7 @@ struct Cfg {
   static constexpr int NO = DUP ? 1 : 2 * NTV;
   static constexpr int NCH = unit_chunks(BITS, MODE, LOG2G_);  // chunks per item
   static constexpr int UNIT = kChunk * NCH;             // tokens per item
-  static constexpr int WARPS = decode_warps(BITS, MODE);
+  static constexpr int WARPS = decode_warps(BITS, MODE, GV);
   static constexpr int THREADS = 32 * WARPS;
   static constexpr EntryLayout E = entry_layout(BITS, KL, VL, UNIT, G);
   static_assert(G >= kChunk, "a chunk never straddles a token group");
@@ -275,21 +278,41 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
   const int c = lc.c;
   const int qb = qk_query<C>(lc.g, lc.hq);  // this lane's B column is column g
   const bool live = qb >= 0;
+  static_assert(qk_wide<C>(), "channel-wise K uses the wide K mapping");
+  // With the wide mapping this lane's channels are 32c .. 32c+31: channel 32c + k is fed at
+  // k-step ks, k-slot 2c + 8r + e (k = 16x + 8e + p at INT2, 8x + 4e + p at INT4, with
+  // p = 2(ks mod (4 or 2)) + r and x the word). Read them four at a time.
   float x[8][2][2];
   float amax = 0.f, zsum = 0.f;
+  const float* qrow = sQ + (live ? qb : 0) * D + 32 * c;
+  const uint2* srow = reinterpret_cast<const uint2*>(s_tau + 32 * c);
+  const uint2* zrow = reinterpret_cast<const uint2*>(z_tau + 32 * c);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
+  for (int k4 = 0; k4 < 8; ++k4) {
+    const float4 q4 = reinterpret_cast<const float4*>(qrow)[k4];
+    const uint2 s4 = srow[k4], z4 = zrow[k4];
+    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+    const float2 s01 = half2_to_float2(s4.x), s23 = half2_to_float2(s4.y);
+    const float2 z01 = half2_to_float2(z4.x), z23 = half2_to_float2(z4.y);
+    const float sv[4] = {s01.x, s01.y, s23.x, s23.y}, zv[4] = {z01.x, z01.y, z23.x, z23.y};
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int ch = qk_channel<C>(ks, 2 * c + 8 * r + e);
-        const float qv = live ? sQ[qb * D + ch] : 0.f;
-        const float v = qv * __half2float(s_tau[ch]) * (1.f / k_mult<C>(ch));
-        x[ks][r][e] = v;
-        amax = fmaxf(amax, fabsf(v));
-        zsum = fmaf(qv, __half2float(z_tau[ch]), zsum);
+    for (int i = 0; i < 4; ++i) {
+      const int k = 4 * k4 + i;
+      int ks, r, e;
+      if (C::BITS == 2) {
+        const int p = k & 7;
+        ks = 4 * (k >> 4) + (p >> 1), r = p & 1, e = (k >> 3) & 1;
+      } else {
+        const int p = k & 3;
+        ks = 2 * (k >> 3) + (p >> 1), r = p & 1, e = (k >> 2) & 1;
       }
+      const float q = live ? qv[i] : 0.f;
+      const float v = q * sv[i] * (1.f / k_mult<C>(k));  // 32c + k has the factor of k
+      x[ks][r][e] = v;
+      amax = fmaxf(amax, fabsf(v));
+      zsum = fmaf(q, zv[i], zsum);
+    }
+  }
   amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
   zsum += __shfl_xor_sync(FULLMASK, zsum, 1);
@@ -617,9 +640,11 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
           for (int j = 0; j < NQ; ++j) x[ch][mt][row][j] = -INFINITY;
       continue;
     }
-    if (KL == 1 && (ch == 0 || (C::G <= C::UNIT && (kChunk * ch) % C::G == 0))) {
-      const int tau = rel0 / C::G;
-      channelwise_q<C>(qBt, cwA, cwB, cwneg, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
+    if constexpr (KL == 1) {
+      if (ch == 0 || (C::G <= C::UNIT && (kChunk * ch) % C::G == 0)) {
+        const int tau = rel0 / C::G;
+        channelwise_q<C>(qBt, cwA, cwB, cwneg, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
+      }
     }
     qk_chunk<C>(x[ch], st, qBt, sqb, cwA, cwB, cwneg, sm, rel0, lc);
     if (!FULL) {
