@@ -55,7 +55,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 struct Plan {
-  int hq, mode, gv, win;
+  int hq, hkv, kv_shift, mode, gv, win;
   int unit_tokens, n_cta;
   int ring_off, ring_per_warp, entry_bytes, smem_bytes, threads;
   size_t off_done, off_ml, off_o, off_wml, off_wo, ws_bytes;
@@ -77,13 +77,17 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   const bool win = d->k_win != nullptr;
   if (win != (d->v_win != nullptr) || win != (d->win_lens != nullptr)) return LBKV_EINVAL;
   if (win && (d->win_cap <= 0 || d->win_cap > 128)) return LBKV_EINVAL;
-  pl->hq = hq;
   // PV columns are (query, V channel group) pairs: a token-wise V side with G channel
   // groups feeds G separately scaled copies of the weights (operand-fold); the kernel
   // holds at most two PV n-tiles of 8 columns.
   const int groups_v = (vl == LBKV_TOKENWISE) ? kHeadDim / group : 1;
   pl->gv = groups_v;
-  pl->mode = decode_mode(hq * groups_v);
+  // 32 pairs (token-wise V with 4 groups, 8 queries per KV head): each KV head is split in
+  // two halves of its queries that read the same cached data (16 pairs each)
+  pl->kv_shift = (hq * groups_v > 16) ? 1 : 0;
+  pl->hq = hq >> pl->kv_shift;
+  pl->hkv = d->num_kv_heads << pl->kv_shift;
+  pl->mode = decode_mode(pl->hq * groups_v);
   if (pl->mode < 0) return LBKV_EUNSUPPORTED;
 
   int sms = 0, smem_optin = 0;
@@ -97,7 +101,7 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   pl->entry_bytes = el.bytes;
   const int warps = decode_warps(bits, pl->mode, pl->gv);
   pl->threads = 32 * warps;
-  pl->ring_off = kPrologueBytes + merge_bytes(hq, warps);
+  pl->ring_off = kPrologueBytes + merge_bytes(pl->hq, warps);
   const int budget = smem_optin - pl->ring_off;
   int r_w = budget / (warps * pl->entry_bytes);
   if (r_w > kMaxRing / (2 * warps)) r_w = kMaxRing / (2 * warps);  // two mbarriers per entry
@@ -107,13 +111,13 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
 
   // Persistent grid, one CTA per SM: the kernel splits the items of all pairs (from the
   // device lengths) evenly over the CTAs. A CTA holds partials of at most two pairs.
-  const long long units = (long long)d->batch * d->num_kv_heads;
+  const long long units = (long long)d->batch * pl->hkv;  // pairs
   pl->win = win ? 1 : 0;
   pl->n_cta = sms;
 
   // workspace: status word | per-pair counters | CTA partials (m, l) | CTA partials O |
   // window partials (m, l) | window partials O
-  const size_t rows = (size_t)pl->n_cta * 2 * hq, wrows = pl->win ? (size_t)units * hq : 0;
+  const size_t rows = (size_t)pl->n_cta * 2 * pl->hq, wrows = pl->win ? (size_t)units * pl->hq : 0;
   pl->off_done = 256;
   pl->off_ml = round_up(pl->off_done + (size_t)units * sizeof(int32_t), 256);
   pl->off_o = round_up(pl->off_ml + rows * sizeof(float2), 256);
@@ -184,8 +188,9 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.out = static_cast<__nv_bfloat16*>(out);
   p.B = desc->batch;
   p.Hq = desc->num_q_heads;
-  p.Hkv = desc->num_kv_heads;
+  p.Hkv = pl.hkv;
   p.hq = pl.hq;
+  p.kv_shift = pl.kv_shift;
   p.T_cap = desc->max_seq_len;
   p.win_cap = desc->k_win ? desc->win_cap : 0;
   const float sigma = desc->sm_scale > 0.f ? desc->sm_scale : 1.f / std::sqrt((float)desc->head_dim);

@@ -130,7 +130,10 @@ struct DecodeParams {
   int32_t* status;
   int32_t* done;    // [B*Hkv] CTAs finished with a pair; the last one merges and resets it to 0
   __nv_bfloat16* out;
-  int B, Hq, Hkv, hq, T_cap, win_cap;
+  // Hkv, hq: KV heads and queries per KV head as the kernel sees them. With kv_shift = 1
+  // every KV head is split into two halves of its queries (two "pairs" per KV head, each
+  // reading the same cached data): the cached KV head of pair u is u >> kv_shift.
+  int B, Hq, Hkv, hq, T_cap, win_cap, kv_shift;
   float sl2;  // softmax scale times log2(e)
   int n_cta, has_win;   // CTAs of the grid; whether a bf16 window is given
   int ring_off, ring_per_warp;  // shared-memory offset of the rings, entries per warp
@@ -991,7 +994,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   auto bar_v = [&](int r) { return bar_w + 16u * r + 8u; };
 
   // Bulk copies of the K or V half of item t of pair u into entry r (lane 0 only).
-  auto copy_half = [&](bool v_half, int u, int t, int r) {
+  auto copy_half = [&](bool v_half, int u_pair, int t, int r) {
+    const int u = u_pair >> p.kv_shift;  // cached KV head (sequence-major)
     const size_t t0 = (size_t)t * UNIT;
     const size_t row0 = (size_t)u * p.T_cap + t0;
     const size_t blocks = (size_t)p.T_cap / C::G;

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(32 * kWinWarps, 1) window_partial_kernel(const
     l[i] = 0.f;
     o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   }
-  const size_t wbase = (size_t)u * p.win_cap;
+  const size_t wbase = (size_t)(u >> p.kv_shift) * p.win_cap;  // the pair's cached KV head
   for (int t = warp; t < W; t += kWinWarps) {
     const uint2 kr = reinterpret_cast<const uint2*>(p.k_win + (wbase + t) * D)[lane];
     const uint2 vr = reinterpret_cast<const uint2*>(p.v_win + (wbase + t) * D)[lane];

@@ -111,8 +111,10 @@ LBKV_API size_t lbkv_workspace_bytes(const lbkv_desc* desc, int bits, int k_layo
  *   (a divisor of head_dim for a token-wise side, a token count for a
  *   channel-wise side).
  * Supported: every combination of bits, layouts and group above with
- *   Hq/Hkv in {1, 2, 4, 8}, except a token-wise V side with group 32 and
- *   Hq/Hkv = 8 (LBKV_EUNSUPPORTED).
+ *   Hq/Hkv in {1, 2, 4, 8} (other ratios, groups or head_dim give
+ *   LBKV_EUNSUPPORTED). For a token-wise V side with group 32 and Hq/Hkv = 8
+ *   the queries of each KV head are processed in two halves, each reading
+ *   the KV head's cached data (twice the cache traffic for that case).
  * Precision: tensor-core products on exact fp16 images of the codes; the bf16
  * query enters exactly (fp16; rounded to fp16 after a channel-wise K scale
  * multiplies it) and the softmax weights as fp16; accumulation and every fold

@@ -72,7 +72,6 @@ def _desc(**kw):
     (dict(T=1000), (2, 0, 0, 128), -1),        # T_cap not a multiple of 128
     (dict(T=0), (2, 0, 0, 128), -1),
     (dict(B=-1), (2, 0, 0, 128), -1),
-    (dict(Hq=64, Hkv=8), (2, 0, 0, 32), -3),   # token-wise V, 4 groups x 8 query heads
 ])
 def test_invalid_decode_arguments_rejected_before_launch(lib, kwargs, fmt, want):
     d = _desc(**kwargs)
@@ -82,7 +81,8 @@ def test_invalid_decode_arguments_rejected_before_launch(lib, kwargs, fmt, want)
     assert lib.lbkv_workspace_bytes(ctypes.byref(d), *fmt) == 0
 
 
-@pytest.mark.parametrize("hq,fmt", [(4, (2, 0, 0, 32)), (8, (2, 0, 0, 64)), (8, (4, 1, 0, 64)), (1, (4, 0, 0, 32))])
+@pytest.mark.parametrize("hq,fmt", [(4, (2, 0, 0, 32)), (8, (2, 0, 0, 64)), (8, (4, 1, 0, 64)), (1, (4, 0, 0, 32)),
+                                    (8, (2, 0, 0, 32)), (8, (4, 1, 0, 32))])
 def test_tokenwise_v_group_combinations_supported(lib, hq, fmt):
     """Up to 16 (query, value channel group) pairs per KV head are supported."""
     d = _desc(Hq=8 * hq, Hkv=8)

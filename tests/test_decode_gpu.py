@@ -143,14 +143,28 @@ def test_repeat_calls_are_bitwise_identical(lbkv):
 
 
 def test_unsupported_combination_raises(lbkv):
-    """Token-wise V with 4 channel groups and 8 query heads per KV head: 32 output
-    column pairs, more than the kernel's two n-tiles hold."""
-    wl = _wl(2, 0, 0, g=32, hq=8, lens=(10,))
+    """Groups of 16 channels are not built."""
+    wl = _wl(2, 0, 0, g=128, hq=4, lens=(10,))
     t = {k: v.cuda() for k, v in inputs.generate(wl, "cpu").items()}
     with pytest.raises(lbkv.LbkvError) as e:
         lbkv.decode_attn(t["q"], t["k_codes"], t["k_scale"], t["k_off"], t["v_codes"], t["v_scale"], t["v_off"],
-                         t["seq_lens"], bits=2, group=32)
+                         t["seq_lens"], bits=2, group=16)
     assert e.value.status == -3
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("kl", [0, 1])
+def test_tokenwise_v_four_groups_eight_queries(lbkv, bits, kl):
+    """32 (query, V group) pairs per KV head: the queries of a KV head are split in two halves."""
+    check(lbkv, _wl(bits, kl, 0, g=32, hq=8, lens=(700, 129, 0), seed=41 + bits + kl))
+
+
+def test_tokenwise_v_four_groups_eight_queries_window(lbkv):
+    wl = _wl(2, 0, 0, g=32, hq=8, lens=(300, 0), seed=43, window=64)
+    t = inputs.generate(wl, "cpu")
+    t["win_lens"] = torch.tensor([64, 5], dtype=torch.int32)
+    got = run_gpu(lbkv, t, wl)
+    assert_parity(got, oracle.decode_ref(to_oracle(t, wl)), "32 pairs + window")
 
 
 def test_no_device_status_after_calls(lbkv):
@@ -228,7 +242,7 @@ def test_mixed_layouts_ragged_sampled(lbkv, bits, kl, vl):
     sampled_parity(lbkv, wl, [(0, 0), (5, 4), (15, 7), (int(np.argmin(wl.lens)), 1)])
 
 
-@pytest.mark.parametrize("g,hq", [(128, 4), (64, 2), (128, 8), (32, 1)])
+@pytest.mark.parametrize("g,hq", [(128, 4), (64, 2), (128, 8), (32, 1), (32, 8)])
 def test_long_context_window_sampled(lbkv, g, hq):
     """100,000-token context: 99,872 INT2 tokens + a 128-token bf16 window."""
     wl = inputs.long_context(1, group=g, hq_per_kv=hq)
