@@ -1,6 +1,6 @@
-// lbkv_device.cuh -- sm_103a building blocks: mbarrier ring, bulk copies into
-// shared memory, the e4m3 tensor-core product and the bit tricks that turn
-// packed 2-/4-bit codes into e4m3 operands.
+// lbkv_device.cuh -- sm_103a building blocks: mbarriers with bounded waits, bulk
+// copies into shared memory, the fp16 tensor-core product and the bit tricks that
+// turn packed 2-/4-bit codes into exact fp16 operands.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -98,28 +98,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Named barrier among `count` threads (a multiple of 32).
-__device__ __forceinline__ void named_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // ------------------------------------------------------- tensor-core product
-// D[16x8] += A[16x32] * B[32x8], e4m3 inputs, fp32 accumulators.
-// Fragments (lane = 4*g + c): A reg0 row g k 4c..4c+3, reg1 row g+8 k 4c..4c+3,
-// reg2 row g k 16+4c.., reg3 row g+8 k 16+4c..; B reg0 k 4c..4c+3 col g,
-// reg1 k 16+4c.. col g; D d0,d1 row g cols 2c,2c+1; d2,d3 row g+8.
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // D[16x8] += A[16x16] * B[16x8], fp16 inputs, fp32 accumulators.
 // Fragments (lane = 4*g + c): A reg0 row g k 2c,2c+1; reg1 row g+8 k 2c,2c+1;
 // reg2 row g k 2c+8,2c+9; reg3 row g+8 k 2c+8,2c+9 (low half = lower k);
-// B reg0 k 2c,2c+1 col g; reg1 k 2c+8,2c+9 col g; D as for the e4m3 form.
+// B reg0 k 2c,2c+1 col g; reg1 k 2c+8,2c+9 col g; D d0,d1 row g cols 2c,2c+1,
+// d2,d3 row g+8 cols 2c,2c+1.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -160,76 +144,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
-}
-
-// Exact split of two non-negative-or-signed finite values x0, x1 (already
-// scaled into e4m3 range) into e4m3 pairs hi + lo: hi = e4m3(fp16(x)),
-// lo = e4m3(fp16(x) - hi); the subtraction is exact in fp16 because hi lies
-// within a factor of two of x (or is zero). Byte 0 holds x0, byte 1 x1.
-__device__ __forceinline__ void split_e4m3_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  uint32_t h2, back, res;
-  uint16_t h, l;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(x1), "f"(x0));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(h2));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(h));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(res) : "r"(h2), "r"(back));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(res));
-  hi = h;
-  lo = l;
-}
-
-// As split_e4m3_pair, and also returns the values actually fed, hi + lo, as
-// floats (exact: hi + lo has at most ten significant bits).
-__device__ __forceinline__ void split_e4m3_pair_fed(float x0, float x1, uint32_t& hi, uint32_t& lo, float& f0,
-                                                    float& f1) {
-  uint32_t h2, back, res, lback, fed;
-  uint16_t h, l;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(x1), "f"(x0));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(h2));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(h));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(res) : "r"(h2), "r"(back));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(res));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lback) : "h"(l));
-  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(fed) : "r"(back), "r"(lback));
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&fed));
-  hi = h;
-  lo = l;
-  f0 = f.x;
-  f1 = f.y;
-}
-
-// Three-part split x = hi + lo + lo2 (about twelve significant bits, the
-// precision of the fp16 value it starts from). Both subtractions are exact.
-__device__ __forceinline__ void split3_e4m3_pair(float x0, float x1, uint32_t& hi, uint32_t& lo, uint32_t& lo2) {
-  uint32_t h2, back, r1, back1, r2;
-  uint16_t h, l, l2;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(x1), "f"(x0));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(h2));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(h));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r1) : "r"(h2), "r"(back));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(r1));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back1) : "h"(l));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r2) : "r"(r1), "r"(back1));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l2) : "r"(r2));
-  hi = h;
-  lo = l;
-  lo2 = l2;
-}
-
-__device__ __forceinline__ float fast_rcp(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// 4x4 byte transpose: out[b] byte j = in[j] byte b.
-__device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t (&t)[4]) {
-  const uint32_t x0 = prmt(w0, w1, 0x5140), x1 = prmt(w0, w1, 0x7362);
-  const uint32_t y0 = prmt(w2, w3, 0x5140), y1 = prmt(w2, w3, 0x7362);
-  t[0] = prmt(x0, y0, 0x5410);
-  t[1] = prmt(x0, y0, 0x7632);
-  t[2] = prmt(x1, y1, 0x5410);
-  t[3] = prmt(x1, y1, 0x7632);
 }
 
 // 2^e for integer e in [-126, 127], exactly.
