@@ -24,7 +24,7 @@ STATUS = {0: "LBKV_OK", -1: "LBKV_EINVAL", -2: "LBKV_EALIGN", -3: "LBKV_EUNSUPPO
           -4: "LBKV_EWORKSPACE", -5: "LBKV_ECUDA", -6: "LBKV_EDEVICE", -7: "LBKV_ESCRATCH"}
 
 EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_device_status", "lbkv_strerror",
-           "lbkv_decode_attn_noalloc", "lbkv_noalloc_scratch_bytes")
+           "lbkv_decode_attn_noalloc", "lbkv_noalloc_scratch_bytes", "lbkv_selftest_wait_timeout")
 
 
 class LbkvError(RuntimeError):
@@ -69,6 +69,8 @@ def load(path: Optional[str] = None):
         L.lbkv_decode_attn.argtypes = [ctypes.POINTER(Desc)] + [vp] * 8 + [i32] * 4 + [vp, vp]
         L.lbkv_pack.restype = i32
         L.lbkv_pack.argtypes = [ctypes.POINTER(Desc), vp, vp, i32, i32, i32, vp, vp, vp, vp]
+        L.lbkv_selftest_wait_timeout.restype = i32
+        L.lbkv_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
         L.lbkv_device_status.restype = i32
         L.lbkv_device_status.argtypes = [ctypes.POINTER(Desc), vp, ctypes.POINTER(ctypes.c_int32)]
         L.lbkv_decode_attn_noalloc.restype = i32
@@ -202,6 +204,17 @@ def pack(x, seq_lens, *, bits, layout=TOKENWISE, group=128, codes=None, scale=No
     if st != 0:
         raise LbkvError(st, "lbkv_pack")
     return codes, scale, off
+
+
+def selftest_wait_timeout(limit_ns: int, device="cuda") -> tuple:
+    """Run the bounded-wait self-test (lbkv_selftest_wait_timeout) and return the two
+    status words (the recorded code, and how many warps went on past the failed wait)."""
+    s = torch.zeros(4, dtype=torch.int32, device=device)
+    st = load().lbkv_selftest_wait_timeout(s.data_ptr(), int(limit_ns), _stream_ptr(None))
+    if st != 0:
+        raise LbkvError(st, "lbkv_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    return int(s[0].item()), int(s[1].item())
 
 
 def device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -54,24 +54,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Slow path of a bounded wait: polls until the phase completes or about one
-// second of wall time has passed; then records `code` and returns false.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int32_t* status, int32_t code) {
+// Slow path of a bounded wait: polls until the phase completes or `limit_ns` of wall
+// time has passed; then records `code` in the status word and returns false.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int32_t* status, int32_t code,
+                                                   uint64_t limit_ns) {
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicExch(status, code);
       return false;
     }
   }
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status, int32_t code) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status, int32_t code,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, status, code);
+  return mbar_wait_slow(bar, parity, status, code, limit_ns);
 }
 
 // Bulk (non-tensor) copy global -> shared, completing on an mbarrier.

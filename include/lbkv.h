@@ -170,6 +170,16 @@ LBKV_API size_t lbkv_noalloc_scratch_bytes(void);
  * not NULL) or LBKV_ECUDA / LBKV_EINVAL / LBKV_EWORKSPACE. */
 LBKV_API int lbkv_device_status(const lbkv_desc* desc, lbkv_stream_t stream, int32_t* code);
 
+/* Self-test of the bounded waits every kernel uses instead of spinning forever:
+ * launches one warp that waits on an mbarrier nothing completes. The wait gives up
+ * after limit_ns nanoseconds (0 < limit_ns <= 1e9), writes 1 (a consumer wait ran
+ * out, the code the decode kernel uses) to status[0], and the warp then adds 1 to
+ * status[1] and exits. status: device int32[2], 16-byte aligned, zeroed by the
+ * caller. Asynchronous on `stream`. Returns LBKV_OK, LBKV_EINVAL, LBKV_EALIGN or
+ * LBKV_ECUDA. (Not part of the method: a check that a failed wait reports instead
+ * of hanging and leaves the context usable.) */
+LBKV_API int lbkv_selftest_wait_timeout(void* status, uint64_t limit_ns, lbkv_stream_t stream);
+
 /* Static English text for a status value. */
 LBKV_API const char* lbkv_strerror(int status);
 

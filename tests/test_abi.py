@@ -124,3 +124,9 @@ def test_empty_batch_is_a_no_op_without_pointers(lib):
     null = ctypes.c_void_p(0)
     assert lib.lbkv_decode_attn(ctypes.byref(d), *([null] * 8), 2, 0, 0, 128, null, null) in (0, -5)
     assert lib.lbkv_pack(ctypes.byref(d), null, null, 2, 0, 128, null, null, null, null) == 0
+
+
+@pytest.mark.parametrize("status,limit,want", [(0, 1000, -1), (4096, 0, -1), (4096, 2_000_000_000, -1), (4100, 1000, -2)])
+def test_selftest_arguments_rejected_before_launch(lib, status, limit, want):
+    assert lib.lbkv_selftest_wait_timeout(ctypes.c_void_p(status), ctypes.c_uint64(limit), ctypes.c_void_p(0)) == want
+

@@ -6,6 +6,8 @@ ragged lengths that span several 128-token slots and end mid-slot, GQA 1..8,
 groups 32/64/128, a bf16 window, empty sequences and peaked softmaxes; at
 the full benchmark sizes on sampled (sequence, KV head) units."""
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -247,3 +249,14 @@ def test_long_context_window_sampled(lbkv, g, hq):
     """100,000-token context: 99,872 INT2 tokens + a 128-token bf16 window."""
     wl = inputs.long_context(1, group=g, hq_per_kv=hq)
     sampled_parity(lbkv, wl, [(0, 0), (0, wl.num_kv_heads - 1)])
+
+
+def test_bounded_wait_reports_and_the_context_survives(lbkv):
+    """A wait that nothing completes gives up after its limit, records the timeout code in
+    the status word and lets the warp go on; the context then still decodes correctly."""
+    t0 = time.perf_counter()
+    code, went_on = lbkv._binding.selftest_wait_timeout(20_000_000)  # 20 ms
+    assert (code, went_on) == (1, 1)
+    assert time.perf_counter() - t0 < 5.0
+    check(lbkv, inputs.tiny_int2())
+
