@@ -86,9 +86,9 @@ __host__ __device__ constexpr int decode_warps(int bits, int mode, int gv) {
 }
 // 32-token chunks per item, such that one ring entry per warp fits in shared memory:
 // 128 tokens at INT2 (64 when group 32 makes the scales and offsets as large as a
-// quarter of the codes), 64 at INT4, 32 for 16 pairs.
+// quarter of the codes), 64 at INT4 and for 16 pairs.
 __host__ __device__ constexpr int unit_chunks(int bits, int mode, int log2g) {
-  return mode == kModeWide ? 1 : bits == 2 ? (log2g == 5 ? 2 : 4) : 2;
+  return mode == kModeWide ? 2 : bits == 2 ? (log2g == 5 ? 2 : 4) : 2;
 }
 
 // Byte layout of one ring entry (one item of `unit` tokens of one pair):
