@@ -59,7 +59,11 @@ constexpr int kBarBytes = kMaxRing * 8;
 constexpr int kPrologueBytes = 8192;
 // token-wise K: the B fragments of Q' shared by all warps, [k-step][lane] pairs of words
 constexpr int kQbOffset = kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq);
-static_assert(kQbOffset % 16 == 0 && kQbOffset + 8 * 32 * 8 <= kPrologueBytes, "prologue fits");
+// token-wise K: per k-step and lane the sum of its four Q' values, and minus the magic
+// bias per accumulator column and channel group
+constexpr int kPartOffset = kQbOffset + 8 * 32 * 8;
+constexpr int kKbOffset = kPartOffset + 4 * 8 * 32;
+static_assert(kQbOffset % 16 == 0 && kKbOffset + 4 * 8 * 4 <= kPrologueBytes, "prologue fits");
 // Per-lane register state a warp beyond the first kMergeWarps hands over (floats):
 // o_run (16 per live column, up to 2), zacc (up to 4), m and l (up to 2 each).
 constexpr int kStateFloats = 16 * 2 + 4 + 2 * 2;
@@ -217,6 +221,16 @@ __device__ __forceinline__ float k_mult(int ch) {
   }
   return (float)(1 << (2 * (ch & 3)));
 }
+// Its exact reciprocal (a power of two formed directly, no division).
+template <class C>
+__device__ __forceinline__ float k_rmult(int ch) {
+  if (C::BITS == 4) return (ch & 1) ? 0.0625f : 1.f;
+  if (qk_wide<C>()) {
+    const int p = ch & 7;
+    return exp2i(-2 * (p <= 4 ? p : p - 5));
+  }
+  return exp2i(-2 * (ch & 3));
+}
 // Position factor of V m-tile mt (both of its rows).
 template <int BITS>
 __host__ __device__ constexpr float v_mult(int mt) {
@@ -310,7 +324,7 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
         ks = 2 * (k >> 3) + (p >> 1), r = p & 1, e = (k >> 2) & 1;
       }
       const float q = live ? qv[i] : 0.f;
-      const float v = q * sv[i] * (1.f / k_mult<C>(k));  // 32c + k has the factor of k
+      const float v = q * sv[i] * k_rmult<C>(k);  // 32c + k has the factor of k
       x[ks][r][e] = v;
       amax = fmaxf(amax, fabsf(v));
       zsum = fmaf(q, zv[i], zsum);
@@ -915,6 +929,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   int* sEq = reinterpret_cast<int*>(sAq + kMaxHq);         // [kMaxHq] query exponent
   float* sBz = sAq + 2 * kMaxHq;                           // [kMaxHq][4] 2^e * sum of Q per channel group
   uint2* sqb = reinterpret_cast<uint2*>(smem + kQbOffset);  // [8 k-steps][32 lanes] token-wise K
+  float* sPart = reinterpret_cast<float*>(smem + kPartOffset);  // [8 k-steps][32 lanes]
+  float* sKb = reinterpret_cast<float*>(smem + kKbOffset);      // [8 columns][4 channel groups]
   MergeArea ma;
   ma.m = reinterpret_cast<float*>(smem + kPrologueBytes);
   ma.l = ma.m + kMergeWarps * kMaxHq;
@@ -1119,7 +1135,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       for (int uu = 0; uu < 4; ++uu) {
         const int ch = 4 * lane + uu;
         const float v = sQ[i * D + ch];
-        amax = fmaxf(amax, fabsf(v) * (1.f / k_mult<C>(ch)));
+        amax = fmaxf(amax, fabsf(v) * k_rmult<C>(ch));
         gs += v;
       }
 #pragma unroll
@@ -1155,42 +1171,45 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
 
     WarpState<C> st;
     if (KL == 0) {
-      // token-wise K: B fragments Q' = Q 2^e / factor (exact fp16) of this lane's column
-      // (column g), fixed for the pair, and minus the magic bias 1024 * sum of Q' per
-      // channel group of accumulator columns 2c and 2c+1
-      const int qb = qk_query<C>(g, hq);
-      const bool live = qb >= 0;
-      const float sc = live ? exp2i(sEq[qb]) : 0.f;
-      float gsum[GK];
-#pragma unroll
-      for (int uu = 0; uu < GK; ++uu) gsum[uu] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
+      // token-wise K: B fragments Q' = Q 2^e / factor (exact fp16) of column g, the same for
+      // every warp, formed once: warp ks < 8 the k-step ks; then minus the magic bias 1024 *
+      // sum of Q' per channel group of each column
+      if (warp < 8) {
+        const int ks = warp;
+        const int qb = qk_query<C>(g, hq);
+        const bool live = qb >= 0;
+        const float sc = live ? exp2i(sEq[qb]) : 0.f;
         uint32_t qbw[2];
+        float part = 0.f;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           float xx[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int ch = qk_channel<C>(ks, 2 * c + 8 * r + e);
-            xx[e] = live ? sQ[qb * D + ch] * sc * (1.f / k_mult<C>(ch)) : 0.f;
+            xx[e] = live ? sQ[qb * D + ch] * sc * k_rmult<C>(ch) : 0.f;
           }
           qbw[r] = f16x2_from(xx[0], xx[1]);
-          gsum[ks / C::KSG] += xx[0] + xx[1];
+          part += xx[0] + xx[1];
         }
-        // the fragments are the same in every warp: warp 0 publishes them
-        if (warp == 0) sqb[ks * 32 + lane] = make_uint2(qbw[0], qbw[1]);
+        sqb[ks * 32 + lane] = make_uint2(qbw[0], qbw[1]);
+        sPart[ks * 32 + lane] = part;
       }
+      __syncthreads();
+      if (threadIdx.x < 32) {  // thread 4 col + uu: column col, channel group uu
+        const int col = lane >> 2, uu = lane & 3;
+        float sum = 0.f;
+        if (uu < GK)
+          for (int ks = uu * C::KSG; ks < (uu + 1) * C::KSG; ++ks)
 #pragma unroll
-      for (int uu = 0; uu < GK; ++uu) {
-        gsum[uu] += __shfl_xor_sync(FULLMASK, gsum[uu], 1);
-        gsum[uu] += __shfl_xor_sync(FULLMASK, gsum[uu], 2);
+            for (int cc = 0; cc < 4; ++cc) sum += sPart[ks * 32 + 4 * col + cc];
+        sKb[lane] = -kMagicF * sum;
       }
+      __syncthreads();
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-        for (int uu = 0; uu < GK; ++uu)
-          st.kbias[jj][uu] = -kMagicF * __shfl_sync(FULLMASK, gsum[uu], 8 * c + 4 * jj);
+        for (int uu = 0; uu < GK; ++uu) st.kbias[jj][uu] = sKb[(2 * c + jj) * 4 + uu];
 #pragma unroll
       for (int j = 0; j < NQ; ++j) {
         const int qs = qk_query<C>(2 * c + j, hq);
