@@ -75,9 +75,13 @@ def measured_hbm_peak():
 
 
 def source_hash() -> str:
+    """Hash of the sources the decode kernel is built from (its traffic does not depend on
+    the pack or append kernels)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_kv_cache_split_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
+        if not (f.startswith("lbkv_decode") or f in ("lbkv_device.cuh", "lbkv_api.cu")):
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -345,6 +349,86 @@ def run_sweep(device, peak):
     return rows
 
 
+def append_bytes(B, Hkv, bits, group, k_layout, v_layout) -> float:
+    """Algorithmic bytes of one lbkv_append call, a group's flush spread over its calls.
+
+    Token-wise sides: the new K/V read, its codes and scales/offsets written, the lengths
+    read and written. With a channel-wise side: the token written to the window; every
+    `group`-th call reads the window's group of tokens and writes its codes and scales."""
+    D = 128
+    new = B * Hkv * 2 * D * 2
+    codes = B * Hkv * 2 * D * bits // 8
+    if k_layout == 0 and v_layout == 0:
+        return new + codes + B * Hkv * 2 * (D // group) * 2 * 2 + B * 4 * 2
+    sz = 0
+    for layout in (k_layout, v_layout):
+        sz += B * Hkv * (group * (D // group) * 2 * 2 if layout == 0 else D * 2 * 2)  # per group of tokens
+    flush = B * Hkv * 2 * group * D * 2 + group * codes + sz
+    return new + new + flush / group + B * 4 * 4  # read + window write, flush share, both lengths
+
+
+def time_append(device, peak, calls=256):
+    """µs per lbkv_append call (one new token for every sequence and KV head), B = 32,
+    8 KV heads: a CUDA graph of `calls` appends, replayed once untimed and once timed."""
+    import bit_kv_cache_split_gb300 as pkg
+
+    rows = []
+    for bits, kl, vl in ((2, 0, 0), (4, 0, 0), (2, 1, 0)):
+        B, Hkv, g, D = 32, 8, 128, 128
+        T = 2 * calls
+        tag = {(0, 0): "tokenwise", (1, 0): "cwK-twV"}[(kl, vl)]
+        name = f"append-int{bits}-{tag}-b{B}-kv{Hkv}"
+        gen = torch.Generator(device=device).manual_seed(7)
+        k_new = torch.randn((B, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+        v_new = torch.randn((B, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+        sides = []
+        for layout in (kl, vl):
+            sshape = (B, Hkv, T, D // g) if layout == 0 else (B, Hkv, T // g, D)
+            sides.append((torch.zeros((B, Hkv, T, D * bits // 8), dtype=torch.uint8, device=device),
+                          torch.zeros(sshape, dtype=torch.float16, device=device),
+                          torch.zeros(sshape, dtype=torch.float16, device=device)))
+        lens = torch.zeros((B,), dtype=torch.int32, device=device)
+        kw = {}
+        if kl or vl:
+            kw = dict(k_win=torch.zeros((B, Hkv, 128, D), dtype=torch.bfloat16, device=device),
+                      v_win=torch.zeros((B, Hkv, 128, D), dtype=torch.bfloat16, device=device),
+                      win_lens=torch.zeros((B,), dtype=torch.int32, device=device))
+        ws = torch.zeros(64, dtype=torch.int32, device=device)
+
+        def one():
+            pkg.append(k_new, v_new, lens, *sides[0], *sides[1], bits=bits, k_layout=kl, v_layout=vl, group=g,
+                       workspace=ws, **kw)
+
+        one()  # loads the kernel before capture
+        torch.cuda.synchronize()
+        lens.zero_()
+        if kw:
+            kw["win_lens"].zero_()
+        side = torch.cuda.Stream(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(calls):
+                    one()
+        torch.cuda.synchronize()
+        graph.replay()  # untimed
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / calls
+        ok = int(lens[0].item()) == 2 * calls and pkg.device_status(ws) == 0
+        nbytes = append_bytes(B, Hkv, bits, g, kl, vl)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        rows.append({"workload": name, "us_per_call": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "bytes": int(nbytes), "lengths_ok": ok})
+        del graph
+        torch.cuda.empty_cache()
+    return rows
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: every rank's timed region is one step of its own replica,
     and the job is done when the last one is (weak scaling, one process per GPU)."""
@@ -476,9 +560,10 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     e2e_val = job_throughput(step_bytes, e2e_ms, world)
 
-    sweep = None
+    sweep = append = None
     if not args.no_sweep and rank == 0:
         sweep = run_sweep(device, peak)
+        append = time_append(device, peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -509,6 +594,7 @@ def main():
             "device_status": status,
             "cpu_baseline": cpu,
             "sweep": sweep,
+            "append": append,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -23,8 +23,8 @@ CHANNELWISE = 1
 STATUS = {0: "LBKV_OK", -1: "LBKV_EINVAL", -2: "LBKV_EALIGN", -3: "LBKV_EUNSUPPORTED",
           -4: "LBKV_EWORKSPACE", -5: "LBKV_ECUDA", -6: "LBKV_EDEVICE", -7: "LBKV_ESCRATCH"}
 
-EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_device_status", "lbkv_strerror",
-           "lbkv_decode_attn_noalloc", "lbkv_noalloc_scratch_bytes", "lbkv_selftest_wait_timeout")
+EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_append", "lbkv_device_status",
+           "lbkv_strerror", "lbkv_decode_attn_noalloc", "lbkv_noalloc_scratch_bytes", "lbkv_selftest_wait_timeout")
 
 
 class LbkvError(RuntimeError):
@@ -69,6 +69,8 @@ def load(path: Optional[str] = None):
         L.lbkv_decode_attn.argtypes = [ctypes.POINTER(Desc)] + [vp] * 8 + [i32] * 4 + [vp, vp]
         L.lbkv_pack.restype = i32
         L.lbkv_pack.argtypes = [ctypes.POINTER(Desc), vp, vp, i32, i32, i32, vp, vp, vp, vp]
+        L.lbkv_append.restype = i32
+        L.lbkv_append.argtypes = [ctypes.POINTER(Desc), vp, vp, vp] + [i32] * 4 + [vp] * 7
         L.lbkv_selftest_wait_timeout.restype = i32
         L.lbkv_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
         L.lbkv_device_status.restype = i32
@@ -204,6 +206,32 @@ def pack(x, seq_lens, *, bits, layout=TOKENWISE, group=128, codes=None, scale=No
     if st != 0:
         raise LbkvError(st, "lbkv_pack")
     return codes, scale, off
+
+
+def append(k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_off, *, bits, k_layout=TOKENWISE,
+           v_layout=TOKENWISE, group=128, k_win=None, v_win=None, win_lens=None, workspace=None, stream=None):
+    """Append the new token k_new/v_new bf16 [B][Hkv][D] through lbkv_append (quantize-on-append).
+
+    The cache tensors, seq_lens (and win_lens with the window) are updated in place."""
+    _check(k_new, "k_new", torch.bfloat16)
+    B, Hkv, D = k_new.shape
+    _check(v_new, "v_new", torch.bfloat16, (B, Hkv, D))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    T = k_codes.shape[2]
+    for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
+        _check(t, name, torch.uint8, (B, Hkv, T, D * bits // 8))
+    for name, t in (("k_scale", k_scale), ("k_off", k_off), ("v_scale", v_scale), ("v_off", v_off)):
+        _check(t, name, torch.float16)
+    if k_win is not None:
+        _check(k_win, "k_win", torch.bfloat16)
+        _check(v_win, "v_win", torch.bfloat16, tuple(k_win.shape))
+        _check(win_lens, "win_lens", torch.int32, (B,))
+    d = make_desc(B, Hkv, Hkv, T, D, k_win=k_win, v_win=v_win, win_lens=win_lens, workspace=workspace)
+    st = load().lbkv_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _ptr(seq_lens), int(bits), int(k_layout),
+                            int(v_layout), int(group), _ptr(k_codes), _ptr(k_scale), _ptr(k_off), _ptr(v_codes),
+                            _ptr(v_scale), _ptr(v_off), _stream_ptr(stream))
+    if st != 0:
+        raise LbkvError(st, "lbkv_append")
 
 
 def selftest_wait_timeout(limit_ns: int, device="cuda") -> tuple:

@@ -229,6 +229,57 @@ int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_lens, int
   return LBKV_OK;
 }
 
+int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int32_t* seq_lens, int bits,
+                int k_layout, int v_layout, int group, uint8_t* k_codes, void* k_scale, void* k_off,
+                uint8_t* v_codes, void* v_scale, void* v_off, lbkv_stream_t stream) {
+  if (!desc) return LBKV_EINVAL;
+  if (desc->batch < 0 || desc->num_kv_heads <= 0) return LBKV_EINVAL;
+  if (desc->head_dim != kHeadDim) return LBKV_EUNSUPPORTED;
+  if (desc->max_seq_len <= 0 || desc->max_seq_len % kSlotTokens) return LBKV_EINVAL;
+  if (bits != 2 && bits != 4) return LBKV_EINVAL;
+  if ((k_layout != LBKV_TOKENWISE && k_layout != LBKV_CHANNELWISE) ||
+      (v_layout != LBKV_TOKENWISE && v_layout != LBKV_CHANNELWISE))
+    return LBKV_EINVAL;
+  if (group != 32 && group != 64 && group != 128) return LBKV_EUNSUPPORTED;
+  const bool windowed = k_layout == LBKV_CHANNELWISE || v_layout == LBKV_CHANNELWISE;
+  const bool win = desc->k_win != nullptr;
+  if (win != (desc->v_win != nullptr) || win != (desc->win_lens != nullptr)) return LBKV_EINVAL;
+  if (windowed && (!win || desc->win_cap < group || desc->win_cap > 128)) return LBKV_EINVAL;
+  if (desc->batch == 0) return LBKV_OK;
+  const void* ptrs[] = {k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_off};
+  for (const void* p : ptrs)
+    if (!p) return LBKV_EINVAL;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LBKV_EALIGN;
+  if (windowed && (!aligned16(desc->k_win) || !aligned16(desc->v_win) || !aligned16(desc->win_lens)))
+    return LBKV_EALIGN;
+  if (desc->workspace && (reinterpret_cast<uintptr_t>(desc->workspace) & 255u)) return LBKV_EALIGN;
+  AppendArgs a{};
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.seq_lens = seq_lens;
+  a.k_win = windowed ? static_cast<__nv_bfloat16*>(const_cast<void*>(desc->k_win)) : nullptr;
+  a.v_win = windowed ? static_cast<__nv_bfloat16*>(const_cast<void*>(desc->v_win)) : nullptr;
+  a.win_lens = windowed ? const_cast<int32_t*>(desc->win_lens) : nullptr;
+  a.status = desc->workspace ? static_cast<int32_t*>(desc->workspace) : nullptr;
+  a.B = desc->batch;
+  a.Hkv = desc->num_kv_heads;
+  a.T_cap = desc->max_seq_len;
+  a.win_cap = windowed ? desc->win_cap : 0;
+  a.bits = bits;
+  a.k_layout = k_layout;
+  a.v_layout = v_layout;
+  a.group = group;
+  a.k_codes = k_codes;
+  a.k_scale = static_cast<__half*>(k_scale);
+  a.k_off = static_cast<__half*>(k_off);
+  a.v_codes = v_codes;
+  a.v_scale = static_cast<__half*>(v_scale);
+  a.v_off = static_cast<__half*>(v_off);
+  if (launch_append(a, reinterpret_cast<cudaStream_t>(stream)) != 0) return LBKV_ECUDA;
+  return LBKV_OK;
+}
+
 int lbkv_device_status(const lbkv_desc* desc, lbkv_stream_t stream, int32_t* code) {
   if (!desc) return LBKV_EINVAL;
   if (!desc->workspace || desc->workspace_bytes < 256) return LBKV_EWORKSPACE;
@@ -254,7 +305,7 @@ const char* lbkv_strerror(int status) {
     case LBKV_EUNSUPPORTED: return "valid but unsupported combination of shape and format";
     case LBKV_EWORKSPACE: return "workspace missing or smaller than lbkv_workspace_bytes";
     case LBKV_ECUDA: return "CUDA launch or runtime error";
-    case LBKV_EDEVICE: return "a kernel reported a device-side error (bounded wait ran out)";
+    case LBKV_EDEVICE: return "a kernel reported a device-side error (a bounded wait ran out, or an appended token did not fit)";
     case LBKV_ESCRATCH: return "the call needs more scratch than the fixed no-allocation array holds";
     default: return "unknown status";
   }

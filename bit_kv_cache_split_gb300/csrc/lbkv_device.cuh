@@ -14,6 +14,7 @@ namespace lbkv {
 enum : int32_t {
   kStatusConsumerTimeout = 1,  // a warp waited ~1 s for its own bulk copies
   kStatusDrainTimeout = 3,     // after that, the copies still in flight did not land
+  kStatusAppendFull = 4,       // an appended token did not fit (capacity or window state)
 };
 
 // A bounded wait gives up after this many nanoseconds of wall time.

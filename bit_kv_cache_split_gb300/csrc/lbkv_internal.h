@@ -17,6 +17,25 @@ struct PackArgs {
 
 int launch_pack(const PackArgs& a, cudaStream_t stream);
 
+struct AppendArgs {
+  const __nv_bfloat16* k_new;  // [B][Hkv][D]
+  const __nv_bfloat16* v_new;
+  int32_t* seq_lens;           // [B], advanced in place
+  __nv_bfloat16* k_win;        // [B][Hkv][win_cap][D] (channel-wise sides only)
+  __nv_bfloat16* v_win;
+  int32_t* win_lens;           // [B], advanced / reset in place
+  int32_t* status;             // status word, or nullptr
+  int B, Hkv, T_cap, win_cap, bits, k_layout, v_layout, group;
+  uint8_t* k_codes;
+  __half* k_scale;
+  __half* k_off;
+  uint8_t* v_codes;
+  __half* v_scale;
+  __half* v_off;
+};
+
+int launch_append(const AppendArgs& a, cudaStream_t stream);
+
 using DecodeKernel = void (*)(const DecodeParams);
 
 // Window partials (one per sequence and KV head) into the last partial slot of each

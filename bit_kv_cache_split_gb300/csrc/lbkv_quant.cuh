@@ -1,0 +1,99 @@
+// lbkv_quant.cuh -- the quantizer of one token row (token-wise groups) and of one
+// channel over a token group (channel-wise groups), shared by the pack and append
+// kernels so that both produce the same bits.
+//
+// Value model s * q + z with unsigned b-bit codes: explainer "FOSCAR speeds up
+// 2-bit KV decode -- Affine folding of KV dequantization", quantization-format
+// paragraph. The quantizer (min/max per group, round-half-even) is this
+// library's reading; every step is one IEEE single-precision operation rounded
+// on its own (no contraction), so the result is bit-exact:
+//   s = fp16((max - min) / (2^b - 1)),  z = fp16(min),
+//   q = clamp(rint((x - z) / s), 0, 2^b - 1),  q = 0 when s == 0.
+#pragma once
+
+#include "lbkv_decode.cuh"
+
+namespace lbkv {
+
+__device__ __forceinline__ int quantize_one(float x, float zf, float sf, int qmax) {
+  if (sf == 0.f) return 0;
+  const float v = __fdiv_rn(__fsub_rn(x, zf), sf);
+  const float r = rintf(v);
+  return r < 0.f ? 0 : (r > (float)qmax ? qmax : (int)r);
+}
+
+// One warp quantizes one token row x[D] with token-wise groups of `group` channels:
+// codes into crow[D * BITS / 8], the group's scale and offset into srow/zrow[D / group].
+// Lane l holds channels 4l..4l+3; a group is group/4 consecutive lanes.
+template <int BITS>
+__device__ __forceinline__ void quantize_token_row(const __nv_bfloat16* __restrict__ x, int group, uint8_t* crow,
+                                                   __half* srow, __half* zrow, int lane) {
+  const uint2 raw = reinterpret_cast<const uint2*>(x)[lane];
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  const float2 a = __bfloat1622float2(h[0]), c = __bfloat1622float2(h[1]);
+  const float v[4] = {a.x, a.y, c.x, c.y};
+  float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
+  float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+  const int lanes = group / 4;
+  for (int o = 1; o < lanes; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  constexpr int qmax = (1 << BITS) - 1;
+  mn = __fadd_rn(mn, 0.f);  // a -0 extreme is read as +0
+  mx = __fadd_rn(mx, 0.f);
+  const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)qmax));
+  const __half zh = __float2half_rn(mn);
+  const float sf = __half2float(sh), zf = __half2float(zh);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) packed |= (uint32_t)quantize_one(v[u], zf, sf, qmax) << (BITS * u);
+  if (BITS == 2)
+    crow[lane] = (uint8_t)packed;
+  else
+    reinterpret_cast<uint16_t*>(crow)[lane] = (uint16_t)packed;
+  if (lane % lanes == 0) {
+    srow[lane / lanes] = sh;
+    zrow[lane / lanes] = zh;
+  }
+}
+
+// Thread d of 128 (channel d) quantizes channel d over one channel-wise token group:
+// tokens x[t * D + d], t < nvalid (rows with t >= nvalid, up to `group`, get code 0);
+// codes into crows[t * D * BITS / 8 + ...], the group's scale and offset into *s / *z.
+// Threads d and d^1 (and d^2, d^3 at INT2) share code bytes: all 128 threads take part.
+template <int BITS>
+__device__ __forceinline__ void quantize_channel_group(const __nv_bfloat16* __restrict__ x, int nvalid, int group,
+                                                       uint8_t* crows, __half* s, __half* z, int d) {
+  constexpr int RB = kHeadDim * BITS / 8;
+  constexpr int per_byte = 8 / BITS;
+  constexpr int qmax = (1 << BITS) - 1;
+  float sf = 0.f, zf = 0.f;
+  if (nvalid > 0) {
+    float mn = __bfloat162float(x[d]), mx = mn;
+    for (int t = 1; t < nvalid; ++t) {
+      const float v = __bfloat162float(x[(size_t)t * kHeadDim + d]);
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+    }
+    mn = __fadd_rn(mn, 0.f);  // a -0 extreme is read as +0
+    mx = __fadd_rn(mx, 0.f);
+    const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)qmax));
+    const __half zh = __float2half_rn(mn);
+    *s = sh;
+    *z = zh;
+    sf = __half2float(sh);
+    zf = __half2float(zh);
+  }
+  for (int t = 0; t < group; ++t) {
+    int q = 0;
+    if (t < nvalid) q = quantize_one(__bfloat162float(x[(size_t)t * kHeadDim + d]), zf, sf, qmax);
+    // gather the codes of the channels sharing this byte (adjacent lanes)
+    uint32_t bits = (uint32_t)q << (BITS * (d % per_byte));
+#pragma unroll
+    for (int o = 1; o < per_byte; o <<= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
+    if (d % per_byte == 0) crows[(size_t)t * RB + d / per_byte] = (uint8_t)bits;
+  }
+}
+
+}  // namespace lbkv

@@ -140,6 +140,31 @@ LBKV_API int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_
 LBKV_API int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_lens, int bits, int layout, int group,
               uint8_t* codes, void* scale, void* off, lbkv_stream_t stream);
 
+/* Quantize-on-append: store the K and V of the token a decode step just produced
+ * (the step before the decode path when serving, which the abstract of "FOSCAR:
+ * Accelerating Decode Attention over 2- and 4-Bit KV Caches through Affine Folding"
+ * integrates into SGLang; how a token is appended is this library's reading), with the
+ * same quantizer as lbkv_pack.
+ *   k_new, v_new: bf16 [B][Hkv][D] device, the new token of every (sequence, KV head).
+ *   seq_lens: int32 [B] device, the cached tokens L_b; advanced in place.
+ * Both sides token-wise: the token is quantized per group of `group` channels into
+ * position L_b, and L_b += 1. Otherwise (a channel-wise side, whose groups span
+ * `group` tokens) both sides go through the bf16 window of desc (k_win, v_win,
+ * win_lens, win_cap >= group required): the token is copied into window slot
+ * W_b = win_lens[b] and W_b += 1; when the window then holds `group` tokens they are
+ * quantized into positions L_b .. L_b + group - 1 (token-wise side: per token;
+ * channel-wise side: as one group), L_b += group and W_b = 0. The cache then holds
+ * exactly what lbkv_pack would produce from the same bf16 history.
+ * A sequence whose token does not fit (L_b == max_seq_len; a channel-wise L_b that is
+ * not a multiple of group or has no room for a group; W_b >= group) is left unchanged,
+ * and if desc->workspace is given its status word records 4 (see lbkv_device_status).
+ * Codes, scales and offsets as for lbkv_pack; all pointers 16-byte aligned.
+ * Uses desc's batch, num_kv_heads, head_dim, max_seq_len, window fields and workspace
+ * (optional). Asynchronous on `stream`. Errors as for lbkv_pack. */
+LBKV_API int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int32_t* seq_lens, int bits,
+                         int k_layout, int v_layout, int group, uint8_t* k_codes, void* k_scale, void* k_off,
+                         uint8_t* v_codes, void* v_scale, void* v_off, lbkv_stream_t stream);
+
 /* Same computation and arguments as lbkv_decode_attn, for callers that cannot
  * allocate device memory (an engine whose allocator owns all device memory, a
  * plugin that only receives its input and output buffers, a loop where an

@@ -130,3 +130,47 @@ def test_empty_batch_is_a_no_op_without_pointers(lib):
 def test_selftest_arguments_rejected_before_launch(lib, status, limit, want):
     assert lib.lbkv_selftest_wait_timeout(ctypes.c_void_p(status), ctypes.c_uint64(limit), ctypes.c_void_p(0)) == want
 
+
+
+def _append(lib, d, fmt, ptrs=None):
+    null = ctypes.c_void_p(0)
+    p = ptrs if ptrs is not None else [null] * 3
+    return lib.lbkv_append(ctypes.byref(d) if d is not None else None, *p, *fmt, *([null] * 6), null)
+
+
+@pytest.mark.parametrize("kwargs,fmt,want", [
+    (dict(), (3, 0, 0, 128), -1),        # bits
+    (dict(), (2, 0, 2, 128), -1),        # layout
+    (dict(), (2, 0, 0, 16), -3),         # group
+    (dict(D=64), (2, 0, 0, 128), -3),    # head_dim
+    (dict(T=1000), (2, 0, 0, 128), -1),  # T_cap not a multiple of 128
+    (dict(B=-1), (2, 0, 0, 128), -1),
+    (dict(), (2, 1, 0, 128), -1),        # a channel-wise side needs the window
+    (dict(), (2, 0, 0, 128), -1),        # null pointers
+])
+def test_invalid_append_arguments_rejected_before_launch(lib, kwargs, fmt, want):
+    assert _append(lib, _desc(**kwargs), fmt) == want
+
+
+def test_append_window_rules(lib):
+    # the window must hold a whole channel-wise group, and all three window fields go together
+    d = _desc()
+    d.k_win = d.v_win = d.win_lens = 4096
+    d.win_cap = 64
+    assert _append(lib, d, (2, 1, 0, 128)) == -1
+    d.win_cap = 128
+    assert _append(lib, d, (2, 1, 0, 128)) == -1  # past the window rules: null cache pointers
+    d.v_win = None
+    assert _append(lib, d, (2, 0, 1, 64)) == -1
+    assert _append(lib, None, (2, 0, 0, 128)) == -1
+
+
+def test_append_misaligned_pointer(lib):
+    d = _desc()
+    ok, bad = ctypes.c_void_p(4096), ctypes.c_void_p(4100)
+    st = lib.lbkv_append(ctypes.byref(d), ok, bad, ok, 2, 0, 0, 128, *([ok] * 6), ctypes.c_void_p(0))
+    assert st == -2
+
+
+def test_append_empty_batch_is_a_no_op(lib):
+    assert _append(lib, _desc(B=0), (2, 0, 0, 128)) == 0
