@@ -19,6 +19,7 @@ shards by sequence and KV head with no exchange); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -429,6 +430,49 @@ def time_append(device, peak, calls=256):
     return rows
 
 
+def time_bf16(device, peak, int2_us, calls=5):
+    """The BF16 comparator (lbkv_decode_bf16) on the headline's shape (batch 32, 32K context,
+    32q/8kv, head_dim 128) over a bf16 cache (4.3 GB, far larger than L2): a CUDA graph of
+    `calls` calls, replayed once untimed and once timed."""
+    import bit_kv_cache_split_gb300 as pkg
+
+    B, Hq, Hkv, T, D = HEADLINE["batch"], 32, 8, HEADLINE["ctx"], 128
+    gen = torch.Generator(device=device).manual_seed(11)
+    q = torch.randn((B, Hq, D), generator=gen, device=device, dtype=torch.bfloat16)
+    k = torch.randn((B, Hkv, T, D), generator=gen, device=device, dtype=torch.bfloat16)
+    v = torch.randn((B, Hkv, T, D), generator=gen, device=device, dtype=torch.bfloat16)
+    lens = torch.full((B,), T, dtype=torch.int32, device=device)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+    d = pkg._binding.make_desc(B, Hq, Hkv, T, D)
+    ws = torch.zeros(pkg._binding.load().lbkv_bf16_workspace_bytes(ctypes.byref(d)), dtype=torch.uint8, device=device)
+    for _ in range(2):
+        pkg.decode_bf16(q, k, v, lens, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(calls):
+                pkg.decode_bf16(q, k, v, lens, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / calls
+    nbytes = B * Hkv * T * D * 2 * 2 + 2 * B * Hq * D * 2 + B * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    status = pkg.device_status(ws)
+    del graph, k, v
+    torch.cuda.empty_cache()
+    return {"workload": f"bf16-b{B}-ctx{T}", "us_per_call": round(us, 2), "gbs": round(gbs, 1),
+            "frac": round(gbs / peak, 4), "bytes": nbytes, "int2_speedup": round(us / int2_us, 2),
+            "device_status": status}
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: every rank's timed region is one step of its own replica,
     and the job is done when the last one is (weak scaling, one process per GPU)."""
@@ -560,10 +604,11 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     e2e_val = job_throughput(step_bytes, e2e_ms, world)
 
-    sweep = append = None
+    sweep = append = bf16 = None
     if not args.no_sweep and rank == 0:
         sweep = run_sweep(device, peak)
         append = time_append(device, peak)
+        bf16 = time_bf16(device, peak, ms * 1e3)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -595,6 +640,7 @@ def main():
             "cpu_baseline": cpu,
             "sweep": sweep,
             "append": append,
+            "bf16_comparator": bf16,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

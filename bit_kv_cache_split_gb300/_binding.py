@@ -23,7 +23,8 @@ CHANNELWISE = 1
 STATUS = {0: "LBKV_OK", -1: "LBKV_EINVAL", -2: "LBKV_EALIGN", -3: "LBKV_EUNSUPPORTED",
           -4: "LBKV_EWORKSPACE", -5: "LBKV_ECUDA", -6: "LBKV_EDEVICE", -7: "LBKV_ESCRATCH"}
 
-EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_append", "lbkv_device_status",
+EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_append", "lbkv_decode_bf16",
+           "lbkv_bf16_workspace_bytes", "lbkv_device_status",
            "lbkv_strerror", "lbkv_decode_attn_noalloc", "lbkv_noalloc_scratch_bytes", "lbkv_selftest_wait_timeout")
 
 
@@ -69,6 +70,10 @@ def load(path: Optional[str] = None):
         L.lbkv_decode_attn.argtypes = [ctypes.POINTER(Desc)] + [vp] * 8 + [i32] * 4 + [vp, vp]
         L.lbkv_pack.restype = i32
         L.lbkv_pack.argtypes = [ctypes.POINTER(Desc), vp, vp, i32, i32, i32, vp, vp, vp, vp]
+        L.lbkv_decode_bf16.restype = i32
+        L.lbkv_decode_bf16.argtypes = [ctypes.POINTER(Desc)] + [vp] * 6
+        L.lbkv_bf16_workspace_bytes.restype = ctypes.c_size_t
+        L.lbkv_bf16_workspace_bytes.argtypes = [ctypes.POINTER(Desc)]
         L.lbkv_append.restype = i32
         L.lbkv_append.argtypes = [ctypes.POINTER(Desc), vp, vp, vp] + [i32] * 4 + [vp] * 7
         L.lbkv_selftest_wait_timeout.restype = i32
@@ -232,6 +237,34 @@ def append(k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_
                             _ptr(v_scale), _ptr(v_off), _stream_ptr(stream))
     if st != 0:
         raise LbkvError(st, "lbkv_append")
+
+
+def decode_bf16(q, k, v, seq_lens, *, sm_scale=0.0, out=None, workspace=None, stream=None):
+    """The BF16 comparator (lbkv_decode_bf16): decode attention over bf16 k, v [B][Hkv][T][D]."""
+    _check(q, "q", torch.bfloat16)
+    B, Hq, D = q.shape
+    _check(k, "k", torch.bfloat16)
+    Hkv, T = k.shape[1], k.shape[2]
+    _check(k, "k", torch.bfloat16, (B, Hkv, T, D))
+    _check(v, "v", torch.bfloat16, (B, Hkv, T, D))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _check(out, "out", torch.bfloat16, (B, Hq, D))
+    d = make_desc(B, Hq, Hkv, T, D, sm_scale=sm_scale)
+    L = load()
+    if workspace is None:
+        n = L.lbkv_bf16_workspace_bytes(ctypes.byref(d))
+        if n == 0:
+            raise LbkvError(-3, "lbkv_bf16_workspace_bytes")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    d.workspace = workspace.data_ptr()
+    d.workspace_bytes = workspace.numel() * workspace.element_size()
+    st = L.lbkv_decode_bf16(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), _ptr(out),
+                            _stream_ptr(stream))
+    if st != 0:
+        raise LbkvError(st, "lbkv_decode_bf16")
+    return out
 
 
 def selftest_wait_timeout(limit_ns: int, device="cuda") -> tuple:

@@ -280,6 +280,99 @@ int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int
   return LBKV_OK;
 }
 
+// BF16 comparator: its K/V tensor maps, encoded through the driver entry point that the
+// runtime hands out (no link against the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+static bool kv_tensor_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// BF16 comparator: status word | chunk partials (m, l) | chunk partials O.
+static int bf16_layout(const lbkv_desc* d, size_t* off_ml, size_t* off_o, size_t* bytes, int* max_chunks) {
+  if (!d) return LBKV_EINVAL;
+  if (d->batch < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0) return LBKV_EINVAL;
+  if (d->num_q_heads % d->num_kv_heads) return LBKV_EINVAL;
+  if (d->head_dim != kHeadDim) return LBKV_EUNSUPPORTED;
+  if (d->max_seq_len <= 0 || d->max_seq_len % kSlotTokens) return LBKV_EINVAL;
+  const int hq = d->num_q_heads / d->num_kv_heads;
+  if (hq > kMaxHq) return LBKV_EUNSUPPORTED;
+  if (d->k_win || d->v_win || d->win_lens) return LBKV_EUNSUPPORTED;  // the comparator has no window
+  if ((long long)d->batch * d->num_kv_heads * d->max_seq_len >= (1ll << 31)) return LBKV_EUNSUPPORTED;  // TMA rows
+  *max_chunks = (d->max_seq_len + kBfChunk - 1) / kBfChunk;
+  const size_t rows = (size_t)d->batch * d->num_kv_heads * (size_t)*max_chunks * hq;
+  *off_ml = 256;
+  *off_o = round_up(*off_ml + rows * sizeof(float2), 256);
+  *bytes = round_up(*off_o + rows * kHeadDim * sizeof(float), 256);
+  return LBKV_OK;
+}
+
+size_t lbkv_bf16_workspace_bytes(const lbkv_desc* desc) {
+  size_t a, b, n;
+  int mc;
+  return bf16_layout(desc, &a, &b, &n, &mc) == LBKV_OK ? n : 0;
+}
+
+int lbkv_decode_bf16(const lbkv_desc* desc, const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                     void* out, lbkv_stream_t stream) {
+  size_t off_ml, off_o, bytes;
+  int max_chunks;
+  int st = bf16_layout(desc, &off_ml, &off_o, &bytes, &max_chunks);
+  if (st) return st;
+  if (desc->batch == 0) return LBKV_OK;
+  const void* ptrs[] = {q, k, v, seq_lens, out};
+  for (const void* p : ptrs)
+    if (!p) return LBKV_EINVAL;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LBKV_EALIGN;
+  if (!desc->workspace || desc->workspace_bytes < bytes) return LBKV_EWORKSPACE;
+  if (reinterpret_cast<uintptr_t>(desc->workspace) & 255u) return LBKV_EALIGN;
+  if (ensure_smem_attr(bf16_split_kernel_fn(), bf16_split_smem_bytes()) != LBKV_OK) return LBKV_ECUDA;
+  uint8_t* ws = static_cast<uint8_t*>(desc->workspace);
+  Bf16Params p{};
+  const uint64_t rows = (uint64_t)desc->batch * desc->num_kv_heads * desc->max_seq_len;
+  if (!kv_tensor_map(&p.tm_k, k, rows) || !kv_tensor_map(&p.tm_v, v, rows)) return LBKV_ECUDA;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.seq_lens = seq_lens;
+  p.part_ml = reinterpret_cast<float2*>(ws + off_ml);
+  p.part_o = reinterpret_cast<float*>(ws + off_o);
+  p.status = reinterpret_cast<int32_t*>(ws);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.B = desc->batch;
+  p.Hq = desc->num_q_heads;
+  p.Hkv = desc->num_kv_heads;
+  p.hq = desc->num_q_heads / desc->num_kv_heads;
+  p.T_cap = desc->max_seq_len;
+  p.max_chunks = max_chunks;
+  const float sigma = desc->sm_scale > 0.f ? desc->sm_scale : 1.f / std::sqrt((float)desc->head_dim);
+  p.sl2 = sigma * 1.4426950408889634f;
+  if (launch_bf16(p, reinterpret_cast<cudaStream_t>(stream)) != 0) return LBKV_ECUDA;
+  return LBKV_OK;
+}
+
 int lbkv_device_status(const lbkv_desc* desc, lbkv_stream_t stream, int32_t* code) {
   if (!desc) return LBKV_EINVAL;
   if (!desc->workspace || desc->workspace_bytes < 256) return LBKV_EWORKSPACE;

@@ -2,6 +2,8 @@
 // (not part of the public interface in include/lbkv.h).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the driver is reached through the runtime's entry points)
+
 #include "lbkv_decode.cuh"
 
 namespace lbkv {
@@ -35,6 +37,26 @@ struct AppendArgs {
 };
 
 int launch_append(const AppendArgs& a, cudaStream_t stream);
+
+// BF16 comparator: tokens per chunk (one CTA each), and the arguments of its two kernels.
+constexpr int kBfChunk = 512;
+struct Bf16Params {
+  CUtensorMap tm_k;        // K and V as 2-D tensors [B*Hkv*T_cap rows][128 channels] bf16,
+  CUtensorMap tm_v;        //   64 x 64 boxes with the 128-byte swizzle
+  const __nv_bfloat16* q;  // [B][Hq][D]
+  const __nv_bfloat16* k;  // [B][Hkv][T_cap][D]
+  const __nv_bfloat16* v;
+  const int32_t* seq_lens;
+  float2* part_ml;         // [B*Hkv*max_chunks][hq] chunk partials (max in log2 units, denominator)
+  float* part_o;           // [B*Hkv*max_chunks][hq][D]
+  int32_t* status;
+  __nv_bfloat16* out;      // [B][Hq][D]
+  int B, Hq, Hkv, hq, T_cap, max_chunks;
+  float sl2;               // softmax scale times log2(e)
+};
+const void* bf16_split_kernel_fn();
+int bf16_split_smem_bytes();
+int launch_bf16(const Bf16Params& p, cudaStream_t stream);
 
 using DecodeKernel = void (*)(const DecodeParams);
 

@@ -165,6 +165,20 @@ LBKV_API int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v
                          int k_layout, int v_layout, int group, uint8_t* k_codes, void* k_scale, void* k_off,
                          uint8_t* v_codes, void* v_scale, void* v_off, lbkv_stream_t stream);
 
+/* BF16 comparator: the same split-KV decode attention over a bf16 cache, without
+ * quantization, so that the speedup that "FOSCAR: Accelerating Decode Attention over 2-
+ * and 4-Bit KV Caches through Affine Folding" (abstract) reports over a BF16 decode
+ * kernel can be measured on this GPU and pipeline.
+ *   q: bf16 [B][Hq][D]; k, v: bf16 [B][Hkv][max_seq_len][D]; seq_lens: int32 [B] device;
+ *   out: bf16 [B][Hq][D]. Softmax over the first L_b tokens (zero output when L_b == 0).
+ * Uses desc's batch, heads, head_dim (128), max_seq_len, sm_scale and workspace (of at
+ * least lbkv_bf16_workspace_bytes bytes, 256-byte aligned, first 256 bytes zeroed once:
+ * the status word). Window fields must be NULL (LBKV_EUNSUPPORTED). Hq/Hkv <= 8.
+ * Errors as for lbkv_decode_attn. Asynchronous on `stream`. */
+LBKV_API size_t lbkv_bf16_workspace_bytes(const lbkv_desc* desc);
+LBKV_API int lbkv_decode_bf16(const lbkv_desc* desc, const void* q, const void* k, const void* v,
+                              const int32_t* seq_lens, void* out, lbkv_stream_t stream);
+
 /* Same computation and arguments as lbkv_decode_attn, for callers that cannot
  * allocate device memory (an engine whose allocator owns all device memory, a
  * plugin that only receives its input and output buffers, a loop where an

@@ -230,6 +230,27 @@ def decode_ref(x: DecodeInputs, rows=None, n_threads: int = 0) -> np.ndarray:
     return out
 
 
+def attention_bf16(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, seq_lens, sm_scale: float = 0.0,
+                   n_threads: int = 0) -> np.ndarray:
+    """Plain softmax attention over a bf16 cache (the BF16 comparator's definition), fp64.
+
+    q [B][Hq][D], k/v [B][Hkv][T][D] as uint16 bf16 bits, seq_lens [B]. It is decode_ref with
+    no quantized tokens and the whole cache as the bf16 window, whose step the decode
+    definition already holds (the window's tokens are attended in full precision)."""
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    B, Hkv, T, D = k.shape
+    tc = 128
+    zc = np.zeros((B, Hkv, tc, D // 4), np.uint8)
+    zs = np.zeros((B, Hkv, tc, D // 128), np.uint16)
+    x = DecodeInputs(q=q, k_codes=zc, k_scale=zs, k_off=zs, v_codes=zc, v_scale=zs, v_off=zs,
+                     seq_lens=np.zeros(B, np.int32), bits=2, k_layout=TOKENWISE, v_layout=TOKENWISE, group=128,
+                     Hkv=Hkv, T_cap=tc, sm_scale=sm_scale, k_win=k, v_win=v,
+                     win_lens=np.ascontiguousarray(seq_lens, dtype=np.int32), win_cap=T)
+    return decode_ref(x, n_threads=n_threads)
+
+
 def decode_folded(x: DecodeInputs, block: int = 64, misorder: int = 0):
     """Folded path with op counting. Returns (out [B][Hq][D] fp64, ops, values)."""
     args = x._struct()
