@@ -76,12 +76,12 @@ def measured_hbm_peak():
 
 
 def source_hash() -> str:
-    """Hash of the sources the decode kernel is built from (its traffic does not depend on
-    the pack or append kernels)."""
+    """Hash of the decode kernel's device sources (its traffic does not depend on the other
+    kernels or on the host entry points)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_kv_cache_split_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if not (f.startswith("lbkv_decode") or f in ("lbkv_device.cuh", "lbkv_api.cu")):
+        if not (f.startswith("lbkv_decode") or f == "lbkv_device.cuh"):
             continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
