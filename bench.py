@@ -473,6 +473,65 @@ def time_bf16(device, peak, int2_us, calls=5):
             "device_status": status}
 
 
+def time_paged(device, peak, contiguous_us, page_tokens=128, calls=20):
+    """The headline workload (INT2 token-wise, batch 32, 32K context) stored in a paged
+    cache: pools of `page_tokens`-token pages in shuffled order behind a page table. Two
+    replicas alternate (each larger than L2); a CUDA graph of `calls` calls is replayed
+    once untimed and, after an L2 flush, once timed."""
+    import bit_kv_cache_split_gb300 as pkg
+
+    wl = inputs.decode_int2(HEADLINE["batch"], HEADLINE["ctx"])
+    reps = []
+    for i in range(2):
+        w = inputs.Workload(**{**wl.__dict__, "seed": wl.seed + 1000 * i})
+        t = inputs.generate(w, device)
+        table, n_pages = inputs.page_table(w.lens, page_tokens, w.t_cap // page_tokens, seed=40 + i)
+        pool = {k: inputs.to_pages(t[k], table, n_pages, page_tokens)
+                for k in ("k_codes", "k_scale", "k_off", "v_codes", "v_scale", "v_off")}
+        reps.append((t["q"], pool, t["seq_lens"], table.to(device)))
+        del t
+    n = pkg.workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.t_cap, wl.bits, wl.k_layout,
+                            wl.v_layout, wl.group)
+    ws = pkg._binding.alloc_workspace(n, device)
+    out = torch.empty((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device=device)
+
+    def call(i):
+        q, c, lens, table = reps[i % 2]
+        pkg.decode_attn(q, c["k_codes"], c["k_scale"], c["k_off"], c["v_codes"], c["v_scale"], c["v_off"], lens,
+                        bits=2, group=128, page_table=table, max_seq_len=wl.t_cap, out=out, workspace=ws)
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(calls):
+                call(i)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    flush = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=device)
+    flush.zero_()
+    del flush
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / calls
+    nbytes = algorithmic_bytes(wl) + wl.batch * (wl.t_cap // page_tokens) * 4  # + the page table
+    gbs = nbytes / (us * 1e-6) / 1e9
+    status = pkg.device_status(ws)
+    del graph, reps
+    torch.cuda.empty_cache()
+    return {"workload": f"{wl.name}-paged{page_tokens}", "us_per_call": round(us, 2), "gbs": round(gbs, 1),
+            "frac": round(gbs / peak, 4), "bytes": nbytes, "paged_over_contiguous": round(us / contiguous_us, 3),
+            "device_status": status}
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: every rank's timed region is one step of its own replica,
     and the job is done when the last one is (weak scaling, one process per GPU)."""
@@ -604,11 +663,12 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     e2e_val = job_throughput(step_bytes, e2e_ms, world)
 
-    sweep = append = bf16 = None
+    sweep = append = bf16 = paged = None
     if not args.no_sweep and rank == 0:
         sweep = run_sweep(device, peak)
         append = time_append(device, peak)
         bf16 = time_bf16(device, peak, ms * 1e3)
+        paged = time_paged(device, peak, ms * 1e3)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -641,6 +701,7 @@ def main():
             "sweep": sweep,
             "append": append,
             "bf16_comparator": bf16,
+            "paged": paged,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

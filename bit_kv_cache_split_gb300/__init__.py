@@ -2,10 +2,10 @@
 
 The computation lives in a CUDA library with a C ABI (include/lbkv.h); this
 package builds it (``build``), binds it (``decode_attn``, ``pack``, ``append``, ``decode_bf16``,
-``workspace_bytes``, ``device_status``) and draws seeded synthetic inputs
+``workspace_bytes``, ``alloc_workspace``, ``device_status``) and draws seeded synthetic inputs
 (``inputs``).
 """
 
-from ._binding import (CHANNELWISE, TOKENWISE, LbkvError, append, decode_attn, decode_bf16,  # noqa: F401
-                       device_status, load, pack, workspace_bytes)
+from ._binding import (CHANNELWISE, TOKENWISE, LbkvError, alloc_workspace, append, decode_attn,  # noqa: F401
+                       decode_bf16, device_status, load, pack, workspace_bytes)
 from . import build, inputs  # noqa: F401

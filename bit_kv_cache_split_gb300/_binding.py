@@ -42,6 +42,8 @@ class Desc(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("sm_scale", ctypes.c_float),
         ("k_win", ctypes.c_void_p), ("v_win", ctypes.c_void_p), ("win_lens", ctypes.c_void_p),
         ("win_cap", ctypes.c_int32), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("page_table", ctypes.c_void_p), ("page_tokens", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
     ]
 
 
@@ -134,6 +136,27 @@ def make_desc(batch, num_q_heads, num_kv_heads, max_seq_len, head_dim=128, sm_sc
     return d
 
 
+def _set_paged(d: Desc, page_table, page_tokens: int, num_pages: int):
+    """Paged-cache fields of d: page_table int32 [B][max_pages] on the device."""
+    _check(page_table, "page_table", torch.int32)
+    if page_table.dim() != 2 or page_table.shape[0] != d.batch:
+        raise ValueError(f"page_table must have shape ({d.batch}, max_pages), got {tuple(page_table.shape)}")
+    d.page_table = page_table.data_ptr()
+    d.page_tokens, d.max_pages, d.num_pages = int(page_tokens), int(page_table.shape[1]), int(num_pages)
+
+
+def _cache_shape(B, Hkv, T, page_table, page_tokens, num_pages):
+    """Leading dims of the cache tensors: [B][Hkv][T] contiguous, [num_pages][Hkv][page_tokens] paged."""
+    return (B, Hkv, T) if page_table is None else (num_pages, Hkv, page_tokens)
+
+
+def _paged_dims(k_codes, page_table, max_seq_len):
+    """(num_pages, page_tokens, max_seq_len) of a paged cache, read from the code pool and the table."""
+    NP, P = k_codes.shape[0], k_codes.shape[2]
+    T = int(max_seq_len) if max_seq_len else int(page_table.shape[1]) * P
+    return NP, P, T
+
+
 def workspace_bytes(batch, num_q_heads, num_kv_heads, max_seq_len, bits, k_layout, v_layout, group,
                     window: bool = False, head_dim=128) -> int:
     """Workspace size for a call with these shapes (0 when the arguments are invalid)."""
@@ -153,17 +176,22 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 def decode_attn(q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, *, bits, k_layout=TOKENWISE,
                 v_layout=TOKENWISE, group=128, sm_scale=0.0, k_win=None, v_win=None, win_lens=None,
-                out=None, workspace=None, stream=None) -> torch.Tensor:
+                page_table=None, max_seq_len=None, out=None, workspace=None, stream=None) -> torch.Tensor:
     """Decode attention through lbkv_decode_attn. Shapes as in include/lbkv.h.
 
     q bf16 [B][Hq][D]; k_codes/v_codes uint8 [B][Hkv][T_cap][D*bits/8]; scales/offsets fp16;
     seq_lens int32 [B] on the device. Returns out bf16 [B][Hq][D] (allocated when not given).
+    Paged cache: page_table int32 [B][max_pages]; the cache tensors are page pools
+    ([num_pages][Hkv][page_tokens]...) and max_seq_len defaults to max_pages * page_tokens.
     """
     B, Hq, D = q.shape
     Hkv, T = k_codes.shape[1], k_codes.shape[2]
+    NP = P = 0
+    if page_table is not None:
+        NP, P, T = _paged_dims(k_codes, page_table, max_seq_len)
     _check(q, "q", torch.bfloat16)
     for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
-        _check(t, name, torch.uint8, (B, Hkv, T, D * bits // 8))
+        _check(t, name, torch.uint8, _cache_shape(B, Hkv, T, page_table, P, NP) + (D * bits // 8,))
     for name, t in (("k_scale", k_scale), ("k_off", k_off), ("v_scale", v_scale), ("v_off", v_off)):
         _check(t, name, torch.float16)
     _check(seq_lens, "seq_lens", torch.int32, (B,))
@@ -181,6 +209,8 @@ def decode_attn(q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, *
             raise LbkvError(-3 if bits in (2, 4) else -1, "lbkv_workspace_bytes")
         workspace = alloc_workspace(n, q.device)
     d = make_desc(B, Hq, Hkv, T, D, sm_scale, k_win, v_win, win_lens, workspace)
+    if page_table is not None:
+        _set_paged(d, page_table, P, NP)
     st = L.lbkv_decode_attn(ctypes.byref(d), _ptr(q), _ptr(k_codes), _ptr(k_scale), _ptr(k_off), _ptr(v_codes),
                             _ptr(v_scale), _ptr(v_off), _ptr(seq_lens), int(bits), int(k_layout), int(v_layout),
                             int(group), _ptr(out), _stream_ptr(stream))
@@ -189,23 +219,35 @@ def decode_attn(q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, *
     return out
 
 
-def pack(x, seq_lens, *, bits, layout=TOKENWISE, group=128, codes=None, scale=None, off=None, stream=None):
-    """Quantize bf16 x [B][Hkv][T_cap][D] through lbkv_pack. Returns (codes, scale, off)."""
+def pack(x, seq_lens, *, bits, layout=TOKENWISE, group=128, codes=None, scale=None, off=None, page_table=None,
+         num_pages=None, page_tokens=None, workspace=None, stream=None):
+    """Quantize bf16 x [B][Hkv][T_cap][D] through lbkv_pack. Returns (codes, scale, off).
+
+    Paged cache: page_table int32 [B][max_pages]; codes, scale and off are page pools
+    [num_pages][Hkv][page_tokens]... (allocated zero-filled from num_pages and page_tokens
+    when not given); workspace (optional) receives the device status."""
     _check(x, "x", torch.bfloat16)
     B, Hkv, T, D = x.shape
     _check(seq_lens, "seq_lens", torch.int32, (B,))
-    sshape = (B, Hkv, T, D // group) if layout == TOKENWISE else (B, Hkv, T // group, D)
+    if page_table is not None and codes is not None:
+        num_pages, page_tokens = codes.shape[0], codes.shape[2]
+    lead = _cache_shape(B, Hkv, T, page_table, page_tokens, num_pages)
+    R = lead[2]
+    sshape = lead + (D // group,) if layout == TOKENWISE else lead[:2] + (R // group, D)
     if codes is None:
-        codes = torch.empty((B, Hkv, T, D * bits // 8), dtype=torch.uint8, device=x.device)
+        alloc = torch.empty if page_table is None else torch.zeros
+        codes = alloc(lead + (D * bits // 8,), dtype=torch.uint8, device=x.device)
     if scale is None:
         scale = torch.zeros(sshape, dtype=torch.float16, device=x.device)
     if off is None:
         off = torch.zeros(sshape, dtype=torch.float16, device=x.device)
-    _check(codes, "codes", torch.uint8, (B, Hkv, T, D * bits // 8))
+    _check(codes, "codes", torch.uint8, lead + (D * bits // 8,))
     _check(scale, "scale", torch.float16, sshape)
     _check(off, "off", torch.float16, sshape)
-    d = make_desc(B, 1, Hkv, T, D)
+    d = make_desc(B, 1, Hkv, T, D, workspace=workspace)
     d.num_q_heads = Hkv
+    if page_table is not None:
+        _set_paged(d, page_table, page_tokens, num_pages)
     st = load().lbkv_pack(ctypes.byref(d), _ptr(x), _ptr(seq_lens), int(bits), int(layout), int(group),
                           _ptr(codes), _ptr(scale), _ptr(off), _stream_ptr(stream))
     if st != 0:
@@ -214,17 +256,22 @@ def pack(x, seq_lens, *, bits, layout=TOKENWISE, group=128, codes=None, scale=No
 
 
 def append(k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_off, *, bits, k_layout=TOKENWISE,
-           v_layout=TOKENWISE, group=128, k_win=None, v_win=None, win_lens=None, workspace=None, stream=None):
+           v_layout=TOKENWISE, group=128, k_win=None, v_win=None, win_lens=None, page_table=None, max_seq_len=None,
+           workspace=None, stream=None):
     """Append the new token k_new/v_new bf16 [B][Hkv][D] through lbkv_append (quantize-on-append).
 
-    The cache tensors, seq_lens (and win_lens with the window) are updated in place."""
+    The cache tensors, seq_lens (and win_lens with the window) are updated in place. Paged
+    cache: page_table int32 [B][max_pages] and page pools, as for decode_attn."""
     _check(k_new, "k_new", torch.bfloat16)
     B, Hkv, D = k_new.shape
     _check(v_new, "v_new", torch.bfloat16, (B, Hkv, D))
     _check(seq_lens, "seq_lens", torch.int32, (B,))
     T = k_codes.shape[2]
+    NP = P = 0
+    if page_table is not None:
+        NP, P, T = _paged_dims(k_codes, page_table, max_seq_len)
     for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
-        _check(t, name, torch.uint8, (B, Hkv, T, D * bits // 8))
+        _check(t, name, torch.uint8, _cache_shape(B, Hkv, T, page_table, P, NP) + (D * bits // 8,))
     for name, t in (("k_scale", k_scale), ("k_off", k_off), ("v_scale", v_scale), ("v_off", v_off)):
         _check(t, name, torch.float16)
     if k_win is not None:
@@ -232,6 +279,8 @@ def append(k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_
         _check(v_win, "v_win", torch.bfloat16, tuple(k_win.shape))
         _check(win_lens, "win_lens", torch.int32, (B,))
     d = make_desc(B, Hkv, Hkv, T, D, k_win=k_win, v_win=v_win, win_lens=win_lens, workspace=workspace)
+    if page_table is not None:
+        _set_paged(d, page_table, P, NP)
     st = load().lbkv_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _ptr(seq_lens), int(bits), int(k_layout),
                             int(v_layout), int(group), _ptr(k_codes), _ptr(k_scale), _ptr(k_off), _ptr(v_codes),
                             _ptr(v_scale), _ptr(v_off), _stream_ptr(stream))

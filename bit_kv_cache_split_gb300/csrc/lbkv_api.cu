@@ -54,6 +54,24 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
+// A paged cache (page_table given): pages of a power of two of at least 128 tokens (whole
+// 128-token slots, so that no kernel item straddles two pages), a non-empty pool and a
+// table row with room for max_seq_len tokens.
+int paged_check(const lbkv_desc* d) {
+  if (!d->page_table) return LBKV_OK;
+  if (d->page_tokens < kSlotTokens || (d->page_tokens & (d->page_tokens - 1))) return LBKV_EINVAL;
+  if (d->max_pages <= 0 || d->num_pages <= 0) return LBKV_EINVAL;
+  if ((long long)d->max_pages * d->page_tokens < d->max_seq_len) return LBKV_EINVAL;
+  if ((long long)d->batch * d->max_pages >= (1ll << 31)) return LBKV_EINVAL;
+  if (reinterpret_cast<uintptr_t>(d->page_table) & 3u) return LBKV_EALIGN;
+  return LBKV_OK;
+}
+
+PagedArgs paged_args(const lbkv_desc* d) {
+  if (!d->page_table) return PagedArgs{nullptr, 0, 0, 0};
+  return PagedArgs{d->page_table, d->page_tokens, d->max_pages, d->num_pages};
+}
+
 struct Plan {
   int hq, hkv, kv_shift, mode, gv, win;
   int unit_tokens, n_cta;
@@ -77,6 +95,7 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   const bool win = d->k_win != nullptr;
   if (win != (d->v_win != nullptr) || win != (d->win_lens != nullptr)) return LBKV_EINVAL;
   if (win && (d->win_cap <= 0 || d->win_cap > 128)) return LBKV_EINVAL;
+  if (int st = paged_check(d)) return st;
   // PV columns are (query, V channel group) pairs: a token-wise V side with G channel
   // groups feeds G separately scaled copies of the weights (operand-fold); the kernel
   // holds at most two PV n-tiles of 8 columns.
@@ -127,14 +146,19 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   return LBKV_OK;
 }
 
-DecodeKernel pick_kernel(int bits, int kl, int vl, int mode, int group) {
-  const int lg = group == 128 ? 7 : group == 64 ? 6 : 5;
+template <bool PAGED>
+DecodeKernel pick_kernel_of(int bits, int kl, int vl, int mode, int lg) {
   if (bits == 2) {
-    if (kl == 0) return vl ? decode_kernel<2, 0, 1>(mode, lg) : decode_kernel<2, 0, 0>(mode, lg);
-    return vl ? decode_kernel<2, 1, 1>(mode, lg) : decode_kernel<2, 1, 0>(mode, lg);
+    if (kl == 0) return vl ? decode_kernel<2, 0, 1, PAGED>(mode, lg) : decode_kernel<2, 0, 0, PAGED>(mode, lg);
+    return vl ? decode_kernel<2, 1, 1, PAGED>(mode, lg) : decode_kernel<2, 1, 0, PAGED>(mode, lg);
   }
-  if (kl == 0) return vl ? decode_kernel<4, 0, 1>(mode, lg) : decode_kernel<4, 0, 0>(mode, lg);
-  return vl ? decode_kernel<4, 1, 1>(mode, lg) : decode_kernel<4, 1, 0>(mode, lg);
+  if (kl == 0) return vl ? decode_kernel<4, 0, 1, PAGED>(mode, lg) : decode_kernel<4, 0, 0, PAGED>(mode, lg);
+  return vl ? decode_kernel<4, 1, 1, PAGED>(mode, lg) : decode_kernel<4, 1, 0, PAGED>(mode, lg);
+}
+
+DecodeKernel pick_kernel(int bits, int kl, int vl, int mode, int group, bool paged) {
+  const int lg = group == 128 ? 7 : group == 64 ? 6 : 5;
+  return paged ? pick_kernel_of<true>(bits, kl, vl, mode, lg) : pick_kernel_of<false>(bits, kl, vl, mode, lg);
 }
 
 }  // namespace
@@ -163,7 +187,7 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   if (desc->k_win && (!aligned16(desc->k_win) || !aligned16(desc->v_win))) return LBKV_EALIGN;
   if (!desc->workspace || desc->workspace_bytes < pl.ws_bytes) return LBKV_EWORKSPACE;
   if (reinterpret_cast<uintptr_t>(desc->workspace) & 255u) return LBKV_EALIGN;
-  DecodeKernel kern = pick_kernel(bits, k_layout, v_layout, pl.mode, group);
+  DecodeKernel kern = pick_kernel(bits, k_layout, v_layout, pl.mode, group, desc->page_table != nullptr);
   if (!kern) return LBKV_EUNSUPPORTED;
 
   uint8_t* ws = static_cast<uint8_t*>(desc->workspace);
@@ -199,6 +223,13 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.has_win = pl.win;
   p.ring_off = pl.ring_off;
   p.ring_per_warp = pl.ring_per_warp;
+  p.page_table = desc->page_table;
+  if (desc->page_table) {
+    p.log2_page = 0;
+    while ((1 << p.log2_page) < desc->page_tokens) ++p.log2_page;
+    p.max_pages = desc->max_pages;
+    p.num_pages = desc->num_pages;
+  }
 
   if (ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem_bytes) != LBKV_OK) return LBKV_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -217,14 +248,17 @@ int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_lens, int
   if (bits != 2 && bits != 4) return LBKV_EINVAL;
   if (layout != LBKV_TOKENWISE && layout != LBKV_CHANNELWISE) return LBKV_EINVAL;
   if (group != 32 && group != 64 && group != 128) return LBKV_EUNSUPPORTED;
+  if (int st = paged_check(desc)) return st;
   if (desc->batch == 0) return LBKV_OK;
   const void* ptrs[] = {x, seq_lens, codes, scale, off};
   for (const void* p : ptrs)
     if (!p) return LBKV_EINVAL;
   for (const void* p : ptrs)
     if (!aligned16(p)) return LBKV_EALIGN;
+  if (desc->workspace && (reinterpret_cast<uintptr_t>(desc->workspace) & 255u)) return LBKV_EALIGN;
   PackArgs a{static_cast<const __nv_bfloat16*>(x), seq_lens, desc->batch, desc->num_kv_heads, desc->max_seq_len,
-             bits, layout, group, codes, static_cast<__half*>(scale), static_cast<__half*>(off)};
+             bits, layout, group, codes, static_cast<__half*>(scale), static_cast<__half*>(off), paged_args(desc),
+             desc->workspace ? static_cast<int32_t*>(desc->workspace) : nullptr};
   if (launch_pack(a, reinterpret_cast<cudaStream_t>(stream)) != 0) return LBKV_ECUDA;
   return LBKV_OK;
 }
@@ -245,6 +279,7 @@ int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int
   const bool win = desc->k_win != nullptr;
   if (win != (desc->v_win != nullptr) || win != (desc->win_lens != nullptr)) return LBKV_EINVAL;
   if (windowed && (!win || desc->win_cap < group || desc->win_cap > 128)) return LBKV_EINVAL;
+  if (int st = paged_check(desc)) return st;
   if (desc->batch == 0) return LBKV_OK;
   const void* ptrs[] = {k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_off};
   for (const void* p : ptrs)
@@ -276,6 +311,7 @@ int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int
   a.v_codes = v_codes;
   a.v_scale = static_cast<__half*>(v_scale);
   a.v_off = static_cast<__half*>(v_off);
+  a.pg = paged_args(desc);
   if (launch_append(a, reinterpret_cast<cudaStream_t>(stream)) != 0) return LBKV_ECUDA;
   return LBKV_OK;
 }
@@ -319,6 +355,7 @@ static int bf16_layout(const lbkv_desc* d, size_t* off_ml, size_t* off_o, size_t
   const int hq = d->num_q_heads / d->num_kv_heads;
   if (hq > kMaxHq) return LBKV_EUNSUPPORTED;
   if (d->k_win || d->v_win || d->win_lens) return LBKV_EUNSUPPORTED;  // the comparator has no window
+  if (d->page_table) return LBKV_EUNSUPPORTED;                         // nor a paged cache
   if ((long long)d->batch * d->num_kv_heads * d->max_seq_len >= (1ll << 31)) return LBKV_EUNSUPPORTED;  // TMA rows
   *max_chunks = (d->max_seq_len + kBfChunk - 1) / kBfChunk;
   const size_t rows = (size_t)d->batch * d->num_kv_heads * (size_t)*max_chunks * hq;

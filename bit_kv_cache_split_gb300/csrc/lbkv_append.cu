@@ -18,11 +18,17 @@ namespace lbkv {
 constexpr int kAppendThreads = 512;  // 16 warps: the 2 Hkv rows of a token at once (Hkv <= 8)
 constexpr int kAppendWarps = kAppendThreads / 32;
 
+// Storage row and channel-group block of position L of KV head kvh of sequence b
+// (`page`: the page-table entry of L in a paged cache).
+__device__ __forceinline__ KvAddr append_addr(const AppendArgs& a, int page, int b, int kvh, int L) {
+  return kv_addr(a.pg.page_tokens, page, (size_t)b * a.Hkv + kvh, kvh, a.Hkv, a.T_cap, a.group, L);
+}
+
 // One side (K or V) of the g window tokens of sequence b, all KV heads, into the cache
-// at positions L .. L + g - 1.
+// at positions L .. L + g - 1 (one group: never split over two pages).
 template <int BITS>
 __device__ void flush_side(const AppendArgs& a, const __nv_bfloat16* win, int layout, uint8_t* codes, __half* scale,
-                           __half* off, int b, int L) {
+                           __half* off, int b, int L, int page) {
   constexpr int RB = kHeadDim * BITS / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = a.group;
@@ -31,7 +37,7 @@ __device__ void flush_side(const AppendArgs& a, const __nv_bfloat16* win, int la
     for (int job = warp; job < a.Hkv * g; job += kAppendWarps) {
       const int kvh = job / g, t = job % g;
       const size_t unit = (size_t)b * a.Hkv + kvh;
-      const size_t row = unit * a.T_cap + L + t;
+      const size_t row = append_addr(a, page, b, kvh, L).row + t;
       const size_t si = row * (kHeadDim / g);
       quantize_token_row<BITS>(win + (unit * a.win_cap + t) * kHeadDim, g, codes + row * RB, scale + si, off + si,
                                lane);
@@ -41,8 +47,9 @@ __device__ void flush_side(const AppendArgs& a, const __nv_bfloat16* win, int la
     for (int kvh = threadIdx.x / kHeadDim; kvh < a.Hkv; kvh += kAppendThreads / kHeadDim) {
       const int d = threadIdx.x % kHeadDim;
       const size_t unit = (size_t)b * a.Hkv + kvh;
-      const size_t row0 = unit * a.T_cap + L;
-      const size_t si = (unit * (a.T_cap / g) + L / g) * kHeadDim + d;
+      const KvAddr ad = append_addr(a, page, b, kvh, L);
+      const size_t row0 = ad.row;
+      const size_t si = ad.block * kHeadDim + d;
       quantize_channel_group<BITS>(win + unit * a.win_cap * kHeadDim, g, g, codes + row0 * RB, scale + si, off + si,
                                    d);
     }
@@ -53,7 +60,7 @@ __device__ void flush_side(const AppendArgs& a, const __nv_bfloat16* win, int la
 template <int BITS>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_constant__ AppendArgs a) {
   constexpr int RB = kHeadDim * BITS / 8;
-  __shared__ int s_L, s_W, s_ok, s_flush;
+  __shared__ int s_L, s_W, s_ok, s_flush, s_page;
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool windowed = a.k_layout == 1 || a.v_layout == 1;
@@ -67,22 +74,32 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
       flush = (W + 1 == a.group);
       ok = W < a.group && (!flush || (L % a.group == 0 && L + a.group <= a.T_cap));
     }
+    if (!ok && a.status) atomicExch(a.status, kStatusAppendFull);
+    // a paged cache: the page of position L (a token-wise store or a group flush)
+    int page = 0;
+    if (ok && a.pg.page_table && (!windowed || flush)) {
+      page = kv_page(a.pg.page_table, a.pg.max_pages, a.pg.num_pages, a.pg.page_tokens, b, L);
+      if (page < 0) {
+        ok = 0;
+        if (a.status) atomicExch(a.status, kStatusBadPage);
+      }
+    }
     s_L = L;
     s_W = W;
     s_ok = ok;
     s_flush = flush;
-    if (!ok && a.status) atomicExch(a.status, kStatusAppendFull);
+    s_page = page;
   }
   __syncthreads();
   if (!s_ok) return;  // nothing is written for this sequence
-  const int L = s_L, W = s_W;
+  const int L = s_L, W = s_W, page = s_page;
 
   if (!windowed) {
     // 2 Hkv token rows: (KV head, side); warp w takes rows w, w + 16, ...
     for (int row = warp; row < 2 * a.Hkv; row += kAppendWarps) {
       const int kvh = row >> 1, side = row & 1;
       const size_t unit = (size_t)b * a.Hkv + kvh;
-      const size_t crow = unit * a.T_cap + L;
+      const size_t crow = append_addr(a, page, b, kvh, L).row;
       const size_t si = crow * (kHeadDim / a.group);
       const __nv_bfloat16* x = (side ? a.v_new : a.k_new) + unit * kHeadDim;
       if (side)
@@ -110,8 +127,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
     return;
   }
   __syncthreads();  // the window's g tokens are in place
-  flush_side<BITS>(a, a.k_win, a.k_layout, a.k_codes, a.k_scale, a.k_off, b, L);
-  flush_side<BITS>(a, a.v_win, a.v_layout, a.v_codes, a.v_scale, a.v_off, b, L);
+  flush_side<BITS>(a, a.k_win, a.k_layout, a.k_codes, a.k_scale, a.k_off, b, L, page);
+  flush_side<BITS>(a, a.v_win, a.v_layout, a.v_codes, a.v_scale, a.v_off, b, L, page);
   __syncthreads();
   if (threadIdx.x == 0) {
     a.seq_lens[b] = L + a.group;

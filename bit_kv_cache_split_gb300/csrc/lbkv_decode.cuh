@@ -141,6 +141,11 @@ struct DecodeParams {
   float sl2;  // softmax scale times log2(e)
   int n_cta, has_win;   // CTAs of the grid; whether a bf16 window is given
   int ring_off, ring_per_warp;  // shared-memory offset of the rings, entries per warp
+  // Paged cache (the kernel's PAGED variant): token t of cached KV head kvh of sequence b
+  // is row t mod 2^log2_page of page page_table[b * max_pages + t / 2^log2_page], in a
+  // pool of num_pages pages of [Hkv][2^log2_page] rows.
+  const int32_t* page_table;
+  int log2_page, max_pages, num_pages;
 };
 
 // Compile-time shape of one kernel variant.
@@ -906,9 +911,10 @@ struct SplitScan {
 };
 
 // ------------------------------------------------------------------------
-// The kernel: see the file comment. C = Cfg<BITS, KL, VL, MODE, LOG2G>.
+// The kernel: see the file comment. C = Cfg<BITS, KL, VL, MODE, LOG2G>; PAGED: the cache
+// is a page pool behind a page table (only the addresses of the bulk copies differ).
 // ------------------------------------------------------------------------
-template <class C>
+template <class C, bool PAGED>
 __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NQ = C::NQ, NO = C::NO;
   constexpr int RB = C::RB, D = kHeadDim, UNIT = C::UNIT, W = C::WARPS;
@@ -1009,25 +1015,34 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   auto bar_k = [&](int r) { return bar_w + 16u * r; };
   auto bar_v = [&](int r) { return bar_w + 16u * r + 8u; };
 
-  // Bulk copies of the K or V half of item t of pair u into entry r (lane 0 only).
+  // Bulk copies of the K or V half of item t of pair u into entry r (lane 0 only). A
+  // paged cache takes the item's page and cached KV head from the issue cursor.
+  int iss_page = 0, iss_kvh = 0;  // paged cache: the issue cursor's page and cached KV head
   auto copy_half = [&](bool v_half, int u_pair, int t, int r) {
     const int u = u_pair >> p.kv_shift;  // cached KV head (sequence-major)
     const size_t t0 = (size_t)t * UNIT;
-    const size_t row0 = (size_t)u * p.T_cap + t0;
-    const size_t blocks = (size_t)p.T_cap / C::G;
+    size_t row0, blk0;  // first code row, first channel-wise scale block
+    if constexpr (PAGED) {
+      const size_t pu = (size_t)iss_page * (p.Hkv >> p.kv_shift) + iss_kvh;
+      row0 = (pu << p.log2_page) + (t0 & ((size_t(1) << p.log2_page) - 1));
+      blk0 = row0 / C::G;
+    } else {
+      row0 = (size_t)u * p.T_cap + t0;
+      blk0 = (size_t)u * ((size_t)p.T_cap / C::G) + t0 / C::G;
+    }
     const uint32_t dst = smem_addr(ring_w + (size_t)r * C::E.bytes);
     const uint64_t pol = l2_evict_first_policy();
     fence_proxy_async_smem();  // earlier reads of the half come before its refill
     if (!v_half) {
       const uint32_t fb = bar_k(r);
-      const size_t ks0 = (KL == 0) ? row0 * C::GK : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
+      const size_t ks0 = (KL == 0) ? row0 * C::GK : blk0 * kHeadDim;
       mbar_arrive_expect_tx(fb, C::E.tx_k);
       bulk_g2s(dst, p.k_codes + row0 * RB, UNIT * RB, fb, pol);
       bulk_g2s(dst + C::E.off_ks, p.k_scale + ks0, C::E.sz_k, fb, pol);
       bulk_g2s(dst + C::E.off_kz, p.k_off + ks0, C::E.sz_k, fb, pol);
     } else {
       const uint32_t fb = bar_v(r);
-      const size_t vs0 = (VL == 0) ? row0 * C::GV : ((size_t)u * blocks + t0 / C::G) * kHeadDim;
+      const size_t vs0 = (VL == 0) ? row0 * C::GV : blk0 * kHeadDim;
       mbar_arrive_expect_tx(fb, C::E.tx_v);
       bulk_g2s(dst + C::E.off_vc, p.v_codes + row0 * RB, UNIT * RB, fb, pol);
       bulk_g2s(dst + C::E.off_vs, p.v_scale + vs0, C::E.sz_v, fb, pol);
@@ -1041,10 +1056,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   struct Cursor {
     int i, u, t, L, n;  // local item index, pair, item within the pair, pair's tokens and items
     int r;              // ring entry of the next copy or read
+    int b, kvh;         // paged cache: the pair's sequence and cached KV head
   };
   auto set_pair = [&](Cursor& k) {
-    k.L = seq_len(k.u / p.Hkv);
+    const int b = k.u / p.Hkv;
+    k.L = seq_len(b);
     k.n = items_of(k.L);
+    if constexpr (PAGED) {
+      k.b = b;
+      k.kvh = (k.u - b * p.Hkv) >> p.kv_shift;
+    }
   };
   auto advance = [&](Cursor& k, int step) {  // step items forward (only while inside the range)
     k.i += step;
@@ -1068,20 +1089,43 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     start.t = (int)(off - (long long)kv0 * n0);
     start.L = L0;
     start.n = n0;
+    start.b = ss.b0;
+    start.kvh = kv0 >> p.kv_shift;
   } else {
     start.u = n_pairs;
     start.t = 0;
     start.L = start.n = 0;
+    start.b = start.kvh = 0;
   }
   Cursor iss = start;
   advance(iss, warp);
   // The issue cursor points at this warp's next item: issue_k() sends its K half,
   // issue_v() its V half and moves on (the K half always goes first).
+  // A paged cache: lane 0 loads the page-table entry of the cursor's item when the cursor
+  // moves there, and checks it (an entry outside the pool is recorded and read as page 0)
+  // when the item's K half is issued.
   bool k_pending = false;
   int n_issued = 0;
+  auto lookup_page = [&]() {
+    if constexpr (PAGED) {
+      if (lane == 0 && iss.i < NL) {
+        iss_page = __ldg(p.page_table + (size_t)iss.b * p.max_pages + (((unsigned)iss.t * UNIT) >> p.log2_page));
+        iss_kvh = iss.kvh;
+      }
+    }
+  };
+  lookup_page();
   auto issue_k = [&]() {
     if (iss.i < NL) {
-      if (lane == 0) copy_half(false, iss.u, iss.t, iss.r);
+      if (lane == 0) {
+        if constexpr (PAGED) {
+          if (iss_page < 0 || iss_page >= p.num_pages) {
+            atomicExch(p.status, kStatusBadPage);
+            iss_page = 0;
+          }
+        }
+        copy_half(false, iss.u, iss.t, iss.r);
+      }
       k_pending = true;
     }
   };
@@ -1092,6 +1136,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     ++n_issued;
     if (++iss.r == R) iss.r = 0;
     advance(iss, W);
+    lookup_page();
   };
   if (lane == 0) {
     for (int r = 0; r < R; ++r) {

@@ -2,12 +2,16 @@
 // 2-bit codes with a channel-wise K side and a token-wise V side.
 #include "lbkv_internal.h"
 
+#ifndef LBKV_PAGED
+#define LBKV_PAGED false  // the contiguous cache (lbkv_decode_*_paged.cu: the paged one)
+#endif
+
 namespace lbkv {
 
 template <>
-DecodeKernel decode_kernel<2, 1, 0>(int mode, int log2g) {
+DecodeKernel decode_kernel<2, 1, 0, LBKV_PAGED>(int mode, int log2g) {
 #define LBKV_PICK(M, LG) \
-  if (mode == M && log2g == LG) return &split_decode_kernel<Cfg<2, 1, 0, M, LG>>;
+  if (mode == M && log2g == LG) return &split_decode_kernel<Cfg<2, 1, 0, M, LG>, LBKV_PAGED>;
   LBKV_PICK(kModeDup, 7)
   LBKV_PICK(kModePair, 7)
   LBKV_PICK(kModeDup, 6)

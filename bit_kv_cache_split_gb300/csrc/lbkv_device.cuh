@@ -15,7 +15,38 @@ enum : int32_t {
   kStatusConsumerTimeout = 1,  // a warp waited ~1 s for its own bulk copies
   kStatusDrainTimeout = 3,     // after that, the copies still in flight did not land
   kStatusAppendFull = 4,       // an appended token did not fit (capacity or window state)
+  kStatusBadPage = 5,          // a page-table entry outside the page pool (read as page 0)
 };
+
+// Where token t of KV head kvh (cache unit `unit` = b * hkv + kvh) is stored: its row of
+// codes (and of token-wise scales) and its block of channel-wise scales (one block per
+// `g` tokens). Contiguous cache (page_tokens == 0): [B][Hkv][T_cap] rows. Paged cache:
+// row t mod page_tokens of `page`, the page-table entry of t, in a pool of
+// [num_pages][Hkv][page_tokens] rows.
+struct KvAddr {
+  size_t row, block;
+};
+__device__ __forceinline__ KvAddr kv_addr(int page_tokens, int page, size_t unit, int kvh, int hkv, int T_cap, int g,
+                                          size_t t) {
+  KvAddr a;
+  if (page_tokens == 0) {
+    a.row = unit * T_cap + t;
+    a.block = unit * (size_t)(T_cap / g) + t / g;
+  } else {
+    const size_t pu = (size_t)page * hkv + kvh, off = t % (size_t)page_tokens;
+    a.row = pu * page_tokens + off;
+    a.block = pu * (size_t)(page_tokens / g) + off / g;
+  }
+  return a;
+}
+
+// The page-table entry of token t of sequence b (table [B][max_pages]), or -1 when it
+// lies outside the pool of num_pages pages.
+__device__ __forceinline__ int kv_page(const int32_t* table, int max_pages, int num_pages, int page_tokens, int b,
+                                       size_t t) {
+  const int page = __ldg(table + (size_t)b * max_pages + t / page_tokens);
+  return (page < 0 || page >= num_pages) ? -1 : page;
+}
 
 // A bounded wait gives up after this many nanoseconds of wall time.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

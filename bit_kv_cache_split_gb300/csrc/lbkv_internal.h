@@ -8,6 +8,13 @@
 
 namespace lbkv {
 
+// A paged cache (page_table != nullptr): token t of sequence b lives in page
+// page_table[b * max_pages + t / page_tokens] of a pool of num_pages pages.
+struct PagedArgs {
+  const int32_t* page_table;
+  int page_tokens, max_pages, num_pages;
+};
+
 struct PackArgs {
   const __nv_bfloat16* x;
   const int32_t* seq_lens;
@@ -15,6 +22,8 @@ struct PackArgs {
   uint8_t* codes;
   __half* scale;
   __half* off;
+  PagedArgs pg;
+  int32_t* status;  // status word, or nullptr
 };
 
 int launch_pack(const PackArgs& a, cudaStream_t stream);
@@ -34,6 +43,7 @@ struct AppendArgs {
   uint8_t* v_codes;
   __half* v_scale;
   __half* v_off;
+  PagedArgs pg;
 };
 
 int launch_append(const AppendArgs& a, cudaStream_t stream);
@@ -64,18 +74,22 @@ using DecodeKernel = void (*)(const DecodeParams);
 // pair; launched before the decode kernel when a bf16 window is present.
 int launch_window_partial(const DecodeParams& p, cudaStream_t stream);
 
-// Instantiated kernel for (column mode, log2 group) of one bit width and K/V
-// layout pair, or nullptr when that combination is not built. One translation
-// unit per specialisation.
-template <int BITS, int KL, int VL>
+// Instantiated kernel for (column mode, log2 group) of one bit width, K/V layout
+// pair and cache kind (contiguous or paged), or nullptr when that combination is not
+// built. One translation unit per specialisation.
+template <int BITS, int KL, int VL, bool PAGED>
 DecodeKernel decode_kernel(int mode, int log2g);
-template <> DecodeKernel decode_kernel<2, 0, 0>(int, int);
-template <> DecodeKernel decode_kernel<2, 0, 1>(int, int);
-template <> DecodeKernel decode_kernel<2, 1, 0>(int, int);
-template <> DecodeKernel decode_kernel<2, 1, 1>(int, int);
-template <> DecodeKernel decode_kernel<4, 0, 0>(int, int);
-template <> DecodeKernel decode_kernel<4, 0, 1>(int, int);
-template <> DecodeKernel decode_kernel<4, 1, 0>(int, int);
-template <> DecodeKernel decode_kernel<4, 1, 1>(int, int);
+#define LBKV_DECLARE_DECODE(B, K, V)                            \
+  template <> DecodeKernel decode_kernel<B, K, V, false>(int, int); \
+  template <> DecodeKernel decode_kernel<B, K, V, true>(int, int);
+LBKV_DECLARE_DECODE(2, 0, 0)
+LBKV_DECLARE_DECODE(2, 0, 1)
+LBKV_DECLARE_DECODE(2, 1, 0)
+LBKV_DECLARE_DECODE(2, 1, 1)
+LBKV_DECLARE_DECODE(4, 0, 0)
+LBKV_DECLARE_DECODE(4, 0, 1)
+LBKV_DECLARE_DECODE(4, 1, 0)
+LBKV_DECLARE_DECODE(4, 1, 1)
+#undef LBKV_DECLARE_DECODE
 
 }  // namespace lbkv

@@ -161,3 +161,55 @@ def long_context(batch: int, group: int = 128, hq_per_kv: int = 4, seed: int = 4
     """100,000-token context = 99,872 INT2 tokens + a 128-token bf16 window; 32 query heads."""
     return Workload(f"longctx-b{batch}-g{group}-gqa{hq_per_kv}", batch, 32, 32 // hq_per_kv, 99872, bits=2,
                     group=group, s_range=(0.01, 0.1), window=128, seed=seed)
+
+
+# ---------------------------------------------------------------- paged cache
+
+def page_table(lens: Sequence[int], page_tokens: int, max_pages: int, spare_pages: int = 3, seed: int = 5):
+    """A page table int32 [B][max_pages] over a shuffled pool: the pages that hold a
+    sequence's first lens[b] tokens take distinct pool pages in random order, the other
+    entries are -1. The pool has `spare_pages` unused pages besides. Returns (table,
+    num_pages)."""
+    need = [(int(L) + page_tokens - 1) // page_tokens for L in lens]
+    if any(n > max_pages for n in need):
+        raise ValueError("a sequence needs more pages than a table row holds")
+    num_pages = sum(need) + spare_pages
+    perm = np.random.default_rng(seed).permutation(num_pages)
+    table = np.full((len(lens), max_pages), -1, dtype=np.int32)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    return torch.from_numpy(table), num_pages
+
+
+def to_pages(x: torch.Tensor, table: torch.Tensor, num_pages: int, page_tokens: int, tokens_per_row: int = 1):
+    """Scatter a contiguous cache tensor [B][Hkv][R][...] (one row per `tokens_per_row`
+    tokens: 1 for codes and token-wise scales, the group for channel-wise scales) into a
+    pool [num_pages][Hkv][page_tokens / tokens_per_row][...] through the page table.
+    Pool pages that no entry names are zero."""
+    B, H, R = x.shape[:3]
+    rp = page_tokens // tokens_per_row
+    max_pages = table.shape[1]
+    if R < max_pages * rp:
+        pad = torch.zeros((B, H, max_pages * rp - R) + tuple(x.shape[3:]), dtype=x.dtype, device=x.device)
+        x = torch.cat([x, pad], dim=2)
+    xs = x[:, :, :max_pages * rp].reshape((B, H, max_pages, rp) + tuple(x.shape[3:])).transpose(1, 2)
+    pool = torch.zeros((num_pages, H, rp) + tuple(x.shape[3:]), dtype=x.dtype, device=x.device)
+    t = table.to(x.device).long()
+    bs, js = torch.nonzero(t >= 0, as_tuple=True)
+    pool[t[bs, js]] = xs[bs, js]
+    return pool
+
+
+def from_pages(pool: torch.Tensor, table: torch.Tensor, rows: int, tokens_per_row: int = 1):
+    """The inverse of to_pages: a contiguous [B][Hkv][rows][...] tensor gathered from the
+    pool (rows of -1 entries are zero)."""
+    NP, H, rp = pool.shape[:3]
+    B, max_pages = table.shape
+    out = torch.zeros((B, max_pages, H, rp) + tuple(pool.shape[3:]), dtype=pool.dtype, device=pool.device)
+    t = table.to(pool.device).long()
+    bs, js = torch.nonzero(t >= 0, as_tuple=True)
+    out[bs, js] = pool[t[bs, js]]
+    out = out.transpose(1, 2).reshape((B, H, max_pages * rp) + tuple(pool.shape[3:]))
+    return out[:, :, :rows].contiguous()

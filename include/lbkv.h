@@ -97,6 +97,19 @@ typedef struct lbkv_desc {
                             ordered (one stream); concurrent calls need their own. After
                             lbkv_device_status reports an error, zero it again. */
   size_t workspace_bytes;
+  /* Paged cache (optional; page_table NULL: the contiguous layout above). The codes,
+   * scales and offsets of every call then live in pools of pages: codes
+   * [num_pages][Hkv][page_tokens][D*bits/8], token-wise scales/offsets
+   * [num_pages][Hkv][page_tokens][D/group], channel-wise [num_pages][Hkv][page_tokens/group][D];
+   * token t of sequence b is row t mod page_tokens of page page_table[b][t / page_tokens].
+   * page_tokens is a power of two >= 128, max_seq_len <= max_pages * page_tokens, and
+   * the entries for the pages that hold a sequence's tokens lie in [0, num_pages) (an entry
+   * outside is read as page 0 and recorded as device status 5). The bf16 window, q and out
+   * are not paged. */
+  const int32_t* page_table; /* int32 [B][max_pages] device, or NULL */
+  int32_t page_tokens;
+  int32_t max_pages;
+  int32_t num_pages;
 } lbkv_desc;
 
 /* Bytes of workspace lbkv_decode_attn needs for this descriptor and format on
@@ -135,8 +148,13 @@ LBKV_API int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_
  * each operation in IEEE single precision rounded on its own. A channel-wise
  * group that ends past L_b uses only its valid tokens. Codes of tokens
  * t >= L_b are written as 0; their scales and offsets are left untouched.
- * Uses desc's batch, num_kv_heads, head_dim (128) and max_seq_len only.
- * Errors as for lbkv_decode_attn. */
+ * Paged cache (desc->page_table): x stays [B][Hkv][T_cap][D]; codes, scales and
+ * offsets are the page pools, of which only the rows of tokens t < L_b (channel-wise:
+ * the groups that hold one) are written. A token whose page-table entry lies outside
+ * the pool is not stored and, if desc->workspace is given (256-byte aligned), its
+ * status word records 5.
+ * Uses desc's batch, num_kv_heads, head_dim (128), max_seq_len, paged fields and
+ * workspace (optional). Errors as for lbkv_decode_attn. */
 LBKV_API int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_lens, int bits, int layout, int group,
               uint8_t* codes, void* scale, void* off, lbkv_stream_t stream);
 
@@ -158,9 +176,10 @@ LBKV_API int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_
  * A sequence whose token does not fit (L_b == max_seq_len; a channel-wise L_b that is
  * not a multiple of group or has no room for a group; W_b >= group) is left unchanged,
  * and if desc->workspace is given its status word records 4 (see lbkv_device_status).
- * Codes, scales and offsets as for lbkv_pack; all pointers 16-byte aligned.
- * Uses desc's batch, num_kv_heads, head_dim, max_seq_len, window fields and workspace
- * (optional). Asynchronous on `stream`. Errors as for lbkv_pack. */
+ * Codes, scales and offsets as for lbkv_pack (paged cache included: a token whose
+ * page-table entry lies outside the pool is not stored, status 5); all pointers 16-byte
+ * aligned. Uses desc's batch, num_kv_heads, head_dim, max_seq_len, window fields, paged
+ * fields and workspace (optional). Asynchronous on `stream`. Errors as for lbkv_pack. */
 LBKV_API int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int32_t* seq_lens, int bits,
                          int k_layout, int v_layout, int group, uint8_t* k_codes, void* k_scale, void* k_off,
                          uint8_t* v_codes, void* v_scale, void* v_off, lbkv_stream_t stream);
@@ -173,7 +192,8 @@ LBKV_API int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v
  *   out: bf16 [B][Hq][D]. Softmax over the first L_b tokens (zero output when L_b == 0).
  * Uses desc's batch, heads, head_dim (128), max_seq_len, sm_scale and workspace (of at
  * least lbkv_bf16_workspace_bytes bytes, 256-byte aligned, first 256 bytes zeroed once:
- * the status word). Window fields must be NULL (LBKV_EUNSUPPORTED). Hq/Hkv <= 8.
+ * the status word). Window fields and page_table must be NULL (LBKV_EUNSUPPORTED).
+ * Hq/Hkv <= 8.
  * Errors as for lbkv_decode_attn. Asynchronous on `stream`. */
 LBKV_API size_t lbkv_bf16_workspace_bytes(const lbkv_desc* desc);
 LBKV_API int lbkv_decode_bf16(const lbkv_desc* desc, const void* q, const void* k, const void* v,
