@@ -66,6 +66,7 @@ class _Args(ctypes.Structure):
         ("k_off", ctypes.c_void_p), ("v_codes", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
         ("v_off", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("k_win", ctypes.c_void_p),
         ("v_win", ctypes.c_void_p), ("win_lens", ctypes.c_void_p), ("win_cap", ctypes.c_int),
+        ("rotation", ctypes.c_int),
     ]
 
 
@@ -100,6 +101,11 @@ def lib():
                                               ctypes.c_void_p, ctypes.c_void_p]
             L.oracle_fold_kind.restype = ctypes.c_int
             L.oracle_fold_kind.argtypes = [ctypes.c_int, ctypes.c_int]
+            L.oracle_hadamard.restype = ctypes.c_int
+            L.oracle_hadamard.argtypes = [ctypes.c_int, ctypes.c_void_p]
+            L.oracle_rotate_rows.restype = ctypes.c_int
+            L.oracle_rotate_rows.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                                             ctypes.c_void_p]
             L.oracle_pack.restype = ctypes.c_int
             L.oracle_pack.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p] * 5
             _lib = L
@@ -165,7 +171,7 @@ class DecodeInputs:
 
     def __init__(self, *, q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens,
                  bits, k_layout, v_layout, group, Hkv, T_cap, sm_scale=0.0,
-                 k_win=None, v_win=None, win_lens=None, win_cap=0):
+                 k_win=None, v_win=None, win_lens=None, win_cap=0, rotation=0):
         self.q = np.ascontiguousarray(q, dtype=np.uint16)
         self.B, self.Hq, self.D = self.q.shape
         self.Hkv, self.T_cap = int(Hkv), int(T_cap)
@@ -182,13 +188,15 @@ class DecodeInputs:
         self.v_win = None if v_win is None else np.ascontiguousarray(v_win, dtype=np.uint16)
         self.win_lens = None if win_lens is None else np.ascontiguousarray(win_lens, dtype=np.int32)
         self.win_cap = int(win_cap)
+        self.rotation = int(rotation)
 
     def _struct(self) -> _Args:
         p = lambda a: None if a is None else a.ctypes.data  # noqa: E731
         return _Args(self.B, self.Hq, self.Hkv, self.D, self.T_cap, self.bits, self.k_layout,
                      self.v_layout, self.group, self.sm_scale, p(self.q), p(self.k_codes),
                      p(self.k_scale), p(self.k_off), p(self.v_codes), p(self.v_scale), p(self.v_off),
-                     p(self.seq_lens), p(self.k_win), p(self.v_win), p(self.win_lens), self.win_cap)
+                     p(self.seq_lens), p(self.k_win), p(self.v_win), p(self.win_lens), self.win_cap,
+                     self.rotation)
 
 
 def _bits16(t) -> np.ndarray:
@@ -197,7 +205,8 @@ def _bits16(t) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def inputs_from_tensors(t: dict, *, bits, k_layout, v_layout, group, Hkv, T_cap, sm_scale=0.0) -> DecodeInputs:
+def inputs_from_tensors(t: dict, *, bits, k_layout, v_layout, group, Hkv, T_cap, sm_scale=0.0,
+                        rotation=0) -> DecodeInputs:
     """Host copies of torch tensors (q, codes, fp16 scales/offsets, seq_lens, optional window)
     as oracle inputs. Only marshalling: raw bit patterns are passed through unchanged."""
     kw = {}
@@ -208,7 +217,7 @@ def inputs_from_tensors(t: dict, *, bits, k_layout, v_layout, group, Hkv, T_cap,
         q=_bits16(t["q"]), k_codes=t["k_codes"].cpu().numpy(), k_scale=_bits16(t["k_scale"]),
         k_off=_bits16(t["k_off"]), v_codes=t["v_codes"].cpu().numpy(), v_scale=_bits16(t["v_scale"]),
         v_off=_bits16(t["v_off"]), seq_lens=t["seq_lens"].cpu().numpy(), bits=bits, k_layout=k_layout,
-        v_layout=v_layout, group=group, Hkv=Hkv, T_cap=T_cap, sm_scale=sm_scale, **kw)
+        v_layout=v_layout, group=group, Hkv=Hkv, T_cap=T_cap, sm_scale=sm_scale, rotation=rotation, **kw)
 
 
 def decode_ref(x: DecodeInputs, rows=None, n_threads: int = 0) -> np.ndarray:
@@ -260,6 +269,26 @@ def decode_folded(x: DecodeInputs, block: int = 64, misorder: int = 0):
     if st != 0:
         raise ValueError(f"oracle_decode_folded rejected the arguments (status {st})")
     return out, float(ops[0]), float(ops[1])
+
+
+def hadamard(n: int) -> np.ndarray:
+    """Normalized Hadamard matrix of order n (fp64), from its closed form."""
+    out = np.zeros((n, n), dtype=np.float64)
+    if lib().oracle_hadamard(int(n), out.ctypes.data) != 0:
+        raise ValueError("n must be a power of two")
+    return out
+
+
+def rotate_rows(x_bf16_bits: np.ndarray):
+    """Rotate bf16 rows [..., n] (uint16 bits) as stored. Returns (fp32 values, bf16 bits)."""
+    x, px = _c(x_bf16_bits, np.uint16)
+    n = x.shape[-1]
+    rows = x.size // n if n else 0
+    y32 = np.zeros(x.shape, dtype=np.float32)
+    y16 = np.zeros(x.shape, dtype=np.uint16)
+    if lib().oracle_rotate_rows(px, rows, n, y32.ctypes.data, y16.ctypes.data) != 0:
+        raise ValueError("the row length must be a power of two")
+    return y32, y16
 
 
 def pack(x_bf16_bits: np.ndarray, seq_lens, bits: int, layout: int, group: int,

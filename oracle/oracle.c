@@ -22,7 +22,16 @@
  *  - codes are packed along head_dim, code i of a byte in bits [b*i, b*i+b);
  *  - query head h reads KV head h / (Hq/Hkv);
  *  - a sequence with no tokens yields an all-zero output row;
- *  - the quantizer is min/max per group with round-to-nearest-even.
+ *  - the quantizer is min/max per group with round-to-nearest-even;
+ *  - the rotation that [EXP] names as an accuracy recipe (OSCAR's rotations;
+ *    the related "KVarN -- Hadamard-rotated 2-bit KV cache" explainer) is the
+ *    normalized Hadamard matrix of order head_dim applied to each stored key
+ *    and/or value row; attention over rotated keys takes the query rotated by
+ *    the same matrix, and the output over rotated values is rotated back by it
+ *    (H is symmetric and orthogonal, so H^-1 = H);
+ *  - a row is rotated as stored in IEEE single precision by the Walsh-Hadamard
+ *    butterflies (stages of span 1, 2, 4, ...; the lower index takes a + b, the
+ *    upper a - b), scaled by fp32(1/sqrt(n)) and rounded to bf16.
  *
  * Parity status of every exported function is pinned by tests under tests/
  * (golden fixtures, closed forms, library routines, brute force); none is
@@ -125,6 +134,8 @@ static int check_args(const oracle_decode_args* a) {
     if (a->seq_lens[b] < 0 || a->seq_lens[b] > a->T_cap) return ORACLE_EINVAL;
     if (a->win_lens && (a->win_lens[b] < 0 || a->win_lens[b] > a->win_cap)) return ORACLE_EINVAL;
   }
+  if (a->rotation & ~(ORACLE_ROTATE_K | ORACLE_ROTATE_V)) return ORACLE_EINVAL;
+  if (a->rotation && (a->D & (a->D - 1))) return ORACLE_EINVAL;
   return ORACLE_OK;
 }
 
@@ -170,6 +181,35 @@ static double scale_of(const oracle_decode_args* a) {
 /* in exact arithmetic, so this is what it must reproduce).             */
 /* ------------------------------------------------------------------ */
 
+static int popcount_u32(unsigned x) {
+  int c = 0;
+  for (; x; x &= x - 1) ++c;
+  return c;
+}
+
+int oracle_hadamard(int n, double* out) {
+  if (n <= 0 || (n & (n - 1))) return ORACLE_EINVAL;
+  double inv = 1.0 / sqrt((double)n);
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j) out[(size_t)i * n + j] = (popcount_u32((unsigned)(i & j)) & 1) ? -inv : inv;
+  return ORACLE_OK;
+}
+
+/* y <- H y (fp64, n x n matrix product). */
+static void hadamard_apply(double* y, int n) {
+  double* H = (double*)malloc(sizeof(double) * n * n);
+  double* t = (double*)malloc(sizeof(double) * n);
+  oracle_hadamard(n, H);
+  for (int i = 0; i < n; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < n; ++j) acc += H[(size_t)i * n + j] * y[j];
+    t[i] = acc;
+  }
+  for (int i = 0; i < n; ++i) y[i] = t[i];
+  free(H);
+  free(t);
+}
+
 static void decode_row_ref(const oracle_decode_args* a, int b, int h, double* out) {
   int hq = a->Hq / a->Hkv;
   int kv = h / hq;
@@ -183,6 +223,8 @@ static void decode_row_ref(const oracle_decode_args* a, int b, int h, double* ou
   double* Q = (double*)malloc(sizeof(double) * D);
   double* S = (double*)malloc(sizeof(double) * n);
   for (int d = 0; d < D; ++d) Q[d] = oracle_bf16_to_f64(a->q[((size_t)b * a->Hq + h) * D + d]);
+  /* keys stored as H k: q . k = (H q) . (H k) */
+  if (a->rotation & ORACLE_ROTATE_K) hadamard_apply(Q, D);
   double sigma = scale_of(a);
 
   /* 1-3: unpack, dequantize, score. Window tokens follow the cached ones. */
@@ -212,6 +254,8 @@ static void decode_row_ref(const oracle_decode_args* a, int b, int h, double* ou
     }
   }
   for (int d = 0; d < D; ++d) out[d] /= l;
+  /* values stored as H v: sum_t p_t v_t = H (sum_t p_t H v_t) */
+  if (a->rotation & ORACLE_ROTATE_V) hadamard_apply(out, D);
   free(Q);
   free(S);
 }
@@ -497,7 +541,7 @@ static void decode_row_folded(const oracle_decode_args* a, int b, int h, int blo
 int oracle_decode_folded(const oracle_decode_args* a, int block, int misorder, double* out, double* ops) {
   int st = check_args(a);
   if (st) return st;
-  if (block <= 0) return ORACLE_EINVAL;
+  if (block <= 0 || a->rotation) return ORACLE_EINVAL;
   if ((a->k_layout == ORACLE_CHANNELWISE || a->v_layout == ORACLE_CHANNELWISE) && block % a->group) return ORACLE_EINVAL;
   ops[0] = ops[1] = 0.0;
   for (int b = 0; b < a->B; ++b)
@@ -520,6 +564,39 @@ static float bf16_to_f32(uint16_t h) {
   float f;
   memcpy(&f, &u, sizeof f);
   return f;
+}
+
+/* bf16 rounding of an fp32 value: nearest, ties to even; NaN stays NaN. */
+static uint16_t f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x0040u);
+  uint32_t lsb = (u >> 16) & 1u;
+  return (uint16_t)((u + 0x7fffu + lsb) >> 16);
+}
+
+int oracle_rotate_rows(const uint16_t* x, size_t rows, int n, float* y32, uint16_t* y16) {
+  if (n <= 0 || (n & (n - 1))) return ORACLE_EINVAL;
+  volatile float c = (float)(1.0 / sqrt((double)n));
+  float* y = (float*)malloc(sizeof(float) * n);
+  for (size_t r = 0; r < rows; ++r) {
+    for (int i = 0; i < n; ++i) y[i] = bf16_to_f32(x[r * n + i]);
+    for (int span = 1; span < n; span <<= 1)
+      for (int i = 0; i < n; ++i) {
+        if (i & span) continue;
+        volatile float lo = y[i], hi = y[i + span];
+        volatile float s = lo + hi, d = lo - hi;
+        y[i] = s;
+        y[i + span] = d;
+      }
+    for (int i = 0; i < n; ++i) {
+      volatile float v = y[i] * c;
+      if (y32) y32[r * n + i] = v;
+      if (y16) y16[r * n + i] = f32_to_bf16(v);
+    }
+  }
+  free(y);
+  return ORACLE_OK;
 }
 
 static void quantize_group(const float* x, int n, int bits, uint16_t* s_out, uint16_t* z_out, int* q_out) {
