@@ -532,6 +532,66 @@ def time_paged(device, peak, contiguous_us, page_tokens=128, calls=20):
             "device_status": status}
 
 
+def time_rotation(device, peak, contiguous_us, calls=20):
+    """A cache stored rotated: the headline workload decoded with both rotation flags (the
+    query rotated in the prologue, the output rotated back at the end), and lbkv_rotate over
+    the rows of one bf16 K side of the headline (batch 32, 8 KV heads, 32K tokens: 2.1 GB)."""
+    import bit_kv_cache_split_gb300 as pkg
+
+    wl = inputs.decode_int2(HEADLINE["batch"], HEADLINE["ctx"])
+    reps = [inputs.generate(inputs.Workload(**{**wl.__dict__, "seed": wl.seed + 1000 * i}), device) for i in range(2)]
+    n = pkg.workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.t_cap, wl.bits, wl.k_layout,
+                            wl.v_layout, wl.group)
+    ws = pkg._binding.alloc_workspace(n, device)
+    out = torch.empty((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device=device)
+    keys = ("k_codes", "k_scale", "k_off", "v_codes", "v_scale", "v_off")
+
+    def graph_time(call, n_calls):
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for i in range(n_calls):
+                    call(i)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        flush = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=device)
+        flush.zero_()
+        del flush
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n_calls
+
+    def decode(i):
+        t = reps[i % 2]
+        pkg.decode_attn(t["q"], *[t[k] for k in keys], t["seq_lens"], bits=2, group=128, rotation=3, out=out,
+                        workspace=ws)
+
+    us = graph_time(decode, calls)
+    status = pkg.device_status(ws)
+    del reps
+    torch.cuda.empty_cache()
+    x = torch.randn((wl.batch * wl.num_kv_heads * wl.t_cap, 128), device=device, dtype=torch.bfloat16)
+    y = torch.empty_like(x)
+    rot_us = graph_time(lambda i: pkg.rotate(x, out=y), 5)
+    rot_bytes = 2 * x.numel() * 2
+    del x, y
+    torch.cuda.empty_cache()
+    return {"workload": f"{wl.name}-rotated", "us_per_call": round(us, 2), "rotated_over_plain": round(us / contiguous_us, 3),
+            "device_status": status,
+            "rotate": {"rows": wl.batch * wl.num_kv_heads * wl.t_cap, "us_per_call": round(rot_us, 2),
+                       "gbs": round(rot_bytes / (rot_us * 1e-6) / 1e9, 1),
+                       "frac": round(rot_bytes / (rot_us * 1e-6) / 1e9 / peak, 4), "bytes": rot_bytes}}
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: every rank's timed region is one step of its own replica,
     and the job is done when the last one is (weak scaling, one process per GPU)."""
@@ -663,12 +723,13 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     e2e_val = job_throughput(step_bytes, e2e_ms, world)
 
-    sweep = append = bf16 = paged = None
+    sweep = append = bf16 = paged = rotation = None
     if not args.no_sweep and rank == 0:
         sweep = run_sweep(device, peak)
         append = time_append(device, peak)
         bf16 = time_bf16(device, peak, ms * 1e3)
         paged = time_paged(device, peak, ms * 1e3)
+        rotation = time_rotation(device, peak, ms * 1e3)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -702,6 +763,7 @@ def main():
             "append": append,
             "bf16_comparator": bf16,
             "paged": paged,
+            "rotation": rotation,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

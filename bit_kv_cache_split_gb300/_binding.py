@@ -19,12 +19,14 @@ from . import build as _build
 
 TOKENWISE = 0
 CHANNELWISE = 1
+ROTATE_K = 1  # keys stored rotated by the normalized Hadamard matrix (lbkv_rotation)
+ROTATE_V = 2  # values stored rotated
 
 STATUS = {0: "LBKV_OK", -1: "LBKV_EINVAL", -2: "LBKV_EALIGN", -3: "LBKV_EUNSUPPORTED",
           -4: "LBKV_EWORKSPACE", -5: "LBKV_ECUDA", -6: "LBKV_EDEVICE", -7: "LBKV_ESCRATCH"}
 
 EXPORTS = ("lbkv_workspace_bytes", "lbkv_decode_attn", "lbkv_pack", "lbkv_append", "lbkv_decode_bf16",
-           "lbkv_bf16_workspace_bytes", "lbkv_device_status",
+           "lbkv_bf16_workspace_bytes", "lbkv_rotate", "lbkv_device_status",
            "lbkv_strerror", "lbkv_decode_attn_noalloc", "lbkv_noalloc_scratch_bytes", "lbkv_selftest_wait_timeout")
 
 
@@ -43,7 +45,7 @@ class Desc(ctypes.Structure):
         ("k_win", ctypes.c_void_p), ("v_win", ctypes.c_void_p), ("win_lens", ctypes.c_void_p),
         ("win_cap", ctypes.c_int32), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("page_table", ctypes.c_void_p), ("page_tokens", ctypes.c_int32), ("max_pages", ctypes.c_int32),
-        ("num_pages", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32), ("rotation", ctypes.c_int32),
     ]
 
 
@@ -78,6 +80,8 @@ def load(path: Optional[str] = None):
         L.lbkv_bf16_workspace_bytes.argtypes = [ctypes.POINTER(Desc)]
         L.lbkv_append.restype = i32
         L.lbkv_append.argtypes = [ctypes.POINTER(Desc), vp, vp, vp] + [i32] * 4 + [vp] * 7
+        L.lbkv_rotate.restype = i32
+        L.lbkv_rotate.argtypes = [vp, vp, ctypes.c_int64, i32, vp]
         L.lbkv_selftest_wait_timeout.restype = i32
         L.lbkv_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
         L.lbkv_device_status.restype = i32
@@ -176,13 +180,15 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 def decode_attn(q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, *, bits, k_layout=TOKENWISE,
                 v_layout=TOKENWISE, group=128, sm_scale=0.0, k_win=None, v_win=None, win_lens=None,
-                page_table=None, max_seq_len=None, out=None, workspace=None, stream=None) -> torch.Tensor:
+                page_table=None, max_seq_len=None, rotation=0, out=None, workspace=None,
+                stream=None) -> torch.Tensor:
     """Decode attention through lbkv_decode_attn. Shapes as in include/lbkv.h.
 
     q bf16 [B][Hq][D]; k_codes/v_codes uint8 [B][Hkv][T_cap][D*bits/8]; scales/offsets fp16;
     seq_lens int32 [B] on the device. Returns out bf16 [B][Hq][D] (allocated when not given).
     Paged cache: page_table int32 [B][max_pages]; the cache tensors are page pools
     ([num_pages][Hkv][page_tokens]...) and max_seq_len defaults to max_pages * page_tokens.
+    rotation: ROTATE_K | ROTATE_V bits of a cache (and window) stored rotated (see rotate).
     """
     B, Hq, D = q.shape
     Hkv, T = k_codes.shape[1], k_codes.shape[2]
@@ -209,6 +215,7 @@ def decode_attn(q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, *
             raise LbkvError(-3 if bits in (2, 4) else -1, "lbkv_workspace_bytes")
         workspace = alloc_workspace(n, q.device)
     d = make_desc(B, Hq, Hkv, T, D, sm_scale, k_win, v_win, win_lens, workspace)
+    d.rotation = int(rotation)
     if page_table is not None:
         _set_paged(d, page_table, P, NP)
     st = L.lbkv_decode_attn(ctypes.byref(d), _ptr(q), _ptr(k_codes), _ptr(k_scale), _ptr(k_off), _ptr(v_codes),
@@ -257,11 +264,12 @@ def pack(x, seq_lens, *, bits, layout=TOKENWISE, group=128, codes=None, scale=No
 
 def append(k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_off, *, bits, k_layout=TOKENWISE,
            v_layout=TOKENWISE, group=128, k_win=None, v_win=None, win_lens=None, page_table=None, max_seq_len=None,
-           workspace=None, stream=None):
+           rotation=0, workspace=None, stream=None):
     """Append the new token k_new/v_new bf16 [B][Hkv][D] through lbkv_append (quantize-on-append).
 
     The cache tensors, seq_lens (and win_lens with the window) are updated in place. Paged
-    cache: page_table int32 [B][max_pages] and page pools, as for decode_attn."""
+    cache: page_table int32 [B][max_pages] and page pools, as for decode_attn. rotation: the sides
+    stored rotated (ROTATE_K | ROTATE_V), rotated on the way in."""
     _check(k_new, "k_new", torch.bfloat16)
     B, Hkv, D = k_new.shape
     _check(v_new, "v_new", torch.bfloat16, (B, Hkv, D))
@@ -279,6 +287,7 @@ def append(k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_
         _check(v_win, "v_win", torch.bfloat16, tuple(k_win.shape))
         _check(win_lens, "win_lens", torch.int32, (B,))
     d = make_desc(B, Hkv, Hkv, T, D, k_win=k_win, v_win=v_win, win_lens=win_lens, workspace=workspace)
+    d.rotation = int(rotation)
     if page_table is not None:
         _set_paged(d, page_table, P, NP)
     st = load().lbkv_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _ptr(seq_lens), int(bits), int(k_layout),
@@ -286,6 +295,21 @@ def append(k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_
                             _ptr(v_scale), _ptr(v_off), _stream_ptr(stream))
     if st != 0:
         raise LbkvError(st, "lbkv_append")
+
+
+def rotate(x, out=None, stream=None):
+    """Rows of bf16 x [..., 128] rotated by the normalized Hadamard matrix (lbkv_rotate):
+    the step that stores a cache rotated. out may be x itself (in place)."""
+    _check(x, "x", torch.bfloat16)
+    if out is None:
+        out = torch.empty_like(x)
+    _check(out, "out", torch.bfloat16, tuple(x.shape))
+    D = x.shape[-1] if x.dim() else 0
+    rows = x.numel() // D if D else 0
+    st = load().lbkv_rotate(_ptr(x), _ptr(out), int(rows), int(D), _stream_ptr(stream))
+    if st != 0:
+        raise LbkvError(st, "lbkv_rotate")
+    return out
 
 
 def decode_bf16(q, k, v, seq_lens, *, sm_scale=0.0, out=None, workspace=None, stream=None):

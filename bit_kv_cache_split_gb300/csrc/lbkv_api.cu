@@ -96,6 +96,7 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   if (win != (d->v_win != nullptr) || win != (d->win_lens != nullptr)) return LBKV_EINVAL;
   if (win && (d->win_cap <= 0 || d->win_cap > 128)) return LBKV_EINVAL;
   if (int st = paged_check(d)) return st;
+  if (d->rotation & ~(LBKV_ROTATE_K | LBKV_ROTATE_V)) return LBKV_EINVAL;
   // PV columns are (query, V channel group) pairs: a token-wise V side with G channel
   // groups feeds G separately scaled copies of the weights (operand-fold); the kernel
   // holds at most two PV n-tiles of 8 columns.
@@ -223,6 +224,7 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.has_win = pl.win;
   p.ring_off = pl.ring_off;
   p.ring_per_warp = pl.ring_per_warp;
+  p.rotation = desc->rotation;
   p.page_table = desc->page_table;
   if (desc->page_table) {
     p.log2_page = 0;
@@ -280,6 +282,7 @@ int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int
   if (win != (desc->v_win != nullptr) || win != (desc->win_lens != nullptr)) return LBKV_EINVAL;
   if (windowed && (!win || desc->win_cap < group || desc->win_cap > 128)) return LBKV_EINVAL;
   if (int st = paged_check(desc)) return st;
+  if (desc->rotation & ~(LBKV_ROTATE_K | LBKV_ROTATE_V)) return LBKV_EINVAL;
   if (desc->batch == 0) return LBKV_OK;
   const void* ptrs[] = {k_new, v_new, seq_lens, k_codes, k_scale, k_off, v_codes, v_scale, v_off};
   for (const void* p : ptrs)
@@ -312,6 +315,7 @@ int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int
   a.v_scale = static_cast<__half*>(v_scale);
   a.v_off = static_cast<__half*>(v_off);
   a.pg = paged_args(desc);
+  a.rotation = desc->rotation;
   if (launch_append(a, reinterpret_cast<cudaStream_t>(stream)) != 0) return LBKV_ECUDA;
   return LBKV_OK;
 }
@@ -355,13 +359,25 @@ static int bf16_layout(const lbkv_desc* d, size_t* off_ml, size_t* off_o, size_t
   const int hq = d->num_q_heads / d->num_kv_heads;
   if (hq > kMaxHq) return LBKV_EUNSUPPORTED;
   if (d->k_win || d->v_win || d->win_lens) return LBKV_EUNSUPPORTED;  // the comparator has no window
-  if (d->page_table) return LBKV_EUNSUPPORTED;                         // nor a paged cache
+  if (d->page_table || d->rotation) return LBKV_EUNSUPPORTED;          // nor a paged or rotated cache
   if ((long long)d->batch * d->num_kv_heads * d->max_seq_len >= (1ll << 31)) return LBKV_EUNSUPPORTED;  // TMA rows
   *max_chunks = (d->max_seq_len + kBfChunk - 1) / kBfChunk;
   const size_t rows = (size_t)d->batch * d->num_kv_heads * (size_t)*max_chunks * hq;
   *off_ml = 256;
   *off_o = round_up(*off_ml + rows * sizeof(float2), 256);
   *bytes = round_up(*off_o + rows * kHeadDim * sizeof(float), 256);
+  return LBKV_OK;
+}
+
+int lbkv_rotate(const void* x, void* y, int64_t rows, int head_dim, lbkv_stream_t stream) {
+  if (head_dim != kHeadDim) return LBKV_EUNSUPPORTED;
+  if (rows < 0 || rows > (int64_t)0x7fffffff * 8) return LBKV_EINVAL;
+  if (rows == 0) return LBKV_OK;
+  if (!x || !y) return LBKV_EINVAL;
+  if (!aligned16(x) || !aligned16(y)) return LBKV_EALIGN;
+  if (launch_rotate(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), (long long)rows,
+                    reinterpret_cast<cudaStream_t>(stream)) != 0)
+    return LBKV_ECUDA;
   return LBKV_OK;
 }
 

@@ -9,11 +9,19 @@
 // token waits in the bf16 window (attended like any window token) until g tokens have
 // gathered; they are then quantized as one group at positions L_b .. L_b + g - 1 and the
 // window empties. When either side is channel-wise, both sides take the window route,
-// so that the cache and the window always hold the same tokens for K and V.
+// so that the cache and the window always hold the same tokens for K and V. A side
+// stored rotated (lbkv_rotate) is rotated on the way in: the window holds it rotated too.
 #include "lbkv_internal.h"
 #include "lbkv_quant.cuh"
 
 namespace lbkv {
+
+// The new token row rotated by H and rounded to bf16, as stored (channels 4 lane .. +3).
+__device__ __forceinline__ void rotate_bf16(float (&v)[4], int lane) {
+  hadamard128(v, lane);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) v[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+}
 
 constexpr int kAppendThreads = 512;  // 16 warps: the 2 Hkv rows of a token at once (Hkv <= 8)
 constexpr int kAppendWarps = kAppendThreads / 32;
@@ -101,25 +109,39 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
       const size_t unit = (size_t)b * a.Hkv + kvh;
       const size_t crow = append_addr(a, page, b, kvh, L).row;
       const size_t si = crow * (kHeadDim / a.group);
-      const __nv_bfloat16* x = (side ? a.v_new : a.k_new) + unit * kHeadDim;
+      float v[4];
+      load_row4((side ? a.v_new : a.k_new) + unit * kHeadDim, lane, v);
+      if (a.rotation & (1 << side)) rotate_bf16(v, lane);
       if (side)
-        quantize_token_row<BITS>(x, a.group, a.v_codes + crow * RB, a.v_scale + si, a.v_off + si, lane);
+        quantize_token_vals<BITS>(v, a.group, a.v_codes + crow * RB, a.v_scale + si, a.v_off + si, lane);
       else
-        quantize_token_row<BITS>(x, a.group, a.k_codes + crow * RB, a.k_scale + si, a.k_off + si, lane);
+        quantize_token_vals<BITS>(v, a.group, a.k_codes + crow * RB, a.k_scale + si, a.k_off + si, lane);
     }
     __syncthreads();
     if (threadIdx.x == 0) a.seq_lens[b] = L + 1;
     return;
   }
 
-  // the token into window slot W (both sides), 8 bf16 per thread and step
-  for (int idx = threadIdx.x; idx < 2 * a.Hkv * (kHeadDim / 8); idx += kAppendThreads) {
-    const int side = idx / (a.Hkv * (kHeadDim / 8));
-    const int rem = idx - side * a.Hkv * (kHeadDim / 8);
-    const int kvh = rem / (kHeadDim / 8), k8 = rem % (kHeadDim / 8);
-    const size_t unit = (size_t)b * a.Hkv + kvh;
-    const uint4 v = reinterpret_cast<const uint4*>((side ? a.v_new : a.k_new) + unit * kHeadDim)[k8];
-    reinterpret_cast<uint4*>((side ? a.v_win : a.k_win) + (unit * a.win_cap + W) * kHeadDim)[k8] = v;
+  // the token into window slot W (both sides), 8 bf16 per thread and step; a side stored
+  // rotated goes in rotated (one warp per row)
+  if (a.rotation) {
+    for (int row = warp; row < 2 * a.Hkv; row += kAppendWarps) {
+      const int kvh = row >> 1, side = row & 1;
+      const size_t unit = (size_t)b * a.Hkv + kvh;
+      float v[4];
+      load_row4((side ? a.v_new : a.k_new) + unit * kHeadDim, lane, v);
+      if (a.rotation & (1 << side)) hadamard128(v, lane);
+      store_row4((side ? a.v_win : a.k_win) + (unit * a.win_cap + W) * kHeadDim, lane, v);
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < 2 * a.Hkv * (kHeadDim / 8); idx += kAppendThreads) {
+      const int side = idx / (a.Hkv * (kHeadDim / 8));
+      const int rem = idx - side * a.Hkv * (kHeadDim / 8);
+      const int kvh = rem / (kHeadDim / 8), k8 = rem % (kHeadDim / 8);
+      const size_t unit = (size_t)b * a.Hkv + kvh;
+      const uint4 v = reinterpret_cast<const uint4*>((side ? a.v_new : a.k_new) + unit * kHeadDim)[k8];
+      reinterpret_cast<uint4*>((side ? a.v_win : a.k_win) + (unit * a.win_cap + W) * kHeadDim)[k8] = v;
+    }
   }
   if (!s_flush) {
     __syncthreads();

@@ -146,6 +146,10 @@ struct DecodeParams {
   // pool of num_pages pages of [Hkv][2^log2_page] rows.
   const int32_t* page_table;
   int log2_page, max_pages, num_pages;
+  // Rotated cache: bit 0, the keys (cache and window) are stored as H k, so the scores
+  // take H q; bit 1, the values are stored as H v, so the output is rotated back by H
+  // (H: the normalized Hadamard matrix, symmetric and orthogonal).
+  int rotation;
 };
 
 // Compile-time shape of one kernel variant.
@@ -947,6 +951,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   // its pairs.
   auto seq_len = [&](int b) { return min(max(__ldg(p.seq_lens + b), 0), p.T_cap); };
   auto items_of = [&](int L) { return (L + UNIT - 1) / UNIT; };
+  // Values stored rotated: n output rows staged in fp32 in shared memory, rotated back by H
+  // and written as the bf16 output rows out_row0 .. out_row0 + n - 1 (one warp per row).
+  auto rotate_out_rows = [&](const float* rows, int n, size_t out_row0) {
+    for (int i = warp; i < n; i += W) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = rows[i * D + 4 * lane + e];
+      hadamard128(v, lane);
+      store_row4(p.out + (out_row0 + i) * D, lane, v);
+    }
+  };
 
   // ---------------------------------------------------- the CTA's share of the items
   {
@@ -1170,9 +1185,21 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS)
       sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
     __syncthreads();
+    if (p.rotation & 1) {  // keys stored rotated: the scores take H q
+      for (int i = warp; i < hq; i += W) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = sQ[i * D + 4 * lane + e];
+        hadamard128(v, lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sQ[i * D + 4 * lane + e] = v[e];
+      }
+      __syncthreads();
+    }
     if (warp < hq) {
       // query exponent e: max |Q / factor| * 2^e in [2^13, 2^14), so Q * 2^e / factor is an
-      // exact fp16 (a bf16 has 8 significant bits); channel-group sums of Q for the K offset
+      // exact fp16 for a bf16 query (8 significant bits; a rotated query is rounded there);
+      // channel-group sums of Q for the K offset
       const int i = warp;
       float amax = 0.f;
       float gs = 0.f;
@@ -1216,7 +1243,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
 
     WarpState<C> st;
     if (KL == 0) {
-      // token-wise K: B fragments Q' = Q 2^e / factor (exact fp16) of column g, the same for
+      // token-wise K: B fragments Q' = Q 2^e / factor (fp16; exact for a bf16 query) of column g, the same for
       // every warp, formed once: warp ks < 8 the k-step ks; then minus the magic bias 1024 *
       // sum of Q' per channel group of each column
       if (warp < 8) {
@@ -1235,7 +1262,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
             xx[e] = live ? sQ[qb * D + ch] * sc * k_rmult<C>(ch) : 0.f;
           }
           qbw[r] = f16x2_from(xx[0], xx[1]);
-          part += xx[0] + xx[1];
+          // the bias is taken from the fp16 values actually fed, so that it cancels exactly
+          // also when Q' is not an exact fp16 (a rotated query)
+          const float2 f = half2_to_float2(qbw[r]);
+          part += f.x + f.y;
         }
         sqb[ks * 32 + lane] = make_uint2(qbw[0], qbw[1]);
         sPart[ks * 32 + lane] = part;
@@ -1466,12 +1496,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
             lt = a * lt + bw * wml.y;
           }
         }
-        p.out[((size_t)b * p.Hq + kvh * hq + i) * D + ch] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
+        const float o = lt > 0.f ? acc / lt : 0.f;
+        if (p.rotation & 2)
+          sQ[idx] = o;  // rotated back below
+        else
+          p.out[((size_t)b * p.Hq + kvh * hq + i) * D + ch] = __float2bfloat16_rn(o);
       } else {
         const size_t prow = ((size_t)cta * 2 + slot_of(cta)) * hq + i;
         p.part_o[prow * D + ch] = acc;
         if (ch == 0) p.part_ml[prow] = make_float2(M, lt);
       }
+    }
+    if (alone && (p.rotation & 2)) {
+      __syncthreads();
+      rotate_out_rows(sQ, hq, (size_t)b * p.Hq + kvh * hq);
     }
     if (!alone) {
       // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s (zero when no token at all)
@@ -1531,7 +1569,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
             acc = fmaf(sc, __ldcg(k == n_span ? &p.win_o[r * D + ch] : &p.part_o[r * D + ch]), acc);
           }
           const float l = s_l[i];
-          p.out[((size_t)b * p.Hq + kvh * hq + i) * D + ch] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
+          const float o = l > 0.f ? acc / l : 0.f;
+          if (p.rotation & 2)
+            sQ[idx] = o;  // rotated back below
+          else
+            p.out[((size_t)b * p.Hq + kvh * hq + i) * D + ch] = __float2bfloat16_rn(o);
+        }
+        if (p.rotation & 2) {
+          __syncthreads();
+          rotate_out_rows(sQ, hq, (size_t)b * p.Hq + kvh * hq);
         }
         if (threadIdx.x == 0) p.done[u] = 0;  // ready for the next call in stream order
       }
@@ -1552,6 +1598,22 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   // Their output is the window's attention alone, or zero.
   for (int bq = cta; bq < p.B; bq += p.n_cta) {
     if (seq_len(bq) != 0) continue;
+    if (p.rotation & 2) {  // values stored rotated: each output row is rotated back
+      for (int r = warp; r < p.Hq; r += W) {
+        const size_t row = (size_t)bq * p.Hq + r;  // the window partial row is the output row
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (p.has_win) {
+          const float2 ml = __ldcg(&p.win_ml[row]);
+          if (ml.y > 0.f) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = __ldcg(&p.win_o[row * D + 4 * lane + e]) / ml.y;
+          }
+        }
+        hadamard128(v, lane);
+        store_row4(p.out + row * D, lane, v);
+      }
+      continue;
+    }
     for (int idx = threadIdx.x; idx < p.Hkv * hq * D; idx += C::THREADS) {
       const int kv = idx / (hq * D), i = (idx / D) % hq, ch = idx % D;
       float o = 0.f;

@@ -18,6 +18,48 @@ enum : int32_t {
   kStatusBadPage = 5,          // a page-table entry outside the page pool (read as page 0)
 };
 
+// Normalized Hadamard rotation of a 128-channel row held by a warp, 4 channels per lane
+// (lane l: channels 4l .. 4l + 3), in place. The butterflies run in stages of span 1, 2,
+// 4, ..., 64; in each, the lower channel of a pair takes a + b and the upper a - b (a the
+// lower's value, b the upper's); then every channel is scaled by fp32(1/sqrt(128)). Each
+// step is one IEEE single-precision operation, so the result is the same bits whatever the
+// hardware. The matrix is symmetric and orthogonal: applying it twice gives the row back.
+__device__ __forceinline__ void hadamard128(float (&v)[4], int lane) {
+  float a, b;
+  a = v[0], b = v[1], v[0] = __fadd_rn(a, b), v[1] = __fsub_rn(a, b);  // span 1
+  a = v[2], b = v[3], v[2] = __fadd_rn(a, b), v[3] = __fsub_rn(a, b);
+  a = v[0], b = v[2], v[0] = __fadd_rn(a, b), v[2] = __fsub_rn(a, b);  // span 2
+  a = v[1], b = v[3], v[1] = __fadd_rn(a, b), v[3] = __fsub_rn(a, b);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {  // span 4m: the partner channel is in lane l ^ m
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[u], m);
+      v[u] = upper ? __fsub_rn(o, v[u]) : __fadd_rn(v[u], o);
+    }
+  }
+  const float c = __uint_as_float(0x3db504f3u);  // 1/sqrt(128) rounded to fp32
+#pragma unroll
+  for (int u = 0; u < 4; ++u) v[u] = __fmul_rn(v[u], c);
+}
+
+// Channels 4 lane .. 4 lane + 3 of a bf16 row, as fp32.
+__device__ __forceinline__ void load_row4(const __nv_bfloat16* row, int lane, float (&v)[4]) {
+  const uint2 raw = reinterpret_cast<const uint2*>(row)[lane];
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  const float2 a = __bfloat1622float2(h[0]), c = __bfloat1622float2(h[1]);
+  v[0] = a.x, v[1] = a.y, v[2] = c.x, v[3] = c.y;
+}
+
+// The same four channels rounded to bf16 (nearest, ties to even) into a bf16 row.
+__device__ __forceinline__ void store_row4(__nv_bfloat16* row, int lane, const float (&v)[4]) {
+  __nv_bfloat162 h[2];
+  h[0] = __floats2bfloat162_rn(v[0], v[1]);
+  h[1] = __floats2bfloat162_rn(v[2], v[3]);
+  reinterpret_cast<uint2*>(row)[lane] = *reinterpret_cast<const uint2*>(h);
+}
+
 // Where token t of KV head kvh (cache unit `unit` = b * hkv + kvh) is stored: its row of
 // codes (and of token-wise scales) and its block of channel-wise scales (one block per
 // `g` tokens). Contiguous cache (page_tokens == 0): [B][Hkv][T_cap] rows. Paged cache:

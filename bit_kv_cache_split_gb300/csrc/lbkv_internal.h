@@ -44,9 +44,13 @@ struct AppendArgs {
   __half* v_scale;
   __half* v_off;
   PagedArgs pg;
+  int rotation;  // bit 0: store the new K rotated, bit 1: the new V
 };
 
 int launch_append(const AppendArgs& a, cudaStream_t stream);
+
+// y[r] = bf16(H x[r]) for rows of 128 channels (H: the normalized Hadamard matrix).
+int launch_rotate(const __nv_bfloat16* x, __nv_bfloat16* y, long long rows, cudaStream_t stream);
 
 // BF16 comparator: tokens per chunk (one CTA each), and the arguments of its two kernels.
 constexpr int kBfChunk = 512;

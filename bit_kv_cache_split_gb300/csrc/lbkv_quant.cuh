@@ -22,16 +22,12 @@ __device__ __forceinline__ int quantize_one(float x, float zf, float sf, int qma
   return r < 0.f ? 0 : (r > (float)qmax ? qmax : (int)r);
 }
 
-// One warp quantizes one token row x[D] with token-wise groups of `group` channels:
-// codes into crow[D * BITS / 8], the group's scale and offset into srow/zrow[D / group].
-// Lane l holds channels 4l..4l+3; a group is group/4 consecutive lanes.
+// One warp quantizes one token row with token-wise groups of `group` channels, given as
+// the fp32 values of channels 4 lane .. 4 lane + 3 in v: codes into crow[D * BITS / 8],
+// the group's scale and offset into srow/zrow[D / group]. A group is group/4 consecutive lanes.
 template <int BITS>
-__device__ __forceinline__ void quantize_token_row(const __nv_bfloat16* __restrict__ x, int group, uint8_t* crow,
-                                                   __half* srow, __half* zrow, int lane) {
-  const uint2 raw = reinterpret_cast<const uint2*>(x)[lane];
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-  const float2 a = __bfloat1622float2(h[0]), c = __bfloat1622float2(h[1]);
-  const float v[4] = {a.x, a.y, c.x, c.y};
+__device__ __forceinline__ void quantize_token_vals(const float (&v)[4], int group, uint8_t* crow, __half* srow,
+                                                    __half* zrow, int lane) {
   float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
   float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
   const int lanes = group / 4;
@@ -56,6 +52,15 @@ __device__ __forceinline__ void quantize_token_row(const __nv_bfloat16* __restri
     srow[lane / lanes] = sh;
     zrow[lane / lanes] = zh;
   }
+}
+
+// The same for the bf16 token row x[D].
+template <int BITS>
+__device__ __forceinline__ void quantize_token_row(const __nv_bfloat16* __restrict__ x, int group, uint8_t* crow,
+                                                   __half* srow, __half* zrow, int lane) {
+  float v[4];
+  load_row4(x, lane, v);
+  quantize_token_vals<BITS>(v, group, crow, srow, zrow, lane);
 }
 
 // Thread d of 128 (channel d) quantizes channel d over one channel-wise token group:

@@ -1,7 +1,8 @@
 // lbkv_window.cu -- attention of each (sequence, KV head) pair's queries over its
 // full-precision bf16 window (the most recent tokens, kept unquantized after the
 // cached ones), written as one partial (m, l, O) per pair; the decode kernel merges
-// it with the cached tokens' partials.
+// it with the cached tokens' partials. A rotated cache keeps its window rotated too, so
+// the partial is in the same (rotated) basis as the cached tokens' partials.
 #include "lbkv_internal.h"
 
 namespace lbkv {
@@ -21,6 +22,17 @@ __global__ void __launch_bounds__(32 * kWinWarps, 1) window_partial_kernel(const
   for (int idx = threadIdx.x; idx < hq * D; idx += 32 * kWinWarps)
     sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
   __syncthreads();
+  if (p.rotation & 1) {  // window keys stored rotated like the cache's: the scores take H q
+    for (int i = warp; i < hq; i += kWinWarps) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = sQ[i * D + 4 * lane + e];
+      hadamard128(v, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sQ[i * D + 4 * lane + e] = v[e];
+    }
+    __syncthreads();
+  }
 
   // warp w scores tokens w, w + W, ...; lane holds channels 4 lane .. 4 lane + 3
   const int W = min(max(p.win_lens[b], 0), p.win_cap);

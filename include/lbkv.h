@@ -66,6 +66,17 @@ typedef enum {
   LBKV_CHANNELWISE = 1  /* a group is `group` consecutive tokens of one channel */
 } lbkv_layout;
 
+/* Rotated cache (lbkv_desc.rotation): the stored rows of a side were rotated over head_dim
+ * by the normalized Hadamard matrix H, H[i][j] = (-1)^popcount(i & j) / sqrt(128), as an
+ * accuracy recipe for 2-bit caches (OSCAR's rotations, accuracy paragraph of the explainer
+ * "FOSCAR speeds up 2-bit KV decode"; the explainer "KVarN -- Hadamard-rotated 2-bit KV
+ * cache"). H is symmetric and orthogonal, so decode folds it into the query (keys) and
+ * the output (values): q . k = (H q) . (H k), and sum_t p_t v_t = H sum_t p_t (H v_t). */
+typedef enum {
+  LBKV_ROTATE_K = 1, /* keys stored as H k (cache and window) */
+  LBKV_ROTATE_V = 2  /* values stored as H v (cache and window) */
+} lbkv_rotation;
+
 typedef enum {
   LBKV_OK = 0,
   LBKV_EINVAL = -1,        /* a null pointer, a bad size or an out-of-range argument */
@@ -110,6 +121,7 @@ typedef struct lbkv_desc {
   int32_t page_tokens;
   int32_t max_pages;
   int32_t num_pages;
+  int32_t rotation; /* lbkv_rotation bits of the stored rows, 0 for none (see above) */
 } lbkv_desc;
 
 /* Bytes of workspace lbkv_decode_attn needs for this descriptor and format on
@@ -132,6 +144,9 @@ LBKV_API size_t lbkv_workspace_bytes(const lbkv_desc* desc, int bits, int k_layo
  * query enters exactly (fp16; rounded to fp16 after a channel-wise K scale
  * multiplies it) and the softmax weights as fp16; accumulation and every fold
  * step in fp32; output rounded to bf16.
+ * Rotated cache (desc->rotation): the query is rotated by H in fp32 before the scores
+ * (LBKV_ROTATE_K) and the output rotated back by H in fp32 before its bf16 rounding
+ * (LBKV_ROTATE_V); the window must be stored the same way.
  * Errors: LBKV_EINVAL / LBKV_EALIGN / LBKV_EUNSUPPORTED / LBKV_EWORKSPACE before
  * any launch; LBKV_ECUDA on a launch failure. A sequence with no cached and no
  * window tokens yields a zero output row. */
@@ -176,13 +191,27 @@ LBKV_API int lbkv_pack(const lbkv_desc* desc, const void* x, const int32_t* seq_
  * A sequence whose token does not fit (L_b == max_seq_len; a channel-wise L_b that is
  * not a multiple of group or has no room for a group; W_b >= group) is left unchanged,
  * and if desc->workspace is given its status word records 4 (see lbkv_device_status).
+ * A side named in desc->rotation is rotated on the way in, as lbkv_rotate does, into the
+ * cache and the window alike.
  * Codes, scales and offsets as for lbkv_pack (paged cache included: a token whose
  * page-table entry lies outside the pool is not stored, status 5); all pointers 16-byte
  * aligned. Uses desc's batch, num_kv_heads, head_dim, max_seq_len, window fields, paged
- * fields and workspace (optional). Asynchronous on `stream`. Errors as for lbkv_pack. */
+ * fields, rotation and workspace (optional). Asynchronous on `stream`. Errors as for lbkv_pack. */
 LBKV_API int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int32_t* seq_lens, int bits,
                          int k_layout, int v_layout, int group, uint8_t* k_codes, void* k_scale, void* k_off,
                          uint8_t* v_codes, void* v_scale, void* v_off, lbkv_stream_t stream);
+
+/* Rotate bf16 rows of head_dim = 128 channels by the normalized Hadamard matrix H (see
+ * lbkv_rotation): y[r] = bf16(H x[r]) for r < rows, the step before lbkv_pack for a cache
+ * stored rotated. Computed as the Walsh-Hadamard butterflies in IEEE single precision
+ * (stages of span 1, 2, 4, ..., 64; the lower channel of a pair takes a + b, the upper
+ * a - b), each value then scaled by fp32(1/sqrt(128)) and rounded to bf16 (nearest, ties
+ * to even), so the bits do not depend on the GPU.
+ *   x, y: bf16 [rows][128] device, 16-byte aligned; y == x rotates in place (other
+ *   overlaps are not allowed). rows >= 0.
+ * Asynchronous on `stream`. Errors: LBKV_EINVAL (null pointer, rows < 0),
+ * LBKV_EUNSUPPORTED (head_dim != 128), LBKV_EALIGN, LBKV_ECUDA. */
+LBKV_API int lbkv_rotate(const void* x, void* y, int64_t rows, int head_dim, lbkv_stream_t stream);
 
 /* BF16 comparator: the same split-KV decode attention over a bf16 cache, without
  * quantization, so that the speedup that "FOSCAR: Accelerating Decode Attention over 2-
@@ -192,7 +221,8 @@ LBKV_API int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v
  *   out: bf16 [B][Hq][D]. Softmax over the first L_b tokens (zero output when L_b == 0).
  * Uses desc's batch, heads, head_dim (128), max_seq_len, sm_scale and workspace (of at
  * least lbkv_bf16_workspace_bytes bytes, 256-byte aligned, first 256 bytes zeroed once:
- * the status word). Window fields and page_table must be NULL (LBKV_EUNSUPPORTED).
+ * the status word). Window fields and page_table must be NULL and rotation 0
+ * (LBKV_EUNSUPPORTED).
  * Hq/Hkv <= 8.
  * Errors as for lbkv_decode_attn. Asynchronous on `stream`. */
 LBKV_API size_t lbkv_bf16_workspace_bytes(const lbkv_desc* desc);
