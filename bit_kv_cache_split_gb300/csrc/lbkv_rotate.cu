@@ -7,20 +7,28 @@
 
 namespace lbkv {
 
-// One warp per row: y[r] = bf16(H x[r]) (x and y may be the same array).
+constexpr int kRotRows = 4;  // rows per warp: their loads are all in flight before the first butterfly
+
+// Each warp rotates rows r0 .. r0 + kRotRows - 1: y[r] = bf16(H x[r]) (x and y may be the
+// same array: a row is read whole before it is written, by the same warp).
 __global__ void __launch_bounds__(256) rotate_rows_kernel(const __nv_bfloat16* x, __nv_bfloat16* y, long long rows) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long r0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRotRows;
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;  // the whole warp leaves together
-  float v[4];
-  load_row4(x + row * kHeadDim, lane, v);
-  hadamard128(v, lane);
-  store_row4(y + row * kHeadDim, lane, v);
+  float v[kRotRows][4];
+#pragma unroll
+  for (int k = 0; k < kRotRows; ++k)
+    if (r0 + k < rows) load_row4(x + (r0 + k) * kHeadDim, lane, v[k]);  // the whole warp takes a row or not
+#pragma unroll
+  for (int k = 0; k < kRotRows; ++k) {
+    if (r0 + k >= rows) break;
+    hadamard128(v[k], lane);
+    store_row4(y + (r0 + k) * kHeadDim, lane, v[k]);
+  }
 }
 
 int launch_rotate(const __nv_bfloat16* x, __nv_bfloat16* y, long long rows, cudaStream_t stream) {
   if (rows == 0) return 0;
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  const unsigned blocks = (unsigned)((rows + 8 * kRotRows - 1) / (8 * kRotRows));
   rotate_rows_kernel<<<blocks, 256, 0, stream>>>(x, y, rows);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
