@@ -174,3 +174,30 @@ def test_append_misaligned_pointer(lib):
 
 def test_append_empty_batch_is_a_no_op(lib):
     assert _append(lib, _desc(B=0), (2, 0, 0, 128)) == 0
+
+
+@pytest.mark.parametrize("args,want", [
+    ((4096, 4096, -1, 128), -1),     # negative row count
+    ((4096, 4096, 8, 64), -3),       # head_dim
+    ((0, 4096, 8, 128), -1),         # null input
+    ((4096, 0, 8, 128), -1),         # null output
+    ((4100, 4096, 8, 128), -2),      # misaligned
+    ((0, 0, 0, 128), 0),             # no rows: nothing to do
+])
+def test_rotate_arguments_rejected_before_launch(lib, args, want):
+    x, y, rows, d = args
+    assert lib.lbkv_rotate(ctypes.c_void_p(x), ctypes.c_void_p(y), ctypes.c_int64(rows), d, ctypes.c_void_p(0)) == want
+
+
+def test_rotation_flags_validated(lib):
+    null = ctypes.c_void_p(0)
+    d = _desc()
+    d.rotation = 4  # no such bit
+    assert lib.lbkv_decode_attn(ctypes.byref(d), *([null] * 8), 2, 0, 0, 128, null, null) == -1
+    assert lib.lbkv_workspace_bytes(ctypes.byref(d), 2, 0, 0, 128) == 0
+    assert lib.lbkv_append(ctypes.byref(d), null, null, null, 2, 0, 0, 128, *([null] * 6), null) == -1
+    d.rotation = 3  # the comparator reads a plain bf16 cache only
+    assert lib.lbkv_bf16_workspace_bytes(ctypes.byref(d)) == 0
+    assert lib.lbkv_decode_bf16(ctypes.byref(d), *([null] * 5), null) == -3
+    # a valid flag passes the format checks (a GPU-less host stops at the device query)
+    assert lib.lbkv_decode_attn(ctypes.byref(d), *([null] * 8), 2, 0, 0, 128, null, null) not in (0, -1, -3)

@@ -404,3 +404,60 @@ def test_rotated_append_equals_packing_the_rotated_history(lbkv, bits, kl, vl, r
         for w, h in ((win["k_win"], hk), (win["v_win"], hv)):
             for b, L in enumerate(final):
                 assert np.array_equal(_bits(w[b, :, :5]), h[b, :, L:L + 5])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kl,vl", [(0, 0), (1, 0)])
+def test_rotated_paged_append_then_decode(lbkv, kl, vl):
+    """Rotation, paging and append together: a paged cache grown by rotated appends holds the
+    oracle's packing of the rotated history, and decodes like its contiguous gather."""
+    from bit_kv_cache_split_gb300 import inputs
+
+    B, Hkv, T, P, g, bits = 2, 2, 512, 256, 128, 2
+    lens0 = [0, 256]
+    n = g + 3
+    gen = torch.Generator().manual_seed(50)
+    xk = torch.randn((B, Hkv, T, D), generator=gen).to(torch.bfloat16)
+    xv = torch.randn((B, Hkv, T, D), generator=gen).to(torch.bfloat16)
+    hk, hv = oracle.rotate_rows(_bits(xk))[1], oracle.rotate_rows(_bits(xv))[1]
+    table, num_pages = inputs.page_table([T] * B, P, T // P, seed=51)
+    tab = table.cuda()
+    l0 = torch.tensor(lens0, dtype=torch.int32).cuda()
+    paged = dict(page_table=tab, num_pages=num_pages, page_tokens=P)
+    k = lbkv.pack(lbkv.rotate(xk.cuda()), l0, bits=bits, layout=kl, group=g, **paged)
+    v = lbkv.pack(lbkv.rotate(xv.cuda()), l0, bits=bits, layout=vl, group=g, **paged)
+    windowed = kl == 1 or vl == 1
+    win = {}
+    if windowed:
+        win = dict(k_win=torch.zeros((B, Hkv, 128, D), dtype=torch.bfloat16, device="cuda"),
+                   v_win=torch.zeros((B, Hkv, 128, D), dtype=torch.bfloat16, device="cuda"),
+                   win_lens=torch.zeros((B,), dtype=torch.int32, device="cuda"))
+    lens = l0.clone()
+    xkd, xvd = xk.cuda(), xv.cuda()
+    for step in range(n):
+        pos = [L + step for L in lens0]
+        kn = torch.stack([xkd[b, :, p] for b, p in enumerate(pos)]).contiguous()
+        vn = torch.stack([xvd[b, :, p] for b, p in enumerate(pos)]).contiguous()
+        lbkv.append(kn, vn, lens, *k, *v, bits=bits, k_layout=kl, v_layout=vl, group=g, rotation=3, page_table=tab,
+                    max_seq_len=T, **win)
+    torch.cuda.synchronize()
+    final = [L + (g if windowed else n) for L in lens0]
+    assert lens.cpu().tolist() == final
+    for (c, s, z), h, layout in ((k, hk, kl), (v, hv, vl)):
+        r = 1 if layout == 0 else g
+        cc, ss, zz = (inputs.from_pages(a, table, T // rr) for a, rr in ((c, 1), (s, r), (z, r)))
+        rc, rs, rz = oracle.pack(h, np.asarray(final, np.int32), bits, layout, g)
+        for b, L in enumerate(final):
+            m = L if layout == 0 else (L + g - 1) // g
+            assert np.array_equal(cc[b, :, :L].cpu().numpy(), rc[b, :, :L]), ("codes", b)
+            assert np.array_equal(_bits(ss[b, :, :m]), rs[b, :, :m]), ("scale", b)
+            assert np.array_equal(_bits(zz[b, :, :m]), rz[b, :, :m]), ("offset", b)
+    q = torch.randn((B, 4 * Hkv, D), generator=gen).to(torch.bfloat16).cuda()
+    common = dict(bits=bits, k_layout=kl, v_layout=vl, group=g, rotation=3, **win)
+    got = lbkv.decode_attn(q, *k, *v, lens, page_table=tab, max_seq_len=T, **common)
+    gather = lambda side, layout: [inputs.from_pages(a, table, T // rr)  # noqa: E731
+                                   for a, rr in ((side[0], 1), (side[1], 1 if layout == 0 else g),
+                                                 (side[2], 1 if layout == 0 else g))]
+    ref = lbkv.decode_attn(q, *gather(k, kl), *gather(v, vl), lens, **common)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
