@@ -319,8 +319,8 @@ def sweep_workloads():
     for b in inputs.BATCHES:
         for ctx in inputs.CONTEXTS:
             ws.append(inputs.decode_int4(b, ctx))
-    for bits in (2, 4):
-        for kl, vl in ((1, 0), (0, 1)):
+    for bits in (2, 4):  # all four K/V layout pairs on the same ragged lengths
+        for kl, vl in ((0, 0), (1, 0), (0, 1), (1, 1)):
             ws.append(inputs.mixed_layout(bits, kl, vl))
     for b in (1, 16, 64):
         ws.append(inputs.long_context(b))

@@ -140,6 +140,7 @@ struct DecodeParams {
   int B, Hq, Hkv, hq, T_cap, win_cap, kv_shift;
   float sl2;  // softmax scale times log2(e)
   int n_cta, has_win;   // CTAs of the grid; whether a bf16 window is given
+  int split_w;          // work split: the cost of a pair boundary, in items
   int ring_off, ring_per_warp;  // shared-memory offset of the rings, entries per warp
   // Paged cache (the kernel's PAGED variant): token t of cached KV head kvh of sequence b
   // is row t mod 2^log2_page of page page_table[b * max_pages + t / 2^log2_page], in a
@@ -886,16 +887,16 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
 
 // ------------------------------------------------------------------------
 // Work split. The items (UNIT tokens; the last one of a pair may be partial) of all
-// (sequence, KV head) pairs with tokens form one sequence in pair order. CTA c of the
-// persistent grid takes items first_item(c) .. first_item(c+1)-1 of it and deals them
-// to its warps in turn. Every CTA derives the item counts from the device lengths.
+// (sequence, KV head) pairs with tokens form one sequence in pair order. On a cost axis
+// every such pair costs split_w (its boundary: prologue, waiting for the slowest warp,
+// merges) followed by one unit per item: item x of the q-th pair with tokens sits at cost
+// x + split_w (q + 1). CTA c of the persistent grid takes the items whose cost lies in
+// [T(c), T(c + 1)), T(c) = ceil(c Ct / n_cta), Ct the total cost, and deals them to its
+// warps in turn; a CTA that would cover many short pairs gets fewer items. Every CTA
+// derives the counts from the device lengths.
 // ------------------------------------------------------------------------
-__device__ __forceinline__ long long first_item(long long c, long long tot, long long n_cta) {
-  return c * tot / n_cta;
-}
-// The CTA whose range holds item x (the last one among CTAs with equal starts).
-__device__ __forceinline__ int cta_of(long long x, long long tot, long long n_cta) {
-  return (int)(((x + 1) * n_cta - 1) / tot);
+__device__ __forceinline__ long long split_threshold(long long c, long long ctot, long long n_cta) {
+  return (c * ctot + n_cta - 1) / n_cta;
 }
 
 // The CTA's warps deposit (m, l, o) per query here for the merge of a pair.
@@ -905,13 +906,17 @@ struct MergeArea {
   float* o;  // [kMergeWarps][hq][D] unnormalised output
 };
 
-// Result of the CTA's scan over the sequence lengths.
+// Result of the CTA's scan over the sequence lengths: the items at the two ends of its
+// range (end 0 its first item, end 1 one past its last), and where its first item is.
 struct SplitScan {
-  long long tot;           // items of all pairs
-  long long sum[32];       // per-warp sums of sequence items
-  long long b0_start;      // first item of sequence b0
-  int k0, b0;              // warp chunk and sequence holding the CTA's first item
-  long long k0_base;       // items before warp chunk k0
+  long long cost[32], items[32], pairs[32];  // per-warp sums over a chunk of sequences
+  long long ctot;                            // total cost
+  int w;                                     // boundary cost in use (0 for small problems)
+  int kw[2];                                 // warp chunk holding end e's threshold
+  long long base_cost[2], base_items[2], base_pairs[2];  // sums of the chunks before it
+  long long x[2];                            // item index of end e
+  int b0, kv0, t0;                           // sequence, pair in it and item in the pair of end 0
+  long long q0;                              // pairs with tokens before the start pair
 };
 
 // ------------------------------------------------------------------------
@@ -967,58 +972,94 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   {
     const int chunk = (p.B + W - 1) / W;  // warp w sums sequences [w chunk, (w+1) chunk)
     const int bb0 = min(p.B, warp * chunk), bb1 = min(p.B, bb0 + chunk);
-    long long s = 0;
-    for (int b = bb0 + lane; b < bb1; b += 32) s += (long long)p.Hkv * items_of(seq_len(b));
+    long long si = 0, sp = 0;
+    for (int b = bb0 + lane; b < bb1; b += 32) {
+      const long long n = items_of(seq_len(b));
+      si += (long long)p.Hkv * n;
+      if (n > 0) sp += p.Hkv;
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULLMASK, s, o);
-    if (lane == 0) ss.sum[warp] = s;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      long long tot = 0;
-      for (int w = 0; w < W; ++w) tot += ss.sum[w];
-      ss.tot = tot;
-      const long long x0 = first_item(cta, tot, p.n_cta), x1 = first_item(cta + 1, tot, p.n_cta);
-      ss.k0 = W;
-      long long acc = 0;
-      if (x0 < x1)
-        for (int w = 0; w < W; ++w) {
-          if (x0 < acc + ss.sum[w]) {
-            ss.k0 = w;
-            ss.k0_base = acc;
-            break;
-          }
-          acc += ss.sum[w];
-        }
+    for (int o = 16; o > 0; o >>= 1) {
+      si += __shfl_xor_sync(FULLMASK, si, o);
+      sp += __shfl_xor_sync(FULLMASK, sp, o);
+    }
+    if (lane == 0) {
+      ss.items[warp] = si;
+      ss.pairs[warp] = sp;
     }
     __syncthreads();
-    if (warp == ss.k0) {  // find the sequence holding the first item
-      const long long x0 = first_item(cta, ss.tot, p.n_cta);
-      long long run = ss.k0_base;
+    if (threadIdx.x == 0) {
+      long long tot = 0, np = 0;
+      for (int w = 0; w < W; ++w) tot += ss.items[w], np += ss.pairs[w];
+      // With few items per warp the split must keep the rounds of items even instead: no
+      // boundary cost there.
+      const int sw = (tot >= 8LL * W * p.n_cta) ? p.split_w : 0;
+      for (int w = 0; w < W; ++w) ss.cost[w] = ss.items[w] + (long long)sw * ss.pairs[w];
+      const long long ctot = tot + (long long)sw * np;
+      ss.w = sw;
+      ss.ctot = ctot;
+      for (int e = 0; e < 2; ++e) {
+        const long long T = split_threshold(cta + e, ctot, p.n_cta);
+        ss.kw[e] = W;  // past the end: no item at or after T
+        ss.x[e] = tot;
+        long long ac = 0, ai = 0, ap = 0;
+        for (int w = 0; w < W; ++w) {
+          if (T < ac + ss.cost[w]) {
+            ss.kw[e] = w;
+            ss.base_cost[e] = ac;
+            ss.base_items[e] = ai;
+            ss.base_pairs[e] = ap;
+            break;
+          }
+          ac += ss.cost[w], ai += ss.items[w], ap += ss.pairs[w];
+        }
+      }
+      ss.b0 = ss.kv0 = ss.t0 = 0;
+      ss.q0 = 0;
+    }
+    __syncthreads();
+    for (int e = 0; e < 2; ++e) {
+      if (warp != ss.kw[e]) continue;  // the warp whose chunk of sequences holds end e
+      const long long T = split_threshold(cta + e, ss.ctot, p.n_cta);
+      long long rc = ss.base_cost[e], ri = ss.base_items[e], rp = ss.base_pairs[e];
       for (int base = bb0; base < bb1; base += 32) {
         const int b = base + lane;
-        const long long n = (b < bb1) ? (long long)p.Hkv * items_of(seq_len(b)) : 0;
-        long long incl = n;
+        const long long n = (b < bb1) ? (long long)items_of(seq_len(b)) : 0;
+        const long long c_b = n > 0 ? (long long)p.Hkv * (n + ss.w) : 0;
+        const long long i_b = (long long)p.Hkv * n, p_b = n > 0 ? p.Hkv : 0;
+        long long ic = c_b, ii = i_b, ip = p_b;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const long long y = __shfl_up_sync(FULLMASK, incl, o);
-          if (lane >= o) incl += y;
+          const long long yc = __shfl_up_sync(FULLMASK, ic, o);
+          const long long yi = __shfl_up_sync(FULLMASK, ii, o);
+          const long long yp = __shfl_up_sync(FULLMASK, ip, o);
+          if (lane >= o) ic += yc, ii += yi, ip += yp;
         }
-        const long long excl = run + incl - n;
-        const unsigned hit = __ballot_sync(FULLMASK, n > 0 && x0 >= excl && x0 < excl + n);
+        const long long ec = rc + ic - c_b;  // cost before sequence b
+        const unsigned hit = __ballot_sync(FULLMASK, c_b > 0 && T >= ec && T < ec + c_b);
         if (hit) {
           if (lane == __ffs(hit) - 1) {
-            ss.b0 = b;
-            ss.b0_start = excl;
+            const long long off = T - ec;
+            const long long kv = off / (n + ss.w), o2 = off - kv * (n + ss.w);
+            const long long t = o2 > ss.w ? o2 - ss.w : 0;
+            ss.x[e] = (ri + ii - i_b) + kv * n + t;
+            if (e == 0) {
+              ss.b0 = b;
+              ss.kv0 = (int)kv;
+              ss.t0 = (int)t;
+              ss.q0 = (rp + ip - p_b) + kv;
+            }
           }
           break;
         }
-        run += __shfl_sync(FULLMASK, incl, 31);
+        rc += __shfl_sync(FULLMASK, ic, 31);
+        ri += __shfl_sync(FULLMASK, ii, 31);
+        rp += __shfl_sync(FULLMASK, ip, 31);
       }
     }
     __syncthreads();
   }
-  const long long tot = ss.tot;
-  const long long X0 = first_item(cta, tot, p.n_cta), X1 = first_item(cta + 1, tot, p.n_cta);
+  const long long X0 = ss.x[0], X1 = ss.x[1];
   const int NL = (int)(X1 - X0);  // items of this CTA
 
   // Each ring entry has a K half (codes, scales, offsets) and a V half, each with its own
@@ -1098,10 +1139,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   start.r = 0;
   if (NL > 0) {
     const int L0 = seq_len(ss.b0), n0 = items_of(L0);
-    const long long off = X0 - ss.b0_start;
-    const int kv0 = (int)(off / n0);
+    const int kv0 = ss.kv0;
     start.u = ss.b0 * p.Hkv + kv0;
-    start.t = (int)(off - (long long)kv0 * n0);
+    start.t = ss.t0;
     start.L = L0;
     start.n = n0;
     start.b = ss.b0;
@@ -1176,6 +1216,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   int u = start.u;
   long long pair_first = X0 - start.t;  // the pair's first item in the item sequence
   int pair_n = start.n;
+  long long q = ss.q0;  // pairs with tokens before pair u
   while (x < X1) {
     const long long xe = min(X1, pair_first + pair_n);
     const int b = u / p.Hkv, kvh = u % p.Hkv;
@@ -1457,16 +1498,27 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     // CTA writes its partial to its slot (1 when the pair is the second one it holds a
     // partial of, else 0) and the last contributor to arrive merges all partials (and the
     // window's) into the output.
+    // The CTAs that hold items of this pair: c_first .. c_last on the cost axis (item x of
+    // it costs x + wq); a CTA between them may hold none (its range inside the boundary).
     const long long pair_last = pair_first + pair_n - 1;
-    const int c_first = cta_of(pair_first, tot, p.n_cta), c_last = cta_of(pair_last, tot, p.n_cta);
-    auto slot_of = [&](int cc) {
-      return (cc == c_first && first_item(cc, tot, p.n_cta) < pair_first) ? 1 : 0;
+    const long long wq = (long long)ss.w * (q + 1);
+    auto cta_at = [&](long long xi) { return (int)min((xi + wq) * p.n_cta / ss.ctot, (long long)p.n_cta - 1); };
+    const int c_first = cta_at(pair_first), c_last = cta_at(pair_last);
+    auto start_in_pair = [&](int cc) -> long long {  // first item of the pair CTA cc holds (clamped)
+      if (cc <= c_first) return pair_first;
+      return min(pair_last + 1, max(pair_first, split_threshold(cc, ss.ctot, p.n_cta) - wq));
     };
+    // When every CTA range covers a cost unit or more, every CTA of the span holds items of
+    // the pair; only smaller problems need the test.
+    const bool sparse = ss.ctot < p.n_cta;
+    auto holds = [&](int cc) { return !sparse || start_in_pair(cc + 1) > start_in_pair(cc); };
+    // partial slot 1 for the last pair of a CTA that began in an earlier pair, else 0
+    const int slot_first = split_threshold(c_first, ss.ctot, p.n_cta) < pair_first + wq - ss.w ? 1 : 0;
+    auto slot_of = [&](int cc) { return cc == c_first ? slot_first : 0; };
     int n_contrib = c_last - c_first + 1;
-    if (tot < p.n_cta) {  // some CTAs hold no item: count only those that do
+    if (sparse) {
       n_contrib = 0;
-      for (int cc = c_first; cc <= c_last; ++cc)
-        n_contrib += first_item(cc + 1, tot, p.n_cta) > first_item(cc, tot, p.n_cta);
+      for (int cc = c_first; cc <= c_last; ++cc) n_contrib += holds(cc);
     }
     const bool alone = (n_contrib == 1);
     for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS) {
@@ -1529,7 +1581,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         auto row_of = [&](int k, int i) -> long long {  // partial row, or -1 for a CTA without items
           if (k == n_span) return (long long)u * hq + i;  // window
           const int cc = c_first + k;
-          if (tot < p.n_cta && first_item(cc + 1, tot, p.n_cta) == first_item(cc, tot, p.n_cta)) return -1;
+          if (!holds(cc)) return -1;
           return ((long long)cc * 2 + slot_of(cc)) * hq + i;
         };
         auto ml_of = [&](int k, int i) -> float2 {
@@ -1591,6 +1643,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         ++u;
         pair_n = items_of(seq_len(u / p.Hkv));
       } while (pair_n == 0);
+      ++q;
     }
   }
 

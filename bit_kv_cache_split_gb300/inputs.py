@@ -149,7 +149,7 @@ def ragged_lens(batch: int = 16, lo: int = 1024, hi: int = 65536, seed: int = 3)
 
 def mixed_layout(bits: int, k_layout: int, v_layout: int, batch: int = 16, seed: int = 3,
                  lens: Optional[Sequence[int]] = None) -> Workload:
-    """32q/8kv, ragged lengths; one side channel-wise over 128-token groups."""
+    """32q/8kv, ragged lengths, the given K/V layout pair (channel-wise over 128-token groups)."""
     lens = list(lens) if lens is not None else ragged_lens(batch, seed=seed)
     s = (0.01, 0.1) if bits == 2 else (0.002, 0.02)
     tag = f"{'cw' if k_layout else 'tw'}K-{'cw' if v_layout else 'tw'}V"
