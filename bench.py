@@ -592,6 +592,45 @@ def time_rotation(device, peak, contiguous_us, calls=20):
                        "frac": round(rot_bytes / (rot_us * 1e-6) / 1e9 / peak, 4), "bytes": rot_bytes}}
 
 
+def time_pack(device, peak, calls=5):
+    """lbkv_pack (the prefill quantizer) of one bf16 side of the headline (batch 32, 8 KV heads,
+    32K tokens: 2.1 GB) into INT2 g128 codes, token-wise and channel-wise."""
+    import bit_kv_cache_split_gb300 as pkg
+
+    B, Hkv, T = HEADLINE["batch"], 8, HEADLINE["ctx"]
+    x = torch.randn((B, Hkv, T, 128), device=device, dtype=torch.bfloat16)
+    lens = torch.full((B,), T, dtype=torch.int32, device=device)
+    rows = []
+    for layout in (0, 1):
+        codes, scale, off = pkg.pack(x, lens, bits=2, layout=layout, group=128)
+        for _ in range(2):
+            pkg.pack(x, lens, bits=2, layout=layout, group=128, codes=codes, scale=scale, off=off)
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(calls):
+                    pkg.pack(x, lens, bits=2, layout=layout, group=128, codes=codes, scale=scale, off=off)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / calls
+        nbytes = x.numel() * 2 + codes.numel() + 2 * scale.numel() * 2
+        rows.append({"workload": f"pack-int2-{'channelwise' if layout else 'tokenwise'}-b{B}-ctx{T}",
+                     "us_per_call": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4), "bytes": nbytes})
+        del graph, codes, scale, off
+    del x
+    torch.cuda.empty_cache()
+    return rows
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: every rank's timed region is one step of its own replica,
     and the job is done when the last one is (weak scaling, one process per GPU)."""
@@ -723,13 +762,14 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     e2e_val = job_throughput(step_bytes, e2e_ms, world)
 
-    sweep = append = bf16 = paged = rotation = None
+    sweep = append = bf16 = paged = rotation = pack = None
     if not args.no_sweep and rank == 0:
         sweep = run_sweep(device, peak)
         append = time_append(device, peak)
         bf16 = time_bf16(device, peak, ms * 1e3)
         paged = time_paged(device, peak, ms * 1e3)
         rotation = time_rotation(device, peak, ms * 1e3)
+        pack = time_pack(device, peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -764,6 +804,7 @@ def main():
             "bf16_comparator": bf16,
             "paged": paged,
             "rotation": rotation,
+            "pack": pack,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
