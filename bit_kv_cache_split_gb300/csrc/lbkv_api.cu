@@ -100,7 +100,7 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   if (hq != 1 && hq != 2 && hq != 4 && hq != 8) return LBKV_EUNSUPPORTED;
   const bool win = d->k_win != nullptr;
   if (win != (d->v_win != nullptr) || win != (d->win_lens != nullptr)) return LBKV_EINVAL;
-  if (win && (d->win_cap <= 0 || d->win_cap > 128)) return LBKV_EINVAL;
+  if (win && (d->win_cap <= 0 || d->win_cap > kWinMax)) return LBKV_EINVAL;
   if (int st = paged_check(d)) return st;
   if (d->rotation & ~(LBKV_ROTATE_K | LBKV_ROTATE_V)) return LBKV_EINVAL;
   // PV columns are (query, V channel group) pairs: a token-wise V side with G channel
@@ -294,7 +294,7 @@ int lbkv_append(const lbkv_desc* desc, const void* k_new, const void* v_new, int
   const bool windowed = k_layout == LBKV_CHANNELWISE || v_layout == LBKV_CHANNELWISE;
   const bool win = desc->k_win != nullptr;
   if (win != (desc->v_win != nullptr) || win != (desc->win_lens != nullptr)) return LBKV_EINVAL;
-  if (windowed && (!win || desc->win_cap < group || desc->win_cap > 128)) return LBKV_EINVAL;
+  if (windowed && (!win || desc->win_cap < group || desc->win_cap > kWinMax)) return LBKV_EINVAL;
   if (int st = paged_check(desc)) return st;
   if (desc->rotation & ~(LBKV_ROTATE_K | LBKV_ROTATE_V)) return LBKV_EINVAL;
   if (desc->batch == 0) return LBKV_OK;

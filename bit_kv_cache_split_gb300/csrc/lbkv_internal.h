@@ -76,6 +76,7 @@ using DecodeKernel = void (*)(const DecodeParams);
 
 // Window partials (one per sequence and KV head) into the last partial slot of each
 // pair; launched before the decode kernel when a bf16 window is present.
+constexpr int kWinMax = 128;  // window capacity limit (tokens)
 int launch_window_partial(const DecodeParams& p, cudaStream_t stream);
 
 // Instantiated kernel for (column mode, log2 group) of one bit width, K/V layout

@@ -7,20 +7,43 @@
 
 namespace lbkv {
 
-__global__ void __launch_bounds__(32 * kWinWarps, 1) window_partial_kernel(const __grid_constant__ DecodeParams p) {
+// One CTA per pair. The window's K rows go to shared memory (rows padded by one word, so
+// that the 32 rows a warp reads at once sit in 32 different banks); then every (query,
+// token) score is one thread's dot product, each query's softmax one warp's reduction, and
+// every output channel of a query one thread's weighted sum over the V rows. The V rows
+// are loaded into registers at the start (their latency overlaps the scores) and moved into
+// the K rows' shared memory once the scores are done.
+constexpr int kWinThreads = 32 * kWinWarps;
+constexpr int kWinKStride = kHeadDim + 2;  // bf16 per shared K row
+
+__global__ void __launch_bounds__(kWinThreads, 1) window_partial_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
+  __shared__ __align__(16) __nv_bfloat16 sK[kWinMax * kWinKStride];
   __shared__ float sQ[kMaxHq * D];
-  __shared__ float sM[kWinWarps][kMaxHq];
-  __shared__ float sL[kWinWarps][kMaxHq];
-  __shared__ float sO[kWinWarps][kMaxHq][D];
+  __shared__ float sS[kMaxHq * kWinMax];  // scores (log2 units), then weights
+  __shared__ float sM[kMaxHq], sL[kMaxHq];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int hq = p.hq;
   const int u = b * p.Hkv + kvh;
-  for (int idx = threadIdx.x; idx < hq * D; idx += 32 * kWinWarps)
+  const int W = min(max(p.win_lens[b], 0), p.win_cap);
+  const size_t wbase = (size_t)(u >> p.kv_shift) * p.win_cap;  // the pair's cached KV head
+  for (int idx = threadIdx.x; idx < hq * D; idx += kWinThreads)
     sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
+  for (int e = threadIdx.x; e < W * (D / 2); e += kWinThreads) {
+    const int t = e / (D / 2), d2 = e % (D / 2);
+    reinterpret_cast<uint32_t*>(sK + t * kWinKStride)[d2] =
+        reinterpret_cast<const uint32_t*>(p.k_win + (wbase + t) * D)[d2];
+  }
+  constexpr int kVWords = kWinMax * (D / 2) / kWinThreads;  // V words (two channels) per thread
+  uint32_t vreg[kVWords];
+#pragma unroll
+  for (int j = 0; j < kVWords; ++j) {
+    const int e = threadIdx.x + j * kWinThreads, t = e / (D / 2), d2 = e % (D / 2);
+    vreg[j] = (t < W) ? reinterpret_cast<const uint32_t*>(p.v_win + (wbase + t) * D)[d2] : 0u;
+  }
   __syncthreads();
   if (p.rotation & 1) {  // window keys stored rotated like the cache's: the scores take H q
     for (int i = warp; i < hq; i += kWinWarps) {
@@ -34,78 +57,65 @@ __global__ void __launch_bounds__(32 * kWinWarps, 1) window_partial_kernel(const
     __syncthreads();
   }
 
-  // warp w scores tokens w, w + W, ...; lane holds channels 4 lane .. 4 lane + 3
-  const int W = min(max(p.win_lens[b], 0), p.win_cap);
-  float m[kMaxHq], l[kMaxHq], o[kMaxHq][4];
-#pragma unroll
-  for (int i = 0; i < kMaxHq; ++i) {
-    m[i] = -INFINITY;
-    l[i] = 0.f;
-    o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  }
-  const size_t wbase = (size_t)(u >> p.kv_shift) * p.win_cap;  // the pair's cached KV head
-  for (int t = warp; t < W; t += kWinWarps) {
-    const uint2 kr = reinterpret_cast<const uint2*>(p.k_win + (wbase + t) * D)[lane];
-    const uint2 vr = reinterpret_cast<const uint2*>(p.v_win + (wbase + t) * D)[lane];
-    const __nv_bfloat162* kh = reinterpret_cast<const __nv_bfloat162*>(&kr);
-    const __nv_bfloat162* vh = reinterpret_cast<const __nv_bfloat162*>(&vr);
-    const float2 k01 = __bfloat1622float2(kh[0]), k23 = __bfloat1622float2(kh[1]);
-    const float2 v01 = __bfloat1622float2(vh[0]), v23 = __bfloat1622float2(vh[1]);
-#pragma unroll
-    for (int i = 0; i < kMaxHq; ++i) {
-      if (i >= hq) break;
-      const float* qrow = sQ + i * D + 4 * lane;
-      float d = qrow[0] * k01.x + qrow[1] * k01.y + qrow[2] * k23.x + qrow[3] * k23.y;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(FULLMASK, d, off);
-      const float s = d * p.sl2;  // log2 units
-      const float mn = fmaxf(m[i], s);
-      const float a = fast_exp2(m[i] - mn);
-      const float pr = fast_exp2(s - mn);
-      m[i] = mn;
-      l[i] = l[i] * a + pr;
-      o[i][0] = o[i][0] * a + pr * v01.x;
-      o[i][1] = o[i][1] * a + pr * v01.y;
-      o[i][2] = o[i][2] * a + pr * v23.x;
-      o[i][3] = o[i][3] * a + pr * v23.y;
+  // scores: thread per (query i, token t)
+  for (int e = threadIdx.x; e < hq * W; e += kWinThreads) {
+    const int i = e / W, t = e % W;
+    const uint32_t* krow = reinterpret_cast<const uint32_t*>(sK + t * kWinKStride);
+    const float* qrow = sQ + i * D;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int d2 = 0; d2 < D / 2; ++d2) {
+      const float2 k2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(krow + d2));
+      acc = fmaf(qrow[2 * d2], k2.x, acc);
+      acc = fmaf(qrow[2 * d2 + 1], k2.y, acc);
     }
+    sS[i * kWinMax + t] = acc * p.sl2;
   }
+  __syncthreads();  // the K rows are read: the V rows take their place
 #pragma unroll
-  for (int i = 0; i < kMaxHq; ++i) {
-    if (i >= hq) break;
+  for (int j = 0; j < kVWords; ++j) {
+    const int e = threadIdx.x + j * kWinThreads, t = e / (D / 2), d2 = e % (D / 2);
+    if (t < W) reinterpret_cast<uint32_t*>(sK + t * kWinKStride)[d2] = vreg[j];
+  }
+
+  // per query: maximum, weights 2^(s - m), their sum (warp i)
+  for (int i = warp; i < hq; i += kWinWarps) {
+    float m = -INFINITY;
+    for (int t = lane; t < W; t += 32) m = fmaxf(m, sS[i * kWinMax + t]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, o));
+    float l = 0.f;
+    for (int t = lane; t < W; t += 32) {
+      const float w = fast_exp2(sS[i * kWinMax + t] - m);
+      sS[i * kWinMax + t] = w;
+      l += w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(FULLMASK, l, o);
     if (lane == 0) {
-      sM[warp][i] = m[i];
-      sL[warp][i] = l[i];
+      sM[i] = m;
+      sL[i] = l;
     }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) sO[warp][i][4 * lane + k] = o[i][k];
   }
   __syncthreads();
 
-  // merge the warps into the window slot of the pair
-  for (int idx = threadIdx.x; idx < hq * D; idx += 32 * kWinWarps) {
-    const int i = idx / D, ch = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWinWarps; ++w) M = fmaxf(M, sM[w][i]);
-    float acc = 0.f, lt = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWinWarps; ++w) {
-        const float sc = (sM[w][i] == -INFINITY) ? 0.f : fast_exp2(sM[w][i] - M);
-        acc = fmaf(sc, sO[w][i][ch], acc);
-        lt = fmaf(sc, sL[w][i], lt);
-      }
-    }
+  // unnormalised output: thread per (query i, channel d)
+  for (int e = threadIdx.x; e < hq * D; e += kWinThreads) {
+    const int i = e / D, d = e % D;
+    const float* w = sS + i * kWinMax;
+    const __nv_bfloat16* vcol = sK + d;  // the V rows, same padded stride
+    float acc = 0.f;
+#pragma unroll 8
+    for (int t = 0; t < W; ++t) acc = fmaf(w[t], __bfloat162float(vcol[t * kWinKStride]), acc);
     const size_t prow = (size_t)u * hq + i;
-    p.win_o[prow * D + ch] = acc;
-    if (ch == 0) p.win_ml[prow] = make_float2(M, lt);
+    p.win_o[prow * D + d] = acc;
+    if (d == 0) p.win_ml[prow] = make_float2(sM[i], sL[i]);
   }
 }
 
 int launch_window_partial(const DecodeParams& p, cudaStream_t stream) {
   dim3 grid((unsigned)p.Hkv, (unsigned)p.B);
-  window_partial_kernel<<<grid, 32 * kWinWarps, 0, stream>>>(p);
+  window_partial_kernel<<<grid, kWinThreads, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
