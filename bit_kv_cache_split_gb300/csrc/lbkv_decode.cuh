@@ -347,22 +347,22 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
   int e2 = 0;
   if (amax > 0.f) e2 = min(100, max(-100, 13 - ilog2f(amax)));
   const float sc = exp2i(e2);
-  float fed = 0.f;  // sum of the fp16 values actually fed (for the magic bias)
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const uint32_t h2 = f16x2_from(x[ks][r][0] * sc, x[ks][r][1] * sc);
-      qB[ks][r] = h2;
-      const float2 f = half2_to_float2(h2);
-      fed += f.x + f.y;
-    }
-  fed += __shfl_xor_sync(FULLMASK, fed, 1);
-  fed += __shfl_xor_sync(FULLMASK, fed, 2);
-  const float fa = sl2 * exp2i(-e2), fb = sl2 * zsum, fc = -kMagicF * fed;
-  // accumulator column 2c + j is B column 2c + j, held by lane 4 (2c + j)
+    for (int r = 0; r < 2; ++r) qB[ks][r] = f16x2_from(x[ks][r][0] * sc, x[ks][r][1] * sc);
+  // The magic bias of each column is 1024 times the sum of the fp16 values actually fed: the
+  // tensor cores form it, with an all-ones A operand against the same B fragments (the
+  // accumulator columns 2c, 2c + 1 of this lane are the columns the bias is needed for).
+  constexpr uint32_t kOnes2 = 0x3c003c00u;  // (1.0, 1.0) in fp16
+  float fed[4];
+  mma_f16_c(fed, kOnes2, kOnes2, kOnes2, kOnes2, qB[0][0], qB[0][1], 0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int jj = 0; jj < 2; ++jj) cwneg[jj] = __shfl_sync(FULLMASK, fc, 8 * c + 4 * jj);
+  for (int ks = 1; ks < 8; ++ks) mma_f16(fed, kOnes2, kOnes2, kOnes2, kOnes2, qB[ks][0], qB[ks][1]);
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) cwneg[jj] = -kMagicF * fed[jj];
+  const float fa = sl2 * exp2i(-e2), fb = sl2 * zsum;
+  // accumulator column 2c + j is B column 2c + j, held by lane 4 (2c + j)
 #pragma unroll
   for (int j = 0; j < C::NQ; ++j) {
     cwA[j] = __shfl_sync(FULLMASK, fa, 8 * c + 4 * j);
