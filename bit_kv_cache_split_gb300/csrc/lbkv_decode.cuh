@@ -816,35 +816,21 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
           f1 = P[mt][1][j] * 8192.f;
         }
         pw[o][mt] = f16x2_from(f0, f1);
-        const float2 fb = half2_to_float2(pw[o][mt]);
-        Fc[o] += fb.x + fb.y;
+        if (VL == 1) {
+          const float2 fb = half2_to_float2(pw[o][mt]);
+          Fc[o] += fb.x + fb.y;
+        }
       }
     }
+    if (VL == 1) {
 #pragma unroll
-    for (int o = 0; o < NO; ++o) {
-      if (VL == 1) st.l[own_slot<C>(o)] += Fc[o] * (1.f / 8192.f);  // this lane's tokens
-      Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 4);
-      Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 8);
-      Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 16);
-      if (VL == 1) Wg[o] += Fc[o];
-    }
-    // accumulator column (v, 2c + e) holds owned combo (DUP ? 0 : 2v + e)
-    float cb[NTV][2];
-#pragma unroll
-    for (int v = 0; v < NTV; ++v)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) cb[v][e] = -kMagicF * Fc[C::DUP ? 0 : 2 * v + e];
-    if (!fresh) {
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int v = 0; v < NTV; ++v)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            if (!C::DUP || e == 0) {  // the duplicate column of a pair is never read
-              accv[mt][v][e] += cb[v][e];
-              accv[mt][v][2 + e] += cb[v][e];
-            }
+      for (int o = 0; o < NO; ++o) {
+        st.l[own_slot<C>(o)] += Fc[o] * (1.f / 8192.f);  // this lane's tokens
+        Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 4);
+        Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 8);
+        Fc[o] += __shfl_xor_sync(FULLMASK, Fc[o], 16);
+        Wg[o] += Fc[o];
+      }
     }
     // PV B fragments: column n = g of n-tile v belongs to lane c_o = g/2 of each token
     // row group; k-slots 2c, 2c+1 (tokens 16kk + 2c + {0,1}) come from lane 4c + c_o and
@@ -867,6 +853,39 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
           pB[v][kk][1] = (g & 1) ? x11 : x10;
         }
       }
+    // Minus the magic bias per accumulator column (v, 2c + e): 1024 times the sum of the fp16
+    // weights fed to that column. Token-wise V: the tensor cores form the sums, with an
+    // all-ones A operand against the same B fragments. Channel-wise V: from the sums above,
+    // per owned combo (DUP ? 0 : 2v + e).
+    float cb[NTV][2];
+    if (VL == 0) {
+      constexpr uint32_t kOnes2 = 0x3c003c00u;  // (1.0, 1.0) in fp16
+#pragma unroll
+      for (int v = 0; v < NTV; ++v) {
+        float fs[4];
+        mma_f16_c(fs, kOnes2, kOnes2, kOnes2, kOnes2, pB[v][0][0], pB[v][0][1], 0.f, 0.f, 0.f, 0.f);
+        mma_f16(fs, kOnes2, kOnes2, kOnes2, kOnes2, pB[v][1][0], pB[v][1][1]);
+        cb[v][0] = -kMagicF * fs[0];
+        cb[v][1] = -kMagicF * fs[1];
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < NTV; ++v)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) cb[v][e] = -kMagicF * Fc[C::DUP ? 0 : 2 * v + e];
+    }
+    if (!fresh) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int v = 0; v < NTV; ++v)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (!C::DUP || e == 0) {  // the duplicate column of a pair is never read
+              accv[mt][v][e] += cb[v][e];
+              accv[mt][v][2 + e] += cb[v][e];
+            }
+    }
     pv_chunk<C>(accv, pB, sm, rel0, lc, fresh, cb);
 
     if (VL == 0) {
