@@ -24,7 +24,8 @@ def declared_functions():
     inc = os.path.join(ROOT, "include")
     for f in sorted(os.listdir(inc)):
         if f.endswith(".h"):
-            text = open(os.path.join(inc, f)).read()
+            with open(os.path.join(inc, f)) as fh:
+                text = fh.read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             names += re.findall(r"^\s*LBKV_API\s+[\w\s\*]+?\b(lbkv_\w+)\s*\(", text, flags=re.M)
     return names
