@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -76,15 +77,20 @@ def measured_hbm_peak():
 
 
 def source_hash() -> str:
-    """Hash of the decode kernel's device sources (its traffic does not depend on the other
-    kernels or on the host entry points)."""
+    """Hash of the decode kernel's device sources, comments and blank space left out (its
+    traffic depends on the code alone: not on comments, the other kernels or the host entry
+    points)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_kv_cache_split_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if not (f.startswith("lbkv_decode") or f == "lbkv_device.cuh"):
             continue
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                # line comments
+        code = " ".join(text.split())
+        h.update(f.encode() + code.encode())
     return h.hexdigest()[:16]
 
 
