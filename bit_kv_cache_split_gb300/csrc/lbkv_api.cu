@@ -136,7 +136,8 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   pl->smem_bytes = pl->ring_off + warps * r_w * pl->entry_bytes;
 
   // Persistent grid, one CTA per SM: the kernel splits the items of all pairs (from the
-  // device lengths) evenly over the CTAs. A CTA holds partials of at most two pairs.
+  // device lengths) over the CTAs, evenly once each pair boundary is counted as
+  // kSplitBoundaryTokens of work. A CTA holds partials of at most two pairs.
   const long long units = (long long)d->batch * pl->hkv;  // pairs
   pl->win = win ? 1 : 0;
   // Small problems: about one item per warp at most (from the capacity, the host's bound on

@@ -10,9 +10,11 @@
 // group boundary) and fold table (token-wise K: acc-fold, channel-wise K:
 // operand-fold on Q, token-wise V: operand-fold on P, channel-wise V: acc-fold).
 //
-// Kernel design (sm_103a). A persistent grid, one CTA per SM. The tokens of all
-// (sequence, KV head) pairs form items of 32, 64 or 128 tokens in one sequence;
-// each CTA takes an equal contiguous share and deals it to its 8 warps in turn.
+// Kernel design (sm_103a). A persistent grid, one CTA per SM (fewer for small
+// problems). The tokens of all (sequence, KV head) pairs form items of 32, 64 or
+// 128 tokens in one sequence; each CTA takes a contiguous share of it, equal once
+// every pair boundary is counted as a fixed amount of work (see the work split
+// below), and deals it to its warps (16, or 8) in turn.
 // Each warp streams its items' packed codes and fp16 scales/offsets through its
 // own ring in shared memory with 1-D bulk copies that it issues itself (an
 // mbarrier per entry, bounded waits, no multicast), so no warp waits on
@@ -22,6 +24,9 @@
 // the next pair, its warps merge into one partial for the pair; the last CTA of
 // a pair to finish merges the pair's partials into the bf16 output. A bf16
 // window after the cached tokens is scored by a separate small kernel first.
+// A paged cache (the PAGED variant) changes only the source addresses of the bulk
+// copies. A cache stored rotated by the Hadamard matrix has the query rotated in
+// the pair prologue and each output row rotated back before its bf16 rounding.
 //
 // Operands. OR-ing a code q (times a power-of-two position factor m) into the
 // mantissa of the fp16 magic number 1024 gives the exact fp16 value 1024 + m q,
@@ -30,7 +35,10 @@
 // accumulator: each accumulator starts at (or, continuing, is lowered by) minus
 // the bias of the operands it is about to take, so it never holds more than one
 // 32-token chunk's (PV) or one channel group's (QK^T) bias.
-// The bf16 query is exact in fp16; the softmax weights are fed as fp16.
+// The bf16 query is exact in fp16 (a rotated query is rounded to it); the
+// softmax weights are fed as fp16. Where a bias sum is formed by the tensor cores
+// (token-wise V weights, channel-wise K queries), an MMA with an all-ones A
+// operand against the same B fragments sums exactly the fp16 values fed.
 // Both products run on mma.sync m16n8k16 fp16 with fp32 accumulators (native
 // on sm_103; the e4m3 form of mma.sync converts its operands to fp16 first):
 //   QK^T: rows = 16 tokens, k = 16 channels, cols = queries;
