@@ -10,7 +10,7 @@ token-wise K/V, group 128, 32 query / 8 KV heads, head_dim 128, batch 32, 32K
 context. The other workloads run as a sweep.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {lbkv,reference}] [--no-sweep]
-       python bench.py --profile [--bits B] [--batch N] [--ctx T] [--steps K] [--warmup W]
+       python bench.py --profile [--bits B] [--batch N] [--ctx T] [--workload NAME] [--steps K] [--warmup W]
 (--profile: only eager calls of one workload, for ncu captures)
 Under torchrun (N > 1) every rank runs its own replica on its GPU (the path
 shards by sequence and KV head with no exchange); rank 0 prints one JSON line.
@@ -94,17 +94,27 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+def profiled_counters(workload: str) -> dict:
+    """Counters of one launch of `workload` from a committed ncu summary (DRAM bytes, SASS
+    instructions), if it was taken on the current decode-kernel sources; else {}."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
-        return None
+        return {}
     if not rec or rec.get("source_hash") != source_hash():
+        return {}
+    return rec
+
+
+def issue_budget(sm_count: int, sm_mhz, hbm_gbs: float):
+    """Lane-slots the GPU can issue per byte streamed at the HBM peak: SMs x 4 schedulers x
+    32 lanes x SM clock / bandwidth (the explainer's instruction-budget arithmetic, which
+    gives 9.99 for H100 and 4.65 for B200)."""
+    if not sm_mhz:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return sm_count * 4 * 32 * sm_mhz * 1e6 / (hbm_gbs * 1e9)
 
 
 # ------------------------------------------------------------------ clocks
@@ -349,8 +359,13 @@ def run_sweep(device, peak):
             torch.cuda.empty_cache()
             continue
         gbs = case.bytes / (ms * 1e-3) / 1e9
-        rows.append({"workload": wl.name, "us_per_call": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-                     "frac": round(gbs / peak, 3), "bytes": case.bytes})
+        row = {"workload": wl.name, "us_per_call": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+               "frac": round(gbs / peak, 3), "bytes": case.bytes}
+        if wl.window:
+            # scale/offset operations per stored value under folding: 2 h_q / g (explainer,
+            # break-even paragraph: folding wins while this is below 1, i.e. g > 2 h_q)
+            row["fold_ops_per_value"] = round(2 * wl.hq_per_kv / wl.group, 4)
+        rows.append(row)
         case.free()
         torch.cuda.empty_cache()
     return rows
@@ -637,6 +652,71 @@ def time_pack(device, peak, calls=5):
     return rows
 
 
+def time_batch1_launches(device, peak, launches=200):
+    """Per-launch CUDA-event times of INT2 token-wise decode at batch 1, 32K context (eager
+    launches, each bracketed by its own events, replicas rotated so that the cache is read
+    from HBM): median, 10th and 90th percentiles."""
+    wl = inputs.decode_int2(1, HEADLINE["ctx"])
+    case = Case(wl, device)
+    for i in range(10):
+        case.call(i)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    for i, (a, b) in enumerate(ev):
+        a.record(s)
+        case.call(i)
+        b.record(s)
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+    med = statistics.median(us)
+    gbs = case.bytes / (med * 1e-6) / 1e9
+    case.free()
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "launches": launches, "median_us": round(med, 2),
+            "p10_us": round(us[len(us) // 10], 2), "p90_us": round(us[(9 * len(us)) // 10], 2),
+            "gbs_at_median": round(gbs, 1), "frac_at_median": round(gbs / peak, 4), "bytes": case.bytes}
+
+
+def quantization_error(device, units=((0, 0), (3, 5), (7, 7))):
+    """Quantize-then-decode at the INT4 decode shape (batch 8, 8 KV heads, 32 query heads,
+    32K context): bf16 K/V ~ N(0, 1) through lbkv_pack (token-wise, g128) and
+    lbkv_decode_attn, compared on sampled (sequence, KV head) units with attention over the
+    unquantized bf16 K/V computed in fp64 (torch). This is the error of 4-bit quantization
+    itself on Gaussian data; the explainer's accuracy paragraph quotes an L2 distance of about
+    0.5-0.6 for INT2 on the paper's own stress test, a different input."""
+    import bit_kv_cache_split_gb300 as pkg
+
+    B, Hkv, Hq, T, g = 8, 8, 32, HEADLINE["ctx"], 128
+    hq = Hq // Hkv
+    rows = []
+    for bits in (4, 2):
+        k, lens = inputs.generate_pack_source(B, Hkv, T, seed=2, device=device)
+        v, _ = inputs.generate_pack_source(B, Hkv, T, seed=12, device=device)
+        q = torch.randn((B, Hq, 128), generator=torch.Generator().manual_seed(22)).to(torch.bfloat16).to(device)
+        kc, ks, kz = pkg.pack(k, lens, bits=bits, layout=0, group=g)
+        vc, vs, vz = pkg.pack(v, lens, bits=bits, layout=0, group=g)
+        out = pkg.decode_attn(q, kc, ks, kz, vc, vs, vz, lens, bits=bits, group=g).double()
+        num = den = 0.0
+        mx = 0.0
+        for b, kvh in units:
+            qq = q[b, kvh * hq:(kvh + 1) * hq].double()
+            kk, vv = k[b, kvh].double(), v[b, kvh].double()
+            p = torch.softmax((qq @ kk.T) / math.sqrt(128.0), dim=-1)
+            ref = p @ vv
+            d = out[b, kvh * hq:(kvh + 1) * hq] - ref
+            num += float((d * d).sum())
+            den += float((ref * ref).sum())
+            mx = max(mx, float(d.abs().max()))
+        rows.append({"workload": f"packed-int{bits}-tokenwise-b{B}-ctx{T}", "bits": bits,
+                     "units": [list(u) for u in units], "rel_l2_vs_unquantized": round(math.sqrt(num / den), 4),
+                     "l2_vs_unquantized": round(math.sqrt(num / len(units)), 4),
+                     "max_abs_vs_unquantized": round(mx, 4)})
+        del k, v, kc, vc, ks, kz, vs, vz
+        torch.cuda.empty_cache()
+    return rows
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: every rank's timed region is one step of its own replica,
     and the job is done when the last one is (weak scaling, one process per GPU)."""
@@ -703,6 +783,7 @@ def main():
     ap.add_argument("--bits", type=int, default=2)
     ap.add_argument("--batch", type=int, default=HEADLINE["batch"])
     ap.add_argument("--ctx", type=int, default=HEADLINE["ctx"])
+    ap.add_argument("--workload", default=None, help="--profile: a sweep workload by name instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_info()
@@ -726,6 +807,11 @@ def main():
 
     if args.profile:
         wl = (inputs.decode_int2 if args.bits == 2 else inputs.decode_int4)(args.batch, args.ctx)
+        if args.workload:
+            named = {w.name: w for w in sweep_workloads()}
+            if args.workload not in named:
+                raise SystemExit(f"unknown workload {args.workload}; one of {sorted(named)}")
+            wl = named[args.workload]
         case = Case(wl, device, min_footprint=0)
         for i in range(args.warmup + args.steps):
             case.call(i)
@@ -768,8 +854,10 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     e2e_val = job_throughput(step_bytes, e2e_ms, world)
 
-    sweep = append = bf16 = paged = rotation = pack = None
+    sweep = append = bf16 = paged = rotation = pack = batch1 = quant = None
     if not args.no_sweep and rank == 0:
+        batch1 = time_batch1_launches(device, peak)
+        quant = quantization_error(device)
         sweep = run_sweep(device, peak)
         append = time_append(device, peak)
         bf16 = time_bf16(device, peak, ms * 1e3)
@@ -784,6 +872,13 @@ def main():
                "sample": f"{n} of {wl.batch * wl.num_kv_heads} (sequence, KV head) units of {wl.name} "
                          f"({rows} query rows, {dt:.1f} s), generated on the host with the same recipe"}
 
+    counters = profiled_counters(wl.name)
+    lane_slots = None
+    if counters.get("inst_per_launch"):
+        lane_slots = round(counters["inst_per_launch"] * 32 / step_bytes, 3)
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    budget = issue_budget(sm_count, clocks.get("sm_mhz"), peak)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -796,15 +891,21 @@ def main():
                        "l2": f"inputs larger than L2: {n_rep} rotating replicas, {footprint / 1e9:.2f} GB, "
                              f"L2 flushed before the timed graph replay"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl.name),
+                         "frac": round(achieved / peak, 4), "traffic": counters.get("dram_bytes_per_launch"),
                          "peak_kind": f"{peak_kind} copy bandwidth", "kernel": "split_decode_kernel INT2 token-wise",
-                         "bytes_per_launch": step_bytes},
+                         "bytes_per_launch": step_bytes,
+                         "lane_slots_per_byte": lane_slots,
+                         "issue_budget": None if budget is None else round(budget, 3),
+                         "issue_budget_how": "SMs x 4 schedulers x 32 lanes x median sampled SM clock / peak",
+                         "counters_from": counters.get("capture")},
             "clocks": clocks,
             "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": args.steps,
             "device_status": status,
             "cpu_baseline": cpu,
+            "batch1_launches": batch1,
+            "quantization_error": quant,
             "sweep": sweep,
             "append": append,
             "bf16_comparator": bf16,

@@ -178,6 +178,18 @@ DecodeKernel pick_kernel(int bits, int kl, int vl, int mode, int group, bool pag
 
 }  // namespace
 
+namespace lbkv {
+
+size_t decode_workspace_plan(const lbkv_desc* desc, int bits, int k_layout, int v_layout, int group,
+                             size_t* zero_bytes) {
+  Plan pl;
+  if (make_plan(desc, bits, k_layout, v_layout, group, &pl) != LBKV_OK) return 0;
+  if (zero_bytes) *zero_bytes = pl.off_ml;
+  return pl.ws_bytes;
+}
+
+}  // namespace lbkv
+
 extern "C" {
 
 size_t lbkv_workspace_bytes(const lbkv_desc* desc, int bits, int k_layout, int v_layout, int group) {

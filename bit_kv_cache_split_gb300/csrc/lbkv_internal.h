@@ -4,6 +4,7 @@
 
 #include <cuda.h>  // CUtensorMap (the driver is reached through the runtime's entry points)
 
+#include "lbkv.h"
 #include "lbkv_decode.cuh"
 
 namespace lbkv {
@@ -71,6 +72,13 @@ struct Bf16Params {
 const void* bf16_split_kernel_fn();
 int bf16_split_smem_bytes();
 int launch_bf16(const Bf16Params& p, cudaStream_t stream);
+
+// Workspace layout of one lbkv_decode_attn call, from the same plan the call uses: the
+// total size (0 when the arguments are invalid or unsupported) and, in *zero_bytes, the
+// length of its head (status word and per-pair split counters) that must read zero when
+// the call starts.
+size_t decode_workspace_plan(const lbkv_desc* desc, int bits, int k_layout, int v_layout, int group,
+                             size_t* zero_bytes);
 
 using DecodeKernel = void (*)(const DecodeParams);
 

@@ -63,7 +63,8 @@ int lbkv_decode_attn_noalloc(const lbkv_desc* desc, const void* q, const uint8_t
   lbkv_desc d = *desc;
   d.workspace = nullptr;
   d.workspace_bytes = 0;
-  const size_t need = lbkv_workspace_bytes(&d, bits, k_layout, v_layout, group);
+  size_t head = 0;
+  const size_t need = lbkv::decode_workspace_plan(&d, bits, k_layout, v_layout, group, &head);
   if (need == 0) {
     // invalid or unsupported arguments: let the regular entry point name the reason
     return lbkv_decode_attn(&d, q, k_codes, k_scale, k_off, v_codes, v_scale, v_off, seq_lens, bits, k_layout,
@@ -73,9 +74,9 @@ int lbkv_decode_attn_noalloc(const lbkv_desc* desc, const void* q, const uint8_t
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != LBKV_OK) return st;
-  // The status word and the per-(sequence, KV head) split counters must start at zero;
-  // they sit in the first 256 + 4 * batch * kv_heads bytes of the workspace layout.
-  const size_t head = 256 + (size_t(4) * (size_t)d.batch * (size_t)d.num_kv_heads + 255) / 256 * 256;
+  // The status word and the split counters (one per pair of the plan, which splits a KV
+  // head into two pairs when it has 32 (query, V group) columns) must start at zero: the
+  // plan gives the length of that head of the layout.
   if (cudaMemsetAsync(scratch, 0, head < need ? head : need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return LBKV_ECUDA;
   d.workspace = scratch;

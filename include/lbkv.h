@@ -244,6 +244,9 @@ LBKV_API int lbkv_decode_bf16(const lbkv_desc* desc, const void* q, const void* 
  *   - Every call on a device shares the array and it keeps the last call's
  *     contents; the call clears the part that must start at zero. Calls that
  *     overlap on the GPU (other streams, other threads) race: order them.
+ *   - The device status word (a bounded wait that ran out) lives in the same array
+ *     and is cleared at the start of every call: lbkv_device_status cannot read it
+ *     for these calls (it takes a caller's workspace).
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. */
 LBKV_API int lbkv_decode_attn_noalloc(const lbkv_desc* desc, const void* q, const uint8_t* k_codes,
                                       const void* k_scale, const void* k_off, const uint8_t* v_codes,

@@ -224,8 +224,10 @@ def sampled_parity(m, wl, units):
     return worst
 
 
-@pytest.mark.parametrize("batch,ctx", [(1, 131072), (8, 32768), (64, 131072)])
+@pytest.mark.parametrize("batch,ctx", [(1, 131072), (8, 32768), (32, 32768), (64, 131072)])
 def test_int2_full_size_sampled(lbkv, batch, ctx):
+    """The INT2 token-wise decode shape at full size (batch 32 at 32K context is the
+    benchmark's headline launch), on sampled (sequence, KV head) units."""
     wl = inputs.decode_int2(batch, ctx)
     sampled_parity(lbkv, wl, [(0, 0), (batch - 1, 7), (batch // 2, 3)])
 

@@ -72,3 +72,27 @@ def test_quantize_then_decode(lbkv, bits, kl, vl):
              v_off=vz.cpu(), seq_lens=lt)
     ref = oracle.decode_ref(to_oracle(t, wl))
     assert_parity(out.float().cpu().numpy().astype(np.float64), ref, f"packed b{bits} k{kl} v{vl}")
+
+
+def test_quantize_then_decode_full_size_int4(lbkv):
+    """bf16 K/V ~ N(0, 1) at the INT4 decode shape (batch 8, 8 KV heads, 32 query heads,
+    32K context) -> lbkv_pack (token-wise, g128) -> lbkv_decode_attn, against the oracle on
+    the packed cache of sampled (sequence, KV head) units."""
+    B, Hkv, Hq, T, g = 8, 8, 32, 32768, 128
+    hq = Hq // Hkv
+    k, lens = inputs.generate_pack_source(B, Hkv, T, seed=2, device="cuda")
+    v, _ = inputs.generate_pack_source(B, Hkv, T, seed=12, device="cuda")
+    q = torch.randn((B, Hq, 128), generator=torch.Generator().manual_seed(22)).to(torch.bfloat16)
+    kc, ks, kz = lbkv.pack(k, lens, bits=4, layout=0, group=g)
+    vc, vs, vz = lbkv.pack(v, lens, bits=4, layout=0, group=g)
+    del k, v
+    out = lbkv.decode_attn(q.cuda(), kc, ks, kz, vc, vs, vz, lens, bits=4, group=g)
+    torch.cuda.synchronize()
+    got_all = out.float().cpu().numpy().astype(np.float64)
+    for b, kvh in [(0, 0), (3, 5), (7, 7)]:
+        sl = lambda x: x[b:b + 1, kvh:kvh + 1].contiguous().cpu()  # noqa: E731
+        t = dict(q=q[b:b + 1, kvh * hq:(kvh + 1) * hq].contiguous(), k_codes=sl(kc), k_scale=sl(ks), k_off=sl(kz),
+                 v_codes=sl(vc), v_scale=sl(vs), v_off=sl(vz), seq_lens=torch.tensor([T], dtype=torch.int32))
+        wl = inputs.Workload("packed-int4-b8-ctx32768", 1, hq, 1, [T], bits=4, group=g)
+        ref = oracle.decode_ref(to_oracle(t, wl))[0]
+        assert_parity(got_all[b, kvh * hq:(kvh + 1) * hq], ref, f"packed INT4 full size unit ({b},{kvh})")
