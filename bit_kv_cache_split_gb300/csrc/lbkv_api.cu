@@ -3,6 +3,8 @@
 // frees or synchronizes (except lbkv_device_status, documented as such).
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <unordered_map>
 
@@ -83,7 +85,24 @@ struct Plan {
   int unit_tokens, n_cta;
   int ring_off, ring_per_warp, entry_bytes, smem_bytes, threads;
   size_t off_done, off_ml, off_o, off_wml, off_wo, ws_bytes;
+  DecodeKernel tc_fn;  // the tensor-core QK^T kernel when it takes the call, else nullptr
 };
+
+// LBKV_DECODE_KERNEL=mma in the environment makes every call take the mma.sync kernel (a
+// diagnostic switch for comparing the two kernels on the same inputs).
+bool mma_kernel_forced() {
+  static const bool forced = [] {
+    const char* e = std::getenv("LBKV_DECODE_KERNEL");
+    return e != nullptr && std::strcmp(e, "mma") == 0;
+  }();
+  return forced;
+}
+
+template <bool PAGED>
+TcKernelInfo pick_tc_of(int bits, int vl, int mode, int lg) {
+  if (bits == 2) return vl ? tc_kernel<2, 1, PAGED>(mode, lg) : tc_kernel<2, 0, PAGED>(mode, lg);
+  return vl ? tc_kernel<4, 1, PAGED>(mode, lg) : tc_kernel<4, 0, PAGED>(mode, lg);
+}
 
 // Validates shapes and format, then fixes the persistent grid and the rings.
 int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl) {
@@ -120,32 +139,62 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   int st = current_device_props(&sms, &smem_optin);
   if (st) return st;
 
-  // ring entry: one item of `ut` tokens, K half then V half
-  const int ut = kChunk * unit_chunks(bits, pl->mode, group == 128 ? 7 : group == 64 ? 6 : 5);
-  const EntryLayout el = entry_layout(bits, kl, vl, ut, group);
-  pl->unit_tokens = ut;
-  pl->entry_bytes = el.bytes;
-  const int warps = decode_warps(bits, pl->mode, pl->gv);
-  pl->threads = 32 * warps;
-  pl->ring_off = kPrologueBytes + merge_bytes(pl->hq, warps);
-  const int budget = smem_optin - pl->ring_off;
-  int r_w = budget / (warps * pl->entry_bytes);
-  if (r_w > kMaxRing / (2 * warps)) r_w = kMaxRing / (2 * warps);  // two mbarriers per entry
-  if (r_w < 1) return LBKV_EUNSUPPORTED;
-  pl->ring_per_warp = r_w;
-  pl->smem_bytes = pl->ring_off + warps * r_w * pl->entry_bytes;
+  const int lg = group == 128 ? 7 : group == 64 ? 6 : 5;
+  // A token-wise K side takes the tensor-core QK^T kernel: items of 128 tokens, one per
+  // group of four warps, a ring per group with at least two entries.
+  pl->tc_fn = nullptr;
+  int ring_units = 0;  // warps or groups sharing the rings
+  if (kl == LBKV_TOKENWISE && !mma_kernel_forced()) {
+    const TcKernelInfo ti = d->page_table ? pick_tc_of<true>(bits, vl, pl->mode, lg)
+                                          : pick_tc_of<false>(bits, vl, pl->mode, lg);
+    if (ti.fn) {
+      const int groups = ti.warps / 4;
+      const int ring_off = (int)round_up((size_t)ti.merge_off + merge_bytes(pl->hq, ti.warps), 128);
+      int r = (smem_optin - ring_off) / (groups * ti.entry_bytes);
+      if (r > ti.max_ring) r = ti.max_ring;
+      if (r >= 2) {
+        pl->tc_fn = ti.fn;
+        pl->unit_tokens = 128;
+        pl->entry_bytes = ti.entry_bytes;
+        pl->threads = 32 * ti.warps;
+        pl->ring_off = ring_off;
+        pl->ring_per_warp = r;
+        pl->smem_bytes = ring_off + groups * r * ti.entry_bytes;
+        ring_units = groups;
+      }
+    }
+  }
+  if (!pl->tc_fn) {
+    // ring entry: one item of `ut` tokens, K half then V half
+    const int ut = kChunk * unit_chunks(bits, pl->mode, lg);
+    const EntryLayout el = entry_layout(bits, kl, vl, ut, group);
+    pl->unit_tokens = ut;
+    pl->entry_bytes = el.bytes;
+    const int warps = decode_warps(bits, pl->mode, pl->gv);
+    pl->threads = 32 * warps;
+    pl->ring_off = kPrologueBytes + merge_bytes(pl->hq, warps);
+    const int budget = smem_optin - pl->ring_off;
+    int r_w = budget / (warps * pl->entry_bytes);
+    if (r_w > kMaxRing / (2 * warps)) r_w = kMaxRing / (2 * warps);  // two mbarriers per entry
+    if (r_w < 1) return LBKV_EUNSUPPORTED;
+    pl->ring_per_warp = r_w;
+    pl->smem_bytes = pl->ring_off + warps * r_w * pl->entry_bytes;
+    ring_units = warps;
+  }
+  const int ut = pl->unit_tokens;
 
   // Persistent grid, one CTA per SM: the kernel splits the items of all pairs (from the
   // device lengths) over the CTAs, evenly once each pair boundary is counted as
   // kSplitBoundaryTokens of work. A CTA holds partials of at most two pairs.
   const long long units = (long long)d->batch * pl->hkv;  // pairs
   pl->win = win ? 1 : 0;
-  // Small problems: about one item per warp at most (from the capacity, the host's bound on
-  // the device lengths), so that a pair is split over fewer CTAs and their partials merge
-  // sooner. Measured on batch 8 at 4K context: 18.3 us against 24.7 us with every SM.
+  // Small problems: about one item per warp (per group of the tensor-core kernel) at most
+  // (from the capacity, the host's bound on the device lengths), so that a pair is split
+  // over fewer CTAs and their partials merge sooner. Measured on batch 8 at 4K context:
+  // 18.3 us against 24.7 us with every SM.
   {
     const long long max_items = units * (((long long)d->max_seq_len + ut - 1) / ut);
-    const long long want = (max_items + warps - 1) / warps;
+    const long long want = (max_items + ring_units - 1) / ring_units;
     pl->n_cta = (int)(want < sms ? (want > 0 ? want : 1) : sms);
   }
 
@@ -214,7 +263,8 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   if (desc->k_win && (!aligned16(desc->k_win) || !aligned16(desc->v_win))) return LBKV_EALIGN;
   if (!desc->workspace || desc->workspace_bytes < pl.ws_bytes) return LBKV_EWORKSPACE;
   if (reinterpret_cast<uintptr_t>(desc->workspace) & 255u) return LBKV_EALIGN;
-  DecodeKernel kern = pick_kernel(bits, k_layout, v_layout, pl.mode, group, desc->page_table != nullptr);
+  DecodeKernel kern = pl.tc_fn ? pl.tc_fn
+                               : pick_kernel(bits, k_layout, v_layout, pl.mode, group, desc->page_table != nullptr);
   if (!kern) return LBKV_EUNSUPPORTED;
 
   uint8_t* ws = static_cast<uint8_t*>(desc->workspace);

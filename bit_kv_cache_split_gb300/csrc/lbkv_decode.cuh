@@ -615,9 +615,10 @@ __device__ __forceinline__ void fold_tokenwise_v(WarpState<C>& st, const float (
 }
 
 // Channel-wise V: acc-fold of one token group tau whose s/z rows are s_tau/z_tau:
-// running output += s_tau,d * (bias-free accumulator) / (2^13 factor) + z_tau,d * W,
-// W = sum of the group's weights (fed sum / 2^13) per owned combo.
-template <class C>
+// running output += s_tau,d * (bias-free accumulator) / (FED factor) + z_tau,d * W,
+// W = sum of the group's weights (fed sum / FED) per owned combo; the weights were fed
+// as P * FED.
+template <class C, int FED = 8192>
 __device__ __forceinline__ void fold_channelwise_v(WarpState<C>& st, const float (&accv)[8][C::NTV][4],
                                                    const float (&Wg)[C::NO], const __half* s_tau,
                                                    const __half* z_tau, const LaneCols& lc) {
@@ -630,7 +631,7 @@ __device__ __forceinline__ void fold_channelwise_v(WarpState<C>& st, const float
 #pragma unroll
   for (int i = 0; i < C::NQ; ++i) {
     const int v = live_tile<C>(i), e = live_col<C>(i, lc);
-    const float W = Wg[C::DUP ? 0 : i] * (1.f / 8192.f);
+    const float W = Wg[C::DUP ? 0 : i] * (1.f / (float)FED);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -641,7 +642,7 @@ __device__ __forceinline__ void fold_channelwise_v(WarpState<C>& st, const float
         const float s = (k & 1) ? s2.y : s2.x;
         const float z = (k & 1) ? z2.y : z2.x;
         const float a = (e == 0) ? accv[mt][v][2 * row] : accv[mt][v][2 * row + 1];
-        st.o_run[mt][row][i] = fmaf(s * (1.f / (8192.f * v_mult<BITS>(mt))), a, fmaf(z, W, st.o_run[mt][row][i]));
+        st.o_run[mt][row][i] = fmaf(s * (1.f / ((float)FED * v_mult<BITS>(mt))), a, fmaf(z, W, st.o_run[mt][row][i]));
       }
   }
 }
