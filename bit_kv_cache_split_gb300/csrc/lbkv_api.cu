@@ -80,6 +80,10 @@ PagedArgs paged_args(const lbkv_desc* d) {
 // token-wise): 81.5 us against 100.8 us without the boundary cost.
 constexpr int kSplitBoundaryTokens = 2048;
 
+// Shared memory the decode kernels declare statically (the split scan and a few words),
+// kept free below the opt-in limit when the rings are sized.
+constexpr int kStaticSmemReserve = 2048;
+
 struct Plan {
   int hq, hkv, kv_shift, mode, gv, win;
   int unit_tokens, n_cta;
@@ -150,7 +154,8 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
     if (ti.fn) {
       const int groups = ti.warps / 4;
       const int ring_off = (int)round_up((size_t)ti.merge_off + merge_bytes(pl->hq, ti.warps), 128);
-      int r = (smem_optin - ring_off) / (groups * ti.entry_bytes);
+      // (the kernel's static shared memory, about 1 KB, counts against the same limit)
+      int r = (smem_optin - kStaticSmemReserve - ring_off) / (groups * ti.entry_bytes);
       if (r > ti.max_ring) r = ti.max_ring;
       if (r >= 2) {
         pl->tc_fn = ti.fn;

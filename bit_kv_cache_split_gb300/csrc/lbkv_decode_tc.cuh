@@ -379,7 +379,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tc_decode_kernel(const __grid_c
   Cursor cv = start, con = start;
   advance(cv, grp);
   advance(con, grp);
-  int cv_pos = 0, con_pos = 0;
+  int cv_pos = 0, con_pos = 0;   // positions in the group's item sequence
+  int cv_r = 0, con_r = 0;       // their ring entries (position mod R)
+  uint32_t cv_ph = 0, con_ph = 0;  // and mbarrier phase parities (position / R mod 2)
+  int kis_r = 0, vis_r = 0;  // ring entries of the next refills (the issue positions mod R)
   bool gf = false;      // the group gave up waiting (uniform: read after a group barrier)
   bool failed = false;  // this thread's own wait gave up
   int n_commit = 0;     // products committed by the leader (S barrier completions issued)
@@ -403,9 +406,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tc_decode_kernel(const __grid_c
 
   // Converts the K half of the item at `k` (position pos) into this warp's lane quadrant of
   // A buffer `buf` and keeps the token's K scales/offsets (half2 (s, z) per group).
-  auto convert = [&](const Cursor& k, int pos, int buf, uint32_t (&ksz)[GK]) {
-    const int r = pos % R;
-    const uint32_t ph = (uint32_t)((pos / R) & 1);
+  auto convert = [&](const Cursor& k, int r, uint32_t ph, int buf, uint32_t (&ksz)[GK]) {
     if (!gf && !failed && !mbar_wait(kbar(r), ph, p.status, kStatusConsumerTimeout)) {
       failed = true;
       gfail[grp] = 1;
@@ -561,9 +562,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tc_decode_kernel(const __grid_c
         for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] = 0.f;
 
     // consumes the item at `k` (position pos, scores in buffer buf, token's K scales ksz)
-    auto consume = [&](const Cursor& k, int pos, int buf, const uint32_t (&ksz)[GK]) {
-      const int r = pos % R;
-      const uint32_t ph = (uint32_t)((pos / R) & 1);
+    auto consume = [&](const Cursor& k, int pos, int r, uint32_t ph, const uint32_t (&ksz)[GK]) {
+      const int buf = pos & 1;
       const uint32_t sph = (uint32_t)((pos >> 1) & 1);
       const int nv = min(UNIT, k.L - k.t * UNIT);
       const int tk = 32 * quad + lane;
@@ -744,39 +744,45 @@ __global__ void __launch_bounds__(C::THREADS, 1) tc_decode_kernel(const __grid_c
     // -------------------------------------------------- the group's items of this segment
     if (cv.i < NL && cv.u == u) {
       uint32_t ksz_cur[GK], ksz_nx[GK];
-      convert(cv, cv_pos, cv_pos & 1, ksz_cur);
+      convert(cv, cv_r, cv_ph, cv_pos & 1, ksz_cur);
       group_barrier(grp);
       gf = gfail[grp] != 0;
       issue_qk(cv_pos & 1);
       if (leader && !gf && !failed && kis.i < NL) {  // the converted entry's K half is free
-        copy_half(false, kis, kis_pos % R);
+        copy_half(false, kis, kis_r);
         advance(kis, NG);
         ++kis_pos;
+        if (++kis_r == R) kis_r = 0;
       }
       advance(cv, NG);
       ++cv_pos;
-      for (; con.i < NL && con.u == u; advance(con, NG), ++con_pos) {
+      if (++cv_r == R) cv_r = 0, cv_ph ^= 1u;
+      for (; con.i < NL && con.u == u; advance(con, NG), ++con_pos, con_r = (con_r + 1 == R) ? 0 : con_r + 1,
+                                        con_ph ^= (con_r == 0) ? 1u : 0u) {
         const bool has_next = cv.i < NL && cv.u == u;
         if (has_next) {
-          convert(cv, cv_pos, cv_pos & 1, ksz_nx);
+          convert(cv, cv_r, cv_ph, cv_pos & 1, ksz_nx);
           group_barrier(grp);
           gf = gfail[grp] != 0;
           issue_qk(cv_pos & 1);
           if (leader && !gf && !failed && kis.i < NL) {
-            copy_half(false, kis, kis_pos % R);
+            copy_half(false, kis, kis_r);
             advance(kis, NG);
             ++kis_pos;
+            if (++kis_r == R) kis_r = 0;
           }
           advance(cv, NG);
           ++cv_pos;
+          if (++cv_r == R) cv_r = 0, cv_ph ^= 1u;
         }
-        consume(con, con_pos, con_pos & 1, ksz_cur);
+        consume(con, con_pos, con_r, con_ph, ksz_cur);
         group_barrier(grp);  // every warp is done with the item's V half and its scores
         gf = gfail[grp] != 0;
         if (leader && !gf && !failed && vis.i < NL) {
-          copy_half(true, vis, vis_pos % R);
+          copy_half(true, vis, vis_r);
           advance(vis, NG);
           ++vis_pos;
+          if (++vis_r == R) vis_r = 0;
         }
         if (has_next) {
 #pragma unroll
