@@ -89,7 +89,7 @@ struct Plan {
   int unit_tokens, n_cta;
   int ring_off, ring_per_warp, entry_bytes, smem_bytes, threads;
   size_t off_done, off_ml, off_o, off_wml, off_wo, ws_bytes;
-  DecodeKernel tc_fn;  // the tensor-core QK^T kernel when it takes the call, else nullptr
+  DecodeKernel tc_fn;  // the tensor-core QK^T variant when it takes the call, else nullptr
 };
 
 // LBKV_DECODE_KERNEL=mma in the environment makes every call take the mma.sync kernel (a
@@ -103,9 +103,9 @@ bool mma_kernel_forced() {
 }
 
 template <bool PAGED>
-TcKernelInfo pick_tc_of(int bits, int vl, int mode, int lg) {
-  if (bits == 2) return vl ? tc_kernel<2, 1, PAGED>(mode, lg) : tc_kernel<2, 0, PAGED>(mode, lg);
-  return vl ? tc_kernel<4, 1, PAGED>(mode, lg) : tc_kernel<4, 0, PAGED>(mode, lg);
+DecodeKernel pick_tcq_of(int bits, int vl, int mode, int lg) {
+  if (bits == 2) return vl ? decode_kernel_tcq<2, 1, PAGED>(mode, lg) : decode_kernel_tcq<2, 0, PAGED>(mode, lg);
+  return vl ? decode_kernel_tcq<4, 1, PAGED>(mode, lg) : decode_kernel_tcq<4, 0, PAGED>(mode, lg);
 }
 
 // Validates shapes and format, then fixes the persistent grid and the rings.
@@ -144,47 +144,26 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   if (st) return st;
 
   const int lg = group == 128 ? 7 : group == 64 ? 6 : 5;
-  // A token-wise K side takes the tensor-core QK^T kernel: items of 128 tokens, one per
-  // group of four warps, a ring per group with at least two entries.
+  // A token-wise K side takes the kernel's tensor-core QK^T variant where it is built for
+  // the shape (its prologue adds the product barriers, the query's B tile and the weight tiles).
   pl->tc_fn = nullptr;
-  int ring_units = 0;  // warps or groups sharing the rings
-  if (kl == LBKV_TOKENWISE && !mma_kernel_forced()) {
-    const TcKernelInfo ti = d->page_table ? pick_tc_of<true>(bits, vl, pl->mode, lg)
-                                          : pick_tc_of<false>(bits, vl, pl->mode, lg);
-    if (ti.fn) {
-      const int groups = ti.warps / 4;
-      const int ring_off = (int)round_up((size_t)ti.merge_off + merge_bytes(pl->hq, ti.warps), 128);
-      // (the kernel's static shared memory, about 1 KB, counts against the same limit)
-      int r = (smem_optin - kStaticSmemReserve - ring_off) / (groups * ti.entry_bytes);
-      if (r > ti.max_ring) r = ti.max_ring;
-      if (r >= 2) {
-        pl->tc_fn = ti.fn;
-        pl->unit_tokens = 128;
-        pl->entry_bytes = ti.entry_bytes;
-        pl->threads = 32 * ti.warps;
-        pl->ring_off = ring_off;
-        pl->ring_per_warp = r;
-        pl->smem_bytes = ring_off + groups * r * ti.entry_bytes;
-        ring_units = groups;
-      }
-    }
-  }
-  if (!pl->tc_fn) {
-    // ring entry: one item of `ut` tokens, K half then V half
+  if (kl == LBKV_TOKENWISE && !mma_kernel_forced())
+    pl->tc_fn = d->page_table ? pick_tcq_of<true>(bits, vl, pl->mode, lg) : pick_tcq_of<false>(bits, vl, pl->mode, lg);
+  // ring entry: one item of `ut` tokens, K half then V half
+  const int warps = decode_warps(bits, pl->mode, pl->gv);
+  {
     const int ut = kChunk * unit_chunks(bits, pl->mode, lg);
     const EntryLayout el = entry_layout(bits, kl, vl, ut, group);
     pl->unit_tokens = ut;
     pl->entry_bytes = el.bytes;
-    const int warps = decode_warps(bits, pl->mode, pl->gv);
     pl->threads = 32 * warps;
-    pl->ring_off = kPrologueBytes + merge_bytes(pl->hq, warps);
-    const int budget = smem_optin - pl->ring_off;
+    pl->ring_off = (pl->tc_fn ? kTcqPrologueBytes : kPrologueBytes) + merge_bytes(pl->hq, warps);
+    const int budget = smem_optin - kStaticSmemReserve - pl->ring_off;
     int r_w = budget / (warps * pl->entry_bytes);
     if (r_w > kMaxRing / (2 * warps)) r_w = kMaxRing / (2 * warps);  // two mbarriers per entry
     if (r_w < 1) return LBKV_EUNSUPPORTED;
     pl->ring_per_warp = r_w;
     pl->smem_bytes = pl->ring_off + warps * r_w * pl->entry_bytes;
-    ring_units = warps;
   }
   const int ut = pl->unit_tokens;
 
@@ -193,13 +172,12 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   // kSplitBoundaryTokens of work. A CTA holds partials of at most two pairs.
   const long long units = (long long)d->batch * pl->hkv;  // pairs
   pl->win = win ? 1 : 0;
-  // Small problems: about one item per warp (per group of the tensor-core kernel) at most
-  // (from the capacity, the host's bound on the device lengths), so that a pair is split
-  // over fewer CTAs and their partials merge sooner. Measured on batch 8 at 4K context:
-  // 18.3 us against 24.7 us with every SM.
+  // Small problems: about one item per warp at most (from the capacity, the host's bound on
+  // the device lengths), so that a pair is split over fewer CTAs and their partials merge
+  // sooner. Measured on batch 8 at 4K context: 18.3 us against 24.7 us with every SM.
   {
     const long long max_items = units * (((long long)d->max_seq_len + ut - 1) / ut);
-    const long long want = (max_items + ring_units - 1) / ring_units;
+    const long long want = (max_items + warps - 1) / warps;
     pl->n_cta = (int)(want < sms ? (want > 0 ? want : 1) : sms);
   }
 

@@ -105,25 +105,17 @@ LBKV_DECLARE_DECODE(4, 1, 0)
 LBKV_DECLARE_DECODE(4, 1, 1)
 #undef LBKV_DECLARE_DECODE
 
-// The tensor-core QK^T kernel (token-wise K side) for (column mode, log2 group) of one bit
-// width, V layout and cache kind: the kernel (nullptr when not built) and what the launch
-// needs to lay out its shared memory.
-struct TcKernelInfo {
-  DecodeKernel fn;
-  int merge_off;    // shared-memory offset of the merge area (the rings follow it)
-  int entry_bytes;  // one ring entry (128 tokens, K half and V half)
-  int warps;        // warps per CTA, in groups of four
-  int max_ring;     // ring entries per group at most
-};
+// The tensor-core QK^T variant of the same kernel (token-wise K side) for (column mode,
+// log2 group), or nullptr when the variant does not fit that shape.
 template <int BITS, int VL, bool PAGED>
-TcKernelInfo tc_kernel(int mode, int log2g);
-#define LBKV_DECLARE_TC(B, V)                                  \
-  template <> TcKernelInfo tc_kernel<B, V, false>(int, int); \
-  template <> TcKernelInfo tc_kernel<B, V, true>(int, int);
-LBKV_DECLARE_TC(2, 0)
-LBKV_DECLARE_TC(2, 1)
-LBKV_DECLARE_TC(4, 0)
-LBKV_DECLARE_TC(4, 1)
-#undef LBKV_DECLARE_TC
+DecodeKernel decode_kernel_tcq(int mode, int log2g);
+#define LBKV_DECLARE_TCQ(B, V)                                        \
+  template <> DecodeKernel decode_kernel_tcq<B, V, false>(int, int); \
+  template <> DecodeKernel decode_kernel_tcq<B, V, true>(int, int);
+LBKV_DECLARE_TCQ(2, 0)
+LBKV_DECLARE_TCQ(2, 1)
+LBKV_DECLARE_TCQ(4, 0)
+LBKV_DECLARE_TCQ(4, 1)
+#undef LBKV_DECLARE_TCQ
 
 }  // namespace lbkv
