@@ -89,17 +89,27 @@ struct Plan {
   int unit_tokens, n_cta;
   int ring_off, ring_per_warp, entry_bytes, smem_bytes, threads;
   size_t off_done, off_ml, off_o, off_wml, off_wo, ws_bytes;
-  DecodeKernel tc_fn;  // the tensor-core QK^T variant when it takes the call, else nullptr
+  DecodeKernel tc_fn;  // the group kernel or the tensor-core QK^T variant when one takes the call
+  bool grp;            // the group kernel (rings per group of four warps)
 };
 
-// LBKV_DECODE_KERNEL=mma in the environment makes every call take the mma.sync kernel (a
-// diagnostic switch for comparing the two kernels on the same inputs).
-bool mma_kernel_forced() {
-  static const bool forced = [] {
+// LBKV_DECODE_KERNEL in the environment selects the kernel for a token-wise K side: "mma"
+// (the mma.sync split-decode kernel), "tcq" (its per-warp tensor-core QK^T variant); by
+// default the group kernel. A diagnostic switch for comparing kernels on the same inputs.
+int kernel_choice() {
+  static const int choice = [] {
     const char* e = std::getenv("LBKV_DECODE_KERNEL");
-    return e != nullptr && std::strcmp(e, "mma") == 0;
+    if (e != nullptr && std::strcmp(e, "mma") == 0) return 0;
+    if (e != nullptr && std::strcmp(e, "tcq") == 0) return 1;
+    return 2;
   }();
-  return forced;
+  return choice;
+}
+
+template <bool PAGED>
+DecodeKernel pick_grp_of(int bits, int vl, int mode, int lg) {
+  if (bits == 2) return vl ? decode_kernel_grp<2, 1, PAGED>(mode, lg) : decode_kernel_grp<2, 0, PAGED>(mode, lg);
+  return vl ? decode_kernel_grp<4, 1, PAGED>(mode, lg) : decode_kernel_grp<4, 0, PAGED>(mode, lg);
 }
 
 template <bool PAGED>
@@ -144,14 +154,36 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   if (st) return st;
 
   const int lg = group == 128 ? 7 : group == 64 ? 6 : 5;
-  // A token-wise K side takes the kernel's tensor-core QK^T variant where it is built for
-  // the shape (its prologue adds the product barriers, the query's B tile and the weight tiles).
-  pl->tc_fn = nullptr;
-  if (kl == LBKV_TOKENWISE && !mma_kernel_forced())
-    pl->tc_fn = d->page_table ? pick_tcq_of<true>(bits, vl, pl->mode, lg) : pick_tcq_of<false>(bits, vl, pl->mode, lg);
-  // ring entry: one item of `ut` tokens, K half then V half
+  // A token-wise K side takes the group kernel (items of 128 tokens, a ring per group of
+  // four warps with at least two entries) where it is built for the shape, else the
+  // split-decode kernel (its tensor-core QK^T variant on request).
   const int warps = decode_warps(bits, pl->mode, pl->gv);
-  {
+  pl->tc_fn = nullptr;
+  pl->grp = false;
+  if (kl == LBKV_TOKENWISE && kernel_choice() == 2) {
+    DecodeKernel fn = d->page_table ? pick_grp_of<true>(bits, vl, pl->mode, lg) : pick_grp_of<false>(bits, vl, pl->mode, lg);
+    if (fn) {
+      const int groups = warps / 4;
+      const EntryLayout el = entry_layout(bits, kl, vl, 128, group);
+      const int ring_off = (int)round_up((size_t)kGrpMergeOffset + merge_bytes(pl->hq, warps), 128);
+      int r = (smem_optin - kStaticSmemReserve - ring_off) / (groups * el.bytes);
+      if (r > 12) r = 12;
+      if (r >= 2) {
+        pl->tc_fn = fn;
+        pl->grp = true;
+        pl->unit_tokens = 128;
+        pl->entry_bytes = el.bytes;
+        pl->threads = 32 * warps;
+        pl->ring_off = ring_off;
+        pl->ring_per_warp = r;
+        pl->smem_bytes = ring_off + groups * r * el.bytes;
+      }
+    }
+  }
+  if (!pl->tc_fn && kl == LBKV_TOKENWISE && kernel_choice() == 1)
+    pl->tc_fn = d->page_table ? pick_tcq_of<true>(bits, vl, pl->mode, lg) : pick_tcq_of<false>(bits, vl, pl->mode, lg);
+  if (!pl->grp) {
+    // ring entry: one item of `ut` tokens, K half then V half
     const int ut = kChunk * unit_chunks(bits, pl->mode, lg);
     const EntryLayout el = entry_layout(bits, kl, vl, ut, group);
     pl->unit_tokens = ut;
@@ -177,7 +209,8 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   // sooner. Measured on batch 8 at 4K context: 18.3 us against 24.7 us with every SM.
   {
     const long long max_items = units * (((long long)d->max_seq_len + ut - 1) / ut);
-    const long long want = (max_items + warps - 1) / warps;
+    const int units_per_cta = pl->grp ? warps / 4 : warps;  // warps, or groups of four
+    const long long want = (max_items + units_per_cta - 1) / units_per_cta;
     pl->n_cta = (int)(want < sms ? (want > 0 ? want : 1) : sms);
   }
 

@@ -957,6 +957,9 @@ constexpr int kTcqBarOffset = kPrologueBytes;
 constexpr int kTcqBOffset = kPrologueBytes + 1024;
 constexpr int kTcqPOffset = kTcqBOffset + 48 * 128;
 constexpr int kTcqPrologueBytes = kTcqPOffset + 8192;
+// The group kernel (lbkv_decode_grp.cuh): shared-memory offset of its merge area, after its
+// mbarriers, counters, prologue, B tile and weight tiles; its rings follow the merge area.
+constexpr int kGrpMergeOffset = 7168 + 96 * 128 + 8192;
 
 template <class C>
 struct TcqShape {

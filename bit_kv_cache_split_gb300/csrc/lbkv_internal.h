@@ -118,4 +118,17 @@ LBKV_DECLARE_TCQ(4, 0)
 LBKV_DECLARE_TCQ(4, 1)
 #undef LBKV_DECLARE_TCQ
 
+// The group kernel (token-wise K side; QK^T on the tensor cores, one product per 128-token
+// item shared by four warps) for (column mode, log2 group), or nullptr when it does not fit.
+template <int BITS, int VL, bool PAGED>
+DecodeKernel decode_kernel_grp(int mode, int log2g);
+#define LBKV_DECLARE_GRP(B, V)                                        \
+  template <> DecodeKernel decode_kernel_grp<B, V, false>(int, int); \
+  template <> DecodeKernel decode_kernel_grp<B, V, true>(int, int);
+LBKV_DECLARE_GRP(2, 0)
+LBKV_DECLARE_GRP(2, 1)
+LBKV_DECLARE_GRP(4, 0)
+LBKV_DECLARE_GRP(4, 1)
+#undef LBKV_DECLARE_GRP
+
 }  // namespace lbkv
