@@ -74,12 +74,17 @@ struct GrpCursor {
   int i, u, t, L, n, b, kvh, pos;  // local item, pair, item in pair, pair tokens and items,
                                    // sequence, cached KV head, position in the group's sequence
 };
+// Arrival counters per group and position parity: a warp converts position j + 2 only after
+// the product of j (so after every warp converted j), and finishes position j + 2 only after
+// every warp converted j + 2 (so after every warp finished j): the four arrivals of a
+// position never interleave with those of the next position of the same parity, while
+// those of consecutive positions may.
 struct GrpShared {
-  unsigned conv_cnt[4];  // warps that converted an item, per group (acquire-release counter)
-  unsigned done_cnt[4];  // warps that finished an item's PV, per group
-  int n_commit[4];       // products committed per group
+  unsigned conv_cnt[4][2];  // warps that converted an item (acquire-release counters)
+  unsigned done_cnt[4][2];  // warps that finished an item's PV
+  int n_commit[4];          // products committed per group
   int pad[4];
-  GrpCursor kc[4], vc[4];  // issue cursors per group
+  GrpCursor kc[4], vc[4];   // issue cursors per group
 };
 
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
@@ -148,7 +153,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) grp_decode_kernel(const __grid_
     for (int G = 0; G < NG; ++G) {
       const uint32_t b0 = smem_addr(smem) + 8u * (uint32_t)(G * (2 * R + 2));
       for (int r = 0; r < 2 * R + 2; ++r) mbar_init(b0 + 8u * r, 1);
-      gs->conv_cnt[G] = gs->done_cnt[G] = 0u;
+      gs->conv_cnt[G][0] = gs->conv_cnt[G][1] = gs->done_cnt[G][0] = gs->done_cnt[G][1] = 0u;
       gs->n_commit[G] = 0;
     }
     mbar_init_fence();
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) grp_decode_kernel(const __grid_
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) {
-      const unsigned prev = atom_add_acq_rel(&gs->conv_cnt[grp], 1u);
+      const unsigned prev = atom_add_acq_rel(&gs->conv_cnt[grp][buf], 1u);
       if ((prev & 3u) == 3u) {  // the group's last warp: product, then the K refill
         tc::fence_after_sync();
         const uint32_t bb = smem_addr(btile);
@@ -694,7 +699,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) grp_decode_kernel(const __grid_
       }
       __syncwarp();  // the weight tile and the entry's V half are read
       if (lane == 0) {
-        const unsigned prev = atom_add_acq_rel(&gs->done_cnt[grp], 1u);
+        const unsigned prev = atom_add_acq_rel(&gs->done_cnt[grp][buf], 1u);
         if ((prev & 3u) == 3u && !failed) issue_next(true);  // the group's last warp: V refill
       }
       __syncwarp();
