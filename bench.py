@@ -10,6 +10,7 @@ token-wise K/V, group 128, 32 query / 8 KV heads, head_dim 128, batch 32, 32K
 context. The other workloads run as a sweep.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {lbkv,reference}] [--no-sweep]
+       python bench.py --micro   (tensor-core operation rates, bit_kv_cache_split_gb300/micro)
        python bench.py --profile [--bits B] [--batch N] [--ctx T] [--workload NAME] [--steps K] [--warmup W]
 (--profile: only eager calls of one workload, for ncu captures)
 Under torchrun (N > 1) every rank runs its own replica on its GPU (the path
@@ -717,6 +718,22 @@ def quantization_error(device, units=((0, 0), (3, 5), (7, 7))):
     return rows
 
 
+def run_micro():
+    """Builds and runs bit_kv_cache_split_gb300/micro/tc_rates.cu: cycles per tcgen05 product
+    (kind::f8f6f4, M = 128, N = 16..256, A in tensor memory) and per tensor-memory store and
+    load, with 1, 4 and 16 warps per SM (one JSON line each)."""
+    from bit_kv_cache_split_gb300 import build as libbuild
+
+    src = os.path.join(ROOT, "bit_kv_cache_split_gb300", "micro", "tc_rates.cu")
+    os.makedirs(libbuild.BUILD, exist_ok=True)
+    exe = os.path.join(libbuild.BUILD, "tc_rates")
+    subprocess.run([libbuild.nvcc(), *libbuild.ARCH, "-O2", src, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    sys.stdout.write(r.stdout)
+    if r.returncode != 0:
+        raise SystemExit(f"microbenchmark failed: {r.stderr.strip()}")
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: every rank's timed region is one step of its own replica,
     and the job is done when the last one is (weak scaling, one process per GPU)."""
@@ -784,12 +801,17 @@ def main():
     ap.add_argument("--batch", type=int, default=HEADLINE["batch"])
     ap.add_argument("--ctx", type=int, default=HEADLINE["ctx"])
     ap.add_argument("--workload", default=None, help="--profile: a sweep workload by name instead")
+    ap.add_argument("--micro", action="store_true",
+                    help="the tensor-core microbenchmark (tcgen05 product, TMEM store and load rates) only")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_info()
 
     if args.impl == "reference":
         reference_arm(args, world, rank)
+        return
+    if args.micro:
+        run_micro()
         return
 
     import bit_kv_cache_split_gb300 as pkg

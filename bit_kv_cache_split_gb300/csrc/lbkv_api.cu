@@ -89,21 +89,17 @@ struct Plan {
   int unit_tokens, n_cta;
   int ring_off, ring_per_warp, entry_bytes, smem_bytes, threads;
   size_t off_done, off_ml, off_o, off_wml, off_wo, ws_bytes;
-  DecodeKernel tc_fn;  // the group kernel or the tensor-core QK^T variant when one takes the call
-  bool grp;            // the group kernel (rings per group of four warps)
+  DecodeKernel tc_fn;  // the tensor-core kernel when it takes the call, else nullptr
+  bool grp;            // the tensor-core kernel (rings per group of four warps)
 };
 
-// LBKV_DECODE_KERNEL in the environment selects the kernel for a token-wise K side: "mma"
-// (the mma.sync split-decode kernel), "tcq" (its per-warp tensor-core QK^T variant); by
-// default the group kernel. A diagnostic switch for comparing kernels on the same inputs.
-int kernel_choice() {
-  static const int choice = [] {
-    const char* e = std::getenv("LBKV_DECODE_KERNEL");
-    if (e != nullptr && std::strcmp(e, "mma") == 0) return 0;
-    if (e != nullptr && std::strcmp(e, "tcq") == 0) return 1;
-    return 2;
-  }();
-  return choice;
+// LBKV_DECODE_KERNEL=tc in the environment (read at every call) makes a token-wise K side
+// take the tensor-core decode kernel (lbkv_decode_grp.cuh) where it is built for the shape;
+// by default every call takes the mma.sync split-decode kernel, which is faster on GB300
+// (measured: 164 us against 288 us at batch 32, 32K context, INT2 token-wise g128).
+bool tc_kernel_requested() {
+  const char* e = std::getenv("LBKV_DECODE_KERNEL");
+  return e != nullptr && std::strcmp(e, "tc") == 0;
 }
 
 template <bool PAGED>
@@ -112,11 +108,6 @@ DecodeKernel pick_grp_of(int bits, int vl, int mode, int lg) {
   return vl ? decode_kernel_grp<4, 1, PAGED>(mode, lg) : decode_kernel_grp<4, 0, PAGED>(mode, lg);
 }
 
-template <bool PAGED>
-DecodeKernel pick_tcq_of(int bits, int vl, int mode, int lg) {
-  if (bits == 2) return vl ? decode_kernel_tcq<2, 1, PAGED>(mode, lg) : decode_kernel_tcq<2, 0, PAGED>(mode, lg);
-  return vl ? decode_kernel_tcq<4, 1, PAGED>(mode, lg) : decode_kernel_tcq<4, 0, PAGED>(mode, lg);
-}
 
 // Validates shapes and format, then fixes the persistent grid and the rings.
 int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl) {
@@ -154,13 +145,13 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
   if (st) return st;
 
   const int lg = group == 128 ? 7 : group == 64 ? 6 : 5;
-  // A token-wise K side takes the group kernel (items of 128 tokens, a ring per group of
-  // four warps with at least two entries) where it is built for the shape, else the
-  // split-decode kernel (its tensor-core QK^T variant on request).
+  // With LBKV_DECODE_KERNEL=tc a token-wise K side takes the tensor-core kernel (items of 128
+  // tokens, a ring per group of four warps with at least two entries) where it is built for
+  // the shape; every other call takes the split-decode kernel.
   const int warps = decode_warps(bits, pl->mode, pl->gv);
   pl->tc_fn = nullptr;
   pl->grp = false;
-  if (kl == LBKV_TOKENWISE && kernel_choice() == 2) {
+  if (kl == LBKV_TOKENWISE && tc_kernel_requested()) {
     DecodeKernel fn = d->page_table ? pick_grp_of<true>(bits, vl, pl->mode, lg) : pick_grp_of<false>(bits, vl, pl->mode, lg);
     if (fn) {
       const int groups = warps / 4;
@@ -180,8 +171,6 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
       }
     }
   }
-  if (!pl->tc_fn && kl == LBKV_TOKENWISE && kernel_choice() == 1)
-    pl->tc_fn = d->page_table ? pick_tcq_of<true>(bits, vl, pl->mode, lg) : pick_tcq_of<false>(bits, vl, pl->mode, lg);
   if (!pl->grp) {
     // ring entry: one item of `ut` tokens, K half then V half
     const int ut = kChunk * unit_chunks(bits, pl->mode, lg);
@@ -189,7 +178,7 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
     pl->unit_tokens = ut;
     pl->entry_bytes = el.bytes;
     pl->threads = 32 * warps;
-    pl->ring_off = (pl->tc_fn ? kTcqPrologueBytes : kPrologueBytes) + merge_bytes(pl->hq, warps);
+    pl->ring_off = kPrologueBytes + merge_bytes(pl->hq, warps);
     const int budget = smem_optin - kStaticSmemReserve - pl->ring_off;
     int r_w = budget / (warps * pl->entry_bytes);
     if (r_w > kMaxRing / (2 * warps)) r_w = kMaxRing / (2 * warps);  // two mbarriers per entry

@@ -52,7 +52,6 @@
 #pragma once
 
 #include "lbkv_device.cuh"
-#include "lbkv_tc.cuh"
 
 namespace lbkv {
 
@@ -73,6 +72,9 @@ constexpr int kQbOffset = kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq);
 constexpr int kPartOffset = kQbOffset + 8 * 32 * 8;
 constexpr int kKbOffset = kPartOffset + 4 * 8 * 32;
 static_assert(kQbOffset % 16 == 0 && kKbOffset + 4 * 8 * 4 <= kPrologueBytes, "prologue fits");
+// The tensor-core decode kernel (lbkv_decode_grp.cuh): shared-memory offset of its merge
+// area, after its mbarriers, counters, prologue, query tile and weight tiles; its rings follow.
+constexpr int kGrpMergeOffset = 7168 + 96 * 128 + 8192;
 // Per-lane register state a warp beyond the first kMergeWarps hands over (floats):
 // o_run (16 per live column, up to 2), zacc (up to 4), m and l (up to 2 each).
 constexpr int kStateFloats = 16 * 2 + 4 + 2 * 2;
@@ -915,372 +917,6 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
 }
 
 // ------------------------------------------------------------------------
-// The tensor-core QK^T variant (token-wise K side).
-//
-// Why. Above, every K code becomes an fp16 operand with one LOP3 per two codes on the
-// half-rate ALU pipe, and QK^T takes 16 mma.sync per 32-token step; on GB300 the whole
-// kernel then needs about 94 % of the instruction-issue budget at the HBM peak. In this
-// variant the K side costs one shift and one AND per four codes and no warp-level products:
-//  - A code q is the e4m3 value q * 2^-9 when written into the low bits of a byte (the
-//    e4m3 subnormals and its first normal binade are evenly spaced, so 2- and 4-bit codes
-//    need no magic-number bias). Each thread owns one token of a 32-token chunk: it spreads
-//    the token's codes into bytes, four codes per word (which permutes the channels), and
-//    stores the 128 bytes as its row of the A operand in tensor memory (TMEM lane = token;
-//    a warp reaches the 32 lanes of its quadrant).
-//  - The B operand is the query: Q 2^e, split into e4m3 terms (the second scaled by 16,
-//    the third by 256; three terms are exact for a bf16 query) in shared memory. With several
-//    K channel groups per token B is block-diagonal, columns (group, query, term), so each
-//    group's partial score has its own accumulator column: an unscaled partial never
-//    crosses a group boundary (explainer, fold rule).
-//  - The warp's first lane issues the four 32-channel K-steps of a kind::f8f6f4 product with
-//    M = 128: the rows of the other three quadrants are whatever those lanes hold (other
-//    warps' rows), and their results, in accumulator columns private to this warp, are not
-//    read. Every thread then reads its token's scores from tensor memory and applies the
-//    acc-fold: s times each group's partial, plus z times the query's sum over the group,
-//    before the softmax (explainer, fold table: token-wise K).
-// The PV product stays on mma.sync (its A operand, V transposed, comes from the magic-number
-// images, two tokens interleaved per PRMT); its B operand, the fed weights, goes from the
-// token-per-thread layout to the fragment layout through shared memory (ldmatrix.trans).
-// The running maximum is raised only when a score exceeds it by more than 2^8 (exponent-2
-// units), so the common case needs one vote and no cross-lane reduction; the fed weights are
-// scaled to stay finite in fp16 for weights up to 2^8.
-// ------------------------------------------------------------------------
-__host__ __device__ constexpr int tmem_pow2(int x) {
-  int n = 32;
-  while (n < x) n <<= 1;
-  return n;
-}
-
-// Shared memory beyond the mma.sync variant's prologue: per-warp product mbarriers | B tile
-// | per-warp weight tiles; the merge area follows.
-constexpr int kTcqBarOffset = kPrologueBytes;
-constexpr int kTcqBOffset = kPrologueBytes + 1024;
-constexpr int kTcqPOffset = kTcqBOffset + 48 * 128;
-constexpr int kTcqPrologueBytes = kTcqPOffset + 8192;
-// The group kernel (lbkv_decode_grp.cuh): shared-memory offset of its merge area, after its
-// mbarriers, counters, prologue, B tile and weight tiles; its rings follow the merge area.
-constexpr int kGrpMergeOffset = 7168 + 96 * 128 + 8192;
-
-template <class C>
-struct TcqShape {
-  // queries per KV head at most, and (query, V group) combos at most, in the column mode
-  static constexpr int MQ = (C::MODE == kModeDup ? 4 : C::MODE == kModePair ? 8 : 16) / C::GV;
-  static constexpr int MC = MQ * C::GV;
-  static constexpr int SETS = C::WARPS / 4;  // warps sharing A columns (one per lane quadrant)
-  // tensor memory: A double-buffered per set (2 x 32 columns), scores per warp (NS columns)
-  static constexpr int NS_MAX = (512 - SETS * 64) / C::WARPS;
-  static constexpr int T = (C::GK * MQ * 3 <= NS_MAX) ? 3 : 2;  // e4m3 terms of the query
-  static constexpr int NS = (C::GK * MQ * T + 15) / 16 * 16;
-  static constexpr bool OK = C::KL == 0 && NS <= NS_MAX && NS <= 48;
-  static constexpr int TMC = tmem_pow2(SETS * 64 + C::WARPS * NS);
-  static constexpr int P_ROW = C::NTV * 16;  // bytes of one token's fed weights
-  static_assert(C::WARPS * 32 * P_ROW <= kTcqPrologueBytes - kTcqPOffset, "weight tiles fit");
-};
-
-// fp32 -> e4m3 (nearest, saturating) and back.
-__device__ __forceinline__ uint32_t e4m3_rn(float x) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(x));
-  return r & 0xffu;
-}
-__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)b));
-  return __half2float(__ushort_as_half((unsigned short)(r & 0xffffu)));
-}
-
-// Channel of K-operand element kappa (0..127) after the spread into bytes (word w of a
-// token's row, shift k, byte b).
-template <int BITS>
-__host__ __device__ constexpr int tcq_k_channel(int kappa) {
-  return BITS == 2 ? 16 * (kappa >> 4) + 4 * (kappa & 3) + ((kappa >> 2) & 3)
-                   : 8 * (kappa >> 3) + 2 * (kappa & 3) + ((kappa >> 2) & 1);
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-
-// Per-warp online-softmax state of the variant, token per thread.
-template <class C>
-struct TcqState {
-  float m_run[TcqShape<C>::MQ];                       // running maximum (exponent-2 units), warp-uniform
-  float lsum[TcqShape<C>::MQ];                        // this thread's tokens' weights
-  float zacc[C::VL == 0 ? TcqShape<C>::MC : 1];       // token-wise V: sum_t P_t z_t,u per combo
-};
-
-// Per-warp constants of the variant.
-struct TcqCtx {
-  uint32_t tm_a[2];   // this warp's A buffers (its lane quadrant)
-  uint32_t tm_d;      // this warp's score columns (its lane quadrant)
-  uint32_t tm_a_all[2];  // the same A buffers from lane 0 (the operand of the product)
-  uint32_t tm_d_all;
-  uint32_t bar;       // product-completion mbarrier of this warp
-  uint32_t btile;     // shared-memory address of the B tile
-  uint32_t idesc;
-  const float* sA;    // [kMaxHq] score factor per query
-  const float* sBz;   // [kMaxHq][4] offset factor per query and K channel group
-  uint8_t* ptile;     // this warp's fed-weight tile [32][P_ROW]
-  int32_t* status;
-};
-
-// One warp item with the tensor-core QK^T: the NCH chunks of 32 tokens of one ring entry.
-// nv: valid tokens of the entry. mid() runs between the two phases and returns false when
-// the V half did not arrive. bphase: parity of this warp's next product completion.
-template <class C, bool FULL, class Mid>
-__device__ __forceinline__ bool process_unit_tc(WarpState<C>& st, TcqState<C>& ts, const SlotSmem& sm, int nv,
-                                                const TcqCtx& tx, uint32_t& bphase, const LaneCols& lc,
-                                                const int (&qslot)[C::NQ], Mid&& mid) {
-  using S = TcqShape<C>;
-  constexpr int BITS = C::BITS, VL = C::VL, GV = C::GV, GK = C::GK, NQ = C::NQ, NO = C::NO, NTV = C::NTV;
-  constexpr int NCH = C::NCH, RB = C::RB, D = kHeadDim, MQ = S::MQ, MC = S::MC, T = S::T, NS = S::NS;
-  constexpr unsigned FULLMASK = 0xffffffffu;
-  constexpr int FED_CW = 32;  // channel-wise V: weights fed as P * 32
-  const int lane = lc.lane;
-
-  // ------------------------------------------------ phase 1: scores, chunk by chunk
-  float xs[NCH][MQ];
-  // Converts chunk ch into A buffer ch & 1 (this warp's lanes) and issues its product.
-  auto convert_issue = [&](int ch, uint32_t (&ksz)[GK]) {
-    const int tk = 32 * ch + lane;
-    uint32_t out[32];
-    if (BITS == 2) {
-      const uint4* row = reinterpret_cast<const uint4*>(sm.kc + tk * RB);
-      const int h = (lane >> 2) & 1;  // read order that keeps 8 lanes on 32 different banks
-      const uint4 a = row[h], b2 = row[h ^ 1];
-      const uint4 lo = h ? b2 : a, hi = h ? a : b2;
-      const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) out[4 * j + kk] = (wv[j] >> (2 * kk)) & 0x03030303u;
-    } else {
-      const uint4* row = reinterpret_cast<const uint4*>(sm.kc + tk * RB);
-#pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4) {
-        const uint4 q4 = row[s4];
-        const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          out[2 * (4 * s4 + j)] = wv[j] & 0x0F0F0F0Fu;
-          out[2 * (4 * s4 + j) + 1] = (wv[j] >> 4) & 0x0F0F0F0Fu;
-        }
-      }
-    }
-#pragma unroll
-    for (int cc = 0; cc < GK; ++cc)
-      ksz[cc] = (uint32_t)__half_as_ushort(sm.ks[tk * GK + cc]) | ((uint32_t)__half_as_ushort(sm.kz[tk * GK + cc]) << 16);
-    tc::st32(tx.tm_a[ch & 1], out);
-    tc::wait_st();
-    tc::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) {
-      tc::fence_after_sync();
-#pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4)
-        tc::mma_f8f6f4_ts(tx.tm_d_all, tx.tm_a_all[ch & 1] + 8u * s4, tc::smem_desc(tx.btile + 256u * s4, 128u, 1024u),
-                          tx.idesc, s4 > 0);
-      tc::commit(tx.bar);
-    }
-    __syncwarp();
-  };
-  // Waits for the product of chunk ch and turns its scores into xs[ch] (exponent-2 units).
-  auto read_scores = [&](int ch, const uint32_t (&ksz)[GK]) -> bool {
-    const bool ok = mbar_wait(tx.bar, bphase, tx.status, kStatusConsumerTimeout);
-    bphase ^= 1u;
-    tc::fence_after_sync();
-    float dcol[NS];
-#pragma unroll
-    for (int cb = 0; cb < NS / 16; ++cb) {
-      float d16[16];
-      tc::ld16(tx.tm_d + 16u * cb, d16);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) dcol[16 * cb + j] = d16[j];
-    }
-    tc::wait_ld();
-    tc::fence_before_sync();
-    const int tk = 32 * ch + lane;
-    float acc[MQ], off[MQ];
-#pragma unroll
-    for (int i = 0; i < MQ; ++i) acc[i] = off[i] = 0.f;
-#pragma unroll
-    for (int cg = 0; cg < GK; ++cg) {
-      const float2 sz = half2_to_float2(ksz[cg]);
-#pragma unroll
-      for (int i = 0; i < MQ; ++i) {
-        const int n0 = (cg * MQ + i) * T;
-        float raw = fmaf(dcol[n0 + 1], 0.0625f, dcol[n0]);
-        if (T == 3) raw = fmaf(dcol[n0 + 2], 0.00390625f, raw);
-        acc[i] = fmaf(sz.x, raw, acc[i]);
-        off[i] = fmaf(sz.y, tx.sBz[i * 4 + cg], off[i]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < MQ; ++i) xs[ch][i] = (FULL || tk < nv) ? fmaf(tx.sA[i], acc[i], off[i]) : -INFINITY;
-    return ok;
-  };
-  bool ok = true;
-  {
-    uint32_t ksz_a[GK], ksz_b[GK];
-    // chunk ch + 1 is converted while the product of chunk ch runs
-    convert_issue(0, ksz_a);
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) {
-      const bool live = FULL || 32 * ch < nv;
-      const bool next = ch + 1 < NCH && (FULL || 32 * (ch + 1) < nv);
-      if (!live) {
-#pragma unroll
-        for (int i = 0; i < MQ; ++i) xs[ch][i] = -INFINITY;
-        continue;
-      }
-      if (ch & 1) {
-        ok &= read_scores(ch, ksz_b);
-        if (next) convert_issue(ch + 1, ksz_a);
-      } else {
-        ok &= read_scores(ch, ksz_a);
-        if (next) convert_issue(ch + 1, ksz_b);
-      }
-    }
-  }
-  if (!ok) return false;
-
-  // ------------------------------------------------ running maximum, raised by more than 2^8 only
-  {
-    bool grow = false;
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-      for (int i = 0; i < MQ; ++i) grow |= (xs[ch][i] > ts.m_run[i] + 8.f);
-    if (__any_sync(FULLMASK, grow)) {
-      float alpha[MQ];
-#pragma unroll
-      for (int i = 0; i < MQ; ++i) {
-        float mx = xs[0][i];
-#pragma unroll
-        for (int ch = 1; ch < NCH; ++ch) mx = fmaxf(mx, xs[ch][i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULLMASK, mx, o));
-        const float mn = fmaxf(ts.m_run[i], mx);
-        alpha[i] = (mn == -INFINITY) ? 1.f : fast_exp2(ts.m_run[i] - mn);
-        ts.m_run[i] = mn;
-        ts.lsum[i] *= alpha[i];
-      }
-      if (VL == 0) {
-#pragma unroll
-        for (int k2 = 0; k2 < MC; ++k2) ts.zacc[k2] *= alpha[k2 / GV];
-      }
-#pragma unroll
-      for (int j = 0; j < NQ; ++j) {
-        float a = 1.f;
-#pragma unroll
-        for (int i = 0; i < MQ; ++i)
-          if (i == qslot[j]) a = alpha[i];
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-          for (int row = 0; row < 2; ++row) st.o_run[mt][row][j] *= a;
-      }
-    }
-  }
-
-  // The K half of the entry is no longer read: mid() refills it and waits for the V half.
-  if (!mid()) return false;
-
-  // ------------------------------------------------ phase 2: weights, PV, V fold per chunk
-#pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) {
-    if (!FULL && 32 * ch >= nv) break;
-    const int tk = 32 * ch + lane;
-    const bool okt = FULL || tk < nv;
-    float P[MQ];
-#pragma unroll
-    for (int i = 0; i < MQ; ++i) {
-      P[i] = fast_exp2(xs[ch][i] - ts.m_run[i]);  // -inf (padding) gives 0
-      ts.lsum[i] += P[i];
-    }
-    // fed weights per (query, V group) combo, fp16: token-wise V P s 2^eP with max(s) 2^eP in
-    // [2^6, 2^7) over the chunk's valid tokens (fed values below 2^15); channel-wise V P * 32
-    float fw[MC];
-    float inv_ps = 1.f;
-    if (VL == 0) {
-      float sv[GV], zv[GV];
-      uint32_t sb = 0;
-#pragma unroll
-      for (int uu = 0; uu < GV; ++uu) {
-        const __half hs = sm.vs[tk * GV + uu], hz = sm.vz[tk * GV + uu];
-        sv[uu] = okt ? __half2float(hs) : 0.f;  // padding tokens may hold any scale bits
-        zv[uu] = okt ? __half2float(hz) : 0.f;
-        sb = max(sb, okt ? (uint32_t)(__half_as_ushort(hs) & 0x7fffu) : 0u);
-      }
-      sb = __reduce_max_sync(FULLMASK, sb);
-      const float smaxf = __half2float(__ushort_as_half((unsigned short)sb));
-      int e2 = 0;
-      if (smaxf > 0.f) e2 = min(100, max(-100, 6 - ilog2f(smaxf)));
-      const float ps = exp2i(e2);
-      inv_ps = exp2i(-e2);
-#pragma unroll
-      for (int k2 = 0; k2 < MC; ++k2) {
-        const int i = k2 / GV, uu = k2 % GV;
-        fw[k2] = P[i] * (sv[uu] * ps);
-        ts.zacc[k2] = fmaf(P[i], zv[uu], ts.zacc[k2]);
-      }
-    } else {
-#pragma unroll
-      for (int k2 = 0; k2 < MC; ++k2) fw[k2] = P[k2] * (float)FED_CW;
-    }
-    // this token's row: column n of PV n-tile v holds combo DUP ? n / 2 : 8 v + n
-    {
-      uint32_t rw[NTV * 4];
-#pragma unroll
-      for (int j = 0; j < NTV * 4; ++j) rw[j] = C::DUP ? f16x2_from(fw[j], fw[j]) : f16x2_from(fw[2 * j], fw[2 * j + 1]);
-#pragma unroll
-      for (int v = 0; v < NTV; ++v)
-        *reinterpret_cast<uint4*>(tx.ptile + lane * S::P_ROW + 16 * v) =
-            make_uint4(rw[4 * v], rw[4 * v + 1], rw[4 * v + 2], rw[4 * v + 3]);
-    }
-    __syncwarp();
-    uint32_t pB[NTV][2][2];
-#pragma unroll
-    for (int v = 0; v < NTV; ++v)
-      ldsm_x4_trans(smem_addr(tx.ptile + lane * S::P_ROW + 16 * v), pB[v][0][0], pB[v][0][1], pB[v][1][0],
-                    pB[v][1][1]);
-    // minus the magic bias of each PV accumulator column: 1024 times the sum of the fp16
-    // weights fed to it, formed by the tensor cores with an all-ones A operand
-    float cb[NTV][2], fsum[NTV][2];
-    {
-      constexpr uint32_t kOnes2 = 0x3c003c00u;
-#pragma unroll
-      for (int v = 0; v < NTV; ++v) {
-        float fs[4];
-        mma_f16_c(fs, kOnes2, kOnes2, kOnes2, kOnes2, pB[v][0][0], pB[v][0][1], 0.f, 0.f, 0.f, 0.f);
-        mma_f16(fs, kOnes2, kOnes2, kOnes2, kOnes2, pB[v][1][0], pB[v][1][1]);
-        cb[v][0] = -kMagicF * fs[0];
-        cb[v][1] = -kMagicF * fs[1];
-        fsum[v][0] = fs[0];
-        fsum[v][1] = fs[1];
-      }
-    }
-    float accv[8][NTV][4];
-    pv_chunk<C>(accv, pB, sm, 32 * ch, lc, true, cb);
-    if (VL == 0) {
-      fold_tokenwise_v<C>(st, accv, inv_ps, lc);
-    } else {
-      float Wg[NO];
-#pragma unroll
-      for (int o = 0; o < NO; ++o) Wg[o] = fsum[0][C::DUP ? 0 : (o & 1)];
-      const int tau = (32 * ch) / C::G;  // the chunk lies inside one token group
-      fold_channelwise_v<C, FED_CW>(st, accv, Wg, sm.vs + tau * D, sm.vz + tau * D, lc);
-    }
-    __syncwarp();  // the weight tile is read before the next chunk writes it
-  }
-  return true;
-}
-
-// ------------------------------------------------------------------------
 // Work split. The items (UNIT tokens; the last one of a pair may be partial) of all
 // (sequence, KV head) pairs with tokens form one sequence in pair order. On a cost axis
 // every such pair costs split_w (its boundary: prologue, waiting for the slowest warp,
@@ -1318,16 +954,14 @@ struct SplitScan {
 // The kernel: see the file comment. C = Cfg<BITS, KL, VL, MODE, LOG2G>; PAGED: the cache
 // is a page pool behind a page table (only the addresses of the bulk copies differ).
 // ------------------------------------------------------------------------
-template <class C, bool PAGED, bool TCQ = false>
+template <class C, bool PAGED>
 __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __grid_constant__ DecodeParams p) {
-  static_assert(!TCQ || TcqShape<C>::OK, "the tensor-core QK^T variant needs a token-wise K side and room in TMEM");
   constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NQ = C::NQ, NO = C::NO;
   constexpr int RB = C::RB, D = kHeadDim, UNIT = C::UNIT, W = C::WARPS;
   constexpr unsigned FULLMASK = 0xffffffffu;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ SplitScan ss;
   __shared__ int s_last;
-  __shared__ uint32_t s_tmem;  // tensor-memory base (tensor-core QK^T variant)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -1344,7 +978,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   float* sPart = reinterpret_cast<float*>(smem + kPartOffset);  // [8 k-steps][32 lanes]
   float* sKb = reinterpret_cast<float*>(smem + kKbOffset);      // [8 columns][4 channel groups]
   MergeArea ma;
-  ma.m = reinterpret_cast<float*>(smem + (TCQ ? kTcqPrologueBytes : kPrologueBytes));
+  ma.m = reinterpret_cast<float*>(smem + kPrologueBytes);
   ma.l = ma.m + kMergeWarps * kMaxHq;
   ma.o = ma.l + kMergeWarps * kMaxHq;
   uint8_t* ring = smem + p.ring_off;
@@ -1364,11 +998,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       store_row4(p.out + (out_row0 + i) * D, lane, v);
     }
   };
-
-  if constexpr (TCQ) {
-    if (warp == 0) tc::alloc(smem_addr(&s_tmem), TcqShape<C>::TMC);
-    tc::fence_before_sync();
-  }
 
   // ---------------------------------------------------- the CTA's share of the items
   {
@@ -1595,40 +1224,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     advance(iss, W);
     lookup_page();
   };
-  const uint32_t bar_mma = smem_addr(smem + kTcqBarOffset) + 8u * warp;  // tensor-core variant
   if (lane == 0) {
     for (int r = 0; r < R; ++r) {
       mbar_init(bar_k(r), 1);
       mbar_init(bar_v(r), 1);
     }
-    if (TCQ) mbar_init(bar_mma, 1);
     mbar_init_fence();
   }
   __syncwarp();
-  uint32_t bphase = 0;  // parity of this warp's next product completion
-  TcqCtx tx{};
-  int qslot[NQ];  // query of this lane's PV accumulator slot j (or -1)
-#pragma unroll
-  for (int j = 0; j < NQ; ++j) qslot[j] = qk_query<C>(2 * c + j, hq);
-  if constexpr (TCQ) {
-    using S = TcqShape<C>;
-    tc::fence_after_sync();
-    const uint32_t base = s_tmem;
-    const uint32_t quad = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t set_a = base + 64u * (uint32_t)(warp >> 2);
-    const uint32_t d0 = base + 64u * S::SETS + (uint32_t)(S::NS * warp);
-    tx.tm_a_all[0] = set_a, tx.tm_a_all[1] = set_a + 32u;
-    tx.tm_a[0] = set_a + quad, tx.tm_a[1] = set_a + 32u + quad;
-    tx.tm_d_all = d0;
-    tx.tm_d = d0 + quad;
-    tx.bar = bar_mma;
-    tx.btile = smem_addr(smem + kTcqBOffset);
-    tx.idesc = tc::idesc_e4m3(128, S::NS);
-    tx.sA = sAq;
-    tx.sBz = sBz;
-    tx.ptile = smem + kTcqPOffset + warp * 32 * S::P_ROW;
-    tx.status = p.status;
-  }
   for (int r = 0; r < R; ++r) {
     issue_k();
     issue_v();
@@ -1665,38 +1268,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       }
       __syncthreads();
     }
-    if (TCQ) {
-      // query exponent e: max |Q| 2^e in [2^7, 2^8) (the e4m3 terms reach 448); per K channel
-      // group the query's sum (the offset term's other operand); queries past hq get zeros
-      for (int i = warp; i < kMaxHq; i += W) {
-        float amax = 0.f, gs = 0.f;
-        if (i < hq) {
-#pragma unroll
-          for (int uu = 0; uu < 4; ++uu) {
-            const float v = sQ[i * D + 4 * lane + uu];
-            amax = fmaxf(amax, fabsf(v));
-            gs += v;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, o));
-        constexpr int lanes_per_group = C::G / 4;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float other = __shfl_xor_sync(FULLMASK, gs, o);
-          if (o < lanes_per_group) gs += other;
-        }
-        int e = 0;
-        if (amax > 0.f) e = min(100, max(-100, 7 - ilog2f(amax)));
-        if (lane == 0) {
-          sEq[i] = e;
-          // scores in exponent-2 units: sl2 * sum_c (s_c raw_c + z_c sum Q_c), raw_c = (product)
-          // 2^(9 - e): the codes enter as q 2^-9, the query as Q 2^e
-          sAq[i] = i < hq ? p.sl2 * exp2i(9 - e) : 0.f;
-        }
-        if ((lane % lanes_per_group) == 0) sBz[i * 4 + lane / lanes_per_group] = i < hq ? p.sl2 * gs : 0.f;
-      }
-    } else if (warp < hq) {
+    if (warp < hq) {
       // query exponent e: max |Q / factor| * 2^e in [2^13, 2^14), so Q * 2^e / factor is an
       // exact fp16 for a bf16 query (8 significant bits; a rotated query is rounded there);
       // channel-group sums of Q for the K offset
@@ -1742,37 +1314,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     }
 
     WarpState<C> st;
-    if constexpr (TCQ) {
-      // B tile of the product: column n = (K channel group cg, query i, term tau), element kappa
-      // (channel tcq_k_channel(kappa)); canonical K-major layout without swizzle (core
-      // matrices of 8 columns x 16 elements); four elements per store
-      using S = TcqShape<C>;
-      uint8_t* btile = smem + kTcqBOffset;
-      for (int wi = threadIdx.x; wi < S::NS * 32; wi += C::THREADS) {
-        const int n = wi >> 5, k4 = (wi & 31) * 4;
-        const int cg = n / (S::MQ * S::T), i = (n / S::T) % S::MQ, tau = n % S::T;
-        uint32_t word = 0;
-        if (n < GK * S::MQ * S::T && i < hq) {
-          const float sc = exp2i(sEq[i]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int ch = tcq_k_channel<BITS>(k4 + j);
-            if (ch / C::G != cg) continue;
-            const float xq = sQ[i * D + ch] * sc;
-            const uint32_t t0 = e4m3_rn(xq);
-            const float r1 = (xq - e4m3_to_f32(t0)) * 16.f;
-            const uint32_t t1 = e4m3_rn(r1);
-            const float r2 = (r1 - e4m3_to_f32(t1)) * 16.f;
-            const uint32_t t2 = e4m3_rn(r2);
-            word |= (tau == 0 ? t0 : tau == 1 ? t1 : t2) << (8 * j);
-          }
-        }
-        *reinterpret_cast<uint32_t*>(btile + (n >> 3) * 1024 + (k4 >> 4) * 128 + (n & 7) * 16 + (k4 & 15)) = word;
-      }
-      fence_proxy_async_smem();  // the tile is read by the tensor cores
-#pragma unroll
-      for (int j = 0; j < NQ; ++j) st.pa[j] = 1.f;
-    } else if (KL == 0) {
+    if (KL == 0) {
       // token-wise K: B fragments Q' = Q 2^e / factor (fp16; exact for a bf16 query) of column g, the same for
       // every warp, formed once: warp ks < 8 the k-step ks; then minus the magic bias 1024 *
       // sum of Q' per channel group of each column
@@ -1839,11 +1381,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       for (int row = 0; row < 2; ++row)
 #pragma unroll
         for (int i = 0; i < NQ; ++i) st.o_run[mt][row][i] = 0.f;
-    TcqState<C> ts;
-#pragma unroll
-    for (int i = 0; i < TcqShape<C>::MQ; ++i) ts.m_run[i] = -INFINITY, ts.lsum[i] = 0.f;
-#pragma unroll
-    for (int k2 = 0; k2 < (VL == 0 ? TcqShape<C>::MC : 1); ++k2) ts.zacc[k2] = 0.f;
 
     __syncthreads();  // the shared query fragments are in place
 
@@ -1874,21 +1411,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         ++n_v_read;
         return true;
       };
-      if constexpr (TCQ) {
-        bool ok;
-        if (nv == UNIT)
-          ok = process_unit_tc<C, true>(st, ts, sm, nv, tx, bphase, lc, qslot, mid);
-        else
-          ok = process_unit_tc<C, false>(st, ts, sm, nv, tx, bphase, lc, qslot, mid);
-        if (!ok && !failed) {
-          failed = true;
-          atomicExch(p.status, kStatusConsumerTimeout);
-        }
-      } else if (nv == UNIT) {
+      if (nv == UNIT)
         process_unit<C, true>(st, sm, nv, sQ, p.sl2, sqb, lc, mid);
-      } else {
+      else
         process_unit<C, false>(st, sm, nv, sQ, p.sl2, sqb, lc, mid);
-      }
       if (failed) break;
       if (++con.r == R) {
         con.r = 0;
@@ -1896,50 +1422,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       }
       __syncwarp();
       issue_v();  // the V half is read: refill it with the next item's V
-    }
-
-    if constexpr (TCQ) {
-      // warp totals of the token-per-thread state into the lane format of the merge: per
-      // lane slot j (query qslot[j]) the running maximum (exponent-2 units, so pa = 1), the
-      // denominator and offset sums held by the lanes with g == 0 only
-      using S = TcqShape<C>;
-      float lt[S::MQ], zt[VL == 0 ? S::MC : 1];
-#pragma unroll
-      for (int i = 0; i < S::MQ; ++i) {
-        float v = ts.lsum[i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULLMASK, v, o);
-        lt[i] = v;
-      }
-      if (VL == 0) {
-#pragma unroll
-        for (int k2 = 0; k2 < S::MC; ++k2) {
-          float v = ts.zacc[k2];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULLMASK, v, o);
-          zt[k2] = v;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < NQ; ++j) {
-        float m = -INFINITY, l = 0.f;
-#pragma unroll
-        for (int i = 0; i < S::MQ; ++i)
-          if (i == qslot[j]) m = ts.m_run[i], l = lt[i];
-        st.m_run[j] = m;
-        st.l[j] = (g == 0) ? l : 0.f;
-      }
-#pragma unroll
-      for (int o = 0; o < NO; ++o) {
-        float z = 0.f;
-        if (VL == 0) {
-          const int combo = own_combo<C>(c, o);
-#pragma unroll
-          for (int k2 = 0; k2 < S::MC; ++k2)
-            if (k2 == combo) z = zt[k2];
-        }
-        st.zacc[o] = (g == 0) ? z : 0.f;
-      }
     }
 
     // ---------------------------------------------------- warps beyond kMergeWarps fold in
@@ -2241,14 +1723,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       if (k >= n_v_read && !mbar_wait(bar_v(rv), pv, p.status, kStatusDrainTimeout)) break;
       if (++rv == R) { rv = 0; pv ^= 1; }
     }
-    // the warp's last product (its completion may have been missed by a wait that gave up)
-    if (TCQ) mbar_wait(bar_mma, bphase ^ 1u, p.status, kStatusDrainTimeout);
-  }
-  if constexpr (TCQ) {
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (warp == 0) tc::dealloc(s_tmem, TcqShape<C>::TMC);
   }
 }
 

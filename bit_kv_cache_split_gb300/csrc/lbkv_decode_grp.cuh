@@ -9,15 +9,22 @@
 // before the softmax; token-wise V: operand-fold on the weights; channel-wise V: acc-fold of
 // each token group's partial output, before the final division).
 //
-// The operands of the QK^T product are those of the split-decode kernel's tensor-core
-// variant (lbkv_decode.cuh): the K codes spread into e4m3 bytes (q 2^-9, four codes per
-// shift and AND) in tensor memory, one TMEM lane per token, and the query as e4m3 terms in
-// shared memory. What differs is who shares a product. A warp issues at most one tcgen05
-// product per ~57 cycles (measured on GB300), and a product with M = 128 rows costs the
-// tensor core the same whether 32 or 128 of its rows are used (~9 cycles for N = 16), so
-// here an item of 128 tokens is one product: the four warps of a group (one per TMEM lane
-// quadrant) each convert 32 of its tokens, and the last of them to finish issues the four
-// K-steps, with no barrier (an arrival counter in shared memory, acquire-release).
+// Operands of the QK^T product (kind::f8f6f4, fp32 accumulators in tensor memory):
+//  - A = the K codes: a code q is the e4m3 value q 2^-9 when written into the low bits of a
+//    byte (the e4m3 subnormals and its first normal binade are evenly spaced, so 2- and 4-bit
+//    codes need no magic-number bias); a thread spreads its token's codes into bytes, four
+//    codes per shift and AND, and stores the 128 bytes as its row in tensor memory (one TMEM
+//    lane per token; a warp reaches the 32 lanes of its quadrant).
+//  - B = the query: Q 2^e split into e4m3 terms (the second scaled by 16, the third by 256;
+//    three terms are exact for a bf16 query) in shared memory. With several K channel groups
+//    per token B is block-diagonal, columns (group, query, term), so each group's partial
+//    score has its own accumulator column: an unscaled partial never crosses a group boundary.
+// Each thread reads its token's scores back from tensor memory and applies the acc-fold. A
+// warp issues at most one tcgen05 product per ~57 cycles (measured on GB300), and a product
+// with M = 128 rows costs the tensor core the same whether 32 or 128 of its rows are used
+// (~9 cycles for N = 16), so an item of 128 tokens is one product: the four warps of a group
+// (one per TMEM lane quadrant) each convert 32 of its tokens, and the last of them to finish
+// issues the four K-steps, with no barrier (an arrival counter in shared memory).
 //
 // Work organisation. A persistent grid, one CTA per SM, warps in groups of four. The items
 // of the CTA's share of the item sequence go to the groups in turn. A group streams its
@@ -34,16 +41,53 @@
 #pragma once
 
 #include "lbkv_decode.cuh"
+#include "lbkv_tc.cuh"
 
 namespace lbkv {
+
+__host__ __device__ constexpr int tmem_pow2(int x) {
+  int n = 32;
+  while (n < x) n <<= 1;
+  return n;
+}
+
+// fp32 -> e4m3 (nearest, saturating) and back.
+__device__ __forceinline__ uint32_t e4m3_rn(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(x));
+  return r & 0xffu;
+}
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)b));
+  return __half2float(__ushort_as_half((unsigned short)(r & 0xffffu)));
+}
+
+// Channel of K-operand element kappa (0..127) after the spread of a token's codes into
+// bytes (word w of the row, shift k, byte b: element 16 w + 4 k + b at INT2, 8 w + 4 k + b at
+// INT4), which permutes the channels; the query tile uses the same order.
+template <int BITS>
+__host__ __device__ constexpr int grp_k_channel(int kappa) {
+  return BITS == 2 ? 16 * (kappa >> 4) + 4 * (kappa & 3) + ((kappa >> 2) & 3)
+                   : 8 * (kappa >> 3) + 2 * (kappa & 3) + ((kappa >> 2) & 1);
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
 
 // Compile-time shape of one variant (token-wise K); C = Cfg<BITS, 0, VL, MODE, LOG2G>.
 template <class C>
 struct GrpShape {
   static constexpr int UNIT = 128;              // tokens per item (4 warps x 32)
   static constexpr int GROUPS = C::WARPS / 4;   // warp groups
-  static constexpr int MQ = TcqShape<C>::MQ;    // queries per KV head at most
-  static constexpr int MC = TcqShape<C>::MC;    // (query, V group) combos at most
+  // queries per KV head at most, and (query, V group) combos at most, in the column mode
+  static constexpr int MQ = (C::MODE == kModeDup ? 4 : C::MODE == kModePair ? 8 : 16) / C::GV;
+  static constexpr int MC = MQ * C::GV;
   // tensor memory of a group: A x2 (32 columns each), scores x2 (NS columns each)
   static constexpr int NS_MAX = (512 / GROUPS - 64) / 2;
   static constexpr int T = (C::GK * MQ * 3 <= NS_MAX) ? 3 : 2;  // e4m3 terms of the query
@@ -500,7 +544,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) grp_decode_kernel(const __grid_
         const float sc = exp2i(sEq[i]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int ch = tcq_k_channel<BITS>(k4 + j);
+          const int ch = grp_k_channel<BITS>(k4 + j);
           if (ch / C::G != cg) continue;
           const float xq = sQ[i * D + ch] * sc;
           const uint32_t t0 = e4m3_rn(xq);

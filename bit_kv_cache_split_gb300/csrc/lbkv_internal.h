@@ -105,21 +105,10 @@ LBKV_DECLARE_DECODE(4, 1, 0)
 LBKV_DECLARE_DECODE(4, 1, 1)
 #undef LBKV_DECLARE_DECODE
 
-// The tensor-core QK^T variant of the same kernel (token-wise K side) for (column mode,
-// log2 group), or nullptr when the variant does not fit that shape.
-template <int BITS, int VL, bool PAGED>
-DecodeKernel decode_kernel_tcq(int mode, int log2g);
-#define LBKV_DECLARE_TCQ(B, V)                                        \
-  template <> DecodeKernel decode_kernel_tcq<B, V, false>(int, int); \
-  template <> DecodeKernel decode_kernel_tcq<B, V, true>(int, int);
-LBKV_DECLARE_TCQ(2, 0)
-LBKV_DECLARE_TCQ(2, 1)
-LBKV_DECLARE_TCQ(4, 0)
-LBKV_DECLARE_TCQ(4, 1)
-#undef LBKV_DECLARE_TCQ
 
-// The group kernel (token-wise K side; QK^T on the tensor cores, one product per 128-token
-// item shared by four warps) for (column mode, log2 group), or nullptr when it does not fit.
+// The tensor-core decode kernel (token-wise K side; QK^T on tcgen05, one product per
+// 128-token item shared by a group of four warps) for (column mode, log2 group), or nullptr
+// when it does not fit that shape.
 template <int BITS, int VL, bool PAGED>
 DecodeKernel decode_kernel_grp(int mode, int log2g);
 #define LBKV_DECLARE_GRP(B, V)                                        \
