@@ -1,7 +1,7 @@
 // tc_rates.cu -- microbenchmark of the 5th-generation tensor-core operations the decode
 // kernels would build on (GB300, sm_103a), one CTA of 16 warps per SM on every SM:
 //   mma   : tcgen05.mma kind::f8f6f4 (A e4m3 in tensor memory, B e4m3 in shared memory, fp32
-//           accumulators), M x N x 32 per product, `iters` back-to-back products per warp and
+//           accumulators), M x N x 32 per product (M = 128, and M = 64 at N = 16), `iters` back-to-back products per warp and
 //           one commit; cycles per product per warp (issue rate) and per SM (throughput);
 //   st    : tcgen05.st 32x32b.x32 (a warp's 32 lanes x 32 columns) + wait::st;
 //   ld    : tcgen05.ld 32x32b.x16 + wait::ld.
@@ -146,6 +146,8 @@ int main() {
   for (int N : {16, 32, 64, 128, 256})
     for (int nw : {1, 4, 16})
       if (32 + nw * N <= kCols && !run("tcgen05.mma f8f6f4 A:tmem B:smem", 0, 128, N, 256, nw)) return 1;
+  for (int nw : {1, 4, 16})  // M = 64: the same rows of tensor memory, half of them used
+    if (!run("tcgen05.mma f8f6f4 A:tmem B:smem", 0, 64, 16, 256, nw)) return 1;
   for (int nw : {1, 4, 16})
     if (!run("tcgen05.st 32x32b.x32 + wait", 1, 0, 0, 1000, nw)) return 1;
   for (int nw : {1, 4, 16})
