@@ -15,9 +15,20 @@
 
 namespace lbkv {
 
-__device__ __forceinline__ int quantize_one(float x, float zf, float sf, int qmax) {
+// q = clamp(rint(fl((x - z) / s)), 0, qmax), with fl the correctly rounded fp32 division;
+// inv = fl(1 / s). The division is done only where it can change the result: the product
+// r = fl(d * inv) differs from fl(d / s) by at most 3 * 2^-24 |d / s| (three roundings),
+// i.e. by less than 3 * 2^-18 (< 2^-16) for |r| < 64, so wherever r is at least 2^-16 away
+// from a half-integer (the only places where rint changes) both round to the same integer,
+// and the clamp sees the same value (r - floor(r) is exact for r >= 0 and off by at most
+// 2^-24 below). Near a half-integer (ties to even among them), for |r| >= 64 and for
+// non-finite values the correctly rounded division decides.
+__device__ __forceinline__ int quantize_one(float x, float zf, float sf, float inv, int qmax) {
   if (sf == 0.f) return 0;
-  const float v = __fdiv_rn(__fsub_rn(x, zf), sf);
+  const float d = __fsub_rn(x, zf);
+  float v = __fmul_rn(d, inv);
+  const float fr = __fsub_rn(v, floorf(v));
+  if (!(fabsf(v) < 64.f) || fabsf(__fsub_rn(fr, 0.5f)) < 1.52587890625e-05f) v = __fdiv_rn(d, sf);
   const float r = rintf(v);
   return r < 0.f ? 0 : (r > (float)qmax ? qmax : (int)r);
 }
@@ -41,9 +52,10 @@ __device__ __forceinline__ void quantize_token_vals(const float (&v)[4], int gro
   const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)qmax));
   const __half zh = __float2half_rn(mn);
   const float sf = __half2float(sh), zf = __half2float(zh);
+  const float inv = __frcp_rn(sf);
   uint32_t packed = 0;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) packed |= (uint32_t)quantize_one(v[u], zf, sf, qmax) << (BITS * u);
+  for (int u = 0; u < 4; ++u) packed |= (uint32_t)quantize_one(v[u], zf, sf, inv, qmax) << (BITS * u);
   if (BITS == 2)
     crow[lane] = (uint8_t)packed;
   else
@@ -73,7 +85,7 @@ __device__ __forceinline__ void quantize_channel_group(const __nv_bfloat16* __re
   constexpr int RB = kHeadDim * BITS / 8;
   constexpr int per_byte = 8 / BITS;
   constexpr int qmax = (1 << BITS) - 1;
-  float sf = 0.f, zf = 0.f;
+  float sf = 0.f, zf = 0.f, inv = 0.f;
   if (nvalid > 0) {
     float mn = __bfloat162float(x[d]), mx = mn;
     for (int t = 1; t < nvalid; ++t) {
@@ -89,10 +101,11 @@ __device__ __forceinline__ void quantize_channel_group(const __nv_bfloat16* __re
     *z = zh;
     sf = __half2float(sh);
     zf = __half2float(zh);
+    inv = __frcp_rn(sf);
   }
   for (int t = 0; t < group; ++t) {
     int q = 0;
-    if (t < nvalid) q = quantize_one(__bfloat162float(x[(size_t)t * kHeadDim + d]), zf, sf, qmax);
+    if (t < nvalid) q = quantize_one(__bfloat162float(x[(size_t)t * kHeadDim + d]), zf, sf, inv, qmax);
     // gather the codes of the channels sharing this byte (adjacent lanes)
     uint32_t bits = (uint32_t)q << (BITS * (d % per_byte));
 #pragma unroll

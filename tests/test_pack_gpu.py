@@ -96,3 +96,33 @@ def test_quantize_then_decode_full_size_int4(lbkv):
         wl = inputs.Workload("packed-int4-b8-ctx32768", 1, hq, 1, [T], bits=4, group=g)
         ref = oracle.decode_ref(to_oracle(t, wl))[0]
         assert_parity(got_all[b, kvh * hq:(kvh + 1) * hq], ref, f"packed INT4 full size unit ({b},{kvh})")
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_pack_quotients_at_rounding_boundaries(lbkv, bits, layout):
+    """Inputs whose quotients (x - z) / s fall exactly on, or within an ulp of, the
+    half-integers where the rounding of a code changes: every group spans 0 .. 2^b - 1 (so
+    s = 1 exactly) plus small bf16 perturbations, and the remaining channels sit on the
+    half-integers (exact ties, rounded to even) and on their bf16 neighbours."""
+    rng = np.random.default_rng(11 + bits + layout)
+    qmax = (1 << bits) - 1
+    T, D = 256, 128
+    base = rng.integers(0, qmax, (1, 2, T, D)).astype(np.float32) + 0.5        # exact half-integers
+    nudge = rng.choice([-1, 0, 0, 1], size=base.shape).astype(np.float32)
+    x = (torch.from_numpy(base).to(torch.bfloat16).view(torch.int16) + torch.from_numpy(nudge).to(torch.int16))
+    x = x.view(torch.bfloat16).float().numpy()
+    if layout == 0:
+        x[..., 0::32] = 0.0          # each group of 32 channels (and of 64, 128) spans [0, qmax]
+        x[..., 1::32] = float(qmax)
+    else:
+        x[:, :, 0::32, :] = 0.0      # each token group spans [0, qmax] per channel
+        x[:, :, 1::32, :] = float(qmax)
+    x[0, 1] *= 0.37                  # a second head with an inexact scale
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    lens = torch.tensor([T], dtype=torch.int32)
+    for g in (32, 128):
+        codes, s, z = lbkv.pack(xt.cuda(), lens.cuda(), bits=bits, layout=layout, group=g)
+        rc, rs, rz = oracle.pack(bits16(xt), lens.numpy(), bits, layout, g)
+        assert np.array_equal(codes.cpu().numpy(), rc), (bits, layout, g)
+        assert np.array_equal(bits16(s), rs) and np.array_equal(bits16(z), rz), (bits, layout, g)
