@@ -78,13 +78,14 @@ def measured_hbm_peak():
 
 
 def source_hash() -> str:
-    """Hash of the decode kernel's device sources, comments and blank space left out (its
-    traffic depends on the code alone: not on comments, the other kernels or the host entry
-    points)."""
+    """Hash of the split-decode kernel's device sources, comments and blank space left out
+    (its traffic depends on the code alone: not on comments, the other kernels, the opt-in
+    tensor-core kernel or the host entry points)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_kv_cache_split_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if not (f.startswith("lbkv_decode") or f == "lbkv_device.cuh"):
+        # the split-decode kernel: its header, its instantiations and the device helpers
+        if not (f in ("lbkv_decode.cuh", "lbkv_device.cuh") or f.startswith("lbkv_decode_int")):
             continue
         with open(os.path.join(csrc, f)) as fh:
             text = fh.read()
@@ -362,6 +363,10 @@ def run_sweep(device, peak):
         gbs = case.bytes / (ms * 1e-3) / 1e9
         row = {"workload": wl.name, "us_per_call": round(ms * 1e3, 2), "gbs": round(gbs, 1),
                "frac": round(gbs / peak, 3), "bytes": case.bytes}
+        rec = profiled_counters(wl.name)
+        if rec:  # ncu counters of this workload on the current kernel sources
+            row["traffic"] = rec["dram_bytes_per_launch"]
+            row["lane_slots_per_byte"] = round(32 * rec["inst_per_launch"] / case.bytes, 2)
         if wl.window:
             # scale/offset operations per stored value under folding: 2 h_q / g (explainer,
             # break-even paragraph: folding wins while this is below 1, i.e. g > 2 h_q)

@@ -51,18 +51,6 @@ __host__ __device__ constexpr int tmem_pow2(int x) {
   return n;
 }
 
-// fp32 -> e4m3 (nearest, saturating) and back.
-__device__ __forceinline__ uint32_t e4m3_rn(float x) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(x));
-  return r & 0xffu;
-}
-__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)b));
-  return __half2float(__ushort_as_half((unsigned short)(r & 0xffffu)));
-}
-
 // Channel of K-operand element kappa (0..127) after the spread of a token's codes into
 // bytes (word w of the row, shift k, byte b: element 16 w + 4 k + b at INT2, 8 w + 4 k + b at
 // INT4), which permutes the channels; the query tile uses the same order.

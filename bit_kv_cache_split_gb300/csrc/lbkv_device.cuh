@@ -197,6 +197,19 @@ __device__ __forceinline__ void mma_f16_c(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
 
+// e4m3 image of x (round to nearest even, saturating to +-448) in the low byte, and
+// the value of an e4m3 byte.
+__device__ __forceinline__ uint32_t e4m3_rn(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(x));
+  return r & 0xffu;
+}
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)b));
+  return __half2float(__ushort_as_half((unsigned short)(r & 0xffffu)));
+}
+
 // fp16 magic number 1024: OR-ing a small integer m into its mantissa gives the
 // fp16 value 1024 + m exactly (m < 1024), two lanes at a time.
 constexpr uint32_t kMagic2 = 0x64006400u;
