@@ -28,17 +28,16 @@
 // copies. A cache stored rotated by the Hadamard matrix has the query rotated in
 // the pair prologue and each output row rotated back before its bf16 rounding.
 //
-// Operands. OR-ing a code q (times a power-of-two position factor m) into the
-// mantissa of the fp16 magic number 1024 gives the exact fp16 value 1024 + m q,
-// two codes per LOP3; the factor 1/m is folded into the other operand and the
-// bias 1024 * (sum of the other operand as fed) is removed inside the fp32
-// accumulator: each accumulator starts at (or, continuing, is lowered by) minus
-// the bias of the operands it is about to take, so it never holds more than one
-// 32-token chunk's (PV) or one channel group's (QK^T) bias.
+// Operands. A code q (times a power-of-two position factor m) masked into the
+// mantissa bits of an fp16 half, with the exponent bits left at zero, is the exact
+// fp16 subnormal m q 2^-24: two codes per LOP3, no bias. The factor 1/m is folded
+// into the other operand and the 2^-24 into the fold constants (scores and outputs
+// are kept in units that carry the 2^24). The tensor cores take the subnormals
+// exactly; measured on this GPU against fp64 sums of query-like operands, the error
+// of a product is 5e-6 of sum |q b|, against 7e-5 with the images 1024 + m q of the
+// magic number 1024 and their bias removed (the large biased terms cost precision).
 // The bf16 query is exact in fp16 (a rotated query is rounded to it); the
-// softmax weights are fed as fp16. Where a bias sum is formed by the tensor cores
-// (token-wise V weights, channel-wise K queries), an MMA with an all-ones A
-// operand against the same B fragments sums exactly the fp16 values fed.
+// softmax weights are fed as fp16.
 // Both products run on mma.sync m16n8k16 fp16 with fp32 accumulators (native
 // on sm_103; the e4m3 form of mma.sync converts its operands to fp16 first):
 //   QK^T: rows = 16 tokens, k = 16 channels, cols = queries;
@@ -67,11 +66,7 @@ constexpr int kBarBytes = kMaxRing * 8;
 constexpr int kPrologueBytes = 8192;
 // token-wise K: the B fragments of Q' shared by all warps, [k-step][lane] pairs of words
 constexpr int kQbOffset = kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq);
-// token-wise K: per k-step and lane the sum of its four Q' values, and minus the magic
-// bias per accumulator column and channel group
-constexpr int kPartOffset = kQbOffset + 8 * 32 * 8;
-constexpr int kKbOffset = kPartOffset + 4 * 8 * 32;
-static_assert(kQbOffset % 16 == 0 && kKbOffset + 4 * 8 * 4 <= kPrologueBytes, "prologue fits");
+static_assert(kQbOffset % 16 == 0 && kQbOffset + 8 * 32 * 8 <= kPrologueBytes, "prologue fits");
 // The tensor-core decode kernel (lbkv_decode_grp.cuh): shared-memory offset of its merge
 // area, after its mbarriers, counters, prologue, query tile and weight tiles; its rings follow.
 constexpr int kGrpMergeOffset = 7168 + 96 * 128 + 8192;
@@ -232,7 +227,7 @@ __device__ __forceinline__ int qk_channel(int ks, int kappa) {
   if (C::BITS == 2) return 32 * blk + 16 * (c >> 1) + 4 * (c & 1) + 8 * e + p;
   return 32 * blk + 8 * c + 4 * e + p;
 }
-// Power-of-two position factor of the fp16 image of K channel ch (1024 + factor * q).
+// Power-of-two position factor of the fp16 image of K channel ch (factor * q * 2^-24).
 template <class C>
 __device__ __forceinline__ float k_mult(int ch) {
   if (C::BITS == 4) return (ch & 1) ? 16.f : 1.f;
@@ -263,15 +258,18 @@ __host__ __device__ constexpr int pv_channel(int mt, int row) {
   return BITS == 2 ? 8 * row + mt : 8 * (mt >> 2) + 4 * row + (mt & 3);
 }
 
-// fp16 images (1024 + factor * code) of position p of an 8-code (INT2) or 4-code
-// (INT4) group of two 16-bit halves: one LOP3 (plus a shared shift).
+// fp16 subnormal images (factor * code * 2^-24) of position p of an 8-code (INT2) or
+// 4-code (INT4) group of two 16-bit halves: one AND (plus a shared shift). Positions
+// past the 10 mantissa bits come from the word shifted right by 10 (INT2) or 8 (INT4).
 __device__ __forceinline__ uint32_t int2_half2(uint32_t x, uint32_t xs10, int p) {
-  return p <= 4 ? and_or(x, 0x00030003u << (2 * p), kMagic2) : and_or(xs10, 0x00030003u << (2 * (p - 5)), kMagic2);
+  return p <= 4 ? (x & (0x00030003u << (2 * p))) : (xs10 & (0x00030003u << (2 * (p - 5))));
 }
 __device__ __forceinline__ uint32_t int4_half2(uint32_t x, uint32_t xs8, int p) {
   const uint32_t src = p < 2 ? x : xs8;
-  return and_or(src, (p & 1) ? 0x00F000F0u : 0x000F000Fu, kMagic2);
+  return src & ((p & 1) ? 0x00F000F0u : 0x000F000Fu);
 }
+// The 2^24 that brings an accumulator of subnormal images back to code units.
+constexpr float kImageUnit = 16777216.f;
 
 __device__ __forceinline__ float2 half2_to_float2(uint32_t h2) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
@@ -280,7 +278,6 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t h2) {
 // Per-warp state, held in registers.
 template <class C>
 struct WarpState {
-  float kbias[2][C::GK];     // token-wise K: -1024 * sum of Q' per group, accumulator columns 2c, 2c+1
   float pa[C::NQ];           // token-wise K: sigma log2(e) 2^-e (scores are kept in units of it); else 1
   float bzq[C::NQ][C::GK];   // token-wise K: 2^e * sum of Q over a channel group
   float m_run[C::NQ], l[C::NQ];
@@ -304,13 +301,13 @@ struct LaneCols {
   int e_live;  // GV >= 2: accumulator column (0/1) of an owned pair whose V group is u_lane, or -1
 };
 
-// Channel-wise K: Q' = Q * s_tau / factor scaled by 2^e2 into exact fp16 for the
-// token group tau whose s/z rows are s_tau/z_tau; the offset becomes sum_d Q_d z_tau,d
-// (one constant per query and group, added before the softmax).
+// Channel-wise K: Q' = Q * s_tau / factor scaled by 2^e2 into fp16 for the token group
+// tau whose s/z rows are s_tau/z_tau; the offset becomes sum_d Q_d z_tau,d (one constant
+// per query and group, added before the softmax).
 template <class C>
 __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)[C::NQ], float (&cwB)[C::NQ],
-                                              float (&cwneg)[2], const __half* s_tau, const __half* z_tau,
-                                              const float* sQ, float sl2, const LaneCols& lc) {
+                                              const __half* s_tau, const __half* z_tau, const float* sQ, float sl2,
+                                              const LaneCols& lc) {
   constexpr int D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
   const int c = lc.c;
@@ -362,17 +359,7 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
   for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
     for (int r = 0; r < 2; ++r) qB[ks][r] = f16x2_from(x[ks][r][0] * sc, x[ks][r][1] * sc);
-  // The magic bias of each column is 1024 times the sum of the fp16 values actually fed: the
-  // tensor cores form it, with an all-ones A operand against the same B fragments (the
-  // accumulator columns 2c, 2c + 1 of this lane are the columns the bias is needed for).
-  constexpr uint32_t kOnes2 = 0x3c003c00u;  // (1.0, 1.0) in fp16
-  float fed[4];
-  mma_f16_c(fed, kOnes2, kOnes2, kOnes2, kOnes2, qB[0][0], qB[0][1], 0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int ks = 1; ks < 8; ++ks) mma_f16(fed, kOnes2, kOnes2, kOnes2, kOnes2, qB[ks][0], qB[ks][1]);
-#pragma unroll
-  for (int jj = 0; jj < 2; ++jj) cwneg[jj] = -kMagicF * fed[jj];
-  const float fa = sl2 * exp2i(-e2), fb = sl2 * zsum;
+  const float fa = sl2 * exp2i(-e2) * kImageUnit, fb = sl2 * zsum;
   // accumulator column 2c + j is B column 2c + j, held by lane 4 (2c + j)
 #pragma unroll
   for (int j = 0; j < C::NQ; ++j) {
@@ -388,7 +375,7 @@ template <class C>
 __device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpState<C>& st, const uint32_t (&qB)[8][2],
                                          const uint2* sqb,
                                          const float (&cwA)[C::NQ], const float (&cwB)[C::NQ],
-                                         const float (&cwneg)[2], const SlotSmem& sm, int rel0, const LaneCols& lc) {
+                                         const SlotSmem& sm, int rel0, const LaneCols& lc) {
   constexpr int BITS = C::BITS, KL = C::KL, GK = C::GK, RB = C::RB, NQ = C::NQ;
   const int g = lc.g, c = lc.c;
 #pragma unroll
@@ -452,10 +439,10 @@ __device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpStat
         }
       } else if (BITS == 2) {
         const uint32_t mA = 0x00030003u << (4 * h), mB = 0x00030003u << (4 * h + 2);
-        a0 = and_or(wA[blk], mA, kMagic2);
-        a1 = and_or(wB[blk], mA, kMagic2);
-        a2 = and_or(wA[blk], mB, kMagic2);
-        a3 = and_or(wB[blk], mB, kMagic2);
+        a0 = wA[blk] & mA;
+        a1 = wB[blk] & mA;
+        a2 = wA[blk] & mB;
+        a3 = wB[blk] & mB;
       } else {
         a0 = int4_half2(wA[blk], sA[blk], 2 * h);
         a1 = int4_half2(wB[blk], sB[blk], 2 * h);
@@ -470,11 +457,9 @@ __device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpStat
         q0 = qB[ks][0], q1 = qB[ks][1];
       }
       if (KL == 0 ? (ks % C::KSG == 0) : (ks == 0)) {
-        // a fresh accumulator per K channel group (token-wise K) or per token group
-        // (channel-wise K), starting at minus the magic bias
-        const float b0 = (KL == 0) ? st.kbias[0][ks / C::KSG] : cwneg[0];
-        const float b1 = (KL == 0) ? st.kbias[1][ks / C::KSG] : cwneg[1];
-        mma_f16_c(acc, a0, a1, a2, a3, q0, q1, b0, b1, b0, b1);
+        // a fresh accumulator per K channel group (token-wise K) or per 32-token chunk
+        // (channel-wise K)
+        mma_f16_c(acc, a0, a1, a2, a3, q0, q1, 0.f, 0.f, 0.f, 0.f);
       } else {
         mma_f16(acc, a0, a1, a2, a3, q0, q1);
       }
@@ -514,12 +499,10 @@ __device__ __forceinline__ void qk_chunk(float (&x)[2][2][C::NQ], const WarpStat
 
 // PV of one 32-token chunk: accv[mt][v] (+)= V^T[16 channels x 16 tokens] * B.
 // Row half `row` of m-tile mt is channel 16 g + pv_channel(mt, row). fresh: the
-// accumulators start at cb (minus the magic bias of each column) instead of
-// continuing.
+// accumulators start at zero instead of continuing.
 template <class C>
 __device__ __forceinline__ void pv_chunk(float (&accv)[8][C::NTV][4], const uint32_t (&pB)[C::NTV][2][2],
-                                         const SlotSmem& sm, int rel0, const LaneCols& lc, bool fresh,
-                                         const float (&cb)[C::NTV][2]) {
+                                         const SlotSmem& sm, int rel0, const LaneCols& lc, bool fresh) {
   constexpr int BITS = C::BITS, RB = C::RB, NTV = C::NTV;
   const int g = lc.g, c = lc.c;
 #pragma unroll
@@ -542,8 +525,7 @@ __device__ __forceinline__ void pv_chunk(float (&accv)[8][C::NTV][4], const uint
 #pragma unroll
         for (int v = 0; v < NTV; ++v) {
           if (first)
-            mma_f16_c(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1], cb[v][0], cb[v][1], cb[v][0],
-                        cb[v][1]);
+            mma_f16_c(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1], 0.f, 0.f, 0.f, 0.f);
           else
             mma_f16(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1]);
         }
@@ -568,8 +550,7 @@ __device__ __forceinline__ void pv_chunk(float (&accv)[8][C::NTV][4], const uint
 #pragma unroll
           for (int v = 0; v < NTV; ++v) {
             if (first)
-              mma_f16_c(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1], cb[v][0], cb[v][1], cb[v][0],
-                        cb[v][1]);
+              mma_f16_c(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1], 0.f, 0.f, 0.f, 0.f);
             else
               mma_f16(accv[mt][v], a0, a1, a2, a3, pB[v][kk][0], pB[v][kk][1]);
           }
@@ -598,7 +579,7 @@ __device__ __forceinline__ int live_col(int i, const LaneCols& lc) {
 }
 
 // Token-wise V: operand-fold of one chunk (the scale is already in the weights):
-// running output += (bias-free accumulator) * 2^-eP / factor.
+// running output += accumulator * inv_ps / factor, inv_ps = 2^-eP * 2^24.
 template <class C>
 __device__ __forceinline__ void fold_tokenwise_v(WarpState<C>& st, const float (&accv)[8][C::NTV][4], float inv_ps,
                                                  const LaneCols& lc) {
@@ -618,7 +599,7 @@ __device__ __forceinline__ void fold_tokenwise_v(WarpState<C>& st, const float (
 }
 
 // Channel-wise V: acc-fold of one token group tau whose s/z rows are s_tau/z_tau:
-// running output += s_tau,d * (bias-free accumulator) / (FED factor) + z_tau,d * W,
+// running output += s_tau,d * accumulator * 2^24 / (FED factor) + z_tau,d * W,
 // W = sum of the group's weights (fed sum / FED) per owned combo; the weights were fed
 // as P * FED.
 template <class C, int FED = 8192>
@@ -645,7 +626,7 @@ __device__ __forceinline__ void fold_channelwise_v(WarpState<C>& st, const float
         const float s = (k & 1) ? s2.y : s2.x;
         const float z = (k & 1) ? z2.y : z2.x;
         const float a = (e == 0) ? accv[mt][v][2 * row] : accv[mt][v][2 * row + 1];
-        st.o_run[mt][row][i] = fmaf(s * (1.f / ((float)FED * v_mult<BITS>(mt))), a, fmaf(z, W, st.o_run[mt][row][i]));
+        st.o_run[mt][row][i] = fmaf(s * (kImageUnit / ((float)FED * v_mult<BITS>(mt))), a, fmaf(z, W, st.o_run[mt][row][i]));
       }
   }
 }
@@ -664,7 +645,7 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
   // ------------------------------------------------ phase 1: scores of the whole unit
   float x[NCH][2][2][NQ];
   uint32_t qBt[8][2];  // channel-wise K: Q' of the current token group
-  float cwA[NQ], cwB[NQ], cwneg[2] = {0.f, 0.f};
+  float cwA[NQ], cwB[NQ];
 #pragma unroll
   for (int j = 0; j < NQ; ++j) cwA[j] = cwB[j] = 0.f;
 #pragma unroll
@@ -682,10 +663,10 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
     if constexpr (KL == 1) {
       if (ch == 0 || (C::G <= C::UNIT && (kChunk * ch) % C::G == 0)) {
         const int tau = rel0 / C::G;
-        channelwise_q<C>(qBt, cwA, cwB, cwneg, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
+        channelwise_q<C>(qBt, cwA, cwB, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
       }
     }
-    qk_chunk<C>(x[ch], st, qBt, sqb, cwA, cwB, cwneg, sm, rel0, lc);
+    qk_chunk<C>(x[ch], st, qBt, sqb, cwA, cwB, sm, rel0, lc);
     if (!FULL) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
@@ -763,13 +744,12 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
     int e2 = 0;
     if (smaxf > 0.f) e2 = min(100, max(-100, 13 - ilog2f(smaxf)));
     ps = exp2i(e2);
-    inv_ps = exp2i(-e2);
+    inv_ps = exp2i(24 - e2);  // 2^-eP times the 2^24 of the subnormal images
   }
 
   // ------------------------------------------------ phase 2: weights, PV, V fold
-  // Each chunk's PV accumulators start at (token-wise V) or are lowered by (channel-wise
-  // V, later chunks of a token group) minus 1024 * the chunk's fed-weight sum, so that
-  // the fp32 accumulator never carries more than one chunk's magic bias.
+  // Each chunk's PV accumulators start at zero (token-wise V, and the first chunk of a
+  // token group) or continue (channel-wise V, later chunks of the group).
   float accv[8][NTV][4];
   float Wg[NO];  // channel-wise V: fed-weight sum of the current token group
 #pragma unroll
@@ -865,40 +845,7 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
           pB[v][kk][1] = (g & 1) ? x11 : x10;
         }
       }
-    // Minus the magic bias per accumulator column (v, 2c + e): 1024 times the sum of the fp16
-    // weights fed to that column. Token-wise V: the tensor cores form the sums, with an
-    // all-ones A operand against the same B fragments. Channel-wise V: from the sums above,
-    // per owned combo (DUP ? 0 : 2v + e).
-    float cb[NTV][2];
-    if (VL == 0) {
-      constexpr uint32_t kOnes2 = 0x3c003c00u;  // (1.0, 1.0) in fp16
-#pragma unroll
-      for (int v = 0; v < NTV; ++v) {
-        float fs[4];
-        mma_f16_c(fs, kOnes2, kOnes2, kOnes2, kOnes2, pB[v][0][0], pB[v][0][1], 0.f, 0.f, 0.f, 0.f);
-        mma_f16(fs, kOnes2, kOnes2, kOnes2, kOnes2, pB[v][1][0], pB[v][1][1]);
-        cb[v][0] = -kMagicF * fs[0];
-        cb[v][1] = -kMagicF * fs[1];
-      }
-    } else {
-#pragma unroll
-      for (int v = 0; v < NTV; ++v)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) cb[v][e] = -kMagicF * Fc[C::DUP ? 0 : 2 * v + e];
-    }
-    if (!fresh) {
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int v = 0; v < NTV; ++v)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            if (!C::DUP || e == 0) {  // the duplicate column of a pair is never read
-              accv[mt][v][e] += cb[v][e];
-              accv[mt][v][2 + e] += cb[v][e];
-            }
-    }
-    pv_chunk<C>(accv, pB, sm, rel0, lc, fresh, cb);
+    pv_chunk<C>(accv, pB, sm, rel0, lc, fresh);
 
     if (VL == 0) {
       fold_tokenwise_v<C>(st, accv, inv_ps, lc);
@@ -975,8 +922,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   int* sEq = reinterpret_cast<int*>(sAq + kMaxHq);         // [kMaxHq] query exponent
   float* sBz = sAq + 2 * kMaxHq;                           // [kMaxHq][4] 2^e * sum of Q per channel group
   uint2* sqb = reinterpret_cast<uint2*>(smem + kQbOffset);  // [8 k-steps][32 lanes] token-wise K
-  float* sPart = reinterpret_cast<float*>(smem + kPartOffset);  // [8 k-steps][32 lanes]
-  float* sKb = reinterpret_cast<float*>(smem + kKbOffset);      // [8 columns][4 channel groups]
   MergeArea ma;
   ma.m = reinterpret_cast<float*>(smem + kPrologueBytes);
   ma.l = ma.m + kMergeWarps * kMaxHq;
@@ -1292,11 +1237,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       }
       int e = 0;
       if (amax > 0.f) e = min(100, max(-100, 13 - ilog2f(amax)));
+      // token-wise K scores are kept in units of sAq; the raw products carry the 2^-24 of the
+      // subnormal code images, so the unit and the offset sums take the 2^24
       if (lane == 0) {
         sEq[i] = e;
-        sAq[i] = p.sl2 * exp2i(-e);
+        sAq[i] = p.sl2 * exp2i(24 - e);
       }
-      if (KL == 0 && (lane % lanes_per_group) == 0) sBz[i * 4 + lane / lanes_per_group] = exp2i(e) * gs;
+      if (KL == 0 && (lane % lanes_per_group) == 0) sBz[i * 4 + lane / lanes_per_group] = exp2i(e - 24) * gs;
     }
     __syncthreads();
 
@@ -1315,16 +1262,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
 
     WarpState<C> st;
     if (KL == 0) {
-      // token-wise K: B fragments Q' = Q 2^e / factor (fp16; exact for a bf16 query) of column g, the same for
-      // every warp, formed once: warp ks < 8 the k-step ks; then minus the magic bias 1024 *
-      // sum of Q' per channel group of each column
+      // token-wise K: B fragments Q' = Q 2^e / factor (fp16; exact for a bf16 query) of
+      // column g, the same for every warp, formed once: warp ks < 8 the k-step ks
       if (warp < 8) {
         const int ks = warp;
         const int qb = qk_query<C>(g, hq);
         const bool live = qb >= 0;
         const float sc = live ? exp2i(sEq[qb]) : 0.f;
         uint32_t qbw[2];
-        float part = 0.f;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           float xx[2];
@@ -1334,29 +1279,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
             xx[e] = live ? sQ[qb * D + ch] * sc * k_rmult<C>(ch) : 0.f;
           }
           qbw[r] = f16x2_from(xx[0], xx[1]);
-          // the bias is taken from the fp16 values actually fed, so that it cancels exactly
-          // also when Q' is not an exact fp16 (a rotated query)
-          const float2 f = half2_to_float2(qbw[r]);
-          part += f.x + f.y;
         }
         sqb[ks * 32 + lane] = make_uint2(qbw[0], qbw[1]);
-        sPart[ks * 32 + lane] = part;
       }
-      __syncthreads();
-      if (threadIdx.x < 32) {  // thread 4 col + uu: column col, channel group uu
-        const int col = lane >> 2, uu = lane & 3;
-        float sum = 0.f;
-        if (uu < GK)
-          for (int ks = uu * C::KSG; ks < (uu + 1) * C::KSG; ++ks)
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) sum += sPart[ks * 32 + 4 * col + cc];
-        sKb[lane] = -kMagicF * sum;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-        for (int uu = 0; uu < GK; ++uu) st.kbias[jj][uu] = sKb[(2 * c + jj) * 4 + uu];
 #pragma unroll
       for (int j = 0; j < NQ; ++j) {
         const int qs = qk_query<C>(2 * c + j, hq);

@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) grp_decode_kernel(const __grid_
           int e2 = 0;
           if (smaxf > 0.f) e2 = min(100, max(-100, 6 - ilog2f(smaxf)));
           const float ps = exp2i(e2);
-          inv_ps = exp2i(-e2);
+          inv_ps = exp2i(24 - e2);  // 2^-eP times the 2^24 of the subnormal V code images
 #pragma unroll
           for (int k2 = 0; k2 < MC; ++k2) {
             const int i = k2 / GV, uu = k2 % GV;
@@ -701,24 +701,22 @@ __global__ void __launch_bounds__(C::THREADS, 1) grp_decode_kernel(const __grid_
         for (int v = 0; v < NTV; ++v)
           ldsm_x4_trans(smem_addr(ptile + lane * S::P_ROW + 16 * v), pB[v][0][0], pB[v][0][1], pB[v][1][0],
                         pB[v][1][1]);
-        // minus the magic bias of each PV accumulator column: 1024 times the sum of the fp16
-        // weights fed to it, formed by the tensor cores with an all-ones A operand
-        float cb[NTV][2], fsum[NTV][2];
-        {
+        // channel-wise V: the sum of the fp16 weights fed to each PV accumulator column,
+        // formed by the tensor cores with an all-ones A operand (the group's weight sum W)
+        float fsum[NTV][2];
+        if (VL == 1) {
           constexpr uint32_t kOnes2 = 0x3c003c00u;
 #pragma unroll
           for (int v = 0; v < NTV; ++v) {
             float fs[4];
             mma_f16_c(fs, kOnes2, kOnes2, kOnes2, kOnes2, pB[v][0][0], pB[v][0][1], 0.f, 0.f, 0.f, 0.f);
             mma_f16(fs, kOnes2, kOnes2, kOnes2, kOnes2, pB[v][1][0], pB[v][1][1]);
-            cb[v][0] = -kMagicF * fs[0];
-            cb[v][1] = -kMagicF * fs[1];
             fsum[v][0] = fs[0];
             fsum[v][1] = fs[1];
           }
         }
         float accv[8][NTV][4];
-        pv_chunk<C>(accv, pB, sm, 32 * quad, lc, true, cb);
+        pv_chunk<C>(accv, pB, sm, 32 * quad, lc, true);
         if (VL == 0) {
           fold_tokenwise_v<C>(st, accv, inv_ps, lc);
         } else {

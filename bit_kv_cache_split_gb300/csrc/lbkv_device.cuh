@@ -210,18 +210,6 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __half2float(__ushort_as_half((unsigned short)(r & 0xffffu)));
 }
 
-// fp16 magic number 1024: OR-ing a small integer m into its mantissa gives the
-// fp16 value 1024 + m exactly (m < 1024), two lanes at a time.
-constexpr uint32_t kMagic2 = 0x64006400u;
-constexpr float kMagicF = 1024.f;
-
-// (a & b) | c in one LOP3.
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t f16x2_from(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
