@@ -578,7 +578,7 @@ __device__ __forceinline__ int live_col(int i, const LaneCols& lc) {
   return C::DUP ? 0 : (C::GV == 1 ? i : max(lc.e_live, 0));
 }
 
-// Token-wise V: operand-fold of one chunk (the scale is already in the weights):
+// Token-wise V: operand-fold of one item (the scale is already in the weights):
 // running output += accumulator * inv_ps / factor, inv_ps = 2^-eP * 2^24.
 template <class C>
 __device__ __forceinline__ void fold_tokenwise_v(WarpState<C>& st, const float (&accv)[8][C::NTV][4], float inv_ps,
@@ -748,8 +748,6 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
   }
 
   // ------------------------------------------------ phase 2: weights, PV, V fold
-  // Each chunk's PV accumulators start at zero (token-wise V, and the first chunk of a
-  // token group) or continue (channel-wise V, later chunks of the group).
   float accv[8][NTV][4];
   float Wg[NO];  // channel-wise V: fed-weight sum of the current token group
 #pragma unroll
@@ -758,7 +756,9 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
   for (int ch = 0; ch < NCH; ++ch) {
     const int rel0 = kChunk * ch;
     if (!FULL && rel0 >= nv) break;
-    const bool fresh = (VL == 0) || (ch == 0) || (C::G <= C::UNIT && (kChunk * ch) % C::G == 0);
+    // The accumulators run over the item (token-wise V: its weights share one exponent) or
+    // over a token group (channel-wise V: one scale row), starting at zero.
+    const bool fresh = (ch == 0) || (VL == 1 && C::G <= C::UNIT && (kChunk * ch) % C::G == 0);
     float P[2][2][NQ];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
@@ -847,10 +847,10 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
       }
     pv_chunk<C>(accv, pB, sm, rel0, lc, fresh);
 
+    const bool last = (ch == NCH - 1) || (!FULL && rel0 + kChunk >= nv);
     if (VL == 0) {
-      fold_tokenwise_v<C>(st, accv, inv_ps, lc);
+      if (last) fold_tokenwise_v<C>(st, accv, inv_ps, lc);
     } else {
-      const bool last = (ch == NCH - 1) || (!FULL && rel0 + kChunk >= nv);
       const bool group_end = C::G <= C::UNIT && ((kChunk * (ch + 1)) % C::G == 0);
       if (last || group_end) {
         const int tau = rel0 / C::G;  // token-group row of the entry

@@ -1,10 +1,136 @@
 // lbkv_pack.cu -- quantizer of a bf16 cache side into packed 2-/4-bit codes
-// with one fp16 scale and offset per group (the arithmetic is in lbkv_quant.cuh), stored
-// contiguously or in the pages of a paged cache.
+// with one fp16 scale and offset per group, stored contiguously or in the pages of a
+// paged cache. The arithmetic is the quantizer of lbkv_quant.cuh (min/max per group,
+// s = fp16((max - min) / (2^b - 1)), z = fp16(min), q = clamp(rint(fl((x - z) / s)))),
+// bit-exact, with a faster route to the same codes:
+//
+// Bracketed quotient. With inv = fl(1/s), inv_lo = fl(inv (1 - 2^-21)) and
+// inv_hi = fl(inv (1 + 2^-21)), every d satisfies d inv_lo <= fl(d / s) <= d inv_hi
+// for d >= 0 (fl(d / s) is within 2^-24 of d / s, inv within 2^-24 of 1 / s). One fused
+// multiply-add per bound, fma(d, inv, 1.5 * 2^23), rounds the exact product to an integer
+// (ties to even) in the low bits of its result; rint is monotone, so where the two bounds
+// round to the same integer, that integer is rint(fl(d / s)). Where they differ (d / s
+// within about 2^-20 d / s of a half-integer) the correctly rounded division decides.
+// A group takes this route when z equals its minimum exactly (a bf16 minimum inside the
+// fp16 normal range) and s is a normal fp16: then 0 <= d / s < qmax + 0.01, so the codes
+// need no clamp; any other group (and any value that is not finite) takes the division
+// for every value.
 #include "lbkv_internal.h"
 #include "lbkv_quant.cuh"
 
 namespace lbkv {
+
+namespace {
+
+constexpr int kPackRows = 64;     // token rows per CTA of the token-wise kernel (divides the 128-token slot)
+constexpr int kPackStride = 272;  // their shared-memory stride: 256 bytes + 16 keeps 16-byte reads conflict-free
+constexpr float kRintMagic = 12582912.f;  // 1.5 * 2^23: x + this has rint(x) in its low bits, |x| < 2^22
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Scale and offset of a group from its extremes, as lbkv_quant.cuh forms them, and the
+// constants of the bracketed quotient. fast: the group may take the bracketed route.
+struct GroupQ {
+  __half sh, zh;
+  float sf, zf, inv, inv_lo, inv_hi;
+  bool fast;
+};
+template <int BITS>
+__device__ __forceinline__ GroupQ group_params(float mn, float mx) {
+  constexpr int qmax = (1 << BITS) - 1;
+  GroupQ g;
+  mn = __fadd_rn(mn, 0.f);  // a -0 extreme is read as +0
+  mx = __fadd_rn(mx, 0.f);
+  g.sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)qmax));
+  g.zh = __float2half_rn(mn);
+  g.sf = __half2float(g.sh);
+  g.zf = __half2float(g.zh);
+  g.inv = __frcp_rn(g.sf);
+  g.inv_lo = __fmul_rn(g.inv, 1.f - 4.76837158203125e-07f);  // 1 - 2^-21
+  g.inv_hi = __fmul_rn(g.inv, 1.f + 4.76837158203125e-07f);  // 1 + 2^-21
+  g.fast = (g.zf == mn) && (g.sf >= 6.103515625e-05f) && (g.sf <= 65504.f);  // z = min, s normal
+  return g;
+}
+
+// Bracketed code of x (see the file comment): the integer in the low bits of the result,
+// and ok &= both bounds agree.
+__device__ __forceinline__ uint32_t bracket_code(float x, const GroupQ& g, bool& ok) {
+  const float d = __fsub_rn(x, g.zf);
+  const float a = __fmaf_rn(d, g.inv_lo, kRintMagic);
+  const float b = __fmaf_rn(d, g.inv_hi, kRintMagic);
+  ok = ok && (a == b);
+  return __float_as_uint(a);
+}
+
+// Packs 16 (INT2) or 8 (INT4) bracketed codes (low bits of each word, anything above bit
+// 21) into one word, code i at bits BITS i: shift-and-add pairs, whose garbage stays above
+// bit 21, then one byte permute for the last level.
+template <int BITS>
+__device__ __forceinline__ uint32_t pack_word(const uint32_t* c) {
+  constexpr int N = 32 / BITS;
+  uint32_t u[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) u[i] = (c[2 * i + 1] << BITS) + c[2 * i];
+  int n = N / 2, sh = 2 * BITS;
+#pragma unroll
+  for (; n > 2; n >>= 1, sh <<= 1)
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) u[i] = (u[2 * i + 1] << sh) + u[2 * i];
+  return __byte_perm(u[0], u[1], 0x5410);  // low 16 bits of each
+}
+
+// Codes of the token-wise group held in w (G bf16 values, pairs (2i, 2i+1) in w[i]) into
+// out[G * BITS / 32] words; returns the group's scale and offset.
+template <int BITS, int G>
+__device__ __forceinline__ void quantize_group_words(const uint32_t (&w)[G / 2], uint32_t (&out)[G * BITS / 32],
+                                                     __half& sh, __half& zh) {
+  constexpr int qmax = (1 << BITS) - 1, PER = 32 / BITS;
+  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mx2 = mn2;
+#pragma unroll
+  for (int i = 1; i < G / 2; ++i) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    mn2 = __hmin2(mn2, v);
+    mx2 = __hmax2(mx2, v);
+  }
+  const float mn = fminf(__low2float(mn2), __high2float(mn2));
+  const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+  const GroupQ g = group_params<BITS>(mn, mx);
+  sh = g.sh;
+  zh = g.zh;
+  if (g.sf == 0.f) {
+#pragma unroll
+    for (int j = 0; j < G * BITS / 32; ++j) out[j] = 0u;
+    return;
+  }
+  bool ok = g.fast;
+  if (ok) {
+#pragma unroll
+    for (int j = 0; j < G * BITS / 32; ++j) {
+      uint32_t c[PER];
+#pragma unroll
+      for (int i = 0; i < PER / 2; ++i) {
+        const uint32_t v = w[j * PER / 2 + i];
+        c[2 * i] = bracket_code(bf16_lo(v), g, ok);
+        c[2 * i + 1] = bracket_code(bf16_hi(v), g, ok);
+      }
+      out[j] = pack_word<BITS>(c);
+    }
+  }
+  if (!ok) {  // the correctly rounded division for every value of the group
+#pragma unroll
+    for (int j = 0; j < G * BITS / 32; ++j) {
+      uint32_t word = 0u;
+#pragma unroll
+      for (int i = 0; i < PER / 2; ++i) {
+        const uint32_t v = w[j * PER / 2 + i];
+        word |= (uint32_t)quantize_one(bf16_lo(v), g.zf, g.sf, g.inv, qmax) << (BITS * 2 * i);
+        word |= (uint32_t)quantize_one(bf16_hi(v), g.zf, g.sf, g.inv, qmax) << (BITS * (2 * i + 1));
+      }
+      out[j] = word;
+    }
+  }
+}
 
 // The storage row and channel-group block of token t of cache unit `unit` (= b * Hkv +
 // kvh), or false when the token lies in no page of the pool (recorded as status 5).
@@ -22,66 +148,174 @@ __device__ __forceinline__ bool pack_addr(const PackArgs& a, size_t unit, int t,
   return true;
 }
 
-// One warp per token row. The contiguous cache has the codes of positions t >= L_b
-// cleared; the paged cache stores positions t < L_b only.
-template <int BITS>
-__global__ void __launch_bounds__(256) pack_tokenwise_kernel(const __grid_constant__ PackArgs a) {
-  constexpr int RB = kHeadDim * BITS / 8;
-  const long long rows = (long long)a.B * a.Hkv * a.T_cap;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const int t = (int)(row % a.T_cap);
-  const size_t unit = (size_t)(row / a.T_cap);
-  const bool valid = t < a.seq_lens[unit / a.Hkv];
+// Token-wise groups: a CTA takes kPackRows consecutive token rows of one cache unit
+// (T_cap is a multiple of 128), stages them in shared memory with coalesced 16-byte loads,
+// and thread (row, group) quantizes one group of G channels. The contiguous cache has the
+// codes of positions t >= L_b cleared; the paged cache stores positions t < L_b only.
+template <int BITS, int G>
+__global__ void __launch_bounds__(kPackRows * (kHeadDim / G)) pack_tokenwise_kernel(const __grid_constant__ PackArgs a) {
+  constexpr int TPR = kHeadDim / G, NT = kPackRows * TPR;
+  constexpr int RB = kHeadDim * BITS / 8, GW = G * BITS / 32;  // code bytes per row, code words per group
+  __shared__ __align__(16) uint8_t tile[kPackRows * kPackStride];
+  const size_t row0 = (size_t)blockIdx.x * kPackRows;
+  const size_t unit = row0 / (size_t)a.T_cap;
+  const int t0 = (int)(row0 - unit * (size_t)a.T_cap);
+  const int L = a.seq_lens[unit / a.Hkv];
+  const int nvalid = min(max(L - t0, 0), kPackRows);
+  if (nvalid == 0 && a.pg.page_table) return;
+  const uint4* src = reinterpret_cast<const uint4*>(a.x + row0 * kHeadDim);
+  for (int i = threadIdx.x; i < nvalid * 16; i += NT)
+    *reinterpret_cast<uint4*>(tile + (i >> 4) * kPackStride + (i & 15) * 16) = __ldcs(src + i);
+  __syncthreads();
+  const int r = threadIdx.x / TPR, gi = threadIdx.x % TPR;
+  const bool valid = r < nvalid;
   if (!valid && a.pg.page_table) return;
   KvAddr ad;
-  if (!pack_addr(a, unit, t, &ad)) return;
-  uint8_t* crow = a.codes + ad.row * RB;
-  if (!valid) {
-    if (BITS == 2)
-      crow[lane] = 0;
-    else
-      reinterpret_cast<uint16_t*>(crow)[lane] = 0;
-    return;
+  if (!pack_addr(a, unit, t0 + r, &ad)) return;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(a.codes + ad.row * RB) + gi * GW;
+  uint32_t out[GW];
+  if (valid) {
+    uint32_t w[G / 2];
+    const uint4* row = reinterpret_cast<const uint4*>(tile + r * kPackStride + gi * G * 2);
+#pragma unroll
+    for (int k = 0; k < G / 8; ++k) {
+      const uint4 v = row[k];
+      w[4 * k] = v.x, w[4 * k + 1] = v.y, w[4 * k + 2] = v.z, w[4 * k + 3] = v.w;
+    }
+    __half sh, zh;
+    quantize_group_words<BITS, G>(w, out, sh, zh);
+    const size_t si = ad.row * (kHeadDim / G) + gi;
+    a.scale[si] = sh;
+    a.off[si] = zh;
+  } else {
+#pragma unroll
+    for (int j = 0; j < GW; ++j) out[j] = 0u;
   }
-  const size_t si = ad.row * (kHeadDim / a.group);
-  quantize_token_row<BITS>(a.x + row * kHeadDim, a.group, crow, a.scale + si, a.off + si, lane);
+  if constexpr (GW % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < GW; j += 4)
+      *reinterpret_cast<uint4*>(dst + j) = make_uint4(out[j], out[j + 1], out[j + 2], out[j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < GW; j += 2) *reinterpret_cast<uint2*>(dst + j) = make_uint2(out[j], out[j + 1]);
+  }
 }
 
-// One block of 128 threads per (unit, token group): thread d owns channel d. The paged
-// cache stores the groups that hold a position t < L_b only.
-template <int BITS>
+// Channel-wise groups: one CTA of 128 threads per (unit, token group tau). The group's
+// valid rows are staged in shared memory; warp w takes its tokens w G/4 .. (w+1) G/4 - 1,
+// lane p the channels 4p .. 4p+3 (one INT2 code byte, two INT4 code bytes, per token).
+// Pass 1: per-warp extremes per channel; thread d combines them for channel d and forms
+// the group's scale, offset and quotient constants. Pass 2: the codes. The paged cache
+// stores the groups that hold a position t < L_b only.
+template <int BITS, int G>
 __global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_constant__ PackArgs a) {
-  constexpr int RB = kHeadDim * BITS / 8;
-  const int unit = blockIdx.x, tau = blockIdx.y, d = threadIdx.x;
+  constexpr int qmax = (1 << BITS) - 1, RB = kHeadDim * BITS / 8, TW = G / 4;  // tokens per warp
+  __shared__ __align__(16) uint8_t tile[G * 256];
+  __shared__ float2 part[4][kHeadDim];
+  __shared__ GroupQ gq[kHeadDim];
+  const int unit = blockIdx.x, tau = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = a.seq_lens[unit / a.Hkv];
-  const int t0 = tau * a.group;
-  const int nvalid = max(0, min(a.group, L - t0));
+  const int t0 = tau * G;
+  const int nvalid = max(0, min(G, L - t0));
   if (nvalid == 0 && a.pg.page_table) return;
   KvAddr ad;
   if (!pack_addr(a, (size_t)unit, t0, &ad)) return;
-  const size_t xrow = (size_t)unit * a.T_cap + t0;
-  const size_t si = ad.block * kHeadDim + d;
-  quantize_channel_group<BITS>(a.x + xrow * kHeadDim, nvalid, a.group, a.codes + ad.row * RB, a.scale + si,
-                               a.off + si, d);
+  const uint4* src = reinterpret_cast<const uint4*>(a.x + ((size_t)unit * a.T_cap + t0) * kHeadDim);
+  for (int i = threadIdx.x; i < nvalid * 16; i += 128) reinterpret_cast<uint4*>(tile)[i] = __ldcs(src + i);
+  __syncthreads();
+  const int tw0 = warp * TW, tw1 = min(tw0 + TW, nvalid);  // this warp's valid tokens
+  if (tw0 < tw1) {
+    uint2 v = *reinterpret_cast<const uint2*>(tile + tw0 * 256 + 8 * lane);
+    __nv_bfloat162 mnA = *reinterpret_cast<__nv_bfloat162*>(&v.x), mxA = mnA;
+    __nv_bfloat162 mnB = *reinterpret_cast<__nv_bfloat162*>(&v.y), mxB = mnB;
+    for (int t = tw0 + 1; t < tw1; ++t) {
+      v = *reinterpret_cast<const uint2*>(tile + t * 256 + 8 * lane);
+      const __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&v.x), y = *reinterpret_cast<__nv_bfloat162*>(&v.y);
+      mnA = __hmin2(mnA, x), mxA = __hmax2(mxA, x);
+      mnB = __hmin2(mnB, y), mxB = __hmax2(mxB, y);
+    }
+    part[warp][4 * lane] = make_float2(__low2float(mnA), __low2float(mxA));
+    part[warp][4 * lane + 1] = make_float2(__high2float(mnA), __high2float(mxA));
+    part[warp][4 * lane + 2] = make_float2(__low2float(mnB), __low2float(mxB));
+    part[warp][4 * lane + 3] = make_float2(__high2float(mnB), __high2float(mxB));
+  }
+  __syncthreads();
+  if (nvalid > 0) {
+    const int d = threadIdx.x;
+    float2 e = part[0][d];
+    for (int w = 1; w < 4 && w * TW < nvalid; ++w) {
+      const float2 f = part[w][d];
+      e.x = fminf(e.x, f.x);
+      e.y = fmaxf(e.y, f.y);
+    }
+    const GroupQ g = group_params<BITS>(e.x, e.y);
+    gq[d] = g;
+    const size_t si = ad.block * kHeadDim + d;
+    a.scale[si] = g.sh;
+    a.off[si] = g.zh;
+  }
+  __syncthreads();
+  GroupQ g4[4];
+  if (nvalid > 0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) g4[u] = gq[4 * lane + u];
+  }
+  for (int t = tw0; t < tw0 + TW; ++t) {
+    uint32_t word = 0u;  // codes of channels 4 lane .. 4 lane + 3 at bits BITS u
+    if (t < nvalid) {
+      const uint2 v = *reinterpret_cast<const uint2*>(tile + t * 256 + 8 * lane);
+      const float x[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const GroupQ& g = g4[u];
+        uint32_t q = 0u;
+        if (g.sf != 0.f) {
+          bool ok = g.fast;
+          const uint32_t c = bracket_code(x[u], g, ok);
+          q = ok ? (c & (uint32_t)qmax) : (uint32_t)quantize_one(x[u], g.zf, g.sf, g.inv, qmax);
+        }
+        word |= q << (BITS * u);
+      }
+    }
+    uint8_t* crow = a.codes + (ad.row + t) * RB;
+    if (BITS == 2)
+      crow[lane] = (uint8_t)word;
+    else
+      reinterpret_cast<uint16_t*>(crow)[lane] = (uint16_t)word;
+  }
 }
 
-int launch_pack(const PackArgs& a, cudaStream_t stream) {
+template <int BITS>
+void launch_pack_bits(const PackArgs& a, cudaStream_t stream) {
   if (a.layout == 0) {
     const long long rows = (long long)a.B * a.Hkv * a.T_cap;
-    const unsigned blocks = (unsigned)((rows + 7) / 8);
-    if (a.bits == 2)
-      pack_tokenwise_kernel<2><<<blocks, 256, 0, stream>>>(a);
+    const unsigned blocks = (unsigned)(rows / kPackRows);  // T_cap is a multiple of kPackRows
+    if (a.group == 128)
+      pack_tokenwise_kernel<BITS, 128><<<blocks, kPackRows, 0, stream>>>(a);
+    else if (a.group == 64)
+      pack_tokenwise_kernel<BITS, 64><<<blocks, kPackRows * 2, 0, stream>>>(a);
     else
-      pack_tokenwise_kernel<4><<<blocks, 256, 0, stream>>>(a);
+      pack_tokenwise_kernel<BITS, 32><<<blocks, kPackRows * 4, 0, stream>>>(a);
   } else {
     dim3 grid((unsigned)(a.B * a.Hkv), (unsigned)(a.T_cap / a.group));
-    if (a.bits == 2)
-      pack_channelwise_kernel<2><<<grid, 128, 0, stream>>>(a);
+    if (a.group == 128)
+      pack_channelwise_kernel<BITS, 128><<<grid, 128, 0, stream>>>(a);
+    else if (a.group == 64)
+      pack_channelwise_kernel<BITS, 64><<<grid, 128, 0, stream>>>(a);
     else
-      pack_channelwise_kernel<4><<<grid, 128, 0, stream>>>(a);
+      pack_channelwise_kernel<BITS, 32><<<grid, 128, 0, stream>>>(a);
   }
+}
+
+}  // namespace
+
+int launch_pack(const PackArgs& a, cudaStream_t stream) {
+  static_assert(kSlotTokens % kPackRows == 0, "a CTA's rows lie in one cache unit");
+  if (a.bits == 2)
+    launch_pack_bits<2>(a, stream);
+  else
+    launch_pack_bits<4>(a, stream);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
