@@ -10,11 +10,15 @@
 // multiply-add per bound, fma(d, inv, 1.5 * 2^23), rounds the exact product to an integer
 // (ties to even) in the low bits of its result; rint is monotone, so where the two bounds
 // round to the same integer, that integer is rint(fl(d / s)). Where they differ (d / s
-// within about 2^-20 d / s of a half-integer) the correctly rounded division decides.
+// within about 2^-20 d / s of a half-integer; with bf16 inputs these are nearly always
+// exact ties, about 6e-4 of the values) the correctly rounded division decides: a thread
+// notes the code words that hold such a value and recomputes them after all its words,
+// so that the lanes of a warp that need a fix-up do it in one pass instead of each
+// stopping the warp at its own word.
 // A group takes this route when z equals its minimum exactly (a bf16 minimum inside the
-// fp16 normal range) and s is a normal fp16: then 0 <= d / s < qmax + 0.01, so the codes
-// need no clamp; any other group (and any value that is not finite) takes the division
-// for every value.
+// fp16 normal range) and s is a normal fp16, or zero: then 0 <= d / s < qmax + 0.01, so
+// the codes need no clamp; any other group (and any value that is not finite) takes the
+// division for every value.
 #include "lbkv_internal.h"
 #include "lbkv_quant.cuh"
 
@@ -37,7 +41,7 @@ struct GroupQ {
   bool fast;
 };
 template <int BITS>
-__device__ __forceinline__ GroupQ group_params(float mn, float mx) {
+__device__ __forceinline__ GroupQ group_params(float mn, float mx, bool has_nan) {
   constexpr int qmax = (1 << BITS) - 1;
   GroupQ g;
   mn = __fadd_rn(mn, 0.f);  // a -0 extreme is read as +0
@@ -49,18 +53,27 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx) {
   g.inv = __frcp_rn(g.sf);
   g.inv_lo = __fmul_rn(g.inv, 1.f - 4.76837158203125e-07f);  // 1 - 2^-21
   g.inv_hi = __fmul_rn(g.inv, 1.f + 4.76837158203125e-07f);  // 1 + 2^-21
-  g.fast = (g.zf == mn) && (g.sf >= 6.103515625e-05f) && (g.sf <= 65504.f);  // z = min, s normal
+  // z = min and s normal; or s = 0 (a constant group: every code 0, as the bounds 0 give)
+  // (a NaN value, which the extremes skip, would break the packing: division route)
+  g.fast = !has_nan && (g.zf == mn) && ((g.sf >= 6.103515625e-05f && g.sf <= 65504.f) || g.sf == 0.f);
+  if (g.sf == 0.f) g.inv_lo = g.inv_hi = 0.f;
   return g;
 }
 
-// Bracketed code of x (see the file comment): the integer in the low bits of the result,
-// and ok &= both bounds agree.
-__device__ __forceinline__ uint32_t bracket_code(float x, const GroupQ& g, bool& ok) {
+// Bracketed code of x (see the file comment): the integer in the low bits of the result;
+// diff collects the bits in which the two bounds differ (zero where they agree).
+__device__ __forceinline__ uint32_t bracket_code(float x, const GroupQ& g, uint32_t& diff) {
   const float d = __fsub_rn(x, g.zf);
-  const float a = __fmaf_rn(d, g.inv_lo, kRintMagic);
-  const float b = __fmaf_rn(d, g.inv_hi, kRintMagic);
-  ok = ok && (a == b);
-  return __float_as_uint(a);
+  const uint32_t a = __float_as_uint(__fmaf_rn(d, g.inv_lo, kRintMagic));
+  const uint32_t b = __float_as_uint(__fmaf_rn(d, g.inv_hi, kRintMagic));
+  diff |= a ^ b;
+  return a;
+}
+// The code of x in a group that takes the bracketed route, by the correctly rounded
+// division (no clamp needed there).
+__device__ __forceinline__ uint32_t exact_code(float x, const GroupQ& g) {
+  if (g.sf == 0.f) return 0u;
+  return (uint32_t)rintf(__fdiv_rn(__fsub_rn(x, g.zf), g.sf));
 }
 
 // Packs 16 (INT2) or 8 (INT4) bracketed codes (low bits of each word, anything above bit
@@ -81,43 +94,41 @@ __device__ __forceinline__ uint32_t pack_word(const uint32_t* c) {
 }
 
 // Codes of the token-wise group held in w (G bf16 values, pairs (2i, 2i+1) in w[i]) into
-// out[G * BITS / 32] words; returns the group's scale and offset.
+// out[G * BITS / 32] words, the group's scale and offset into sh, zh. Returns the mask of
+// the words that hold a value whose bounds differ (to be recomputed by fix_word).
 template <int BITS, int G>
-__device__ __forceinline__ void quantize_group_words(const uint32_t (&w)[G / 2], uint32_t (&out)[G * BITS / 32],
-                                                     __half& sh, __half& zh) {
+__device__ __forceinline__ uint32_t quantize_group_words(const uint32_t (&w)[G / 2], uint32_t (&out)[G * BITS / 32],
+                                                         __half& sh, __half& zh, GroupQ& g) {
   constexpr int qmax = (1 << BITS) - 1, PER = 32 / BITS;
-  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mx2 = mn2;
+  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mx2 = mn2, nan2 = mn2;
 #pragma unroll
   for (int i = 1; i < G / 2; ++i) {
     const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
     mn2 = __hmin2(mn2, v);
     mx2 = __hmax2(mx2, v);
+    nan2 = __hmin2_nan(nan2, v);  // NaN if any value is
   }
   const float mn = fminf(__low2float(mn2), __high2float(mn2));
   const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
-  const GroupQ g = group_params<BITS>(mn, mx);
+  const float nn = __low2float(nan2) + __high2float(nan2);
+  g = group_params<BITS>(mn, mx, nn != nn);
   sh = g.sh;
   zh = g.zh;
-  if (g.sf == 0.f) {
-#pragma unroll
-    for (int j = 0; j < G * BITS / 32; ++j) out[j] = 0u;
-    return;
-  }
-  bool ok = g.fast;
-  if (ok) {
+  uint32_t bad = 0u;
+  if (g.fast) {
 #pragma unroll
     for (int j = 0; j < G * BITS / 32; ++j) {
-      uint32_t c[PER];
+      uint32_t c[PER], diff = 0u;
 #pragma unroll
       for (int i = 0; i < PER / 2; ++i) {
         const uint32_t v = w[j * PER / 2 + i];
-        c[2 * i] = bracket_code(bf16_lo(v), g, ok);
-        c[2 * i + 1] = bracket_code(bf16_hi(v), g, ok);
+        c[2 * i] = bracket_code(bf16_lo(v), g, diff);
+        c[2 * i + 1] = bracket_code(bf16_hi(v), g, diff);
       }
       out[j] = pack_word<BITS>(c);
+      bad |= (diff != 0u ? 1u : 0u) << j;
     }
-  }
-  if (!ok) {  // the correctly rounded division for every value of the group
+  } else {  // the correctly rounded division for every value of the group
 #pragma unroll
     for (int j = 0; j < G * BITS / 32; ++j) {
       uint32_t word = 0u;
@@ -130,6 +141,18 @@ __device__ __forceinline__ void quantize_group_words(const uint32_t (&w)[G / 2],
       out[j] = word;
     }
   }
+  return bad;
+}
+
+// Code word j of a bracketed group recomputed by the division, from the group's bf16
+// values x[0 .. G-1].
+template <int BITS>
+__device__ __forceinline__ uint32_t fix_word(const __nv_bfloat16* x, int j, const GroupQ& g) {
+  constexpr int PER = 32 / BITS;
+  uint32_t word = 0u;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) word |= exact_code(__bfloat162float(x[j * PER + i]), g) << (BITS * i);
+  return word;
 }
 
 // The storage row and channel-group block of token t of cache unit `unit` (= b * Hkv +
@@ -146,6 +169,18 @@ __device__ __forceinline__ bool pack_addr(const PackArgs& a, size_t unit, int t,
   }
   *ad = kv_addr(a.pg.page_tokens, page, unit, kvh, a.Hkv, a.T_cap, a.group, t);
   return true;
+}
+
+template <int GW>
+__device__ __forceinline__ void store_words(uint32_t* dst, const uint32_t (&out)[GW]) {
+  if constexpr (GW % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < GW; j += 4)
+      *reinterpret_cast<uint4*>(dst + j) = make_uint4(out[j], out[j + 1], out[j + 2], out[j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < GW; j += 2) *reinterpret_cast<uint2*>(dst + j) = make_uint2(out[j], out[j + 1]);
+  }
 }
 
 // Token-wise groups: a CTA takes kPackRows consecutive token rows of one cache unit
@@ -183,21 +218,22 @@ __global__ void __launch_bounds__(kPackRows * (kHeadDim / G)) pack_tokenwise_ker
       w[4 * k] = v.x, w[4 * k + 1] = v.y, w[4 * k + 2] = v.z, w[4 * k + 3] = v.w;
     }
     __half sh, zh;
-    quantize_group_words<BITS, G>(w, out, sh, zh);
+    GroupQ g;
+    uint32_t bad = quantize_group_words<BITS, G>(w, out, sh, zh, g);
     const size_t si = ad.row * (kHeadDim / G) + gi;
     a.scale[si] = sh;
     a.off[si] = zh;
+    store_words<GW>(dst, out);
+    const __nv_bfloat16* xg = reinterpret_cast<const __nv_bfloat16*>(tile + r * kPackStride + gi * G * 2);
+    while (bad) {  // rare: words with a value on a rounding boundary, after the plain stores
+      const int j = __ffs(bad) - 1;
+      bad &= bad - 1u;
+      dst[j] = fix_word<BITS>(xg, j, g);
+    }
   } else {
 #pragma unroll
     for (int j = 0; j < GW; ++j) out[j] = 0u;
-  }
-  if constexpr (GW % 4 == 0) {
-#pragma unroll
-    for (int j = 0; j < GW; j += 4)
-      *reinterpret_cast<uint4*>(dst + j) = make_uint4(out[j], out[j + 1], out[j + 2], out[j + 3]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < GW; j += 2) *reinterpret_cast<uint2*>(dst + j) = make_uint2(out[j], out[j + 1]);
+    store_words<GW>(dst, out);
   }
 }
 
@@ -212,6 +248,7 @@ __global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_cons
   constexpr int qmax = (1 << BITS) - 1, RB = kHeadDim * BITS / 8, TW = G / 4;  // tokens per warp
   __shared__ __align__(16) uint8_t tile[G * 256];
   __shared__ float2 part[4][kHeadDim];
+  __shared__ uint32_t part_nan[4][kHeadDim / 4];  // per warp and lane: a NaN among its values
   __shared__ GroupQ gq[kHeadDim];
   const int unit = blockIdx.x, tau = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -227,14 +264,16 @@ __global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_cons
   const int tw0 = warp * TW, tw1 = min(tw0 + TW, nvalid);  // this warp's valid tokens
   if (tw0 < tw1) {
     uint2 v = *reinterpret_cast<const uint2*>(tile + tw0 * 256 + 8 * lane);
-    __nv_bfloat162 mnA = *reinterpret_cast<__nv_bfloat162*>(&v.x), mxA = mnA;
-    __nv_bfloat162 mnB = *reinterpret_cast<__nv_bfloat162*>(&v.y), mxB = mnB;
+    __nv_bfloat162 mnA = *reinterpret_cast<__nv_bfloat162*>(&v.x), mxA = mnA, nA = mnA;
+    __nv_bfloat162 mnB = *reinterpret_cast<__nv_bfloat162*>(&v.y), mxB = mnB, nB = mnB;
     for (int t = tw0 + 1; t < tw1; ++t) {
       v = *reinterpret_cast<const uint2*>(tile + t * 256 + 8 * lane);
       const __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&v.x), y = *reinterpret_cast<__nv_bfloat162*>(&v.y);
-      mnA = __hmin2(mnA, x), mxA = __hmax2(mxA, x);
-      mnB = __hmin2(mnB, y), mxB = __hmax2(mxB, y);
+      mnA = __hmin2(mnA, x), mxA = __hmax2(mxA, x), nA = __hmin2_nan(nA, x);
+      mnB = __hmin2(mnB, y), mxB = __hmax2(mxB, y), nB = __hmin2_nan(nB, y);
     }
+    const float nn = __low2float(nA) + __high2float(nA) + __low2float(nB) + __high2float(nB);
+    part_nan[warp][lane] = nn != nn ? 1u : 0u;
     part[warp][4 * lane] = make_float2(__low2float(mnA), __low2float(mxA));
     part[warp][4 * lane + 1] = make_float2(__high2float(mnA), __high2float(mxA));
     part[warp][4 * lane + 2] = make_float2(__low2float(mnB), __low2float(mxB));
@@ -244,12 +283,14 @@ __global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_cons
   if (nvalid > 0) {
     const int d = threadIdx.x;
     float2 e = part[0][d];
+    bool has_nan = part_nan[0][d / 4] != 0u;
     for (int w = 1; w < 4 && w * TW < nvalid; ++w) {
       const float2 f = part[w][d];
       e.x = fminf(e.x, f.x);
       e.y = fmaxf(e.y, f.y);
+      has_nan = has_nan || part_nan[w][d / 4] != 0u;
     }
-    const GroupQ g = group_params<BITS>(e.x, e.y);
+    const GroupQ g = group_params<BITS>(e.x, e.y, has_nan);
     gq[d] = g;
     const size_t si = ad.block * kHeadDim + d;
     a.scale[si] = g.sh;
@@ -257,32 +298,53 @@ __global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_cons
   }
   __syncthreads();
   GroupQ g4[4];
+  bool fast4 = true;
   if (nvalid > 0) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) g4[u] = gq[4 * lane + u];
+    for (int u = 0; u < 4; ++u) {
+      g4[u] = gq[4 * lane + u];
+      fast4 = fast4 && g4[u].fast;
+    }
   }
-  for (int t = tw0; t < tw0 + TW; ++t) {
+  uint8_t* crow = a.codes + (ad.row + tw0) * RB + (BITS / 2) * lane;  // this lane's code byte(s), token tw0
+  const uint8_t* xrow = tile + tw0 * 256 + 8 * lane;
+  uint32_t bad = 0u;  // tokens whose codes are recomputed by the division
+#pragma unroll 4
+  for (int k = 0; k < TW; ++k, crow += RB, xrow += 256) {
     uint32_t word = 0u;  // codes of channels 4 lane .. 4 lane + 3 at bits BITS u
-    if (t < nvalid) {
-      const uint2 v = *reinterpret_cast<const uint2*>(tile + t * 256 + 8 * lane);
+    if (tw0 + k < nvalid) {
+      const uint2 v = *reinterpret_cast<const uint2*>(xrow);
       const float x[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+      if (fast4) {
+        uint32_t c[4], diff = 0u;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const GroupQ& g = g4[u];
-        uint32_t q = 0u;
-        if (g.sf != 0.f) {
-          bool ok = g.fast;
-          const uint32_t c = bracket_code(x[u], g, ok);
-          q = ok ? (c & (uint32_t)qmax) : (uint32_t)quantize_one(x[u], g.zf, g.sf, g.inv, qmax);
-        }
-        word |= q << (BITS * u);
+        for (int u = 0; u < 4; ++u) c[u] = bracket_code(x[u], g4[u], diff);
+        word = ((((c[3] << BITS) + c[2]) << (2 * BITS)) + (c[1] << BITS) + c[0]) & ((1u << (4 * BITS)) - 1u);
+        bad |= (diff != 0u ? 1u : 0u) << k;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          word |= (uint32_t)quantize_one(x[u], g4[u].zf, g4[u].sf, g4[u].inv, qmax) << (BITS * u);
       }
     }
-    uint8_t* crow = a.codes + (ad.row + t) * RB;
     if (BITS == 2)
-      crow[lane] = (uint8_t)word;
+      *crow = (uint8_t)word;
     else
-      reinterpret_cast<uint16_t*>(crow)[lane] = (uint16_t)word;
+      *reinterpret_cast<uint16_t*>(crow) = (uint16_t)word;
+  }
+  while (bad) {  // rare: tokens with a value on a rounding boundary, after the plain stores
+    const int k = __ffs(bad) - 1;
+    bad &= bad - 1u;
+    const uint2 v = *reinterpret_cast<const uint2*>(tile + (tw0 + k) * 256 + 8 * lane);
+    const float x[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+    uint32_t word = 0u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) word |= exact_code(x[u], g4[u]) << (BITS * u);
+    uint8_t* cr = a.codes + (ad.row + tw0 + k) * RB + (BITS / 2) * lane;
+    if (BITS == 2)
+      *cr = (uint8_t)word;
+    else
+      *reinterpret_cast<uint16_t*>(cr) = (uint16_t)word;
   }
 }
 
