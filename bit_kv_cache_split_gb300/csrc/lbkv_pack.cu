@@ -93,20 +93,44 @@ __device__ __forceinline__ uint32_t pack_word(const uint32_t* c) {
   return __byte_perm(u[0], u[1], 0x5410);  // low 16 bits of each
 }
 
-// Codes of the token-wise group held in w (G bf16 values, pairs (2i, 2i+1) in w[i]) into
-// out[G * BITS / 32] words, the group's scale and offset into sh, zh. Returns the mask of
-// the words that hold a value whose bounds differ (to be recomputed by fix_word).
-template <int BITS, int G>
-__device__ __forceinline__ uint32_t quantize_group_words(const uint32_t (&w)[G / 2], uint32_t (&out)[G * BITS / 32],
-                                                         __half& sh, __half& zh, GroupQ& g) {
-  constexpr int qmax = (1 << BITS) - 1, PER = 32 / BITS;
-  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mx2 = mn2, nan2 = mn2;
+template <int GW>
+__device__ __forceinline__ void store_words(uint32_t* dst, const uint32_t (&out)[GW]) {
+  if constexpr (GW % 4 == 0) {
 #pragma unroll
-  for (int i = 1; i < G / 2; ++i) {
-    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-    mn2 = __hmin2(mn2, v);
-    mx2 = __hmax2(mx2, v);
-    nan2 = __hmin2_nan(nan2, v);  // NaN if any value is
+    for (int j = 0; j < GW; j += 4)
+      *reinterpret_cast<uint4*>(dst + j) = make_uint4(out[j], out[j + 1], out[j + 2], out[j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < GW; j += 2) *reinterpret_cast<uint2*>(dst + j) = make_uint2(out[j], out[j + 1]);
+  }
+}
+
+// Codes of the token-wise group of G bf16 values at x (shared memory, 16-byte aligned) into
+// the code words dst[0 .. G * BITS / 32 - 1], its scale and offset into sh, zh, its
+// quotient constants into g. Two passes over x: extremes, then codes (fewer registers
+// than holding the group, so more CTAs share an SM). Returns the mask of the words that
+// hold a value whose bounds differ (to be recomputed by fix_word).
+template <int BITS, int G>
+__device__ __forceinline__ uint32_t quantize_group_smem(const uint4* x, uint32_t* dst, __half& sh, __half& zh,
+                                                        GroupQ& g) {
+  constexpr int qmax = (1 << BITS) - 1, PER = 32 / BITS, GW = G * BITS / 32;
+  constexpr int CPW = PER / 8;  // 16-byte chunks (8 values) per code word: 2 at INT2, 1 at INT4
+  __nv_bfloat162 mn2, mx2, nan2;
+#pragma unroll
+  for (int k = 0; k < G / 8; ++k) {
+    const uint4 v = x[k];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+      if (k == 0 && i == 0) {
+        mn2 = mx2 = nan2 = b;
+      } else {
+        mn2 = __hmin2(mn2, b);
+        mx2 = __hmax2(mx2, b);
+        nan2 = __hmin2_nan(nan2, b);  // NaN if any value is
+      }
+    }
   }
   const float mn = fminf(__low2float(mn2), __high2float(mn2));
   const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
@@ -114,33 +138,35 @@ __device__ __forceinline__ uint32_t quantize_group_words(const uint32_t (&w)[G /
   g = group_params<BITS>(mn, mx, nn != nn);
   sh = g.sh;
   zh = g.zh;
-  uint32_t bad = 0u;
-  if (g.fast) {
+  uint32_t bad = 0u, out[GW];
 #pragma unroll
-    for (int j = 0; j < G * BITS / 32; ++j) {
+  for (int j = 0; j < GW; ++j) {
+    uint32_t w[PER / 2];
+#pragma unroll
+    for (int cc = 0; cc < CPW; ++cc) {
+      const uint4 v = x[j * CPW + cc];
+      w[4 * cc] = v.x, w[4 * cc + 1] = v.y, w[4 * cc + 2] = v.z, w[4 * cc + 3] = v.w;
+    }
+    if (g.fast) {
       uint32_t c[PER], diff = 0u;
 #pragma unroll
       for (int i = 0; i < PER / 2; ++i) {
-        const uint32_t v = w[j * PER / 2 + i];
-        c[2 * i] = bracket_code(bf16_lo(v), g, diff);
-        c[2 * i + 1] = bracket_code(bf16_hi(v), g, diff);
+        c[2 * i] = bracket_code(bf16_lo(w[i]), g, diff);
+        c[2 * i + 1] = bracket_code(bf16_hi(w[i]), g, diff);
       }
       out[j] = pack_word<BITS>(c);
       bad |= (diff != 0u ? 1u : 0u) << j;
-    }
-  } else {  // the correctly rounded division for every value of the group
-#pragma unroll
-    for (int j = 0; j < G * BITS / 32; ++j) {
+    } else {  // the correctly rounded division for every value of the group
       uint32_t word = 0u;
 #pragma unroll
       for (int i = 0; i < PER / 2; ++i) {
-        const uint32_t v = w[j * PER / 2 + i];
-        word |= (uint32_t)quantize_one(bf16_lo(v), g.zf, g.sf, g.inv, qmax) << (BITS * 2 * i);
-        word |= (uint32_t)quantize_one(bf16_hi(v), g.zf, g.sf, g.inv, qmax) << (BITS * (2 * i + 1));
+        word |= (uint32_t)quantize_one(bf16_lo(w[i]), g.zf, g.sf, g.inv, qmax) << (BITS * 2 * i);
+        word |= (uint32_t)quantize_one(bf16_hi(w[i]), g.zf, g.sf, g.inv, qmax) << (BITS * (2 * i + 1));
       }
       out[j] = word;
     }
   }
+  store_words<GW>(dst, out);
   return bad;
 }
 
@@ -171,24 +197,13 @@ __device__ __forceinline__ bool pack_addr(const PackArgs& a, size_t unit, int t,
   return true;
 }
 
-template <int GW>
-__device__ __forceinline__ void store_words(uint32_t* dst, const uint32_t (&out)[GW]) {
-  if constexpr (GW % 4 == 0) {
-#pragma unroll
-    for (int j = 0; j < GW; j += 4)
-      *reinterpret_cast<uint4*>(dst + j) = make_uint4(out[j], out[j + 1], out[j + 2], out[j + 3]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < GW; j += 2) *reinterpret_cast<uint2*>(dst + j) = make_uint2(out[j], out[j + 1]);
-  }
-}
-
 // Token-wise groups: a CTA takes kPackRows consecutive token rows of one cache unit
 // (T_cap is a multiple of 128), stages them in shared memory with coalesced 16-byte loads,
 // and thread (row, group) quantizes one group of G channels. The contiguous cache has the
 // codes of positions t >= L_b cleared; the paged cache stores positions t < L_b only.
 template <int BITS, int G>
-__global__ void __launch_bounds__(kPackRows * (kHeadDim / G)) pack_tokenwise_kernel(const __grid_constant__ PackArgs a) {
+__global__ void __launch_bounds__(kPackRows * (kHeadDim / G), 13 * kPackRows / (kPackRows * (kHeadDim / G)))
+    pack_tokenwise_kernel(const __grid_constant__ PackArgs a) {
   constexpr int TPR = kHeadDim / G, NT = kPackRows * TPR;
   constexpr int RB = kHeadDim * BITS / 8, GW = G * BITS / 32;  // code bytes per row, code words per group
   __shared__ __align__(16) uint8_t tile[kPackRows * kPackStride];
@@ -208,22 +223,14 @@ __global__ void __launch_bounds__(kPackRows * (kHeadDim / G)) pack_tokenwise_ker
   KvAddr ad;
   if (!pack_addr(a, unit, t0 + r, &ad)) return;
   uint32_t* dst = reinterpret_cast<uint32_t*>(a.codes + ad.row * RB) + gi * GW;
-  uint32_t out[GW];
   if (valid) {
-    uint32_t w[G / 2];
     const uint4* row = reinterpret_cast<const uint4*>(tile + r * kPackStride + gi * G * 2);
-#pragma unroll
-    for (int k = 0; k < G / 8; ++k) {
-      const uint4 v = row[k];
-      w[4 * k] = v.x, w[4 * k + 1] = v.y, w[4 * k + 2] = v.z, w[4 * k + 3] = v.w;
-    }
     __half sh, zh;
     GroupQ g;
-    uint32_t bad = quantize_group_words<BITS, G>(w, out, sh, zh, g);
+    uint32_t bad = quantize_group_smem<BITS, G>(row, dst, sh, zh, g);
     const size_t si = ad.row * (kHeadDim / G) + gi;
     a.scale[si] = sh;
     a.off[si] = zh;
-    store_words<GW>(dst, out);
     const __nv_bfloat16* xg = reinterpret_cast<const __nv_bfloat16*>(tile + r * kPackStride + gi * G * 2);
     while (bad) {  // rare: words with a value on a rounding boundary, after the plain stores
       const int j = __ffs(bad) - 1;
@@ -231,24 +238,64 @@ __global__ void __launch_bounds__(kPackRows * (kHeadDim / G)) pack_tokenwise_ker
       dst[j] = fix_word<BITS>(xg, j, g);
     }
   } else {
+    uint32_t out[GW];
 #pragma unroll
     for (int j = 0; j < GW; ++j) out[j] = 0u;
     store_words<GW>(dst, out);
   }
 }
 
-// Channel-wise groups: one CTA of 128 threads per (unit, token group tau). The group's
-// valid rows are staged in shared memory; warp w takes its tokens w G/4 .. (w+1) G/4 - 1,
-// lane p the channels 4p .. 4p+3 (one INT2 code byte, two INT4 code bytes, per token).
-// Pass 1: per-warp extremes per channel; thread d combines them for channel d and forms
-// the group's scale, offset and quotient constants. Pass 2: the codes. The paged cache
-// stores the groups that hold a position t < L_b only.
+// Channel-wise groups: one CTA of kCwWarps warps per (unit, token group tau). Warp w takes
+// the group's tokens w G/kCwWarps .. (w+1) G/kCwWarps - 1, lane p the channels 4p .. 4p+3
+// (one INT2 code byte, two INT4 code bytes, per token); a warp reads each token row whole
+// (256 bytes). A thread loads all its values at once and holds them in registers for both
+// passes (no shared-memory tile). Pass 1: per-warp extremes per channel; thread d < 128
+// combines them for channel d and forms the group's scale, offset and quotient constants.
+// Pass 2: the codes. Full groups (the common case) take a path without per-token tests.
+// The paged cache stores the groups that hold a position t < L_b only.
+constexpr int kCwWarps = 8;
+
+template <int BITS, int TW, bool FULL>
+__device__ __forceinline__ void cw_codes(const uint2 (&xv)[TW], int nv, const float (&zf)[4], const float (&lo)[4],
+                                         const float (&hi)[4], bool fast4, const GroupQ* gq, int lane, uint8_t* crow,
+                                         uint32_t& bad) {
+  constexpr int qmax = (1 << BITS) - 1, RB = kHeadDim * BITS / 8;
+#pragma unroll
+  for (int k = 0; k < TW; ++k) {
+    uint32_t word = 0u;  // codes of channels 4 lane .. 4 lane + 3 at bits BITS u
+    if (FULL || k < nv) {
+      const float x[4] = {bf16_lo(xv[k].x), bf16_hi(xv[k].x), bf16_lo(xv[k].y), bf16_hi(xv[k].y)};
+      if (fast4) {
+        uint32_t c[4], diff = 0u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float d = __fsub_rn(x[u], zf[u]);
+          c[u] = __float_as_uint(__fmaf_rn(d, lo[u], kRintMagic));
+          diff |= c[u] ^ __float_as_uint(__fmaf_rn(d, hi[u], kRintMagic));
+        }
+        word = ((((c[3] << BITS) + c[2]) << (2 * BITS)) + (c[1] << BITS) + c[0]) & ((1u << (4 * BITS)) - 1u);
+        bad |= (diff != 0u ? 1u : 0u) << k;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const GroupQ& g = gq[4 * lane + u];
+          word |= (uint32_t)quantize_one(x[u], g.zf, g.sf, g.inv, qmax) << (BITS * u);
+        }
+      }
+    }
+    uint8_t* cr = crow + k * RB;
+    if (BITS == 2)
+      *cr = (uint8_t)word;
+    else
+      *reinterpret_cast<uint16_t*>(cr) = (uint16_t)word;
+  }
+}
+
 template <int BITS, int G>
-__global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_constant__ PackArgs a) {
-  constexpr int qmax = (1 << BITS) - 1, RB = kHeadDim * BITS / 8, TW = G / 4;  // tokens per warp
-  __shared__ __align__(16) uint8_t tile[G * 256];
-  __shared__ float2 part[4][kHeadDim];
-  __shared__ uint32_t part_nan[4][kHeadDim / 4];  // per warp and lane: a NaN among its values
+__global__ void __launch_bounds__(32 * kCwWarps) pack_channelwise_kernel(const __grid_constant__ PackArgs a) {
+  constexpr int RB = kHeadDim * BITS / 8, TW = G / kCwWarps;  // tokens per warp
+  __shared__ float2 part[kCwWarps][kHeadDim];
+  __shared__ uint32_t part_nan[kCwWarps][kHeadDim / 4];  // per warp and lane: a NaN among its values
   __shared__ GroupQ gq[kHeadDim];
   const int unit = blockIdx.x, tau = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -258,17 +305,27 @@ __global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_cons
   if (nvalid == 0 && a.pg.page_table) return;
   KvAddr ad;
   if (!pack_addr(a, (size_t)unit, t0, &ad)) return;
-  const uint4* src = reinterpret_cast<const uint4*>(a.x + ((size_t)unit * a.T_cap + t0) * kHeadDim);
-  for (int i = threadIdx.x; i < nvalid * 16; i += 128) reinterpret_cast<uint4*>(tile)[i] = __ldcs(src + i);
-  __syncthreads();
-  const int tw0 = warp * TW, tw1 = min(tw0 + TW, nvalid);  // this warp's valid tokens
-  if (tw0 < tw1) {
-    uint2 v = *reinterpret_cast<const uint2*>(tile + tw0 * 256 + 8 * lane);
-    __nv_bfloat162 mnA = *reinterpret_cast<__nv_bfloat162*>(&v.x), mxA = mnA, nA = mnA;
-    __nv_bfloat162 mnB = *reinterpret_cast<__nv_bfloat162*>(&v.y), mxB = mnB, nB = mnB;
-    for (int t = tw0 + 1; t < tw1; ++t) {
-      v = *reinterpret_cast<const uint2*>(tile + t * 256 + 8 * lane);
-      const __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&v.x), y = *reinterpret_cast<__nv_bfloat162*>(&v.y);
+  // this lane's 4 channels of the warp's first token (rows of 32 uint2)
+  const int tw0 = warp * TW;
+  const uint2* src = reinterpret_cast<const uint2*>(a.x + ((size_t)unit * a.T_cap + t0 + tw0) * kHeadDim) + lane;
+  const int nv = min(max(nvalid - tw0, 0), TW);  // this warp's valid tokens
+  const bool full = nvalid == G;
+  uint2 xv[TW];
+  if (full) {
+#pragma unroll
+    for (int k = 0; k < TW; ++k) xv[k] = __ldcs(src + k * 32);
+  } else {
+#pragma unroll
+    for (int k = 0; k < TW; ++k) xv[k] = (k < nv) ? __ldcs(src + k * 32) : make_uint2(0u, 0u);
+  }
+  if (nv > 0) {
+    __nv_bfloat162 mnA = *reinterpret_cast<__nv_bfloat162*>(&xv[0].x), mxA = mnA, nA = mnA;
+    __nv_bfloat162 mnB = *reinterpret_cast<__nv_bfloat162*>(&xv[0].y), mxB = mnB, nB = mnB;
+#pragma unroll
+    for (int k = 1; k < TW; ++k) {
+      if (!full && k >= nv) break;
+      const __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&xv[k].x);
+      const __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&xv[k].y);
       mnA = __hmin2(mnA, x), mxA = __hmax2(mxA, x), nA = __hmin2_nan(nA, x);
       mnB = __hmin2(mnB, y), mxB = __hmax2(mxB, y), nB = __hmin2_nan(nB, y);
     }
@@ -280,11 +337,11 @@ __global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_cons
     part[warp][4 * lane + 3] = make_float2(__high2float(mnB), __high2float(mxB));
   }
   __syncthreads();
-  if (nvalid > 0) {
+  if (nvalid > 0 && threadIdx.x < kHeadDim) {
     const int d = threadIdx.x;
     float2 e = part[0][d];
     bool has_nan = part_nan[0][d / 4] != 0u;
-    for (int w = 1; w < 4 && w * TW < nvalid; ++w) {
+    for (int w = 1; w < kCwWarps && w * TW < nvalid; ++w) {
       const float2 f = part[w][d];
       e.x = fminf(e.x, f.x);
       e.y = fmaxf(e.y, f.y);
@@ -297,50 +354,31 @@ __global__ void __launch_bounds__(128) pack_channelwise_kernel(const __grid_cons
     a.off[si] = g.zh;
   }
   __syncthreads();
-  GroupQ g4[4];
+  float zf[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
   bool fast4 = true;
   if (nvalid > 0) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      g4[u] = gq[4 * lane + u];
-      fast4 = fast4 && g4[u].fast;
+      const GroupQ& g = gq[4 * lane + u];
+      zf[u] = g.zf, lo[u] = g.inv_lo, hi[u] = g.inv_hi;
+      fast4 = fast4 && g.fast;
     }
   }
   uint8_t* crow = a.codes + (ad.row + tw0) * RB + (BITS / 2) * lane;  // this lane's code byte(s), token tw0
-  const uint8_t* xrow = tile + tw0 * 256 + 8 * lane;
   uint32_t bad = 0u;  // tokens whose codes are recomputed by the division
-#pragma unroll 4
-  for (int k = 0; k < TW; ++k, crow += RB, xrow += 256) {
-    uint32_t word = 0u;  // codes of channels 4 lane .. 4 lane + 3 at bits BITS u
-    if (tw0 + k < nvalid) {
-      const uint2 v = *reinterpret_cast<const uint2*>(xrow);
-      const float x[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
-      if (fast4) {
-        uint32_t c[4], diff = 0u;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) c[u] = bracket_code(x[u], g4[u], diff);
-        word = ((((c[3] << BITS) + c[2]) << (2 * BITS)) + (c[1] << BITS) + c[0]) & ((1u << (4 * BITS)) - 1u);
-        bad |= (diff != 0u ? 1u : 0u) << k;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          word |= (uint32_t)quantize_one(x[u], g4[u].zf, g4[u].sf, g4[u].inv, qmax) << (BITS * u);
-      }
-    }
-    if (BITS == 2)
-      *crow = (uint8_t)word;
-    else
-      *reinterpret_cast<uint16_t*>(crow) = (uint16_t)word;
-  }
+  if (full)
+    cw_codes<BITS, TW, true>(xv, nv, zf, lo, hi, fast4, gq, lane, crow, bad);
+  else
+    cw_codes<BITS, TW, false>(xv, nv, zf, lo, hi, fast4, gq, lane, crow, bad);
   while (bad) {  // rare: tokens with a value on a rounding boundary, after the plain stores
     const int k = __ffs(bad) - 1;
     bad &= bad - 1u;
-    const uint2 v = *reinterpret_cast<const uint2*>(tile + (tw0 + k) * 256 + 8 * lane);
+    const uint2 v = src[k * 32];
     const float x[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
     uint32_t word = 0u;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) word |= exact_code(x[u], g4[u]) << (BITS * u);
-    uint8_t* cr = a.codes + (ad.row + tw0 + k) * RB + (BITS / 2) * lane;
+    for (int u = 0; u < 4; ++u) word |= exact_code(x[u], gq[4 * lane + u]) << (BITS * u);
+    uint8_t* cr = crow + k * RB;
     if (BITS == 2)
       *cr = (uint8_t)word;
     else
@@ -362,11 +400,11 @@ void launch_pack_bits(const PackArgs& a, cudaStream_t stream) {
   } else {
     dim3 grid((unsigned)(a.B * a.Hkv), (unsigned)(a.T_cap / a.group));
     if (a.group == 128)
-      pack_channelwise_kernel<BITS, 128><<<grid, 128, 0, stream>>>(a);
+      pack_channelwise_kernel<BITS, 128><<<grid, 32 * kCwWarps, 0, stream>>>(a);
     else if (a.group == 64)
-      pack_channelwise_kernel<BITS, 64><<<grid, 128, 0, stream>>>(a);
+      pack_channelwise_kernel<BITS, 64><<<grid, 32 * kCwWarps, 0, stream>>>(a);
     else
-      pack_channelwise_kernel<BITS, 32><<<grid, 128, 0, stream>>>(a);
+      pack_channelwise_kernel<BITS, 32><<<grid, 32 * kCwWarps, 0, stream>>>(a);
   }
 }
 
