@@ -1037,6 +1037,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   }
   const long long X0 = ss.x[0], X1 = ss.x[1];
   const int NL = (int)(X1 - X0);  // items of this CTA
+  // The first pair's query rows, loaded now so that their latency passes while the ring's
+  // first copies are issued (staged into shared memory by the first segment's prologue).
+  constexpr int kQPre = (kMaxHq * kHeadDim + C::THREADS - 1) / C::THREADS;
+  float qpre[kQPre];
+  if (NL > 0) {
+    const size_t q0 = ((size_t)ss.b0 * p.Hq + (size_t)ss.kv0 * hq) * D;
+#pragma unroll
+    for (int j = 0; j < kQPre; ++j) {
+      const int idx = threadIdx.x + j * C::THREADS;
+      qpre[j] = idx < hq * D ? __bfloat162float(p.q[q0 + idx]) : 0.f;
+    }
+  }
 
   // Each ring entry has a K half (codes, scales, offsets) and a V half, each with its own
   // mbarrier, so that the next item's K half loads while this item's PV phase runs and
@@ -1199,8 +1211,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
 
     // Stage Q (fp32) and the per-query constants of pair u.
     __syncthreads();  // the previous segment's merge is done with sQ and the merge area
-    for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS)
-      sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
+    if (x == X0) {  // the first segment: its rows were loaded before the ring started
+#pragma unroll
+      for (int j = 0; j < kQPre; ++j) {
+        const int idx = threadIdx.x + j * C::THREADS;
+        if (idx < hq * D) sQ[idx] = qpre[j];
+      }
+    } else {
+      for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS)
+        sQ[idx] = __bfloat162float(p.q[((size_t)b * p.Hq + kvh * hq) * D + idx]);
+    }
     __syncthreads();
     if (p.rotation & 1) {  // keys stored rotated: the scores take H q
       for (int i = warp; i < hq; i += W) {
@@ -1534,29 +1554,39 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         // window's partial comes last
         const int n_span = c_last - c_first + 1;
         const int n_used = n_span + p.has_win;
-        auto row_of = [&](int k, int i) -> long long {  // partial row, or -1 for a CTA without items
-          if (k == n_span) return (long long)u * hq + i;  // window
-          const int cc = c_first + k;
-          if (!holds(cc)) return -1;
-          return ((long long)cc * 2 + slot_of(cc)) * hq + i;
-        };
+        // in the merge area (free again): per contributor and query the scale 2^(m_s - M),
+        // then per contributor the partial row of query 0 (-1 without items); per query the
+        // merged denominator
+        float* s_sc = ma.o;                                  // [n_used][hq]
+        int* s_row = reinterpret_cast<int*>(s_sc + n_used * hq);  // [n_used]
+        float* s_l = ma.l;                                   // [hq]
+        for (int k = threadIdx.x; k < n_used; k += C::THREADS) {
+          int r = u * hq;  // window
+          if (k < n_span) {
+            const int cc = c_first + k;
+            r = holds(cc) ? (cc * 2 + slot_of(cc)) * hq : -1;
+          }
+          s_row[k] = r;
+        }
+        __syncthreads();
         auto ml_of = [&](int k, int i) -> float2 {
-          const long long r = row_of(k, i);
+          const int r = s_row[k];
           if (r < 0) return make_float2(-INFINITY, 0.f);
-          return __ldcg(k == n_span ? &p.win_ml[r] : &p.part_ml[r]);
+          return __ldcg(k == n_span ? &p.win_ml[r + i] : &p.part_ml[r + i]);
         };
-        // warp i: the maximum over the partials of query i, each partial's scale 2^(m_s - M)
-        // (into the merge area, free again) and the merged denominator
-        float* s_sc = ma.o;  // [n_used][hq]
-        float* s_l = ma.l;   // [hq]
+        // warp i: the maximum over the partials of query i, each partial's scale and the
+        // merged denominator (the partials' (m, l) of lane k held between the two steps)
         for (int i = warp; i < hq; i += W) {
           float M = -INFINITY;
-          for (int k = lane; k < n_used; k += 32) M = fmaxf(M, ml_of(k, i).x);
+          float2 ml0 = make_float2(-INFINITY, 0.f);
+          if (lane < n_used) ml0 = ml_of(lane, i);
+          M = ml0.x;
+          for (int k = lane + 32; k < n_used; k += 32) M = fmaxf(M, ml_of(k, i).x);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULLMASK, M, o));
           float lt = 0.f;
           for (int k = lane; k < n_used; k += 32) {
-            const float2 ml = ml_of(k, i);
+            const float2 ml = (k == lane) ? ml0 : ml_of(k, i);
             const float sc = (M == -INFINITY || ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
             s_sc[k * hq + i] = sc;
             lt = fmaf(sc, ml.y, lt);
@@ -1566,15 +1596,27 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
           if (lane == 0) s_l[i] = lt;
         }
         __syncthreads();
+        // the weighted sums: a thread's loads of up to 16 partials are issued together
         for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS) {
           const int i = idx / D, ch = idx % D;
           float acc = 0.f;
-#pragma unroll 4
-          for (int k = 0; k < n_used; ++k) {
-            const float sc = s_sc[k * hq + i];
-            if (sc == 0.f) continue;
-            const long long r = row_of(k, i);
-            acc = fmaf(sc, __ldcg(k == n_span ? &p.win_o[r * D + ch] : &p.part_o[r * D + ch]), acc);
+          for (int k0 = 0; k0 < n_used; k0 += 16) {
+            float sc[16], v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int k = k0 + j;
+              sc[j] = 0.f;
+              v[j] = 0.f;
+              if (k < n_used) {
+                sc[j] = s_sc[k * hq + i];
+                if (sc[j] != 0.f) {
+                  const size_t r = (size_t)(s_row[k] + i) * D + ch;
+                  v[j] = __ldcg(k == n_span ? &p.win_o[r] : &p.part_o[r]);
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc = fmaf(sc[j], v[j], acc);
           }
           const float l = s_l[i];
           const float o = l > 0.f ? acc / l : 0.f;
