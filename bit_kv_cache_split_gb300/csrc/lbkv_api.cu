@@ -318,7 +318,19 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   if (ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem_bytes) != LBKV_OK) return LBKV_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pl.win && launch_window_partial(p, s) != 0) return LBKV_ECUDA;
-  kern<<<(unsigned)pl.n_cta, (unsigned)pl.threads, pl.smem_bytes, s>>>(p);
+  // With a window the decode kernel is a programmatic dependent of the window kernel: it
+  // starts while the window is scored and waits for it only where it reads its partials.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pl.n_cta);
+  cfg.blockDim = dim3((unsigned)pl.threads);
+  cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pl.win ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return LBKV_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;
   return LBKV_OK;
 }

@@ -1497,6 +1497,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       for (int cc = c_first; cc <= c_last; ++cc) n_contrib += holds(cc);
     }
     const bool alone = (n_contrib == 1);
+    // the window kernel launched before this grid (programmatic dependent launch) wrote the
+    // window partials read below
+    if (p.has_win) grid_dependency_wait();
     for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS) {
       const int i = idx / D, ch = idx % D;
       float M = -INFINITY;
@@ -1647,6 +1650,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
 
   // ---------------------------------------------------- pairs without cached tokens
   // Their output is the window's attention alone, or zero.
+  if (p.has_win) grid_dependency_wait();
   for (int bq = cta; bq < p.B; bq += p.n_cta) {
     if (seq_len(bq) != 0) continue;
     if (p.rotation & 2) {  // values stored rotated: each output row is rotated back

@@ -223,6 +223,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
+// Programmatic dependent launch: a grid lets its dependent grid start launching
+// (launch_dependents), and a dependent grid's thread waits until its prerequisite grid has
+// completed with its memory visible (wait; it returns at once when the grid was launched
+// without a prerequisite).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 2^e for integer e in [-126, 127], exactly.
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 

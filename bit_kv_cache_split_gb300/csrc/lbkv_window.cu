@@ -24,6 +24,9 @@ __global__ void __launch_bounds__(kWinThreads, 1) window_partial_kernel(const __
   __shared__ float sS[kMaxHq * kWinMax];  // scores (log2 units), then weights
   __shared__ float sM[kMaxHq], sL[kMaxHq];
 
+  // the decode kernel may start launching now: it waits for this grid only where it reads
+  // the window partials
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int hq = p.hq;
