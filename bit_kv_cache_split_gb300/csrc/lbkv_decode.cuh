@@ -301,69 +301,84 @@ struct LaneCols {
   int e_live;  // GV >= 2: accumulator column (0/1) of an owned pair whose V group is u_lane, or -1
 };
 
-// Channel-wise K: Q' = Q * s_tau / factor scaled by 2^e2 into fp16 for the token group
-// tau whose s/z rows are s_tau/z_tau; the offset becomes sum_d Q_d z_tau,d (one constant
-// per query and group, added before the softmax).
+// Channel-wise K: Q' = Q * s_tau / factor scaled into fp16 for the token group tau whose
+// s/z rows are s_tau/z_tau; the offset becomes sum_d Q_d z_tau,d (one constant per query
+// and group, added before the softmax).
+// The pair prologue has formed, per query and lane, W = Q / factor * 2^ea (fp16, in the
+// order of this lane's B fragment; max |W| in [2^7, 2^8)), in sW. Per group this lane pairs
+// its 32 scales in the same order (one byte permute per word), scales them by 2^es so that
+// the largest of the group's 128 is in [2^6, 2^7), and multiplies: Q' = W * s 2^es in fp16,
+// one rounding of the exact product, at most 2^15. Scores come out in units of
+// 2^-(ea + es) (times the 2^-24 of the code images).
 template <class C>
 __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)[C::NQ], float (&cwB)[C::NQ],
-                                              const __half* s_tau, const __half* z_tau, const float* sQ, float sl2,
-                                              const LaneCols& lc) {
+                                              const __half* s_tau, const __half* z_tau, const float* sQ,
+                                              const uint32_t* sW, float sl2, const LaneCols& lc) {
   constexpr int D = kHeadDim;
   constexpr unsigned FULLMASK = 0xffffffffu;
   const int c = lc.c;
   const int qb = qk_query<C>(lc.g, lc.hq);  // this lane's B column is column g
   const bool live = qb >= 0;
   static_assert(qk_wide<C>(), "channel-wise K uses the wide K mapping");
-  // With the wide mapping this lane's channels are 32c .. 32c+31: channel 32c + k is fed at
-  // k-step ks, k-slot 2c + 8r + e (k = 16x + 8e + p at INT2, 8x + 4e + p at INT4, with
-  // p = 2(ks mod (4 or 2)) + r and x the word). Read them four at a time.
-  float x[8][2][2];
-  float amax = 0.f, zsum = 0.f;
-  const float* qrow = sQ + (live ? qb : 0) * D + 32 * c;
-  const uint2* srow = reinterpret_cast<const uint2*>(s_tau + 32 * c);
-  const uint2* zrow = reinterpret_cast<const uint2*>(z_tau + 32 * c);
+  const int* sEq = reinterpret_cast<const int*>(sQ + kMaxHq * D + kMaxHq);
+  // the maximum of the group's 128 scales (>= 0): this lane's 32, then the row's 4 lanes
+  const uint32_t* s32 = reinterpret_cast<const uint32_t*>(s_tau + 32 * c);  // two scales per word
+  __half2 m2;
 #pragma unroll
-  for (int k4 = 0; k4 < 8; ++k4) {
-    const float4 q4 = reinterpret_cast<const float4*>(qrow)[k4];
-    const uint2 s4 = srow[k4], z4 = zrow[k4];
-    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-    const float2 s01 = half2_to_float2(s4.x), s23 = half2_to_float2(s4.y);
-    const float2 z01 = half2_to_float2(z4.x), z23 = half2_to_float2(z4.y);
-    const float sv[4] = {s01.x, s01.y, s23.x, s23.y}, zv[4] = {z01.x, z01.y, z23.x, z23.y};
+  for (int k = 0; k < 4; ++k) {
+    const uint4 v = reinterpret_cast<const uint4*>(s32)[k];
+    const __half2 a2 = __hmax2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y));
+    const __half2 b2 = __hmax2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w));
+    m2 = k == 0 ? __hmax2(a2, b2) : __hmax2(m2, __hmax2(a2, b2));
+  }
+  float smax = fmaxf(__low2float(m2), __high2float(m2));
+  smax = fmaxf(smax, __shfl_xor_sync(FULLMASK, smax, 1));
+  smax = fmaxf(smax, __shfl_xor_sync(FULLMASK, smax, 2));
+  const int es = smax > 0.f ? min(15, max(-14, 6 - ilog2f(smax))) : 15;
+  const uint32_t sc_bits = (uint32_t)(es + 15) << 10;
+  const uint32_t sc2w = sc_bits | (sc_bits << 16);
+  const __half2 sc2 = *reinterpret_cast<const __half2*>(&sc2w);
+  // the B fragment: per scale word pair (wa, wb) the two words of k-step ks (r = 0, 1); the
+  // pair's channels are k0 and k0 + 8 (INT2) or k0 + 4 (INT4) of this lane's 32
+  // (a column without a query reads the zero row kMaxHq - 1, which no query has then)
+  const uint2* wrow = reinterpret_cast<const uint2*>(sW + ((live ? qb : kMaxHq - 1) * 4 + c) * 16);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int k = 4 * k4 + i;
-      int ks, r, e;
-      if (C::BITS == 2) {
-        const int p = k & 7;
-        ks = 4 * (k >> 4) + (p >> 1), r = p & 1, e = (k >> 3) & 1;
-      } else {
-        const int p = k & 3;
-        ks = 2 * (k >> 3) + (p >> 1), r = p & 1, e = (k >> 2) & 1;
-      }
-      const float q = live ? qv[i] : 0.f;
-      const float v = q * sv[i] * k_rmult<C>(k);  // 32c + k has the factor of k
-      x[ks][r][e] = v;
-      amax = fmaxf(amax, fabsf(v));
-      zsum = fmaf(q, zv[i], zsum);
+  for (int ks = 0; ks < 8; ++ks) {
+    const int wa = (C::BITS == 2) ? 8 * (ks >> 2) + (ks & 3) : 4 * (ks >> 1) + (ks & 1);
+    const int wb = wa + (C::BITS == 2 ? 4 : 2);
+    const uint32_t sa = s32[wa], sb = s32[wb];
+    const uint2 w2 = wrow[ks];  // words 2 ks (r = 0) and 2 ks + 1 (r = 1)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t sp = prmt(sa, sb, r ? 0x7632 : 0x5410);
+      const __half2 s2 = __hmul2(*reinterpret_cast<const __half2*>(&sp), sc2);
+      const uint32_t wv = r ? w2.y : w2.x;
+      const __half2 q2 = __hmul2(*reinterpret_cast<const __half2*>(&wv), s2);
+      qB[ks][r] = *reinterpret_cast<const uint32_t*>(&q2);
     }
   }
-  amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
+  // the offset: sum over the lane's 32 channels of Q z, then over the 4 lanes of the row
+  float zsum = 0.f;
+  {
+    const float* qrow = sQ + (live ? qb : 0) * D + 32 * c;
+    const uint2* zrow = reinterpret_cast<const uint2*>(z_tau + 32 * c);
+#pragma unroll 2
+    for (int k4 = 0; k4 < 8; ++k4) {
+      const float4 q4 = reinterpret_cast<const float4*>(qrow)[k4];
+      const uint2 z4 = zrow[k4];
+      const float2 z01 = half2_to_float2(z4.x), z23 = half2_to_float2(z4.y);
+      zsum = fmaf(q4.x, z01.x, fmaf(q4.y, z01.y, fmaf(q4.z, z23.x, fmaf(q4.w, z23.y, zsum))));
+    }
+  }
+  zsum = live ? zsum : 0.f;
   zsum += __shfl_xor_sync(FULLMASK, zsum, 1);
   zsum += __shfl_xor_sync(FULLMASK, zsum, 2);
-  int e2 = 0;
-  if (amax > 0.f) e2 = min(100, max(-100, 13 - ilog2f(amax)));
-  const float sc = exp2i(e2);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) qB[ks][r] = f16x2_from(x[ks][r][0] * sc, x[ks][r][1] * sc);
-  const float fa = sl2 * exp2i(-e2) * kImageUnit, fb = sl2 * zsum;
+  const float fb = sl2 * zsum;
   // accumulator column 2c + j is B column 2c + j, held by lane 4 (2c + j)
 #pragma unroll
   for (int j = 0; j < C::NQ; ++j) {
-    cwA[j] = __shfl_sync(FULLMASK, fa, 8 * c + 4 * j);
+    const int qj = qk_query<C>(2 * c + j, lc.hq);
+    cwA[j] = qj >= 0 ? sl2 * exp2i(-(sEq[qj] + es)) * kImageUnit : 0.f;
     cwB[j] = __shfl_sync(FULLMASK, fb, 8 * c + 4 * j);
   }
 }
@@ -663,7 +678,8 @@ __device__ __forceinline__ void process_unit(WarpState<C>& st, const SlotSmem& s
     if constexpr (KL == 1) {
       if (ch == 0 || (C::G <= C::UNIT && (kChunk * ch) % C::G == 0)) {
         const int tau = rel0 / C::G;
-        channelwise_q<C>(qBt, cwA, cwB, sm.ks + tau * D, sm.kz + tau * D, sQ, sl2, lc);
+        channelwise_q<C>(qBt, cwA, cwB, sm.ks + tau * D, sm.kz + tau * D, sQ,
+                         reinterpret_cast<const uint32_t*>(sqb), sl2, lc);
       }
     }
     qk_chunk<C>(x[ch], st, qBt, sqb, cwA, cwB, sm, rel0, lc);
@@ -1257,7 +1273,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         if (o < lanes_per_group) gs += other;
       }
       int e = 0;
-      if (amax > 0.f) e = min(100, max(-100, 13 - ilog2f(amax)));
+      // (channel-wise K: max |Q / factor| * 2^e in [2^7, 2^8), the W of channelwise_q)
+      if (amax > 0.f) e = min(100, max(-100, (KL == 1 ? 7 : 13) - ilog2f(amax)));
       // token-wise K scores are kept in units of sAq; the raw products carry the 2^-24 of the
       // subnormal code images, so the unit and the offset sums take the 2^24
       if (lane == 0) {
@@ -1311,6 +1328,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         for (int uu = 0; uu < GK; ++uu) st.bzq[j][uu] = qs >= 0 ? sBz[qs * 4 + uu] : 0.f;
       }
     } else {
+      // channel-wise K: W = Q / factor * 2^e (fp16) per query and lane, in the order of the
+      // lane's B fragment (word 2 ks + r: k-slots 2c + 8r, 2c + 8r + 1 of k-step ks)
+      // (rows of queries q >= hq are zero: a column without a query reads one of them)
+      uint32_t* sW = reinterpret_cast<uint32_t*>(sqb);  // [kMaxHq][4][16]
+      for (int t = threadIdx.x; t < kMaxHq * 64; t += C::THREADS) {
+        const int qi = t >> 6, cc = (t >> 4) & 3, wi = t & 15, ks = wi >> 1, r = wi & 1;
+        uint32_t w = 0u;
+        if (qi < hq) {
+          const float sc = exp2i(sEq[qi]);
+          const int ch0 = qk_channel<C>(ks, 2 * cc + 8 * r), ch1 = qk_channel<C>(ks, 2 * cc + 8 * r + 1);
+          w = f16x2_from(sQ[qi * D + ch0] * sc * k_rmult<C>(ch0), sQ[qi * D + ch1] * sc * k_rmult<C>(ch1));
+        }
+        sW[t] = w;
+      }
 #pragma unroll
       for (int j = 0; j < NQ; ++j) st.pa[j] = 1.f;
     }
