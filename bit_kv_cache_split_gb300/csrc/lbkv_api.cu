@@ -40,7 +40,7 @@ int current_device_props(int* sms, int* smem_optin) {
 std::mutex g_attr_mu;
 std::unordered_map<uint64_t, int> g_attr_smem;
 
-int ensure_smem_attr(const void* fn, int bytes) {
+int ensure_smem_attr(const void* fn, int bytes, bool big_clusters = false) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LBKV_ECUDA;
   const uint64_t key = (reinterpret_cast<uint64_t>(fn) << 6) ^ (uint64_t)dev;
@@ -48,8 +48,45 @@ int ensure_smem_attr(const void* fn, int bytes) {
   auto it = g_attr_smem.find(key);
   if (it != g_attr_smem.end() && it->second >= bytes) return LBKV_OK;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return LBKV_ECUDA;
+  // clusters of more than 8 CTAs (a non-portable size)
+  if (big_clusters && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return LBKV_ECUDA;
   g_attr_smem[key] = bytes;
   return LBKV_OK;
+}
+
+// Clusters of `cpp` CTAs of kernel fn (with its shared memory) that the device holds at
+// once, cached per (device, kernel, cluster size).
+std::unordered_map<uint64_t, int> g_max_clusters;
+
+int max_active_clusters(const void* fn, int cpp, int threads, int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const uint64_t key = ((reinterpret_cast<uint64_t>(fn) << 10) ^ ((uint64_t)cpp << 4)) ^ (uint64_t)dev;
+  {
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    auto it = g_max_clusters.find(key);
+    if (it != g_max_clusters.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cpp);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cpp;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  g_max_clusters[key] = n;
+  return n;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -91,6 +128,7 @@ struct Plan {
   size_t off_done, off_ml, off_o, off_wml, off_wo, ws_bytes;
   DecodeKernel tc_fn;  // the tensor-core kernel when it takes the call, else nullptr
   bool grp;            // the tensor-core kernel (rings per group of four warps)
+  int cluster_ctas;    // cluster mode: CTAs per pair (one thread-block cluster each), else 0
 };
 
 // LBKV_DECODE_KERNEL=tc in the environment (read at every call) makes a token-wise K side
@@ -202,6 +240,18 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
     const long long want = (max_items + units_per_cta - 1) / units_per_cta;
     pl->n_cta = (int)(want < sms ? (want > 0 ? want : 1) : sms);
   }
+  // Cluster mode: with few pairs (at most a quarter of the SMs), one thread-block cluster
+  // of up to cluster_ctas CTAs per pair (a power of two from 4 to 16, no more than about one
+  // item per warp from the capacity; the launch lowers it until all clusters fit in one
+  // wave); its CTAs merge their partials in distributed shared memory instead of through
+  // the workspace, with no length scan.
+  pl->cluster_ctas = 0;
+  if (!pl->grp && units * 4 <= sms) {
+    const long long items_pair = ((long long)d->max_seq_len + ut - 1) / ut;
+    int cpp = 16;
+    while (cpp > 4 && (units * cpp > sms || (long long)(cpp / 2) * warps >= items_pair)) cpp >>= 1;
+    pl->cluster_ctas = cpp;
+  }
 
   // workspace: status word | per-pair counters | CTA partials (m, l) | CTA partials O |
   // window partials (m, l) | window partials O
@@ -216,18 +266,20 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
 }
 
 template <bool PAGED>
-DecodeKernel pick_kernel_of(int bits, int kl, int vl, int mode, int lg) {
+DecodeKernel pick_kernel_of(int bits, int kl, int vl, int mode, int lg, bool cl) {
   if (bits == 2) {
-    if (kl == 0) return vl ? decode_kernel<2, 0, 1, PAGED>(mode, lg) : decode_kernel<2, 0, 0, PAGED>(mode, lg);
-    return vl ? decode_kernel<2, 1, 1, PAGED>(mode, lg) : decode_kernel<2, 1, 0, PAGED>(mode, lg);
+    if (kl == 0)
+      return vl ? decode_kernel<2, 0, 1, PAGED>(mode, lg, cl) : decode_kernel<2, 0, 0, PAGED>(mode, lg, cl);
+    return vl ? decode_kernel<2, 1, 1, PAGED>(mode, lg, cl) : decode_kernel<2, 1, 0, PAGED>(mode, lg, cl);
   }
-  if (kl == 0) return vl ? decode_kernel<4, 0, 1, PAGED>(mode, lg) : decode_kernel<4, 0, 0, PAGED>(mode, lg);
-  return vl ? decode_kernel<4, 1, 1, PAGED>(mode, lg) : decode_kernel<4, 1, 0, PAGED>(mode, lg);
+  if (kl == 0) return vl ? decode_kernel<4, 0, 1, PAGED>(mode, lg, cl) : decode_kernel<4, 0, 0, PAGED>(mode, lg, cl);
+  return vl ? decode_kernel<4, 1, 1, PAGED>(mode, lg, cl) : decode_kernel<4, 1, 0, PAGED>(mode, lg, cl);
 }
 
-DecodeKernel pick_kernel(int bits, int kl, int vl, int mode, int group, bool paged) {
+DecodeKernel pick_kernel(int bits, int kl, int vl, int mode, int group, bool paged, bool cluster = false) {
   const int lg = group == 128 ? 7 : group == 64 ? 6 : 5;
-  return paged ? pick_kernel_of<true>(bits, kl, vl, mode, lg) : pick_kernel_of<false>(bits, kl, vl, mode, lg);
+  return paged ? pick_kernel_of<true>(bits, kl, vl, mode, lg, cluster)
+               : pick_kernel_of<false>(bits, kl, vl, mode, lg, cluster);
 }
 
 }  // namespace
@@ -321,14 +373,49 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   // With a window the decode kernel is a programmatic dependent of the window kernel: it
   // starts while the window is scored and waits for it only where it reads its partials.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)pl.n_cta);
   cfg.blockDim = dim3((unsigned)pl.threads);
   cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+  if (pl.cluster_ctas > 0 && !pl.tc_fn) {
+    // cluster mode; a device that cannot hold the clusters takes the split-decode grid
+    DecodeKernel kc = pick_kernel(bits, k_layout, v_layout, pl.mode, group, desc->page_table != nullptr, true);
+    const long long units = (long long)desc->batch * pl.hkv;
+    // the largest cluster size (down to 4) whose clusters, one per pair, the device holds at once
+    int cpp = pl.cluster_ctas;
+    if (kc && ensure_smem_attr(reinterpret_cast<const void*>(kc), pl.smem_bytes, true) == LBKV_OK) {
+      while (cpp >= 4 && max_active_clusters(reinterpret_cast<const void*>(kc), cpp, pl.threads, pl.smem_bytes) < units)
+        cpp >>= 1;
+    }
+    // (only when the cluster grid is at least half the split-decode grid: the cheaper merge
+    // must not cost much parallelism. Measured: clusters of 16 CTAs of this size fit 7 at a
+    // time, of 8 CTAs 15, of 4 CTAs 36; batch 1 at 32K takes clusters of 8, 64 CTAs against
+    // 128, 17.9 against 18.2 us; INT4 batch 1 at 16K 14.9 against 16.5 us)
+    if (kc && cpp >= 4 && units * cpp * 2 >= pl.n_cta) {
+      const int n = (int)units * cpp;
+      DecodeParams pc = p;
+      pc.n_cta = n;
+      cfg.gridDim = dim3((unsigned)n);
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = (unsigned)cpp;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      if (pl.win) {
+        cfg.numAttrs = 2;
+      } else {
+        attr[0] = attr[1];
+        cfg.numAttrs = 1;
+      }
+      if (cudaLaunchKernelEx(&cfg, kc, pc) == cudaSuccess && cudaGetLastError() == cudaSuccess) return LBKV_OK;
+      (void)cudaGetLastError();
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
+  }
+  cfg.gridDim = dim3((unsigned)pl.n_cta);
   cfg.numAttrs = pl.win ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return LBKV_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;

@@ -911,13 +911,14 @@ struct SplitScan {
   long long x[2];                            // item index of end e
   int b0, kv0, t0;                           // sequence, pair in it and item in the pair of end 0
   long long q0;                              // pairs with tokens before the start pair
+  float cm[kMaxHq], cl[kMaxHq];              // cluster mode: the CTA partial's (m, l) per query
 };
 
 // ------------------------------------------------------------------------
 // The kernel: see the file comment. C = Cfg<BITS, KL, VL, MODE, LOG2G>; PAGED: the cache
 // is a page pool behind a page table (only the addresses of the bulk copies differ).
 // ------------------------------------------------------------------------
-template <class C, bool PAGED>
+template <class C, bool PAGED, bool CLUSTER>
 __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int BITS = C::BITS, KL = C::KL, VL = C::VL, GV = C::GV, GK = C::GK, NQ = C::NQ, NO = C::NO;
   constexpr int RB = C::RB, D = kHeadDim, UNIT = C::UNIT, W = C::WARPS;
@@ -961,7 +962,28 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   };
 
   // ---------------------------------------------------- the CTA's share of the items
-  {
+  // Cluster mode (small problems): cluster i takes pair i, its CTA of rank r the r-th of
+  // equal contiguous slices of the pair's items; no scan.
+  bool cluster_pair = false;  // cluster mode: the pair has tokens (its CTAs merge in the cluster)
+  if constexpr (CLUSTER) {
+    const int ncta = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
+    const int up = (int)cluster_id_x();
+    const int b = up / p.Hkv, kv = up % p.Hkv;
+    const int n = up < n_pairs ? items_of(seq_len(b)) : 0;
+    cluster_pair = n > 0;
+    if (threadIdx.x == 0) {
+      const long long t0 = (long long)n * crank / ncta, t1 = (long long)n * (crank + 1) / ncta;
+      ss.x[0] = t0;
+      ss.x[1] = t1;
+      ss.b0 = b;
+      ss.kv0 = kv;
+      ss.t0 = (int)t0;
+      ss.q0 = 0;
+      ss.w = 0;
+      ss.ctot = 1;
+    }
+    __syncthreads();
+  } else {
     const int chunk = (p.B + W - 1) / W;  // warp w sums sequences [w chunk, (w+1) chunk)
     const int bb0 = min(p.B, warp * chunk), bb1 = min(p.B, bb0 + chunk);
     long long si = 0, sp = 0;
@@ -1058,7 +1080,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   // first copies are issued (staged into shared memory by the first segment's prologue).
   constexpr int kQPre = (kMaxHq * kHeadDim + C::THREADS - 1) / C::THREADS;
   float qpre[kQPre];
-  if (NL > 0) {
+  if (NL > 0 || cluster_pair) {
     const size_t q0 = ((size_t)ss.b0 * p.Hq + (size_t)ss.kv0 * hq) * D;
 #pragma unroll
     for (int j = 0; j < kQPre; ++j) {
@@ -1142,7 +1164,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   Cursor start;  // the CTA's first item
   start.i = 0;
   start.r = 0;
-  if (NL > 0) {
+  if (NL > 0 || cluster_pair) {
     const int L0 = seq_len(ss.b0), n0 = items_of(L0);
     const int kv0 = ss.kv0;
     start.u = ss.b0 * p.Hkv + kv0;
@@ -1222,7 +1244,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   long long pair_first = X0 - start.t;  // the pair's first item in the item sequence
   int pair_n = start.n;
   long long q = ss.q0;  // pairs with tokens before pair u
-  while (x < X1) {
+  // (cluster mode: one segment for every CTA of a pair with tokens, also without items, so
+  // that all of them reach the cluster barriers of the merge)
+  bool cluster_once = cluster_pair;
+  while (x < X1 || cluster_once) {
+    cluster_once = false;
     const long long xe = min(X1, pair_first + pair_n);
     const int b = u / p.Hkv, kvh = u % p.Hkv;
 
@@ -1502,6 +1528,76 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
     __syncthreads();
 
     // ---------------------------------------------------- merge the warps
+    if constexpr (CLUSTER) {
+      // Cluster mode: the CTA's partial stays in its shared memory (O over ma.o's first
+      // block, (m, l) in ss.cm / ss.cl); after a cluster barrier the CTA of rank r merges
+      // query rows r, r + n, ... from every CTA of the cluster (distributed shared memory)
+      // with the window's partial, and a second barrier keeps each CTA's partial in place
+      // until all have been read.
+      for (int idx = threadIdx.x; idx < hq * D; idx += C::THREADS) {
+        const int i = idx / D, ch = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, ma.m[w * kMaxHq + i]);
+        float acc = 0.f, lt = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kMergeWarps; ++w) {
+            const float mw = ma.m[w * kMaxHq + i];
+            const float sc = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+            acc = fmaf(sc, ma.o[(w * hq + i) * D + ch], acc);
+            lt = fmaf(sc, ma.l[w * kMaxHq + i], lt);
+          }
+        }
+        ma.o[idx] = acc;  // read above by this thread only
+        if (ch == 0) {
+          ss.cm[i] = M;
+          ss.cl[i] = lt;
+        }
+      }
+      if (p.has_win) grid_dependency_wait();
+      cluster_sync();
+      {
+        const int ncta = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
+        const uint32_t o_base = smem_addr(ma.o), m_base = smem_addr(ss.cm), l_base = smem_addr(ss.cl);
+        for (int i = crank + ncta * warp; i < hq; i += ncta * W) {  // one warp per query row
+          float M = -INFINITY;
+          for (int k = 0; k < ncta; ++k) M = fmaxf(M, ld_cluster_f32(cluster_map(m_base + 4u * i, k)));
+          float2 wml = make_float2(-INFINITY, 0.f);
+          const size_t wr = (size_t)u * hq + i;
+          if (p.has_win) {
+            wml = __ldcg(&p.win_ml[wr]);
+            M = fmaxf(M, wml.x);
+          }
+          float v[4] = {0.f, 0.f, 0.f, 0.f};
+          float lt = 0.f;
+          if (M != -INFINITY) {
+            for (int k = 0; k < ncta; ++k) {
+              const float mk = ld_cluster_f32(cluster_map(m_base + 4u * i, k));
+              if (mk == -INFINITY) continue;
+              const float sc = fast_exp2(mk - M);
+              lt = fmaf(sc, ld_cluster_f32(cluster_map(l_base + 4u * i, k)), lt);
+              const float4 o4 = ld_cluster_f32x4(cluster_map(o_base + 4u * (i * D + 4 * lane), k));
+              v[0] = fmaf(sc, o4.x, v[0]);
+              v[1] = fmaf(sc, o4.y, v[1]);
+              v[2] = fmaf(sc, o4.z, v[2]);
+              v[3] = fmaf(sc, o4.w, v[3]);
+            }
+            if (p.has_win && wml.x != -INFINITY) {
+              const float sc = fast_exp2(wml.x - M);
+              lt = fmaf(sc, wml.y, lt);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) v[e] = fmaf(sc, __ldcg(&p.win_o[wr * D + 4 * lane + e]), v[e]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = lt > 0.f ? v[e] / lt : 0.f;
+          if (p.rotation & 2) hadamard128(v, lane);
+          store_row4(p.out + ((size_t)b * p.Hq + kvh * hq + i) * D, lane, v);
+        }
+      }
+      cluster_sync();
+    } else {
     // A pair held by this CTA alone is finished here (with the window's partial). Otherwise the
     // CTA writes its partial to its slot (1 when the pair is the second one it holds a
     // partial of, else 0) and the last contributor to arrive merges all partials (and the
@@ -1666,6 +1762,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         }
         if (threadIdx.x == 0) p.done[u] = 0;  // ready for the next call in stream order
       }
+    }
+
     }
 
     // next pair with tokens

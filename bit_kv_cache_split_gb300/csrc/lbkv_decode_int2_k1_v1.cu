@@ -9,9 +9,11 @@
 namespace lbkv {
 
 template <>
-DecodeKernel decode_kernel<2, 1, 1, LBKV_PAGED>(int mode, int log2g) {
+DecodeKernel decode_kernel<2, 1, 1, LBKV_PAGED>(int mode, int log2g, bool cluster) {
 #define LBKV_PICK(M, LG) \
-  if (mode == M && log2g == LG) return &split_decode_kernel<Cfg<2, 1, 1, M, LG>, LBKV_PAGED>;
+  if (mode == M && log2g == LG)                                                            \
+    return cluster ? &split_decode_kernel<Cfg<2, 1, 1, M, LG>, LBKV_PAGED, true> \
+                   : &split_decode_kernel<Cfg<2, 1, 1, M, LG>, LBKV_PAGED, false>;
   LBKV_PICK(kModeDup, 7)
   LBKV_PICK(kModePair, 7)
   LBKV_PICK(kModeDup, 6)

@@ -88,13 +88,14 @@ constexpr int kWinMax = 128;  // window capacity limit (tokens)
 int launch_window_partial(const DecodeParams& p, cudaStream_t stream);
 
 // Instantiated kernel for (column mode, log2 group) of one bit width, K/V layout
-// pair and cache kind (contiguous or paged), or nullptr when that combination is not
-// built. One translation unit per specialisation.
+// pair and cache kind (contiguous or paged), in its cluster mode (one thread-block
+// cluster per pair, merged in distributed shared memory) or not, or nullptr when that
+// combination is not built. One translation unit per specialisation.
 template <int BITS, int KL, int VL, bool PAGED>
-DecodeKernel decode_kernel(int mode, int log2g);
-#define LBKV_DECLARE_DECODE(B, K, V)                            \
-  template <> DecodeKernel decode_kernel<B, K, V, false>(int, int); \
-  template <> DecodeKernel decode_kernel<B, K, V, true>(int, int);
+DecodeKernel decode_kernel(int mode, int log2g, bool cluster);
+#define LBKV_DECLARE_DECODE(B, K, V)                                  \
+  template <> DecodeKernel decode_kernel<B, K, V, false>(int, int, bool); \
+  template <> DecodeKernel decode_kernel<B, K, V, true>(int, int, bool);
 LBKV_DECLARE_DECODE(2, 0, 0)
 LBKV_DECLARE_DECODE(2, 0, 1)
 LBKV_DECLARE_DECODE(2, 1, 0)
