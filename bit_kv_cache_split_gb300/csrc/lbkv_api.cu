@@ -240,16 +240,18 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
     const long long want = (max_items + units_per_cta - 1) / units_per_cta;
     pl->n_cta = (int)(want < sms ? (want > 0 ? want : 1) : sms);
   }
-  // Cluster mode: with few pairs (at most a quarter of the SMs), one thread-block cluster
-  // of up to cluster_ctas CTAs per pair (a power of two from 4 to 16, no more than about one
-  // item per warp from the capacity; the launch lowers it until all clusters fit in one
-  // wave); its CTAs merge their partials in distributed shared memory instead of through
-  // the workspace, with no length scan.
+  // Cluster mode: with few pairs (at most half as many as SMs), one thread-block cluster of
+  // up to cluster_ctas CTAs per pair (a power of two from 2 to 16: no more than about one item
+  // per warp from the capacity, but at least 4 where the pairs allow it, and all CTAs in one
+  // wave; the launch lowers it until the GPU holds all clusters at once and takes the mode only
+  // where it costs a warp at most one item more); its CTAs merge their partials in
+  // distributed shared memory instead of through the workspace, with no length scan.
   pl->cluster_ctas = 0;
-  if (!pl->grp && units * 4 <= sms) {
+  if (!pl->grp && units * 2 <= sms) {
     const long long items_pair = ((long long)d->max_seq_len + ut - 1) / ut;
     int cpp = 16;
-    while (cpp > 4 && (units * cpp > sms || (long long)(cpp / 2) * warps >= items_pair)) cpp >>= 1;
+    while (cpp > 4 && (long long)(cpp / 2) * warps >= items_pair) cpp >>= 1;  // short pairs
+    while (cpp > 2 && units * cpp > sms) cpp >>= 1;                           // one wave
     pl->cluster_ctas = cpp;
   }
 
@@ -384,17 +386,23 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
     // cluster mode; a device that cannot hold the clusters takes the split-decode grid
     DecodeKernel kc = pick_kernel(bits, k_layout, v_layout, pl.mode, group, desc->page_table != nullptr, true);
     const long long units = (long long)desc->batch * pl.hkv;
-    // the largest cluster size (down to 4) whose clusters, one per pair, the device holds at once
+    // the largest cluster size (down to 2) whose clusters, one per pair, the device holds at once
     int cpp = pl.cluster_ctas;
     if (kc && ensure_smem_attr(reinterpret_cast<const void*>(kc), pl.smem_bytes, true) == LBKV_OK) {
-      while (cpp >= 4 && max_active_clusters(reinterpret_cast<const void*>(kc), cpp, pl.threads, pl.smem_bytes) < units)
+      while (cpp >= 2 && max_active_clusters(reinterpret_cast<const void*>(kc), cpp, pl.threads, pl.smem_bytes) < units)
         cpp >>= 1;
     }
-    // (only when the cluster grid is at least half the split-decode grid: the cheaper merge
-    // must not cost much parallelism. Measured: clusters of 16 CTAs of this size fit 7 at a
-    // time, of 8 CTAs 15, of 4 CTAs 36; batch 1 at 32K takes clusters of 8, 64 CTAs against
-    // 128, 17.9 against 18.2 us; INT4 batch 1 at 16K 14.9 against 16.5 us)
-    if (kc && cpp >= 4 && units * cpp * 2 >= pl.n_cta) {
+    // Taken only when it gives a warp at most one item more than the split-decode grid (an
+    // item costs a warp about 4.6 us among 16, the cluster merge saves about 6 us of fixed
+    // costs). Measured (graph replay, INT2): batch 8 at 16K 32.1 -> 26.8 us and at 32K 47.9 ->
+    // 44.7 us with clusters of 2, but at 64K 77.9 -> 80.5 us and at 128K 140.4 -> 152.4 us (two
+    // and more items more per warp). Clusters of 16 CTAs of this size fit 7 at a time, of 8
+    // CTAs 15, of 4 CTAs 36.
+    const long long wpc = pl.threads / 32;  // warps per CTA
+    const long long items_pair = ((long long)desc->max_seq_len + pl.unit_tokens - 1) / pl.unit_tokens;
+    const long long ipw_split = (units * items_pair + (long long)pl.n_cta * wpc - 1) / ((long long)pl.n_cta * wpc);
+    const long long ipw_cluster = (items_pair + (long long)cpp * wpc - 1) / ((long long)cpp * wpc);
+    if (kc && cpp >= 2 && ipw_cluster <= ipw_split + 1) {
       const int n = (int)units * cpp;
       DecodeParams pc = p;
       pc.n_cta = n;
