@@ -43,7 +43,7 @@ std::unordered_map<uint64_t, int> g_attr_smem;
 int ensure_smem_attr(const void* fn, int bytes, bool big_clusters = false) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LBKV_ECUDA;
-  const uint64_t key = (reinterpret_cast<uint64_t>(fn) << 6) ^ (uint64_t)dev;
+  const uint64_t key = ((reinterpret_cast<uint64_t>(fn) << 6) ^ (uint64_t)dev) ^ (big_clusters ? 1ull << 63 : 0ull);
   std::lock_guard<std::mutex> lock(g_attr_mu);
   auto it = g_attr_smem.find(key);
   if (it != g_attr_smem.end() && it->second >= bytes) return LBKV_OK;
@@ -55,14 +55,28 @@ int ensure_smem_attr(const void* fn, int bytes, bool big_clusters = false) {
   return LBKV_OK;
 }
 
-// Clusters of `cpp` CTAs of kernel fn (with its shared memory) that the device holds at
-// once, cached per (device, kernel, cluster size).
-std::unordered_map<uint64_t, int> g_max_clusters;
+// Clusters of `cpp` CTAs of kernel fn (with its block size and shared memory) that the
+// device holds at once, cached per (device, kernel, cluster size, block size, shared memory).
+struct ClusterKey {
+  const void* fn;
+  int dev, cpp, threads, smem;
+  bool operator==(const ClusterKey& o) const {
+    return fn == o.fn && dev == o.dev && cpp == o.cpp && threads == o.threads && smem == o.smem;
+  }
+};
+struct ClusterKeyHash {
+  size_t operator()(const ClusterKey& k) const {
+    uint64_t h = reinterpret_cast<uint64_t>(k.fn);
+    for (int v : {k.dev, k.cpp, k.threads, k.smem}) h = h * 0x9E3779B97F4A7C15ull ^ (uint64_t)(uint32_t)v;
+    return (size_t)h;
+  }
+};
+std::unordered_map<ClusterKey, int, ClusterKeyHash> g_max_clusters;
 
 int max_active_clusters(const void* fn, int cpp, int threads, int smem) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  const uint64_t key = ((reinterpret_cast<uint64_t>(fn) << 10) ^ ((uint64_t)cpp << 4)) ^ (uint64_t)dev;
+  const ClusterKey key{fn, dev, cpp, threads, smem};
   {
     std::lock_guard<std::mutex> lock(g_attr_mu);
     auto it = g_max_clusters.find(key);
