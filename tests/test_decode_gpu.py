@@ -238,6 +238,16 @@ def test_int4_full_size_sampled(lbkv, batch, ctx):
     sampled_parity(lbkv, wl, [(0, 0), (batch - 1, 5)])
 
 
+@pytest.mark.parametrize("bits,batch,ctx", [(2, 1, 4096), (2, 1, 16384), (2, 1, 32768), (2, 8, 16384), (4, 1, 16384),
+                                            (4, 8, 4096)])
+def test_few_pairs_every_unit(lbkv, bits, batch, ctx):
+    """Few (sequence, KV head) pairs at full context: on a 152-SM GPU these shapes run one
+    thread-block cluster per pair (2 to 8 CTAs that merge in distributed shared memory);
+    every unit is compared with the oracle."""
+    wl = (inputs.decode_int2 if bits == 2 else inputs.decode_int4)(batch, ctx)
+    sampled_parity(lbkv, wl, [(b, h) for b in range(batch) for h in range(wl.num_kv_heads)])
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("kl,vl", [(1, 0), (0, 1)])
 def test_mixed_layouts_ragged_sampled(lbkv, bits, kl, vl):
