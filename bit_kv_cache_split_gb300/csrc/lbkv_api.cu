@@ -253,6 +253,10 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
     const int units_per_cta = pl->grp ? warps / 4 : warps;  // warps, or groups of four
     const long long want = (max_items + units_per_cta - 1) / units_per_cta;
     pl->n_cta = (int)(want < sms ? (want > 0 ? want : 1) : sms);
+    // With a window and few pairs, the window kernel's CTAs (one per pair, launched first)
+    // hold their SMs while the decode kernel starts: the grid leaves those SMs out, so that
+    // no decode CTA waits for one of them to finish.
+    if (win && units * 16 <= sms && pl->n_cta > sms - units) pl->n_cta = (int)(sms - units);
   }
   // Cluster mode: with few pairs (at most half as many as SMs), one thread-block cluster of
   // up to cluster_ctas CTAs per pair (a power of two from 2 to 16: no more than about one item
