@@ -546,16 +546,23 @@ __device__ __forceinline__ void pv_chunk(float (&accv)[8][C::NTV][4], const uint
         }
       }
     } else {
-      const uint2 wa0 = reinterpret_cast<const uint2*>(sm.vc + tA * RB)[g];
-      const uint2 wa1 = reinterpret_cast<const uint2*>(sm.vc + (tA + 1) * RB)[g];
-      const uint2 wb0 = reinterpret_cast<const uint2*>(sm.vc + (tA + 8) * RB)[g];
-      const uint2 wb1 = reinterpret_cast<const uint2*>(sm.vc + (tA + 9) * RB)[g];
+      // Lanes with odd c read the odd token row of each pair first: rows are 64 bytes (half
+      // the banks), so the four row groups of one load then fall in both bank halves (two
+      // shared-memory wavefronts per load instead of four); their byte permutes take the two
+      // rows in the other order. (INT2 rows, 32 bytes, conflict only two ways on 32-bit loads:
+      // measured, the same change there cost more than it saved.)
+      const int swp = c & 1;
+      const uint32_t selL = swp ? 0x1054u : 0x5410u, selH = swp ? 0x3276u : 0x7632u;
+      const uint2 wa0 = reinterpret_cast<const uint2*>(sm.vc + (tA + swp) * RB)[g];
+      const uint2 wa1 = reinterpret_cast<const uint2*>(sm.vc + (tA + 1 - swp) * RB)[g];
+      const uint2 wb0 = reinterpret_cast<const uint2*>(sm.vc + (tA + 8 + swp) * RB)[g];
+      const uint2 wb1 = reinterpret_cast<const uint2*>(sm.vc + (tA + 9 - swp) * RB)[g];
 #pragma unroll
       for (int uu = 0; uu < 2; ++uu) {
         const uint32_t ea0 = uu ? wa0.y : wa0.x, ea1 = uu ? wa1.y : wa1.x;
         const uint32_t eb0 = uu ? wb0.y : wb0.x, eb1 = uu ? wb1.y : wb1.x;
-        const uint32_t xal = prmt(ea0, ea1, 0x5410), xah = prmt(ea0, ea1, 0x7632);
-        const uint32_t xbl = prmt(eb0, eb1, 0x5410), xbh = prmt(eb0, eb1, 0x7632);
+        const uint32_t xal = prmt(ea0, ea1, selL), xah = prmt(ea0, ea1, selH);
+        const uint32_t xbl = prmt(eb0, eb1, selL), xbh = prmt(eb0, eb1, selH);
         const uint32_t sal = xal >> 8, sah = xah >> 8, sbl = xbl >> 8, sbh = xbh >> 8;
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
