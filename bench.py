@@ -251,11 +251,13 @@ class Case:
 
 def time_e2e(wl, steps, warmup, device):
     """Same metric through the public API from pinned host buffers: every step copies the
-    step's inputs host->device, decodes, and reads the output back."""
+    step's inputs host->device, decodes, and reads the output back. The copies of step i + 1
+    (on a copy stream, into the other of two device buffer sets) overlap the decode of step i,
+    as a serving loop would run it; the timed region still holds every step's copies."""
     import bit_kv_cache_split_gb300 as pkg
 
     host = {k: v.pin_memory() for k, v in inputs.generate(wl, "cpu").items()}
-    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    bufs = [{k: torch.empty_like(v, device=device) for k, v in host.items()} for _ in range(2)]
     out_h = torch.empty((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16).pin_memory()
     out_d = torch.empty_like(out_h, device=device)
     n = pkg.workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.t_cap, wl.bits, wl.k_layout, wl.v_layout,
@@ -263,26 +265,47 @@ def time_e2e(wl, steps, warmup, device):
     ws = pkg._binding.alloc_workspace(n, device)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_h.numel() * out_h.element_size()
+    compute = torch.cuda.current_stream()
+    copier = torch.cuda.Stream()
+    ready = [torch.cuda.Event(), torch.cuda.Event()]  # a buffer set holds its step's inputs
+    done = [torch.cuda.Event(), torch.cuda.Event()]   # the decode that read a buffer set ended
 
-    def step():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
+    def copy_in(i, start=None):
+        b = i % 2
+        with torch.cuda.stream(copier):
+            if start is not None:
+                copier.wait_event(start)
+            copier.wait_event(done[b])
+            for k in host:
+                bufs[b][k].copy_(host[k], non_blocking=True)
+            ready[b].record(copier)
+
+    def decode(i):
+        b = i % 2
+        dev = bufs[b]
+        compute.wait_event(ready[b])
         win = {}
         if "k_win" in dev:
             win = dict(k_win=dev["k_win"], v_win=dev["v_win"], win_lens=dev["win_lens"])
         pkg.decode_attn(dev["q"], dev["k_codes"], dev["k_scale"], dev["k_off"], dev["v_codes"], dev["v_scale"],
                         dev["v_off"], dev["seq_lens"], bits=wl.bits, k_layout=wl.k_layout, v_layout=wl.v_layout,
                         group=wl.group, out=out_d, workspace=ws, **win)
+        done[b].record(compute)
         out_h.copy_(out_d, non_blocking=True)
 
-    for _ in range(warmup):
-        step()
+    def run(n_steps, start=None):
+        copy_in(0, start)
+        for i in range(n_steps):
+            if i + 1 < n_steps:
+                copy_in(i + 1)
+            decode(i)
+
+    run(warmup)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
+    e0.record(compute)
+    run(steps, start=e0)
+    e1.record(compute)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     return ms, h2d, d2h
