@@ -143,6 +143,7 @@ struct Plan {
   DecodeKernel tc_fn;  // the tensor-core kernel when it takes the call, else nullptr
   bool grp;            // the tensor-core kernel (rings per group of four warps)
   int cluster_ctas;    // cluster mode: CTAs per pair (one thread-block cluster each), else 0
+  int sms;             // SMs of the device
 };
 
 // LBKV_DECODE_KERNEL=tc in the environment (read at every call) makes a token-wise K side
@@ -253,6 +254,7 @@ int make_plan(const lbkv_desc* d, int bits, int kl, int vl, int group, Plan* pl)
     const int units_per_cta = pl->grp ? warps / 4 : warps;  // warps, or groups of four
     const long long want = (max_items + units_per_cta - 1) / units_per_cta;
     pl->n_cta = (int)(want < sms ? (want > 0 ? want : 1) : sms);
+    pl->sms = sms;
     // With a window and few pairs, the window kernel's CTAs (one per pair, launched first)
     // hold their SMs while the decode kernel starts: the grid leaves those SMs out, so that
     // no decode CTA waits for one of them to finish.
@@ -375,6 +377,7 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   p.sl2 = sigma * 1.4426950408889634f;
   p.n_cta = pl.n_cta;
   p.split_w = kSplitBoundaryTokens / pl.unit_tokens;
+  p.cluster_split = 1;
   p.has_win = pl.win;
   p.ring_off = pl.ring_off;
   p.ring_per_warp = pl.ring_per_warp;
@@ -419,11 +422,34 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
     const long long wpc = pl.threads / 32;  // warps per CTA
     const long long items_pair = ((long long)desc->max_seq_len + pl.unit_tokens - 1) / pl.unit_tokens;
     const long long ipw_split = (units * items_pair + (long long)pl.n_cta * wpc - 1) / ((long long)pl.n_cta * wpc);
-    const long long ipw_cluster = (items_pair + (long long)cpp * wpc - 1) / ((long long)cpp * wpc);
-    if (kc && cpp >= 2 && ipw_cluster <= ipw_split + 1) {
-      const int n = (int)units * cpp;
+    long long ipw_cluster = (items_pair + (long long)cpp * wpc - 1) / ((long long)cpp * wpc);
+    bool take = kc && cpp >= 2 && ipw_cluster <= ipw_split + 1;
+    // Two levels: several clusters per pair (each merges its CTAs in distributed shared memory
+    // and writes one partial; the pair's last cluster merges those), where that gives a warp
+    // fewer items than one cluster per pair and no more than the split-decode grid. The
+    // partials take CTA-partial rows of the workspace (2 per CTA of the split-decode grid).
+    int split = 1;
+    if (kc) {
+      long long best = take ? ipw_cluster : ipw_split + 1;
+      for (int c2 = 16; c2 >= 2; c2 >>= 1) {
+        for (int s2 = 2; s2 <= 8; s2 <<= 1) {
+          if (units * c2 * s2 > pl.sms || units * s2 > 2LL * pl.n_cta) continue;
+          const long long ipw2 = (items_pair + (long long)c2 * s2 * wpc - 1) / ((long long)c2 * s2 * wpc);
+          if (ipw2 >= best || ipw2 > ipw_split) continue;
+          if (max_active_clusters(reinterpret_cast<const void*>(kc), c2, pl.threads, pl.smem_bytes) < units * s2)
+            continue;
+          best = ipw2;
+          cpp = c2;
+          split = s2;
+          take = true;
+        }
+      }
+    }
+    if (take) {
+      const int n = (int)(units * cpp * split);
       DecodeParams pc = p;
       pc.n_cta = n;
+      pc.cluster_split = split;
       cfg.gridDim = dim3((unsigned)n);
       attr[1].id = cudaLaunchAttributeClusterDimension;
       attr[1].val.clusterDim.x = (unsigned)cpp;

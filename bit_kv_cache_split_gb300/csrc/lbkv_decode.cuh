@@ -147,6 +147,9 @@ struct DecodeParams {
   float sl2;  // softmax scale times log2(e)
   int n_cta, has_win;   // CTAs of the grid; whether a bf16 window is given
   int split_w;          // work split: the cost of a pair boundary, in items
+  // Cluster mode: thread-block clusters per pair (1: the cluster writes the output; more: each
+  // cluster writes its merged partial to the CTA partials, and the last one merges them)
+  int cluster_split;
   int ring_off, ring_per_warp;  // shared-memory offset of the rings, entries per warp
   // Paged cache (the kernel's PAGED variant): token t of cached KV head kvh of sequence b
   // is row t mod 2^log2_page of page page_table[b * max_pages + t / 2^log2_page], in a
@@ -969,17 +972,21 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
   };
 
   // ---------------------------------------------------- the CTA's share of the items
-  // Cluster mode (small problems): cluster i takes pair i, its CTA of rank r the r-th of
-  // equal contiguous slices of the pair's items; no scan.
+  // Cluster mode (small problems): clusters s·i .. s·i + s - 1 take pair i (s = cluster_split),
+  // the CTA of rank r in the j-th of them the (j·n + r)-th of equal contiguous slices of the
+  // pair's items (n CTAs per cluster); no scan.
   bool cluster_pair = false;  // cluster mode: the pair has tokens (its CTAs merge in the cluster)
   if constexpr (CLUSTER) {
     const int ncta = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
-    const int up = (int)cluster_id_x();
+    const int cid = (int)cluster_id_x();
+    const int up = cid / p.cluster_split;
+    const int cluster_sub = cid - up * p.cluster_split;  // which of the pair's clusters
     const int b = up / p.Hkv, kv = up % p.Hkv;
     const int n = up < n_pairs ? items_of(seq_len(b)) : 0;
     cluster_pair = n > 0;
     if (threadIdx.x == 0) {
-      const long long t0 = (long long)n * crank / ncta, t1 = (long long)n * (crank + 1) / ncta;
+      const long long parts = (long long)ncta * p.cluster_split, rr = (long long)cluster_sub * ncta + crank;
+      const long long t0 = (long long)n * rr / parts, t1 = (long long)n * (rr + 1) / parts;
       ss.x[0] = t0;
       ss.x[1] = t1;
       ss.b0 = b;
@@ -1572,7 +1579,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
           for (int k = 0; k < ncta; ++k) M = fmaxf(M, ld_cluster_f32(cluster_map(m_base + 4u * i, k)));
           float2 wml = make_float2(-INFINITY, 0.f);
           const size_t wr = (size_t)u * hq + i;
-          if (p.has_win) {
+          if (p.has_win && p.cluster_split == 1) {  // (with several clusters the last adds it)
             wml = __ldcg(&p.win_ml[wr]);
             M = fmaxf(M, wml.x);
           }
@@ -1590,6 +1597,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
               v[2] = fmaf(sc, o4.z, v[2]);
               v[3] = fmaf(sc, o4.w, v[3]);
             }
+          }
+          if (p.cluster_split > 1) {
+            const int sub = (int)cluster_id_x() % p.cluster_split;  // which of the pair's clusters
+            const size_t prow = ((size_t)u * p.cluster_split + sub) * hq + i;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p.part_o[prow * D + 4 * lane + e] = v[e];
+            if (lane == 0) p.part_ml[prow] = make_float2(M, lt);
+            __threadfence();  // before the cluster barrier and the arrival count below
+            continue;
+          }
+          if (M != -INFINITY) {
             if (p.has_win && wml.x != -INFINITY) {
               const float sc = fast_exp2(wml.x - M);
               lt = fmaf(sc, wml.y, lt);
@@ -1604,6 +1622,54 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         }
       }
       cluster_sync();
+      if (p.cluster_split > 1 && cluster_ctarank() == 0) {
+        // The pair's clusters count their arrivals; the last merges their partials (and the
+        // window's) into the output, one warp per query row.
+        if (threadIdx.x == 0) {
+          __threadfence();
+          const int prev = atomicAdd(p.done + u, 1);
+          s_last = (prev == p.cluster_split - 1);
+        }
+        __syncthreads();
+        if (s_last) {
+          __threadfence();
+          const int ns = p.cluster_split;
+          for (int i = warp; i < hq; i += W) {
+            const size_t wr = (size_t)u * hq + i;
+            float M = -INFINITY;
+            for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(&p.part_ml[((size_t)u * ns + k) * hq + i]).x);
+            float2 wml = make_float2(-INFINITY, 0.f);
+            if (p.has_win) {
+              wml = __ldcg(&p.win_ml[wr]);
+              M = fmaxf(M, wml.x);
+            }
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            float lt = 0.f;
+            if (M != -INFINITY) {
+              for (int k = 0; k < ns; ++k) {
+                const size_t prow = ((size_t)u * ns + k) * hq + i;
+                const float2 ml = __ldcg(&p.part_ml[prow]);
+                if (ml.x == -INFINITY) continue;
+                const float sc = fast_exp2(ml.x - M);
+                lt = fmaf(sc, ml.y, lt);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = fmaf(sc, __ldcg(&p.part_o[prow * D + 4 * lane + e]), v[e]);
+              }
+              if (p.has_win && wml.x != -INFINITY) {
+                const float sc = fast_exp2(wml.x - M);
+                lt = fmaf(sc, wml.y, lt);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = fmaf(sc, __ldcg(&p.win_o[wr * D + 4 * lane + e]), v[e]);
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = lt > 0.f ? v[e] / lt : 0.f;
+            if (p.rotation & 2) hadamard128(v, lane);
+            store_row4(p.out + ((size_t)b * p.Hq + kvh * hq + i) * D, lane, v);
+          }
+          if (threadIdx.x == 0) p.done[u] = 0;  // ready for the next call in stream order
+        }
+      }
     } else {
     // A pair held by this CTA alone is finished here (with the window's partial). Otherwise the
     // CTA writes its partial to its slot (1 when the pair is the second one it holds a

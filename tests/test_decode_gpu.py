@@ -238,14 +238,26 @@ def test_int4_full_size_sampled(lbkv, batch, ctx):
     sampled_parity(lbkv, wl, [(0, 0), (batch - 1, 5)])
 
 
-@pytest.mark.parametrize("bits,batch,ctx", [(2, 1, 4096), (2, 1, 16384), (2, 1, 32768), (2, 8, 16384), (4, 1, 16384),
-                                            (4, 8, 4096)])
+@pytest.mark.parametrize("bits,batch,ctx", [(2, 1, 4096), (2, 1, 16384), (2, 1, 32768), (2, 1, 65536), (2, 8, 16384),
+                                            (4, 1, 16384), (4, 8, 4096)])
 def test_few_pairs_every_unit(lbkv, bits, batch, ctx):
-    """Few (sequence, KV head) pairs at full context: on a 152-SM GPU these shapes run one
-    thread-block cluster per pair (2 to 8 CTAs that merge in distributed shared memory);
-    every unit is compared with the oracle."""
+    """Few (sequence, KV head) pairs at full context: on a 152-SM GPU these shapes run as
+    thread-block clusters, one per pair (2 to 8 CTAs that merge in distributed shared memory)
+    or several per pair (batch 1 from 32K: four clusters of four, whose partials the last
+    cluster merges); every unit is compared with the oracle."""
     wl = (inputs.decode_int2 if bits == 2 else inputs.decode_int4)(batch, ctx)
     sampled_parity(lbkv, wl, [(b, h) for b in range(batch) for h in range(wl.num_kv_heads)])
+
+
+@pytest.mark.parametrize("lens,window", [([32768], 128), ([32000, 1999], 0), ([30000, 0, 12345], 64),
+                                         ([65536, 17], 0)])
+def test_few_pairs_ragged_and_window(lbkv, lens, window):
+    """Few pairs with ragged lengths, an empty sequence or a bf16 window, in the cluster
+    modes (clusters of one pair with fewer items than CTAs, the window merged by the last
+    cluster of a pair); every unit is compared with the oracle."""
+    wl = inputs.Workload(f"few-pairs-{len(lens)}", len(lens), 32, 8, lens, bits=2, group=128, s_range=(0.01, 0.1),
+                         window=window, seed=11)
+    sampled_parity(lbkv, wl, [(b, h) for b in range(len(lens)) for h in range(wl.num_kv_heads)])
 
 
 @pytest.mark.parametrize("bits", [2, 4])
