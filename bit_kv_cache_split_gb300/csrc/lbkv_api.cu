@@ -431,8 +431,8 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
     int split = 1;
     if (kc) {
       long long best = take ? ipw_cluster : ipw_split + 1;
-      for (int c2 = 16; c2 >= 2; c2 >>= 1) {
-        for (int s2 = 2; s2 <= 8; s2 <<= 1) {
+      for (int c2 = 16; c2 >= 2; c2 >>= 1) {  // (larger clusters first: fewer partials per pair)
+        for (int s2 = 2; s2 <= 16; ++s2) {
           if (units * c2 * s2 > pl.sms || units * s2 > 2LL * pl.n_cta) continue;
           const long long ipw2 = (items_pair + (long long)c2 * s2 * wpc - 1) / ((long long)c2 * s2 * wpc);
           if (ipw2 >= best || ipw2 > ipw_split) continue;
