@@ -1575,45 +1575,60 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         const int ncta = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
         const uint32_t o_base = smem_addr(ma.o), m_base = smem_addr(ss.cm), l_base = smem_addr(ss.cl);
         for (int i = crank + ncta * warp; i < hq; i += ncta * W) {  // one warp per query row
-          float M = -INFINITY;
-          for (int k = 0; k < ncta; ++k) M = fmaxf(M, ld_cluster_f32(cluster_map(m_base + 4u * i, k)));
+          // lane k < ncta reads CTA k's (m, l) of the row; the maximum, the scales and the
+          // denominator are warp reductions; every lane then reads its 4 channels of all the
+          // CTAs' rows, four loads in flight at a time
+          float mk = -INFINITY, lk = 0.f;
+          if (lane < ncta) {
+            mk = ld_cluster_f32(cluster_map(m_base + 4u * i, lane));
+            lk = ld_cluster_f32(cluster_map(l_base + 4u * i, lane));
+          }
+          float M = mk;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULLMASK, M, o));
           float2 wml = make_float2(-INFINITY, 0.f);
           const size_t wr = (size_t)u * hq + i;
           if (p.has_win && p.cluster_split == 1) {  // (with several clusters the last adds it)
             wml = __ldcg(&p.win_ml[wr]);
             M = fmaxf(M, wml.x);
           }
+          const float sck = (M == -INFINITY || mk == -INFINITY) ? 0.f : fast_exp2(mk - M);
+          float lt = sck * lk;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(FULLMASK, lt, o);
           float v[4] = {0.f, 0.f, 0.f, 0.f};
-          float lt = 0.f;
-          if (M != -INFINITY) {
-            for (int k = 0; k < ncta; ++k) {
-              const float mk = ld_cluster_f32(cluster_map(m_base + 4u * i, k));
-              if (mk == -INFINITY) continue;
-              const float sc = fast_exp2(mk - M);
-              lt = fmaf(sc, ld_cluster_f32(cluster_map(l_base + 4u * i, k)), lt);
-              const float4 o4 = ld_cluster_f32x4(cluster_map(o_base + 4u * (i * D + 4 * lane), k));
-              v[0] = fmaf(sc, o4.x, v[0]);
-              v[1] = fmaf(sc, o4.y, v[1]);
-              v[2] = fmaf(sc, o4.z, v[2]);
-              v[3] = fmaf(sc, o4.w, v[3]);
+          for (int k0 = 0; k0 < ncta; k0 += 4) {
+            float4 o4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (k0 + j < ncta) o4[j] = ld_cluster_f32x4(cluster_map(o_base + 4u * (i * D + 4 * lane), k0 + j));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float sc = __shfl_sync(FULLMASK, sck, (k0 + j) & 31);
+              if (k0 + j < ncta && sc != 0.f) {
+                v[0] = fmaf(sc, o4[j].x, v[0]);
+                v[1] = fmaf(sc, o4[j].y, v[1]);
+                v[2] = fmaf(sc, o4[j].z, v[2]);
+                v[3] = fmaf(sc, o4[j].w, v[3]);
+              }
             }
           }
           if (p.cluster_split > 1) {
             const int sub = (int)cluster_id_x() % p.cluster_split;  // which of the pair's clusters
             const size_t prow = ((size_t)u * p.cluster_split + sub) * hq + i;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) p.part_o[prow * D + 4 * lane + e] = v[e];
+            reinterpret_cast<float4*>(p.part_o + prow * D)[lane] = make_float4(v[0], v[1], v[2], v[3]);
             if (lane == 0) p.part_ml[prow] = make_float2(M, lt);
             __threadfence();  // before the cluster barrier and the arrival count below
             continue;
           }
-          if (M != -INFINITY) {
-            if (p.has_win && wml.x != -INFINITY) {
-              const float sc = fast_exp2(wml.x - M);
-              lt = fmaf(sc, wml.y, lt);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) v[e] = fmaf(sc, __ldcg(&p.win_o[wr * D + 4 * lane + e]), v[e]);
-            }
+          if (p.has_win && M != -INFINITY && wml.x != -INFINITY) {
+            const float sc = fast_exp2(wml.x - M);
+            lt = fmaf(sc, wml.y, lt);
+            const float4 w4 = __ldcg(reinterpret_cast<const float4*>(p.win_o + wr * D) + lane);
+            v[0] = fmaf(sc, w4.x, v[0]);
+            v[1] = fmaf(sc, w4.y, v[1]);
+            v[2] = fmaf(sc, w4.z, v[2]);
+            v[3] = fmaf(sc, w4.w, v[3]);
           }
 #pragma unroll
           for (int e = 0; e < 4; ++e) v[e] = lt > 0.f ? v[e] / lt : 0.f;
@@ -1634,33 +1649,48 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         if (s_last) {
           __threadfence();
           const int ns = p.cluster_split;
-          for (int i = warp; i < hq; i += W) {
+          for (int i = warp; i < hq; i += W) {  // as in the cluster merge: lane k reads partial k
             const size_t wr = (size_t)u * hq + i;
-            float M = -INFINITY;
-            for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(&p.part_ml[((size_t)u * ns + k) * hq + i]).x);
+            float2 mlk = make_float2(-INFINITY, 0.f);
+            if (lane < ns) mlk = __ldcg(&p.part_ml[((size_t)u * ns + lane) * hq + i]);
+            float M = mlk.x;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULLMASK, M, o));
             float2 wml = make_float2(-INFINITY, 0.f);
             if (p.has_win) {
               wml = __ldcg(&p.win_ml[wr]);
               M = fmaxf(M, wml.x);
             }
+            const float sck = (M == -INFINITY || mlk.x == -INFINITY) ? 0.f : fast_exp2(mlk.x - M);
+            float lt = sck * mlk.y;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(FULLMASK, lt, o);
             float v[4] = {0.f, 0.f, 0.f, 0.f};
-            float lt = 0.f;
-            if (M != -INFINITY) {
-              for (int k = 0; k < ns; ++k) {
-                const size_t prow = ((size_t)u * ns + k) * hq + i;
-                const float2 ml = __ldcg(&p.part_ml[prow]);
-                if (ml.x == -INFINITY) continue;
-                const float sc = fast_exp2(ml.x - M);
-                lt = fmaf(sc, ml.y, lt);
+            for (int k0 = 0; k0 < ns; k0 += 4) {
+              float4 o4[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = fmaf(sc, __ldcg(&p.part_o[prow * D + 4 * lane + e]), v[e]);
-              }
-              if (p.has_win && wml.x != -INFINITY) {
-                const float sc = fast_exp2(wml.x - M);
-                lt = fmaf(sc, wml.y, lt);
+              for (int j = 0; j < 4; ++j)
+                if (k0 + j < ns)
+                  o4[j] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (((size_t)u * ns + k0 + j) * hq + i) * D) + lane);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = fmaf(sc, __ldcg(&p.win_o[wr * D + 4 * lane + e]), v[e]);
+              for (int j = 0; j < 4; ++j) {
+                const float sc = __shfl_sync(FULLMASK, sck, (k0 + j) & 31);
+                if (k0 + j < ns && sc != 0.f) {
+                  v[0] = fmaf(sc, o4[j].x, v[0]);
+                  v[1] = fmaf(sc, o4[j].y, v[1]);
+                  v[2] = fmaf(sc, o4[j].z, v[2]);
+                  v[3] = fmaf(sc, o4[j].w, v[3]);
+                }
               }
+            }
+            if (p.has_win && M != -INFINITY && wml.x != -INFINITY) {
+              const float sc = fast_exp2(wml.x - M);
+              lt = fmaf(sc, wml.y, lt);
+              const float4 w4 = __ldcg(reinterpret_cast<const float4*>(p.win_o + wr * D) + lane);
+              v[0] = fmaf(sc, w4.x, v[0]);
+              v[1] = fmaf(sc, w4.y, v[1]);
+              v[2] = fmaf(sc, w4.z, v[2]);
+              v[3] = fmaf(sc, w4.w, v[3]);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) v[e] = lt > 0.f ? v[e] / lt : 0.f;
@@ -1670,6 +1700,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
           if (threadIdx.x == 0) p.done[u] = 0;  // ready for the next call in stream order
         }
       }
+      break;  // a cluster holds one pair: its only segment is done
     } else {
     // A pair held by this CTA alone is finished here (with the window's partial). Otherwise the
     // CTA writes its partial to its slot (1 when the pair is the second one it holds a
