@@ -281,6 +281,32 @@ def test_rotated_decode_single_split_and_many_splits(lbkv):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("kl,vl", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_rotated_decode_two_level_clusters(lbkv, kl, vl):
+    """Batch 1, 2 KV heads, 131,000 cached tokens and a window: on a 152-SM GPU each pair runs as
+    several thread-block clusters whose partials the pair's last cluster merges with the
+    window's (and rotates back)."""
+    _check_rotated_decode(lbkv, _rot_wl(2, kl, vl, lens=(131000,), window=100), 3)
+
+
+@pytest.mark.gpu
+def test_two_level_clusters_paged_equals_contiguous(lbkv):
+    from bit_kv_cache_split_gb300 import inputs
+
+    wl = _rot_wl(2, 0, 0, lens=(131000,), window=0)
+    t = inputs.generate(wl, "cpu")
+    dev = {k: v.cuda() for k, v in t.items()}
+    keys = ("k_codes", "k_scale", "k_off", "v_codes", "v_scale", "v_off")
+    ref = lbkv.decode_attn(dev["q"], *[dev[k] for k in keys], dev["seq_lens"], bits=2, group=128)
+    table, n = inputs.page_table(wl.lens, 256, wl.t_cap // 256, seed=4)
+    pool = [inputs.to_pages(dev[k], table, n, 256) for k in keys]
+    got = lbkv.decode_attn(dev["q"], *pool, dev["seq_lens"], bits=2, group=128, page_table=table.cuda(),
+                           max_seq_len=wl.t_cap)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.gpu
 def test_rotated_paged_decode_equals_rotated_contiguous(lbkv):
     from bit_kv_cache_split_gb300 import inputs
 
