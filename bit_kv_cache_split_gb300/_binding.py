@@ -90,6 +90,8 @@ def load(path: Optional[str] = None):
         L.lbkv_decode_attn_noalloc.argtypes = [ctypes.POINTER(Desc)] + [vp] * 8 + [i32] * 4 + [vp, vp]
         L.lbkv_noalloc_scratch_bytes.restype = ctypes.c_size_t
         L.lbkv_noalloc_scratch_bytes.argtypes = []
+        L.lbkv_decode_launch_info.restype = i32
+        L.lbkv_decode_launch_info.argtypes = [ctypes.POINTER(Desc)] + [i32] * 4 + [ctypes.POINTER(ctypes.c_int)] * 3
         L.lbkv_strerror.restype = ctypes.c_char_p
         L.lbkv_strerror.argtypes = [i32]
         if path is None:
@@ -169,6 +171,28 @@ def workspace_bytes(batch, num_q_heads, num_kv_heads, max_seq_len, bits, k_layou
         d.k_win = d.v_win = d.win_lens = 16  # any non-null value: only presence matters here
         d.win_cap = 1
     return int(load().lbkv_workspace_bytes(ctypes.byref(d), bits, k_layout, v_layout, group))
+
+
+def decode_launch_info(batch, num_q_heads, num_kv_heads, max_seq_len, bits, k_layout=TOKENWISE, v_layout=TOKENWISE,
+                       group=128, window: bool = False, paged_tokens: int = 0, head_dim=128) -> dict:
+    """The launch lbkv_decode_launch_info reports for a call with these shapes on the current
+    device: {"grid": CTAs, "cluster": CTAs per cluster (0: the split-decode grid), "split":
+    clusters per (sequence, KV head) pair}. Raises LbkvError for invalid arguments."""
+    d = make_desc(batch, num_q_heads, num_kv_heads, max_seq_len, head_dim)
+    if window:
+        d.k_win = d.v_win = d.win_lens = 16  # any non-null value: only presence matters here
+        d.win_cap = 1
+    if paged_tokens:
+        d.page_table = 16
+        d.page_tokens = paged_tokens
+        d.max_pages = max(1, max_seq_len // paged_tokens)
+        d.num_pages = d.max_pages * max(1, batch)
+    g, c, s = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = load().lbkv_decode_launch_info(ctypes.byref(d), bits, k_layout, v_layout, group, ctypes.byref(g),
+                                        ctypes.byref(c), ctypes.byref(s))
+    if st != 0:
+        raise LbkvError(st, "lbkv_decode_launch_info")
+    return {"grid": g.value, "cluster": c.value, "split": s.value}
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:

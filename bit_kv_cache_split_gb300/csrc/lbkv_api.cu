@@ -318,6 +318,61 @@ size_t decode_workspace_plan(const lbkv_desc* desc, int bits, int k_layout, int 
 
 }  // namespace lbkv
 
+// Cluster mode: the kernel, CTAs per cluster and clusters per pair a call takes, or no kernel
+// (the split-decode grid). A device that cannot hold the clusters takes the split-decode grid.
+struct ClusterChoice {
+  DecodeKernel fn = nullptr;
+  int cpp = 0, split = 1;
+};
+ClusterChoice choose_clusters(const lbkv_desc* desc, const Plan& pl, int bits, int k_layout, int v_layout,
+                              int group) {
+  ClusterChoice ch;
+  if (pl.cluster_ctas <= 0 || pl.tc_fn) return ch;
+  DecodeKernel kc = pick_kernel(bits, k_layout, v_layout, pl.mode, group, desc->page_table != nullptr, true);
+  if (!kc || ensure_smem_attr(reinterpret_cast<const void*>(kc), pl.smem_bytes, true) != LBKV_OK) return ch;
+  const long long units = (long long)desc->batch * pl.hkv;
+  // the largest cluster size (down to 2) whose clusters, one per pair, the device holds at once
+  int cpp = pl.cluster_ctas;
+  while (cpp >= 2 && max_active_clusters(reinterpret_cast<const void*>(kc), cpp, pl.threads, pl.smem_bytes) < units)
+    cpp >>= 1;
+  // Taken only when it gives a warp at most one item more than the split-decode grid (an
+  // item costs a warp about 4.6 us among 16, the cluster merge saves about 6 us of fixed
+  // costs). Measured (graph replay, INT2): batch 8 at 16K 32.1 -> 26.8 us and at 32K 47.9 ->
+  // 44.7 us with clusters of 2, but at 64K 77.9 -> 80.5 us and at 128K 140.4 -> 152.4 us (two
+  // and more items more per warp). Clusters of 16 CTAs of this size fit 7 at a time, of 8
+  // CTAs 15, of 4 CTAs 36.
+  const long long wpc = pl.threads / 32;  // warps per CTA
+  const long long items_pair = ((long long)desc->max_seq_len + pl.unit_tokens - 1) / pl.unit_tokens;
+  const long long ipw_split = (units * items_pair + (long long)pl.n_cta * wpc - 1) / ((long long)pl.n_cta * wpc);
+  const long long ipw_cluster = (items_pair + (long long)cpp * wpc - 1) / ((long long)cpp * wpc);
+  bool take = cpp >= 2 && ipw_cluster <= ipw_split + 1;
+  // Two levels: several clusters per pair (each merges its CTAs in distributed shared memory
+  // and writes one partial; the pair's last cluster merges those), where that gives a warp
+  // fewer items than one cluster per pair and no more than the split-decode grid. The
+  // partials take CTA-partial rows of the workspace (2 per CTA of the split-decode grid).
+  int split = 1;
+  long long best = take ? ipw_cluster : ipw_split + 1;
+  for (int c2 = 16; c2 >= 2; c2 >>= 1) {  // (larger clusters first: fewer partials per pair)
+    for (int s2 = 2; s2 <= 16; ++s2) {
+      if (units * c2 * s2 > pl.sms || units * s2 > 2LL * pl.n_cta) continue;
+      const long long ipw2 = (items_pair + (long long)c2 * s2 * wpc - 1) / ((long long)c2 * s2 * wpc);
+      if (ipw2 >= best || ipw2 > ipw_split) continue;
+      if (max_active_clusters(reinterpret_cast<const void*>(kc), c2, pl.threads, pl.smem_bytes) < units * s2)
+        continue;
+      best = ipw2;
+      cpp = c2;
+      split = s2;
+      take = true;
+    }
+  }
+  if (take) {
+    ch.fn = kc;
+    ch.cpp = cpp;
+    ch.split = split;
+  }
+  return ch;
+}
+
 extern "C" {
 
 size_t lbkv_workspace_bytes(const lbkv_desc* desc, int bits, int k_layout, int v_layout, int group) {
@@ -403,74 +458,54 @@ int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_t* k_code
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  if (pl.cluster_ctas > 0 && !pl.tc_fn) {
-    // cluster mode; a device that cannot hold the clusters takes the split-decode grid
-    DecodeKernel kc = pick_kernel(bits, k_layout, v_layout, pl.mode, group, desc->page_table != nullptr, true);
-    const long long units = (long long)desc->batch * pl.hkv;
-    // the largest cluster size (down to 2) whose clusters, one per pair, the device holds at once
-    int cpp = pl.cluster_ctas;
-    if (kc && ensure_smem_attr(reinterpret_cast<const void*>(kc), pl.smem_bytes, true) == LBKV_OK) {
-      while (cpp >= 2 && max_active_clusters(reinterpret_cast<const void*>(kc), cpp, pl.threads, pl.smem_bytes) < units)
-        cpp >>= 1;
+  const ClusterChoice cc = choose_clusters(desc, pl, bits, k_layout, v_layout, group);
+  if (cc.fn) {  // cluster mode (if the launch fails, the split-decode grid takes the call)
+    const int n = (int)((long long)desc->batch * pl.hkv * cc.cpp * cc.split);
+    DecodeParams pc = p;
+    pc.n_cta = n;
+    pc.cluster_split = cc.split;
+    cfg.gridDim = dim3((unsigned)n);
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cc.cpp;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    if (pl.win) {
+      cfg.numAttrs = 2;
+    } else {
+      attr[0] = attr[1];
+      cfg.numAttrs = 1;
     }
-    // Taken only when it gives a warp at most one item more than the split-decode grid (an
-    // item costs a warp about 4.6 us among 16, the cluster merge saves about 6 us of fixed
-    // costs). Measured (graph replay, INT2): batch 8 at 16K 32.1 -> 26.8 us and at 32K 47.9 ->
-    // 44.7 us with clusters of 2, but at 64K 77.9 -> 80.5 us and at 128K 140.4 -> 152.4 us (two
-    // and more items more per warp). Clusters of 16 CTAs of this size fit 7 at a time, of 8
-    // CTAs 15, of 4 CTAs 36.
-    const long long wpc = pl.threads / 32;  // warps per CTA
-    const long long items_pair = ((long long)desc->max_seq_len + pl.unit_tokens - 1) / pl.unit_tokens;
-    const long long ipw_split = (units * items_pair + (long long)pl.n_cta * wpc - 1) / ((long long)pl.n_cta * wpc);
-    long long ipw_cluster = (items_pair + (long long)cpp * wpc - 1) / ((long long)cpp * wpc);
-    bool take = kc && cpp >= 2 && ipw_cluster <= ipw_split + 1;
-    // Two levels: several clusters per pair (each merges its CTAs in distributed shared memory
-    // and writes one partial; the pair's last cluster merges those), where that gives a warp
-    // fewer items than one cluster per pair and no more than the split-decode grid. The
-    // partials take CTA-partial rows of the workspace (2 per CTA of the split-decode grid).
-    int split = 1;
-    if (kc) {
-      long long best = take ? ipw_cluster : ipw_split + 1;
-      for (int c2 = 16; c2 >= 2; c2 >>= 1) {  // (larger clusters first: fewer partials per pair)
-        for (int s2 = 2; s2 <= 16; ++s2) {
-          if (units * c2 * s2 > pl.sms || units * s2 > 2LL * pl.n_cta) continue;
-          const long long ipw2 = (items_pair + (long long)c2 * s2 * wpc - 1) / ((long long)c2 * s2 * wpc);
-          if (ipw2 >= best || ipw2 > ipw_split) continue;
-          if (max_active_clusters(reinterpret_cast<const void*>(kc), c2, pl.threads, pl.smem_bytes) < units * s2)
-            continue;
-          best = ipw2;
-          cpp = c2;
-          split = s2;
-          take = true;
-        }
-      }
-    }
-    if (take) {
-      const int n = (int)(units * cpp * split);
-      DecodeParams pc = p;
-      pc.n_cta = n;
-      pc.cluster_split = split;
-      cfg.gridDim = dim3((unsigned)n);
-      attr[1].id = cudaLaunchAttributeClusterDimension;
-      attr[1].val.clusterDim.x = (unsigned)cpp;
-      attr[1].val.clusterDim.y = 1;
-      attr[1].val.clusterDim.z = 1;
-      if (pl.win) {
-        cfg.numAttrs = 2;
-      } else {
-        attr[0] = attr[1];
-        cfg.numAttrs = 1;
-      }
-      if (cudaLaunchKernelEx(&cfg, kc, pc) == cudaSuccess && cudaGetLastError() == cudaSuccess) return LBKV_OK;
-      (void)cudaGetLastError();
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-    }
+    if (cudaLaunchKernelEx(&cfg, cc.fn, pc) == cudaSuccess && cudaGetLastError() == cudaSuccess) return LBKV_OK;
+    (void)cudaGetLastError();
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
   }
   cfg.gridDim = dim3((unsigned)pl.n_cta);
   cfg.numAttrs = pl.win ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return LBKV_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return LBKV_ECUDA;
+  return LBKV_OK;
+}
+
+int lbkv_decode_launch_info(const lbkv_desc* desc, int bits, int k_layout, int v_layout, int group, int* grid,
+                            int* cluster, int* split) {
+  if (!grid || !cluster || !split) return LBKV_EINVAL;
+  Plan pl;
+  int st = make_plan(desc, bits, k_layout, v_layout, group, &pl);
+  if (st) return st;
+  *grid = pl.n_cta;
+  *cluster = 0;
+  *split = 1;
+  if (desc->batch == 0) {
+    *grid = 0;
+    return LBKV_OK;
+  }
+  const ClusterChoice cc = choose_clusters(desc, pl, bits, k_layout, v_layout, group);
+  if (cc.fn) {
+    *grid = (int)((long long)desc->batch * pl.hkv * cc.cpp * cc.split);
+    *cluster = cc.cpp;
+    *split = cc.split;
+  }
   return LBKV_OK;
 }
 

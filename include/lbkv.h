@@ -155,6 +155,22 @@ LBKV_API int lbkv_decode_attn(const lbkv_desc* desc, const void* q, const uint8_
                      const int32_t* seq_lens, int bits, int k_layout, int v_layout, int group, void* out,
                      lbkv_stream_t stream);
 
+/* The launch lbkv_decode_attn makes for this descriptor and format on the current device,
+ * without running it (the device is queried for its SM count and thread-block cluster
+ * occupancy; desc's pointers are only tested for NULL, as lbkv_decode_attn tests them):
+ *   grid: CTAs of the decode kernel (0 for an empty batch);
+ *   cluster: CTAs per thread-block cluster, or 0 for the split-decode grid (the CTAs take
+ *     equal shares of all pairs' items after a scan of the lengths, and the last CTA of a
+ *     pair merges its partials);
+ *   split: clusters per (sequence, KV head) pair: 1, the cluster merges its CTAs in
+ *     distributed shared memory and writes the output; more, each cluster writes one partial
+ *     and the pair's last cluster merges them.
+ * A call whose cluster launch the device refuses runs on the split-decode grid instead.
+ * Errors: those lbkv_decode_attn returns for invalid arguments; LBKV_EINVAL for a NULL
+ * output pointer. */
+LBKV_API int lbkv_decode_launch_info(const lbkv_desc* desc, int bits, int k_layout, int v_layout, int group,
+                                     int* grid, int* cluster, int* split);
+
 /* Quantize a bf16 cache side x [B][Hkv][T_cap][D] into the layout above
  * (the value model s * q + z is the explainer's quantization-format
  * paragraph; the quantizer is this library's reading): per group

@@ -284,3 +284,19 @@ def test_bounded_wait_reports_and_the_context_survives(lbkv):
     assert time.perf_counter() - t0 < 5.0
     check(lbkv, inputs.tiny_int2())
 
+
+
+@pytest.mark.parametrize("bits,batch,ctx,window,want", [
+    (2, 32, 32768, False, (152, 0, 1)),   # the headline: the split-decode grid
+    (2, 8, 32768, False, (128, 2, 1)),    # one cluster of 2 per pair
+    (2, 1, 16384, False, (64, 8, 1)),     # one cluster of 8 per pair
+    (2, 1, 32768, False, (128, 4, 4)),    # four clusters of 4 per pair
+    (2, 1, 99968, True, (144, 2, 9)),     # long context with a window: nine clusters of 2
+])
+def test_launch_modes_on_this_device(lbkv, bits, batch, ctx, window, want):
+    """The launch each mode's parity tests rely on (on a 152-SM GB300; other devices may
+    choose other shapes, which the parity tests cover as well)."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("launch shapes are stated for 152 SMs")
+    info = lbkv.decode_launch_info(batch, 32, 8, ctx, bits, window=window)
+    assert (info["grid"], info["cluster"], info["split"]) == want, info
