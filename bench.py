@@ -385,7 +385,9 @@ def run_sweep(device, peak):
             continue
         gbs = case.bytes / (ms * 1e-3) / 1e9
         row = {"workload": wl.name, "us_per_call": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-               "frac": round(gbs / peak, 3), "bytes": case.bytes}
+               "frac": round(gbs / peak, 3), "bytes": case.bytes,
+               "launch": pkg.decode_launch_info(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.t_cap, wl.bits,
+                                                wl.k_layout, wl.v_layout, wl.group, window=bool(wl.window))}
         rec = profiled_counters(wl.name)
         if rec:  # ncu counters of this workload on the current kernel sources
             row["traffic"] = rec["dram_bytes_per_launch"]
