@@ -239,7 +239,7 @@ def test_int4_full_size_sampled(lbkv, batch, ctx):
 
 
 @pytest.mark.parametrize("bits,batch,ctx", [(2, 1, 4096), (2, 1, 16384), (2, 1, 32768), (2, 1, 65536), (2, 8, 16384),
-                                            (4, 1, 16384), (4, 8, 4096)])
+                                            (4, 1, 16384), (4, 8, 4096), (4, 1, 131072)])
 def test_few_pairs_every_unit(lbkv, bits, batch, ctx):
     """Few (sequence, KV head) pairs at full context: on a 152-SM GPU these shapes run as
     thread-block clusters, one per pair (2 to 8 CTAs that merge in distributed shared memory)
@@ -292,6 +292,7 @@ def test_bounded_wait_reports_and_the_context_survives(lbkv):
     (2, 1, 16384, False, (64, 8, 1)),     # one cluster of 8 per pair
     (2, 1, 32768, False, (128, 4, 4)),    # four clusters of 4 per pair
     (2, 1, 99968, True, (144, 2, 9)),     # long context with a window: nine clusters of 2
+    (4, 1, 131072, False, (152, 0, 1)),   # INT4 batch 1 at 128K: the split-decode grid
 ])
 def test_launch_modes_on_this_device(lbkv, bits, batch, ctx, window, want):
     """The launch each mode's parity tests rely on (on a 152-SM GB300; other devices may
