@@ -110,6 +110,27 @@ def test_invalid_pack_arguments_rejected(lib, fmt, want):
     assert lib.lbkv_pack(ctypes.byref(d), null, null, *fmt, null, null, null, null) == want
 
 
+@pytest.mark.parametrize("kwargs,fmt,want", [
+    (dict(), (3, 0, 0, 128), -1),              # bits
+    (dict(), (2, 0, 0, 16), -3),               # group
+    (dict(Hq=24, Hkv=8), (2, 0, 0, 128), -3),  # Hq/Hkv = 3
+    (dict(T=1000), (2, 0, 0, 128), -1),        # T_cap not a multiple of 128
+])
+def test_launch_info_rejects_what_decode_rejects(lib, kwargs, fmt, want):
+    d = _desc(**kwargs)
+    g, c, s = ctypes.c_int(-7), ctypes.c_int(-7), ctypes.c_int(-7)
+    assert lib.lbkv_decode_launch_info(ctypes.byref(d), *fmt, ctypes.byref(g), ctypes.byref(c), ctypes.byref(s)) == want
+    null = ctypes.c_void_p(0)
+    assert lib.lbkv_decode_attn(ctypes.byref(d), *([null] * 8), *fmt, null, null) == want
+
+
+def test_launch_info_needs_its_outputs(lib):
+    d = _desc()
+    g = ctypes.c_int(0)
+    assert lib.lbkv_decode_launch_info(ctypes.byref(d), 2, 0, 0, 128, ctypes.byref(g), None, None) == -1
+    assert lib.lbkv_decode_launch_info(None, 2, 0, 0, 128, ctypes.byref(g), ctypes.byref(g), ctypes.byref(g)) == -1
+
+
 def test_null_descriptor(lib):
     null = ctypes.c_void_p(0)
     assert lib.lbkv_decode_attn(None, *([null] * 8), 2, 0, 0, 128, null, null) == -1
