@@ -286,6 +286,22 @@ def test_bounded_wait_reports_and_the_context_survives(lbkv):
 
 
 
+@pytest.mark.parametrize("bits,hq_total,hkv,ctx,kl,vl,g", [
+    (2, 32, 4, 65536, 0, 0, 128),   # 8 queries per KV head (8-warp kernel)
+    (4, 8, 8, 65536, 0, 0, 128),    # 1 query per KV head
+    (2, 16, 8, 65536, 1, 1, 128),   # channel-wise K and V
+    (2, 32, 8, 65536, 0, 0, 32),    # token-wise V with 4 channel groups (16 columns, 8 warps)
+    (4, 32, 8, 49152, 0, 1, 64),
+])
+def test_few_pairs_other_shapes(lbkv, bits, hq_total, hkv, ctx, kl, vl, g):
+    """Batch 1 at long context for other query ratios, layouts and groups (cluster modes with
+    8-warp kernels and other column modes); every unit is compared with the oracle."""
+    s = (0.01, 0.1) if bits == 2 else (0.002, 0.02)
+    wl = inputs.Workload(f"few-pairs-hq{hq_total}-kv{hkv}", 1, hq_total, hkv, ctx - 77, bits=bits, k_layout=kl,
+                         v_layout=vl, group=g, s_range=s, seed=12)
+    sampled_parity(lbkv, wl, [(0, h) for h in range(hkv)])
+
+
 @pytest.mark.parametrize("bits,batch,ctx,window,want", [
     (2, 32, 32768, False, (152, 0, 1)),   # the headline: the split-decode grid
     (2, 8, 32768, False, (128, 2, 1)),    # one cluster of 2 per pair
