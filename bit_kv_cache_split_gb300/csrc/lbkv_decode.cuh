@@ -67,6 +67,10 @@ constexpr int kPrologueBytes = 8192;
 // token-wise K: the B fragments of Q' shared by all warps, [k-step][lane] pairs of words
 constexpr int kQbOffset = kBarBytes + 4 * (kMaxHq * kHeadDim + 6 * kMaxHq);
 static_assert(kQbOffset % 16 == 0 && kQbOffset + 8 * 32 * 8 <= kPrologueBytes, "prologue fits");
+// channel-wise K: words per (query, lane c) row of the W fragments (16, padded so that the 16
+// rows a warp reads at one k-step fall in different bank pairs)
+constexpr int kWRow = 18;
+static_assert(kQbOffset + 4 * kMaxHq * 4 * kWRow <= kPrologueBytes, "prologue fits");
 // The tensor-core decode kernel (lbkv_decode_grp.cuh): shared-memory offset of its merge
 // area, after its mbarriers, counters, prologue, query tile and weight tiles; its rings follow.
 constexpr int kGrpMergeOffset = 7168 + 96 * 128 + 8192;
@@ -344,7 +348,7 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
   // the B fragment: per scale word pair (wa, wb) the two words of k-step ks (r = 0, 1); the
   // pair's channels are k0 and k0 + 8 (INT2) or k0 + 4 (INT4) of this lane's 32
   // (a column without a query reads the zero row kMaxHq - 1, which no query has then)
-  const uint2* wrow = reinterpret_cast<const uint2*>(sW + ((live ? qb : kMaxHq - 1) * 4 + c) * 16);
+  const uint2* wrow = reinterpret_cast<const uint2*>(sW + ((live ? qb : kMaxHq - 1) * 4 + c) * kWRow);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int wa = (C::BITS == 2) ? 8 * (ks >> 2) + (ks & 3) : 4 * (ks >> 1) + (ks & 1);
@@ -365,10 +369,14 @@ __device__ __forceinline__ void channelwise_q(uint32_t (&qB)[8][2], float (&cwA)
   {
     const float* qrow = sQ + (live ? qb : 0) * D + 32 * c;
     const uint2* zrow = reinterpret_cast<const uint2*>(z_tau + 32 * c);
+    // the lanes' 16 (query, c) rows start their 8 quads at different offsets, so that one
+    // load of a warp falls in different banks (in order, all 16 rows would share 4 banks)
+    const int rot = (2 * c + (live ? qb : 0)) & 7;
 #pragma unroll 2
     for (int k4 = 0; k4 < 8; ++k4) {
-      const float4 q4 = reinterpret_cast<const float4*>(qrow)[k4];
-      const uint2 z4 = zrow[k4];
+      const int kk = (k4 + rot) & 7;
+      const float4 q4 = reinterpret_cast<const float4*>(qrow)[kk];
+      const uint2 z4 = zrow[kk];
       const float2 z01 = half2_to_float2(z4.x), z23 = half2_to_float2(z4.y);
       zsum = fmaf(q4.x, z01.x, fmaf(q4.y, z01.y, fmaf(q4.z, z23.x, fmaf(q4.w, z23.y, zsum))));
     }
@@ -1384,7 +1392,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
       // channel-wise K: W = Q / factor * 2^e (fp16) per query and lane, in the order of the
       // lane's B fragment (word 2 ks + r: k-slots 2c + 8r, 2c + 8r + 1 of k-step ks)
       // (rows of queries q >= hq are zero: a column without a query reads one of them)
-      uint32_t* sW = reinterpret_cast<uint32_t*>(sqb);  // [kMaxHq][4][16]
+      uint32_t* sW = reinterpret_cast<uint32_t*>(sqb);  // [kMaxHq][4][kWRow]
       for (int t = threadIdx.x; t < kMaxHq * 64; t += C::THREADS) {
         const int qi = t >> 6, cc = (t >> 4) & 3, wi = t & 15, ks = wi >> 1, r = wi & 1;
         uint32_t w = 0u;
@@ -1393,7 +1401,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
           const int ch0 = qk_channel<C>(ks, 2 * cc + 8 * r), ch1 = qk_channel<C>(ks, 2 * cc + 8 * r + 1);
           w = f16x2_from(sQ[qi * D + ch0] * sc * k_rmult<C>(ch0), sQ[qi * D + ch1] * sc * k_rmult<C>(ch1));
         }
-        sW[t] = w;
+        sW[(t >> 4) * kWRow + (t & 15)] = w;
       }
 #pragma unroll
       for (int j = 0; j < NQ; ++j) st.pa[j] = 1.f;
