@@ -79,8 +79,11 @@ constexpr int kGrpMergeOffset = 7168 + 96 * 128 + 8192;
 constexpr int kStateFloats = 16 * 2 + 4 + 2 * 2;
 // Merge area for hq queries per KV head: per merge warp (m, l) of kMaxHq queries and o of
 // hq queries; with more than kMergeWarps warps it also holds the handed-over states.
+// Row stride (floats) of a deposited output row in the merge area: 4 past the head dim, so that
+// a warp's deposit stores (query c, channels 16 g + p) fall in 8 banks instead of 2.
+constexpr int kODep = kHeadDim + 4;
 __host__ __device__ constexpr int merge_bytes(int hq, int warps) {
-  const int deposit = 4 * kMergeWarps * (2 * kMaxHq + hq * kHeadDim);
+  const int deposit = 4 * kMergeWarps * (2 * kMaxHq + hq * kODep);
   const int states = (warps > kMergeWarps) ? 4 * kMergeWarps * 32 * kStateFloats : 0;
   return ((deposit > states ? deposit : states) + 127) / 128 * 128;
 }
@@ -1557,7 +1560,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
           for (int row = 0; row < 2; ++row)
-            ma.o[(warp * hq + q) * D + 16 * g + pv_channel<BITS>(mt, row)] = st.o_run[mt][row][i] + zt;
+            ma.o[(warp * hq + q) * kODep + 16 * g + pv_channel<BITS>(mt, row)] = st.o_run[mt][row][i] + zt;
       }
     }
     __syncthreads();
@@ -1580,11 +1583,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
           for (int w = 0; w < kMergeWarps; ++w) {
             const float mw = ma.m[w * kMaxHq + i];
             const float sc = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-            acc = fmaf(sc, ma.o[(w * hq + i) * D + ch], acc);
+            acc = fmaf(sc, ma.o[(w * hq + i) * kODep + ch], acc);
             lt = fmaf(sc, ma.l[w * kMaxHq + i], lt);
           }
         }
-        ma.o[idx] = acc;  // read above by this thread only
+        ma.o[i * kODep + ch] = acc;  // read above by this thread only
         if (ch == 0) {
           ss.cm[i] = M;
           ss.cl[i] = lt;
@@ -1622,7 +1625,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
             float4 o4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              if (k0 + j < ncta) o4[j] = ld_cluster_f32x4(cluster_map(o_base + 4u * (i * D + 4 * lane), k0 + j));
+              if (k0 + j < ncta) o4[j] = ld_cluster_f32x4(cluster_map(o_base + 4u * (i * kODep + 4 * lane), k0 + j));
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float sc = __shfl_sync(FULLMASK, sck, (k0 + j) & 31);
@@ -1764,7 +1767,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) split_decode_kernel(const __gri
         for (int w = 0; w < kMergeWarps; ++w) {
           const float mw = ma.m[w * kMaxHq + i];
           const float sc = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-          acc = fmaf(sc, ma.o[(w * hq + i) * D + ch], acc);
+          acc = fmaf(sc, ma.o[(w * hq + i) * kODep + ch], acc);
           lt = fmaf(sc, ma.l[w * kMaxHq + i], lt);
         }
       }
