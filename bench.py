@@ -749,19 +749,23 @@ def quantization_error(device, units=((0, 0), (3, 5), (7, 7))):
 
 
 def run_micro():
-    """Builds and runs bit_kv_cache_split_gb300/micro/tc_rates.cu: cycles per tcgen05 product
-    (kind::f8f6f4, M = 128, N = 16..256, A in tensor memory) and per tensor-memory store and
-    load, with 1, 4 and 16 warps per SM (one JSON line each)."""
+    """Builds and runs the tensor-core microbenchmarks under bit_kv_cache_split_gb300/micro
+    (one JSON line per measurement):
+    - tc_rates.cu: cycles per tcgen05 product (kind::f8f6f4, M = 128, N = 16..256, A in tensor
+      memory) and per tensor-memory store and load, with 1, 4 and 16 warps per SM;
+    - mma_sync_rates.cu: SM cycles per warp-level product (f16 m16n8k16, e4m3 and u8 x s8
+      m16n8k32, loop-variant A operands) with 4, 8 and 16 warps per SM."""
     from bit_kv_cache_split_gb300 import build as libbuild
 
-    src = os.path.join(ROOT, "bit_kv_cache_split_gb300", "micro", "tc_rates.cu")
     os.makedirs(libbuild.BUILD, exist_ok=True)
-    exe = os.path.join(libbuild.BUILD, "tc_rates")
-    subprocess.run([libbuild.nvcc(), *libbuild.ARCH, "-O2", src, "-o", exe], check=True)
-    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
-    sys.stdout.write(r.stdout)
-    if r.returncode != 0:
-        raise SystemExit(f"microbenchmark failed: {r.stderr.strip()}")
+    for name in ("tc_rates", "mma_sync_rates"):
+        src = os.path.join(ROOT, "bit_kv_cache_split_gb300", "micro", name + ".cu")
+        exe = os.path.join(libbuild.BUILD, name)
+        subprocess.run([libbuild.nvcc(), *libbuild.ARCH, "-O2", src, "-o", exe], check=True)
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+        sys.stdout.write(r.stdout)
+        if r.returncode != 0:
+            raise SystemExit(f"microbenchmark {name} failed: {r.stderr.strip()}")
 
 
 def max_over_ranks(ms: float, world: int, device=None) -> float:
